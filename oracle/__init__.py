@@ -1,0 +1,156 @@
+"""Float64 CPU oracle for paged-KV decode attention.
+
+TEST INFRASTRUCTURE ONLY: tests/, ``__graft_entry__.smoke()`` and bench.py's
+CPU-baseline and reference legs are the only callers.  The product path (the
+CUDA library and its binding in ``paged_kv_decode_20_gb300``) never imports
+this package, and this package never imports that one.
+
+The arithmetic lives in ``xqa_oracle.c`` (plain C loops in double precision,
+OpenMP over output rows); this module only compiles it with gcc, marshals
+CPU tensors and calls it.  Semantics follow the FlashInfer ``xqa`` API page
+(parameter list and shape-inference note) and, for the MLA latent variant, the
+vLLM Kimi-K3 MultiHeadLatentAttention page (``head_size``, ``scale`` and the
+``forward_mqa`` call): see the header of ``xqa_oracle.c``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "xqa_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "liboracle_xqa.so")
+_lock = threading.Lock()
+_lib = None
+
+# element codes of the oracle's own C entry point
+_F16, _BF16, _E4M3 = 0, 1, 2
+_DTYPE_CODE = {torch.float16: _F16, torch.bfloat16: _BF16, torch.float8_e4m3fn: _E4M3}
+
+
+def build(force: bool = False) -> str:
+    """Compile xqa_oracle.c into a shared library (gcc, -O2, OpenMP)."""
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    stale = not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)
+    if force or stale:
+        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        cmd = ["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c11", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            lib.oracle_xqa_attention.restype = ctypes.c_int
+            lib.oracle_xqa_attention.argtypes = [
+                ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_void_p, ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                ctypes.c_int, ctypes.c_double, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                ctypes.c_void_p, ctypes.c_int,
+            ]
+            lib.oracle_decode.restype = ctypes.c_double
+            lib.oracle_decode.argtypes = [ctypes.c_int, ctypes.c_uint32]
+            _lib = lib
+    return _lib
+
+
+def decode(dtype: torch.dtype, bits: int) -> float:
+    """Decode one element from its bit pattern, as the oracle does."""
+    return _load().oracle_decode(_DTYPE_CODE[dtype], bits)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _cpu_contig(t, dtype=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        t = torch.as_tensor(np.asarray(t))
+    t = t.detach().to("cpu")
+    if dtype is not None and t.dtype != dtype:
+        t = t.to(dtype)
+    return t.contiguous()
+
+
+def xqa_attention(q, k_cache, v_cache, page_table, seq_lens, *, num_kv_heads, page_size,
+                  kv_layout="NHD", v_head_dim=None, sinks=None, q_scale=1.0, kv_scale=1.0,
+                  softmax_scale=None, sliding_win_size=0, rcp_out_scale=1.0, q_seq_len=None,
+                  mask=None, units=None, threads=0):
+    """Exact float64 paged decode attention.
+
+    q: [B, q_seq_len, Hq, D] (or [B, Hq, D]) fp16/bf16.  k_cache, v_cache:
+    [num_pages, page_size, Hkv, D] (NHD) or [num_pages, Hkv, page_size, D]
+    (HND), fp16/bf16/float8_e4m3fn; for the MLA variant pass the same latent
+    cache twice and v_head_dim < D.  page_table: int32 [B, pages_per_seq].
+    seq_lens: [B] (uint32 semantics).  softmax_scale None means 1/sqrt(D).
+    units: optional flat row ids (b * q_seq_len + i) * Hq + h; the result is
+    then [len(units), Dv], otherwise [B, q_seq_len, Hq, Dv].  float64 tensor.
+    """
+    q = _cpu_contig(q)
+    if q.dim() == 3:
+        q = q.unsqueeze(1)
+    B, qs, Hq, D = q.shape
+    if q_seq_len is not None and q_seq_len != qs:
+        raise ValueError(f"q has {qs} query tokens per sequence, q_seq_len={q_seq_len}")
+    k_cache = _cpu_contig(k_cache)
+    v_cache = k_cache if v_cache is None else _cpu_contig(v_cache)
+    if k_cache.dtype != v_cache.dtype:
+        raise ValueError("k_cache and v_cache must share one dtype")
+    if k_cache.shape[-1] != D:
+        raise ValueError("cache head_dim differs from q head_dim")
+    Dv = D if v_head_dim is None else int(v_head_dim)
+    page_table = _cpu_contig(page_table, torch.int32)
+    seq_lens = _cpu_contig(seq_lens).to(torch.int64).to(torch.int32)  # uint32 bits
+    sinks = _cpu_contig(sinks, torch.float32)
+    mask = _cpu_contig(mask)
+    if mask is not None:
+        mask = mask.view(torch.int16) if mask.dtype == torch.uint16 else mask.to(torch.int16)
+        words = ((qs + 31) // 32) * 2
+        if tuple(mask.shape) != (B, qs, words):
+            raise ValueError(f"mask must be [{B}, {qs}, {words}], got {tuple(mask.shape)}")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    layout_hnd = {"NHD": 0, "HND": 1}[kv_layout.upper()]
+    q_bits = q.view(torch.int16)
+    kv_code = _DTYPE_CODE[k_cache.dtype]
+    k_bits = k_cache.view(torch.uint8) if kv_code == _E4M3 else k_cache.view(torch.int16)
+    v_bits = v_cache.view(torch.uint8) if kv_code == _E4M3 else v_cache.view(torch.int16)
+    if units is not None:
+        units = _cpu_contig(units, torch.int64)
+        out = torch.empty((units.numel(), Dv), dtype=torch.float64)
+        n_units = units.numel()
+    else:
+        out = torch.empty((B, qs, Hq, Dv), dtype=torch.float64)
+        n_units = 0
+    rc = _load().oracle_xqa_attention(
+        _ptr(q_bits), _DTYPE_CODE[q.dtype], _ptr(k_bits), _ptr(v_bits), kv_code, layout_hnd,
+        k_cache.shape[0], _ptr(page_table), page_table.shape[1], _ptr(seq_lens), B, Hq,
+        int(num_kv_heads), D, Dv, int(page_size), qs, _ptr(sinks), float(q_scale),
+        float(kv_scale), float(softmax_scale), int(sliding_win_size), float(rcp_out_scale),
+        _ptr(mask), _ptr(units), n_units, _ptr(out), int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the problem (code {rc})")
+    return out
+
+
+def unit_ids(batch_idx, q_idx, head_idx, q_seq_len, num_q_heads):
+    """Flat row ids understood by ``xqa_attention(units=...)``."""
+    b = torch.as_tensor(batch_idx, dtype=torch.int64)
+    i = torch.as_tensor(q_idx, dtype=torch.int64)
+    h = torch.as_tensor(head_idx, dtype=torch.int64)
+    return (b * q_seq_len + i) * num_q_heads + h
