@@ -1,0 +1,389 @@
+"""Benchmark of paged decode attention on GB300 (one JSON line on rank 0).
+
+Default workload: the Llama-3-8B-shaped decode (B64 Hq32 Hkv8 D128, page 64,
+HND, seq_lens uniform in [1024, 8192], bf16).  A step is one decode call over
+the whole batch (one launch of the decode kernel).  value = algorithmic KV
+GB/s (every visible token's K and V row read once) over all ranks;
+decode tokens/s = B * q_seq_len / step time.  The KV cache (1.2 GB) is larger
+than L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5]
+  python bench.py --impl reference ...   (the float64 CPU oracle, bounded sample)
+
+Multi-GPU: one process per GPU (torchrun); decode sequences are independent,
+so every rank runs its own replica of the workload with no collective on the
+data path (weak scaling); only the timing is reduced (max over ranks).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_decode_20_gb300 import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention: KV GB/s & % of GB300 HBM peak; decode tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_NAMES = {1: "gqa_decode_kernel", 2: "gqa_decode_kernel", 3: "gqa_decode_kernel",
+                4: "gqa_decode_kernel", 5: "mla_decode_kernel"}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_decode_20_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(f.encode())
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        d = json.load(open(path))[str(workload)]
+    except Exception:
+        return None
+    return d["dram_bytes_per_launch"] if d.get("kernel_hash") == kernel_source_hash() else None
+
+
+class Clocks:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [x for x in out.splitlines() if x.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def build_case(idx, device, rank):
+    case = W.workload(idx, device=device, poison=False)
+    return case
+
+
+def run_gb300(args):
+    from paged_kv_decode_20_gb300 import build as B
+    from paged_kv_decode_20_gb300 import xqa as X
+    from paged_kv_decode_20_gb300.runner import Decoder
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if rank == 0 or world == 1:
+        B.build()
+    if world > 1:
+        dist.barrier()
+    X.load()
+
+    case = build_case(args.workload, dev, rank)
+    dec = Decoder(case, error_word=False)
+    stream = torch.cuda.current_stream(dev)
+    kv_bytes = case.kv_bytes()
+    q_bytes = case.q_bytes()
+    tokens = case.batch * case.q_seq_len
+
+    # ---- device-resident timing: K steps, events around each launch
+    for _ in range(args.warmup):
+        dec.run(stream)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with Clocks(local) as clk:
+        t0.record(stream)
+        for s in range(args.steps):
+            ev[s][0].record(stream)
+            dec.run(stream)
+            ev[s][1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    total_ms = t0.elapsed_time(t1)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    avg_launch_ms = sum(launch_ms) / len(launch_ms)
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = {n: getattr(case, n).cpu().pin_memory() for n in
+                ("q", "k_cache", "v_cache", "page_table", "seq_lens")}
+        if case.mla:
+            host["v_cache"] = host["k_cache"]
+        out_host = torch.empty(dec.output.shape, dtype=dec.output.dtype).pin_memory()
+        names = ["q", "k_cache", "page_table", "seq_lens"] + ([] if case.mla else ["v_cache"])
+        h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+        d2h = out_host.numel() * out_host.element_size()
+
+        def e2e_step():
+            for n in names:
+                getattr(case, n).copy_(host[n], non_blocking=True)
+            dec.run(stream)
+            out_host.copy_(dec.output, non_blocking=True)
+
+        for _ in range(max(1, args.warmup // 2)):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e_steps = max(3, args.steps // 4)
+        e0.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = e0.elapsed_time(e1) / e_steps
+        if world > 1:
+            tt = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e_ms = float(tt.item())
+        e2e = {"value": round(kv_bytes * world / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "ms_per_step": round(e_ms, 4), "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+
+    # ---- CPU baseline: the oracle, all rows of this workload once (rank 0)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(case.to("cpu"), args.workload)
+
+    if world > 1:
+        dist.barrier()
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    peak, peak_kind = peaks()
+    achieved = (kv_bytes + q_bytes) / (avg_launch_ms * 1e-3) / 1e9
+    value = kv_bytes * world / (ms_per_step * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": {torch.bfloat16: "bf16", torch.float16: "f16",
+                  torch.float8_e4m3fn: "e4m3 kv, bf16 q"}[case.k_cache.dtype],
+        "data": "synthetic (seeded N(0,1) q/K/V, shuffled page pool)",
+        "config": {"workload": W.WORKLOADS[args.workload], "global_batch": case.batch * world,
+                   "kv_bytes_per_step": kv_bytes * world, "q_bytes_per_step": q_bytes * world,
+                   "l2": "inputs larger than L2 (no flush)" if kv_bytes > 129e6
+                   else "KV fits in L2: numbers are L2-assisted",
+                   "parallelism": f"replicas x{world} (no collective)"},
+        "decode_tokens_per_s": round(tokens * world / (ms_per_step * 1e-3), 1),
+        "pct_hbm_peak": round(100 * achieved / peak, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": peak_kind,
+                     "traffic": recorded_traffic(args.workload),
+                     "kernel": KERNEL_NAMES[args.workload],
+                     "algorithmic_bytes_per_launch": kv_bytes + q_bytes,
+                     "avg_launch_ms": round(avg_launch_ms, 5)},
+        "gpu_launches": args.steps,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def cpu_baseline(case, idx, max_rows=None):
+    """Time the float64 oracle on all rows of the workload (or a bounded
+    sample of whole (b, kv head) units) with every host thread."""
+    import oracle
+    B, qs, Hq, _ = case.q.shape
+    G = Hq // case.num_kv_heads
+    threads = os.cpu_count() or 1
+    units = None
+    frac = 1.0
+    rows = B * qs * Hq
+    budget_rows = max_rows if max_rows is not None else {1: rows, 2: rows, 3: 256, 4: rows, 5: 128}[idx]
+    if budget_rows < rows:
+        # whole (b, kvh) units, spread over the batch
+        per_unit = qs * G
+        n_units = max(1, budget_rows // per_unit)
+        sel = torch.linspace(0, B * case.num_kv_heads - 1, n_units).round().long().unique()
+        ids = []
+        for u in sel.tolist():
+            b, kvh = divmod(u, case.num_kv_heads)
+            for i in range(qs):
+                for g in range(G):
+                    ids.append((b * qs + i) * Hq + kvh * G + g)
+        units = torch.tensor(ids, dtype=torch.int64)
+        lens = case.seq_lens.to(torch.int64)
+        if case.sliding_win_size > 0:
+            lens = lens.clamp(max=case.sliding_win_size + qs - 1)
+        per_b = lens.to(torch.float64)
+        frac = float(sum(per_b[u // case.num_kv_heads] for u in sel.tolist()) /
+                     (per_b.sum() * case.num_kv_heads))
+        sample = f"{len(sel)} of {B * case.num_kv_heads} (sequence, kv head) units, all their rows"
+    else:
+        sample = f"all {rows} output rows of the workload, once"
+    kw = case.kwargs()
+    t = time.perf_counter()
+    oracle.xqa_attention(case.q, case.k_cache, case.v_cache, case.page_table, case.seq_lens,
+                         units=units, threads=threads, **kw)
+    dt = time.perf_counter() - t
+    kv = case.kv_bytes() * frac
+    return {"value": round(kv / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": sample, "seconds": round(dt, 3)}
+
+
+def run_reference(args):
+    """The reference arm: the float64 CPU oracle as it stands, each step a
+    bounded sample of the workload, on the host cores of rank 0."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    case = W.workload(args.workload, device="cpu", poison=False)
+    B = case.batch
+    # each step: a few whole (sequence, kv head) units
+    rows_per_step = {1: 16, 2: 32, 3: 8, 4: 64, 5: 128}[args.workload]
+    for _ in range(args.warmup):
+        cpu_baseline(case, args.workload, max_rows=rows_per_step)
+    times, vals = [], []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        r = cpu_baseline(case, args.workload, max_rows=rows_per_step)
+        times.append(r["seconds"])
+        vals.append(r["value"])
+    total = time.perf_counter() - t0
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total / args.steps, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) q/K/V, shuffled page pool)",
+        "config": {"workload": W.WORKLOADS[args.workload], "global_batch": B,
+                   "parallelism": "CPU oracle, rank 0 only"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": r["sample"] + " per step"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gb300(args)
+
+
+if __name__ == "__main__":
+    main()

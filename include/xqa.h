@@ -1,0 +1,146 @@
+/*
+ * xqa.h — C ABI of the GB300 (sm_103a) paged-KV decode attention library.
+ *
+ * Operation (FlashInfer "flashinfer.xqa.xqa" API page: signature, parameter
+ * list and the shape-inference note; beam_width is fixed to 1, the only width
+ * that page supports): one or a few speculative query tokens per sequence
+ * attend to a paged KV cache.  For batch b, query token i < q_seq_len and
+ * query head h (kv head kvh = h / G, G = Hq / Hkv):
+ *
+ *   L = seq_lens[b] (it counts the q_seq_len new tokens), p = L - q_seq_len + i
+ *   token t lives in page page_table[b][t / page_size], slot t % page_size
+ *   visible(t): t < L, and t > p - sliding_win_size (window on), and for the
+ *               new tokens t >= L - q_seq_len the mask bit (i, t - L + q_seq_len)
+ *   s_t = softmax_scale * q_scale * kv_scale * <q[b,i,h,:], K[t,:]>
+ *   out[b,i,h,:] = rcp_out_scale * kv_scale * sum_t e^{s_t - M} V[t,:] / Z
+ *   with M = max(max_t s_t, sink) and Z = sum_t e^{s_t - M} + e^{sink - M};
+ *   sink = sinks[kvh][h % G] (a logit, not scaled), absent when sinks is NULL.
+ *   A row with nothing visible and no sink is written as zeros.
+ *
+ * The MLA latent variant (vLLM Kimi-K3 MultiHeadLatentAttention page:
+ * head_size = kv_lora_rank + qk_rope_head_dim, scale = qk_head_dim^-0.5, and
+ * the forward_mqa call on the absorbed query) is the same operation with one
+ * kv head of width head_dim = kv_lora_rank + rope and V = the first v_head_dim
+ * (= kv_lora_rank) elements of each latent row.
+ *
+ * Conventions
+ *  - Every pointer is DEVICE memory owned by the caller; the library never
+ *    allocates, frees or synchronises.  Calls are asynchronous on `stream`.
+ *  - `output` is written in place (the API page: "modified in place").
+ *  - Host-side validation returns a status before anything is launched; a
+ *    launch failure returns XQA_ERR_CUDA.
+ *  - Device code never traps.  A page_table entry outside [0, num_pages)
+ *    reads as zeros (TMA bounds fill) and a seq_len above
+ *    pages_per_seq * page_size is clamped to it; both set bit 0 of
+ *    `error_word` when the caller provides one.
+ */
+#ifndef XQA_GB300_H
+#define XQA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* xqa_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  XQA_OK = 0,
+  XQA_ERR_INVALID_ARG = 1,         /* malformed argument (null pointer, bad shape, bad value) */
+  XQA_ERR_UNSUPPORTED = 2,         /* well-formed but outside what the kernels implement */
+  XQA_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < xqa_workspace_size(), or no semaphores */
+  XQA_ERR_CUDA = 4                 /* a CUDA runtime call or kernel launch failed */
+} xqa_status;
+
+typedef enum { XQA_F16 = 0, XQA_BF16 = 1, XQA_E4M3 = 2 } xqa_dtype;
+
+/* NHD: cache [num_pages, page_size, Hkv, head_dim]; HND: [num_pages, Hkv, page_size, head_dim]. */
+typedef enum { XQA_NHD = 0, XQA_HND = 1 } xqa_layout;
+
+typedef struct xqa_params {
+  /* q [batch, q_seq_len, num_q_heads, head_dim], fp16 or bf16, contiguous. */
+  const void* q;
+  xqa_dtype q_dtype;
+  /* K and V caches: kv_dtype is q_dtype or XQA_E4M3 (then "fp8 compute"),
+     shared by both; both use kv_layout.  They may alias (MLA latent cache). */
+  const void* k_cache;
+  const void* v_cache;
+  xqa_dtype kv_dtype;
+  xqa_layout kv_layout;
+  int64_t num_pages;
+  /* int32 [batch, pages_per_seq], shared by K and V. */
+  const int32_t* page_table;
+  int32_t pages_per_seq;
+  /* uint32 [batch]; max_seq_len = pages_per_seq * page_size. */
+  const uint32_t* seq_lens;
+  /* output [batch, q_seq_len, num_q_heads, v_head_dim]; out_dtype must equal q_dtype. */
+  void* output;
+  xqa_dtype out_dtype;
+  int32_t batch_size;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t page_size;  /* 16, 32, 64 or 128 */
+  int32_t q_seq_len;  /* >= 1; > 1 is speculative decoding */
+  /* fp32 [num_kv_heads, num_q_heads / num_kv_heads] or NULL (no sinks). */
+  const float* sinks;
+  /* Scale factors for q and the KV cache.  A non-NULL *_dev pointer names one
+     device float that replaces the host value (the "float or Tensor" form). */
+  float q_scale;
+  float kv_scale;
+  const float* q_scale_dev;
+  const float* kv_scale_dev;
+  /* Logit scale; 0 means 1/sqrt(head_dim).  The API page's call has no such
+     argument; the MLA variant needs (qk_nope + qk_rope)^-0.5. */
+  float softmax_scale;
+  int32_t sliding_win_size; /* 0 = no window */
+  float rcp_out_scale;      /* reciprocal of the output scale; multiplies the output */
+  /* uint16 [batch, q_seq_len, ((q_seq_len + 31) / 32) * 2], bit-packed in
+     little-endian 32-bit words (bit j % 32 of word j / 32: may see new token j),
+     or NULL (all new tokens visible). */
+  const uint16_t* mask;
+  int32_t sm_count;   /* SMs to plan for; 0 = the current device's count */
+  int32_t enable_pdl; /* programmatic dependent launch; accepted, no numeric effect */
+  uint32_t* error_word; /* optional device word; bit 0 = clamped length or bad page index */
+} xqa_params;
+
+/* Bytes of workspace xqa_decode needs for these parameters when planning for
+   sm_count SMs (0 = current device).  0 means the call needs none.  Returns
+   (size_t)-1 for parameters xqa_decode would reject. */
+size_t xqa_workspace_size(const xqa_params* params, int sm_count);
+
+/* Number of uint32 semaphores xqa_decode needs.  They must be zero on the
+   first call; every call leaves them zero again (the last CTA to finish a
+   split-KV reduction resets its counter). */
+size_t xqa_semaphore_count(const xqa_params* params);
+
+/* Paged decode attention (the XQA-style call).  workspace: caller-owned device
+   scratch of at least xqa_workspace_size() bytes (any contents); semaphores:
+   xqa_semaphore_count() zeroed uint32.  Both may be NULL when their size is 0.
+   Two calls that share workspace or semaphores must not overlap on the GPU. */
+xqa_status xqa_decode(const xqa_params* params, void* workspace, size_t workspace_bytes,
+                      uint32_t* semaphores, xqa_stream_t stream);
+
+/* Same sizing queries for the MLA latent variant (num_kv_heads = 1). */
+size_t xqa_mla_workspace_size(const xqa_params* params, int v_head_dim, int sm_count);
+size_t xqa_mla_semaphore_count(const xqa_params* params, int v_head_dim);
+
+/* MLA latent decode: params->num_kv_heads must be 1, head_dim the latent width
+   (kv_lora_rank + rope) and v_head_dim the kv_lora_rank prefix used as V.
+   k_cache and v_cache may be the same pointer (the latent cache). */
+xqa_status xqa_mla_decode(const xqa_params* params, int v_head_dim, void* workspace,
+                          size_t workspace_bytes, uint32_t* semaphores, xqa_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* xqa_status_string(xqa_status status);
+
+/* Detail of the most recent non-OK status returned on the calling thread
+   (static per-thread buffer; "" when none). */
+const char* xqa_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* XQA_GB300_H */

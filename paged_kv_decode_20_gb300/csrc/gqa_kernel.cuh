@@ -1,0 +1,595 @@
+// Grouped-query paged decode attention for sm_103a (the XQA-style call of the
+// FlashInfer "flashinfer.xqa.xqa" API page).
+//
+// One CTA owns (sequence b, kv head kvh, row group rg, KV split).  Its rows are
+// the q_seq_len x G query rows that share kv head kvh (speculative tokens and
+// the GQA group stacked), padded to 16-row MMA blocks.
+//
+//   warp 4 (producer, one lane): walks page_table and issues one TMA tile load
+//     per (page, 128-byte column chunk) for K and for V into a ring of 64-token
+//     stages, each guarded by a full/empty mbarrier pair.  NHD and HND differ
+//     only in the tensor map and the coordinates.  TMA writes the rows with the
+//     128-byte swizzle, so ldmatrix reads are bank-conflict free.
+//   warps 0-3 (consumers): each takes 16 tokens of every stage.
+//     S = Q K^T with mma.sync m16n8k16 (rows on M, tokens on N), fp32 online
+//     softmax in the exp2 domain with window / spec-mask / tail masking by
+//     select, then O += P V (P re-used from the S accumulator registers).
+//     fp8 K/V is widened to f16 in registers (cvt e4m3x2 -> f16x2, exact); a
+//     consistent permutation of the contraction index lets each lane convert
+//     whole 32-bit words, and a permutation of the V columns lets fp8 V be
+//     read as words instead of transposed bytes.
+//   epilogue: the four warps' (m, l, O) merge through shared memory.  With one
+//     split the CTA finalises (sinks, scales) and writes the output; otherwise
+//     it writes its partial to the workspace and takes a ticket on its
+//     semaphore, and the last CTA to arrive merges every split (the same
+//     log-sum-exp merge as merge_attn_states on the Kimi-K3 MLA page), writes
+//     the output and resets the semaphore to zero.  No CTA ever waits on
+//     another.
+#pragma once
+#include "kernel_args.h"
+#include "ptx.cuh"
+
+namespace xqa {
+
+enum KvKind { kKvF16 = 0, kKvBf16 = 1, kKvE4m3 = 2 };
+
+template <int KV, int D, int RB>
+struct GqaCfg {
+  static constexpr bool kF8 = (KV == kKvE4m3);
+  static constexpr int kElt = kF8 ? 1 : 2;
+  static constexpr int kRowBytes = D * kElt;  // 128 or 256
+  static_assert(kRowBytes == 128 || kRowBytes == 256, "row must be 1 or 2 swizzle chunks");
+  static constexpr int kChunks = kRowBytes / 128;
+  static constexpr int kTok = 64;                          // tokens per stage
+  static constexpr int kTile = kTok * kRowBytes;           // K (or V) bytes per stage
+  static constexpr int kStage = 2 * kTile;
+  static constexpr int kNumStages = kStage >= 32768 ? 3 : 5;
+  static constexpr int kRows = 16 * RB;
+  static constexpr int kThreads = 160;
+  static constexpr int kScratch = 4 * kRows * D * 4 + 2 * 4 * kRows * 4;
+  static constexpr int kRing = kNumStages * kStage;
+  static_assert(kScratch <= kRing, "epilogue scratch reuses the stage ring");
+  static constexpr int kBarOff = kRing;
+  static constexpr int kSmem = 1024 + kRing + 2 * kNumStages * 8 + 16;
+};
+
+__device__ __forceinline__ float load_scale(const float* dev, float host) {
+  return dev ? __ldg(dev) : host;
+}
+
+template <int KV, int D, int RB>
+__global__ void __launch_bounds__(160, 2)
+    gqa_decode_kernel(const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const DecodeArgs a) {
+  using C = GqaCfg<KV, D, RB>;
+  constexpr bool kF8 = C::kF8;
+  constexpr bool kMmaBf16 = (KV == kKvBf16);
+  constexpr int kKSteps = D / 16;
+  constexpr int kDvTiles = D / 8;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* empty = full + C::kNumStages;
+  int* flags = reinterpret_cast<int*>(empty + C::kNumStages);  // [0] abort, [1] last-CTA
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int split = blockIdx.x;
+  const int kvh = blockIdx.y / a.rg_count, rg = blockIdx.y % a.rg_count;
+  const int b = blockIdx.z;
+
+  // ---- sequence geometry (identical in every CTA of this (b, kvh, rg))
+  const int64_t max_len = int64_t(a.pps) * a.ps;
+  const int64_t len_raw = a.seq_lens[b];
+  const int L = int(len_raw < max_len ? len_raw : max_len);
+  if (len_raw > max_len && a.err && tid == 0 && split == 0 && blockIdx.y == 0)
+    atomicOr(a.err, kErrClamped);
+  const int spec0 = L - a.qs;                       // first new (speculative) token
+  const int t_lo_all = a.win > 0 ? max(0, spec0 - a.win + 1) : 0;
+  const int pg_first = t_lo_all / a.ps;
+  const int pg_last = (L + a.ps - 1) / a.ps;
+  const int npages = max(0, pg_last - pg_first);
+  const int nvalid = (npages + a.split_pages - 1) / a.split_pages;
+  if (split >= max(nvalid, 1)) return;
+  const int pg_lo = pg_first + split * a.split_pages;
+  const int pg_hi = min(pg_lo + a.split_pages, pg_last);
+  const int t_begin = pg_lo * a.ps;
+  const int t_end = min(pg_hi * a.ps, L);
+  const int nst = (nvalid == 0 || t_end <= t_begin) ? 0 : (t_end - t_begin + C::kTok - 1) / C::kTok;
+
+  if (tid == 0) {
+    for (int i = 0; i < C::kNumStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 4);
+    }
+    flags[0] = 0;
+    flags[1] = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int unit = (b * a.Hkv + kvh) * a.rg_count + rg;
+  float* scratch = reinterpret_cast<float*>(smem);  // epilogue: [4][rows][D] O, then m, l
+  float* sc_m = scratch + 4 * C::kRows * D;
+  float* sc_l = sc_m + 4 * C::kRows;
+
+  if (warp == 4) {
+    // ================= producer =================
+    if (lane == 0 && nst > 0) {
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+      const int32_t* pt = a.page_table + int64_t(b) * a.pps;
+      const int box_rows = a.ps < C::kTok ? a.ps : C::kTok;
+      const uint32_t box_bytes = uint32_t(box_rows) * 128u;
+      constexpr int kChunkElems = 128 / C::kElt;
+      bool bad_page = false;
+      int s = 0;
+      for (; s < nst; ++s) {
+        const int slot = s % C::kNumStages;
+        const int round = s / C::kNumStages;
+        if (s >= C::kNumStages && !mbar_wait(&empty[slot], (round & 1) ^ 1)) {
+          flags[0] = 1;
+          break;
+        }
+        uint8_t* kdst = smem + slot * C::kStage;
+        uint8_t* vdst = kdst + C::kTile;
+        const int tok0 = t_begin + s * C::kTok;
+        // pieces of this stage: (logical page, first slot, destination row)
+        int n_piece = 0;
+        if (a.ps <= C::kTok) {
+          const int per = C::kTok / a.ps;
+          const int lp0 = tok0 / a.ps;
+          n_piece = min(per, pg_hi - lp0);
+        } else {
+          n_piece = 1;
+        }
+        mbar_arrive_expect_tx(&full[slot], uint32_t(n_piece) * box_bytes * 2u * C::kChunks);
+        for (int j = 0; j < n_piece; ++j) {
+          int lp, sub;
+          if (a.ps <= C::kTok) {
+            lp = tok0 / a.ps + j;
+            sub = 0;
+          } else {
+            lp = tok0 / a.ps;
+            sub = tok0 % a.ps;
+          }
+          int page = __ldg(pt + lp);
+          if (page < 0 || int64_t(page) >= a.num_pages) {
+            bad_page = true;
+            page = -1;  // every coordinate out of bounds: TMA fills zeros
+          }
+          const int row_off = j * box_rows;
+          for (int c = 0; c < C::kChunks; ++c) {
+            const int off = c * C::kTok * 128 + row_off * 128;
+            if (a.hnd) {
+              tma_load_3d(kdst + off, &tmK, &full[slot], c * kChunkElems, sub, page * a.Hkv + kvh);
+              tma_load_3d(vdst + off, &tmV, &full[slot], c * kChunkElems, sub, page * a.Hkv + kvh);
+            } else {
+              tma_load_3d(kdst + off, &tmK, &full[slot], c * kChunkElems, kvh, page * a.ps + sub);
+              tma_load_3d(vdst + off, &tmV, &full[slot], c * kChunkElems, kvh, page * a.ps + sub);
+            }
+          }
+        }
+      }
+      if (bad_page && a.err) atomicOr(a.err, kErrClamped);
+      // Leave no copy in flight: wait (bounded) for the last stages issued.
+      const int first = max(0, s - C::kNumStages);
+      for (int t = first; t < s; ++t) {
+        if (!mbar_wait(&full[t % C::kNumStages], (t / C::kNumStages) & 1)) flags[0] = 1;
+      }
+      if (flags[0] && a.err) atomicOr(a.err, kErrTimeout);
+    }
+  } else {
+    // ================= consumers =================
+    const int g = lane >> 2, qd = lane & 3;
+    const float q_scale = load_scale(a.q_scale_dev, a.q_scale);
+    const float kv_scale = load_scale(a.kv_scale_dev, a.kv_scale);
+    float lscale = a.softmax_scale * q_scale * kv_scale * kLog2e;
+
+    // ---- query fragments (A operand), rows of this CTA's row group
+    uint32_t qa[RB][kKSteps][4];
+    {
+      const bool qbf = a.q_bf16 != 0;
+      const uint16_t* q16 = static_cast<const uint16_t*>(a.q);
+      float qv[RB][kKSteps][8];
+      float amax = 0.f;
+#pragma unroll
+      for (int rb = 0; rb < RB; ++rb) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int r = rg * C::kRows + rb * 16 + g + 8 * hh;
+          const bool ok = r < a.R;
+          const int i = ok ? r / a.G : 0, gg = ok ? r % a.G : 0;
+          const uint16_t* src =
+              q16 + ((int64_t(b) * a.qs + i) * a.Hq + int64_t(kvh) * a.G + gg) * D;
+#pragma unroll
+          for (int kc = 0; kc < kKSteps; ++kc) {
+            // element pairs of this lane: (d0, d0+1) and (d1, d1+1)
+            int d0, d1;
+            if (kF8) {
+              d0 = 16 * kc + 4 * qd;
+              d1 = d0 + 2;
+            } else {
+              d0 = 16 * kc + 2 * qd;
+              d1 = d0 + 8;
+            }
+            uint32_t w0 = ok ? __ldg(reinterpret_cast<const uint32_t*>(src + d0)) : 0u;
+            uint32_t w1 = ok ? __ldg(reinterpret_cast<const uint32_t*>(src + d1)) : 0u;
+            float2 f0 = unpack_16x2(w0, qbf), f1 = unpack_16x2(w1, qbf);
+            // fragment slots: [0,1] row g lo-k, [2,3] row g+8 lo-k, [4,5] row g hi-k, [6,7] row g+8 hi-k
+            qv[rb][kc][2 * hh + 0] = f0.x;
+            qv[rb][kc][2 * hh + 1] = f0.y;
+            qv[rb][kc][4 + 2 * hh + 0] = f1.x;
+            qv[rb][kc][4 + 2 * hh + 1] = f1.y;
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y))));
+          }
+        }
+      }
+      float qmul = 1.f;
+      if (kF8 && qbf) {
+        // bf16 q feeds an f16 MMA: rescale by a power of two into f16 range
+        // (exact) and fold the inverse into the logit scale.
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        int e = 0;
+        if (amax > 0.f && amax < 3.0e38f) e = 14 - ilogbf(amax);
+        e = max(-60, min(60, e));
+        qmul = ldexpf(1.f, e);
+        lscale *= ldexpf(1.f, -e);
+      }
+#pragma unroll
+      for (int rb = 0; rb < RB; ++rb)
+#pragma unroll
+        for (int kc = 0; kc < kKSteps; ++kc)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (kF8 && qbf)
+              qa[rb][kc][j] = pack_f32x2(qv[rb][kc][2 * j] * qmul, qv[rb][kc][2 * j + 1] * qmul, false);
+            else
+              qa[rb][kc][j] = pack_f32x2(qv[rb][kc][2 * j], qv[rb][kc][2 * j + 1], kMmaBf16);
+          }
+    }
+
+    // ---- per-row metadata for the rows this lane holds (g and g+8 of each block)
+    int row_lb[RB][2];       // first visible token (window), per row
+    uint32_t row_mw[RB][2];  // spec-mask word of the row
+#pragma unroll
+    for (int rb = 0; rb < RB; ++rb)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int r = rg * C::kRows + rb * 16 + g + 8 * hh;
+        const int i = r < a.R ? r / a.G : 0;
+        row_lb[rb][hh] = a.win > 0 ? spec0 + i - a.win + 1 : INT_MIN;
+        uint32_t mw = 0xffffffffu;
+        if (a.mask) {
+          const uint16_t* mrow = a.mask + (int64_t(b) * a.qs + i) * a.mask_words;
+          mw = uint32_t(__ldg(mrow)) | (uint32_t(__ldg(mrow + 1)) << 16);
+        }
+        row_mw[rb][hh] = mw;
+      }
+    const int lb_max = a.win > 0 ? spec0 + a.qs - 1 - a.win + 1 : INT_MIN;
+
+    float m_run[RB][2], l_run[RB][2];
+    float o[RB][kDvTiles][4];
+#pragma unroll
+    for (int rb = 0; rb < RB; ++rb) {
+      m_run[rb][0] = m_run[rb][1] = -INFINITY;
+      l_run[rb][0] = l_run[rb][1] = 0.f;
+#pragma unroll
+      for (int j = 0; j < kDvTiles; ++j) o[rb][j][0] = o[rb][j][1] = o[rb][j][2] = o[rb][j][3] = 0.f;
+    }
+
+    for (int s = 0; s < nst; ++s) {
+      const int slot = s % C::kNumStages;
+      if (!mbar_wait(&full[slot], (s / C::kNumStages) & 1)) {
+        flags[0] = 1;
+        if (a.err && lane == 0) atomicOr(a.err, kErrTimeout);
+        break;
+      }
+      const int ta = t_begin + s * C::kTok + 16 * warp;  // this warp's first token
+      if (ta < t_end) {
+        const uint32_t kt = smem_u32(smem + slot * C::kStage);
+        const uint32_t vt = kt + C::kTile;
+        const bool edge = (ta + 16 > t_end) || (ta < lb_max) || (a.mask && ta + 16 > spec0);
+
+        // ---- S = Q K^T over this warp's 16 tokens (two n-tiles of 8)
+        float sacc[RB][2][4];
+#pragma unroll
+        for (int rb = 0; rb < RB; ++rb)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) sacc[rb][nt][0] = sacc[rb][nt][1] = sacc[rb][nt][2] = sacc[rb][nt][3] = 0.f;
+        const int mat = lane >> 3;
+        if constexpr (!kF8) {
+          const int tr = 16 * warp + (mat >> 1) * 8 + (lane & 7);
+#pragma unroll
+          for (int kc = 0; kc < kKSteps; ++kc) {
+            const int u = 2 * kc + (mat & 1);
+            const uint32_t addr = kt + (u >> 3) * (C::kTok * 128) + tr * 128 + (((u & 7) ^ (tr & 7)) << 4);
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4(addr, r0, r1, r2, r3);
+#pragma unroll
+            for (int rb = 0; rb < RB; ++rb) {
+              mma16816<kMmaBf16>(sacc[rb][0], qa[rb][kc], r0, r1);
+              mma16816<kMmaBf16>(sacc[rb][1], qa[rb][kc], r2, r3);
+            }
+          }
+        } else {
+          const int tr = 16 * warp + (mat & 1) * 8 + (lane & 7);
+#pragma unroll
+          for (int kc2 = 0; kc2 < kKSteps / 2; ++kc2) {
+            const int u = 2 * kc2 + (mat >> 1);
+            const uint32_t addr = kt + tr * 128 + (((u & 7) ^ (tr & 7)) << 4);
+            uint32_t r[4];
+            ldsm_x4(addr, r[0], r[1], r[2], r[3]);
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              const int nt = x & 1, kc = 2 * kc2 + (x >> 1);
+              const uint32_t b01 = e4m3x2_to_f16x2(r[x] & 0xffffu);
+              const uint32_t b23 = e4m3x2_to_f16x2(r[x] >> 16);
+#pragma unroll
+              for (int rb = 0; rb < RB; ++rb) mma16816<false>(sacc[rb][nt], qa[rb][kc], b01, b23);
+            }
+          }
+        }
+
+        // ---- scale, mask, online softmax (exp2 domain)
+        uint32_t pa[RB][4];
+        bool any_rescale = false;
+        float corr[RB][2];
+#pragma unroll
+        for (int rb = 0; rb < RB; ++rb) {
+          float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float x = sacc[rb][nt][e] * lscale;
+              if (edge) {
+                const int hh = e >> 1;
+                const int t = ta + 8 * nt + 2 * qd + (e & 1);
+                bool vis = t < t_end && t >= row_lb[rb][hh];
+                if (a.mask && t >= spec0) vis = vis && ((row_mw[rb][hh] >> (t - spec0)) & 1u);
+                x = vis ? x : -INFINITY;
+              }
+              sacc[rb][nt][e] = x;
+              mx[e >> 1] = fmaxf(mx[e >> 1], x);
+            }
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xffffffffu, mx[hh], 1));
+            mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xffffffffu, mx[hh], 2));
+            const float m_new = fmaxf(m_run[rb][hh], mx[hh]);
+            corr[rb][hh] = (m_new == -INFINITY) ? 1.f : exp2f(m_run[rb][hh] - m_new);
+            any_rescale |= corr[rb][hh] != 1.f;
+            m_run[rb][hh] = m_new;
+          }
+          float p[2][4];
+          float rs[2] = {0.f, 0.f};
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float mm = m_run[rb][e >> 1];
+              const float v = (mm == -INFINITY) ? 0.f : exp2f(sacc[rb][nt][e] - mm);
+              p[nt][e] = v;
+              rs[e >> 1] += v;
+            }
+          l_run[rb][0] = l_run[rb][0] * corr[rb][0] + rs[0];
+          l_run[rb][1] = l_run[rb][1] * corr[rb][1] + rs[1];
+          constexpr bool kPBf16 = kMmaBf16;
+          pa[rb][0] = pack_f32x2(p[0][0], p[0][1], kPBf16);
+          pa[rb][1] = pack_f32x2(p[0][2], p[0][3], kPBf16);
+          pa[rb][2] = pack_f32x2(p[1][0], p[1][1], kPBf16);
+          pa[rb][3] = pack_f32x2(p[1][2], p[1][3], kPBf16);
+        }
+        if (__any_sync(0xffffffffu, any_rescale)) {
+#pragma unroll
+          for (int rb = 0; rb < RB; ++rb)
+#pragma unroll
+            for (int j = 0; j < kDvTiles; ++j) {
+              o[rb][j][0] *= corr[rb][0];
+              o[rb][j][1] *= corr[rb][0];
+              o[rb][j][2] *= corr[rb][1];
+              o[rb][j][3] *= corr[rb][1];
+            }
+        }
+
+        // ---- O += P V
+        if constexpr (!kF8) {
+          // V tokens held by this lane: (ta+2qd, +1) in r0/r2 and (ta+8+2qd, +1) in r1/r3
+          uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+          if (edge) {
+            const int t0 = ta + 2 * qd, t1 = ta + 8 + 2 * qd;
+            vm0 = ((t0 < t_end && t0 >= t_lo_all) ? 0x0000ffffu : 0u) |
+                  ((t0 + 1 < t_end && t0 + 1 >= t_lo_all) ? 0xffff0000u : 0u);
+            vm1 = ((t1 < t_end && t1 >= t_lo_all) ? 0x0000ffffu : 0u) |
+                  ((t1 + 1 < t_end && t1 + 1 >= t_lo_all) ? 0xffff0000u : 0u);
+          }
+          const int tr = 16 * warp + (mat & 1) * 8 + (lane & 7);
+#pragma unroll
+          for (int j2 = 0; j2 < kDvTiles / 2; ++j2) {
+            const int u = 2 * j2 + (mat >> 1);
+            const uint32_t addr = vt + (u >> 3) * (C::kTok * 128) + tr * 128 + (((u & 7) ^ (tr & 7)) << 4);
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4_t(addr, r0, r1, r2, r3);
+            r0 &= vm0;
+            r1 &= vm1;
+            r2 &= vm0;
+            r3 &= vm1;
+#pragma unroll
+            for (int rb = 0; rb < RB; ++rb) {
+              mma16816<kMmaBf16>(o[rb][2 * j2], pa[rb], r0, r1);
+              mma16816<kMmaBf16>(o[rb][2 * j2 + 1], pa[rb], r2, r3);
+            }
+          }
+        } else {
+          const int tl[4] = {16 * warp + 2 * qd, 16 * warp + 2 * qd + 1, 16 * warp + 8 + 2 * qd,
+                             16 * warp + 9 + 2 * qd};
+          bool tv[4] = {true, true, true, true};
+          if (edge) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int t = t_begin + s * C::kTok + tl[k];
+              tv[k] = t < t_end && t >= t_lo_all;
+            }
+          }
+#pragma unroll
+          for (int j4 = 0; j4 < D / 32; ++j4) {
+            const int u = 2 * j4 + (g >> 2);
+            uint32_t w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t addr = vt + tl[k] * 128 + (((u & 7) ^ (tl[k] & 7)) << 4) + 4 * (g & 3);
+              uint32_t x;
+              asm volatile("ld.shared.b32 %0, [%1];" : "=r"(x) : "r"(addr));
+              w[k] = tv[k] ? x : 0u;
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const uint32_t sel = uint32_t(c) | (uint32_t(c + 4) << 4);
+              const uint32_t b01 = e4m3x2_to_f16x2(prmt(w[0], w[1], sel) & 0xffffu);
+              const uint32_t b23 = e4m3x2_to_f16x2(prmt(w[2], w[3], sel) & 0xffffu);
+#pragma unroll
+              for (int rb = 0; rb < RB; ++rb) mma16816<false>(o[rb][4 * j4 + c], pa[rb], b01, b23);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+
+    // ---- row sums across the quad, then publish (m, l, O) of this warp
+#pragma unroll
+    for (int rb = 0; rb < RB; ++rb)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float v = l_run[rb][hh];
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        l_run[rb][hh] = v;
+      }
+    named_bar(1, 128);  // every consumer is done with the stage ring
+#pragma unroll
+    for (int rb = 0; rb < RB; ++rb) {
+#pragma unroll
+      for (int j = 0; j < kDvTiles; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int row = rb * 16 + g + 8 * (e >> 1);
+          const int n = 2 * qd + (e & 1);
+          const int dv = kF8 ? (32 * (j >> 2) + 4 * n + (j & 3)) : (8 * j + n);
+          scratch[(warp * C::kRows + row) * D + dv] = o[rb][j][e];
+        }
+      if (qd == 0) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int row = rb * 16 + g + 8 * hh;
+          sc_m[warp * C::kRows + row] = m_run[rb][hh];
+          sc_l[warp * C::kRows + row] = l_run[rb][hh];
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (flags[0]) return;  // a wait gave up: the error word says so, write nothing
+
+  // ================= epilogue (all 160 threads) =================
+  const float kv_scale = load_scale(a.kv_scale_dev, a.kv_scale);
+  const float out_mul = kv_scale * a.rcp_out_scale;
+  const bool single = nvalid <= 1;
+  const int rows_here = min(C::kRows, a.R - rg * C::kRows);
+  const int row_stride = D + 2;
+  float* ws_unit = a.ws + (int64_t(unit) * a.nsplit) * C::kRows * row_stride;
+  uint16_t* out16 = static_cast<uint16_t*>(a.out);
+  const bool obf = a.q_bf16 != 0;
+
+  for (int idx = tid; idx < rows_here * (D / 2); idx += C::kThreads) {
+    const int row = idx / (D / 2);
+    const int dv = 2 * (idx % (D / 2));
+    float mw[4], M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      mw[w] = sc_m[w * C::kRows + row];
+      M = fmaxf(M, mw[w]);
+    }
+    float o0 = 0.f, o1 = 0.f, l = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float f = (mw[w] == -INFINITY) ? 0.f : exp2f(mw[w] - M);
+      o0 += f * scratch[(w * C::kRows + row) * D + dv];
+      o1 += f * scratch[(w * C::kRows + row) * D + dv + 1];
+      l += f * sc_l[w * C::kRows + row];
+    }
+    const int r = rg * C::kRows + row;
+    const int i = r / a.G, gg = r % a.G;
+    if (single) {
+      const float sig = a.sinks ? __ldg(a.sinks + kvh * a.G + gg) * kLog2e : -INFINITY;
+      const float Mf = fmaxf(M, sig);
+      float v0 = 0.f, v1 = 0.f;
+      if (Mf != -INFINITY) {
+        const float f = (M == -INFINITY) ? 0.f : exp2f(M - Mf);
+        const float den = l * f + ((sig == -INFINITY) ? 0.f : exp2f(sig - Mf));
+        const float mul = f * out_mul / den;
+        v0 = o0 * mul;
+        v1 = o1 * mul;
+      }
+      const int64_t oi = ((int64_t(b) * a.qs + i) * a.Hq + int64_t(kvh) * a.G + gg) * a.Dv + dv;
+      *reinterpret_cast<uint32_t*>(out16 + oi) = pack_f32x2(v0, v1, obf);
+    } else {
+      float* dst = ws_unit + (int64_t(split) * C::kRows + row) * row_stride;
+      dst[dv] = o0;
+      dst[dv + 1] = o1;
+      if (dv == 0) {
+        dst[D] = M;
+        dst[D + 1] = l;
+      }
+    }
+  }
+  if (single) return;
+
+  // ---- split-KV: the last CTA of this unit to finish merges every split
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const uint32_t prev = atomicAdd(a.sems + unit, 1u);
+    flags[1] = (prev == uint32_t(nvalid - 1)) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!flags[1]) return;
+  __threadfence();
+  for (int idx = tid; idx < rows_here * (D / 2); idx += C::kThreads) {
+    const int row = idx / (D / 2);
+    const int dv = 2 * (idx % (D / 2));
+    float M = -INFINITY;
+    for (int sp = 0; sp < nvalid; ++sp)
+      M = fmaxf(M, __ldcg(ws_unit + (int64_t(sp) * C::kRows + row) * row_stride + D));
+    float o0 = 0.f, o1 = 0.f, l = 0.f;
+    for (int sp = 0; sp < nvalid; ++sp) {
+      const float* src = ws_unit + (int64_t(sp) * C::kRows + row) * row_stride;
+      const float ms = __ldcg(src + D);
+      const float f = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
+      o0 += f * __ldcg(src + dv);
+      o1 += f * __ldcg(src + dv + 1);
+      l += f * __ldcg(src + D + 1);
+    }
+    const int r = rg * C::kRows + row;
+    const int i = r / a.G, gg = r % a.G;
+    const float sig = a.sinks ? __ldg(a.sinks + kvh * a.G + gg) * kLog2e : -INFINITY;
+    const float Mf = fmaxf(M, sig);
+    float v0 = 0.f, v1 = 0.f;
+    if (Mf != -INFINITY) {
+      const float f = (M == -INFINITY) ? 0.f : exp2f(M - Mf);
+      const float den = l * f + ((sig == -INFINITY) ? 0.f : exp2f(sig - Mf));
+      const float mul = f * out_mul / den;
+      v0 = o0 * mul;
+      v1 = o1 * mul;
+    }
+    const int64_t oi = ((int64_t(b) * a.qs + i) * a.Hq + int64_t(kvh) * a.G + gg) * a.Dv + dv;
+    *reinterpret_cast<uint32_t*>(out16 + oi) = pack_f32x2(v0, v1, obf);
+  }
+  if (tid == 0) a.sems[unit] = 0u;
+}
+
+}  // namespace xqa

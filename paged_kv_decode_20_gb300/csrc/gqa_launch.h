@@ -1,0 +1,24 @@
+// Host-side entry points of the grouped-query decode kernels (one translation
+// unit per KV element type, so they compile in parallel).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "kernel_args.h"
+
+namespace xqa {
+
+// kv: 0 f16, 1 bf16, 2 e4m3.  Returns cudaErrorInvalidValue when no kernel is
+// built for (kv, head_dim, row_blocks).  With launch == false only the
+// occupancy (CTAs per SM) is reported.
+cudaError_t gqa_launch_f16(int head_dim, int row_blocks, bool launch, dim3 grid,
+                           const CUtensorMap* tk, const CUtensorMap* tv, const DecodeArgs* args,
+                           cudaStream_t stream, int* ctas_per_sm);
+cudaError_t gqa_launch_bf16(int head_dim, int row_blocks, bool launch, dim3 grid,
+                            const CUtensorMap* tk, const CUtensorMap* tv, const DecodeArgs* args,
+                            cudaStream_t stream, int* ctas_per_sm);
+cudaError_t gqa_launch_e4m3(int head_dim, int row_blocks, bool launch, dim3 grid,
+                            const CUtensorMap* tk, const CUtensorMap* tv, const DecodeArgs* args,
+                            cudaStream_t stream, int* ctas_per_sm);
+
+}  // namespace xqa

@@ -1,0 +1,24 @@
+// Shared body of the per-dtype launch functions.
+#pragma once
+#include "gqa_kernel.cuh"
+#include "gqa_launch.h"
+
+namespace xqa {
+
+template <int KV, int D, int RB>
+cudaError_t gqa_launch_one(bool launch, dim3 grid, const CUtensorMap* tk, const CUtensorMap* tv,
+                           const DecodeArgs* args, cudaStream_t stream, int* ctas_per_sm) {
+  using C = GqaCfg<KV, D, RB>;
+  auto kern = gqa_decode_kernel<KV, D, RB>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  if (ctas_per_sm) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, kern, C::kThreads, C::kSmem);
+    if (e != cudaSuccess) return e;
+  }
+  if (!launch) return cudaSuccess;
+  kern<<<grid, C::kThreads, C::kSmem, stream>>>(*tk, *tv, *args);
+  return cudaGetLastError();
+}
+
+}  // namespace xqa

@@ -1,0 +1,356 @@
+// C ABI of the paged decode attention library (declared in include/xqa.h):
+// argument validation, split-KV planning, TMA descriptor set-up and launch.
+//
+// Validation mirrors the XQA API page's stated constraints (FlashInfer
+// "flashinfer.xqa.xqa": page_size in {16, 32, 64, 128}; K/V dtype equal to
+// q's or float8_e4m3fn; page_table int32 [B, pages_per_seq]; sinks
+// [num_kv_heads, head_group_ratio]; mask [B, q_seq_len,
+// ((q_seq_len + 31) // 32) * 2]) and rejects before launching anything.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "gqa_launch.h"
+#include "kernel_args.h"
+#include "mla_launch.h"
+#include "xqa.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+xqa_status fail(xqa_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+xqa_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(XQA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// ---------------------------------------------------------------- driver entry
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// ---------------------------------------------------------------- device facts
+constexpr int kMaxDevices = 64;
+
+int device_sm_count(int dev) {
+  static int cache[kMaxDevices] = {0};
+  if (dev < 0 || dev >= kMaxDevices) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+bool is_16bit(xqa_dtype t) { return t == XQA_F16 || t == XQA_BF16; }
+int elt_bytes(xqa_dtype t) { return t == XQA_E4M3 ? 1 : 2; }
+
+// ---------------------------------------------------------------- planning
+struct Plan {
+  bool mla = false;
+  int D = 0, Dv = 0, G = 0, R = 0;
+  int row_blocks = 1, rows = 16, rg_count = 1;
+  int nsplit = 1, split_pages = 1;
+  int max_pages = 1;
+  size_t ws_bytes = 0;
+  size_t nsems = 0;
+};
+
+xqa_status validate_common(const xqa_params* p) {
+  if (!p) return fail(XQA_ERR_INVALID_ARG, "params is NULL");
+  if (!p->q || !p->k_cache || !p->v_cache || !p->page_table || !p->seq_lens || !p->output)
+    return fail(XQA_ERR_INVALID_ARG, "q, k_cache, v_cache, page_table, seq_lens and output are required");
+  if (p->batch_size < 1) return fail(XQA_ERR_INVALID_ARG, "batch_size must be >= 1, got %d", p->batch_size);
+  if (p->num_q_heads < 1 || p->num_kv_heads < 1)
+    return fail(XQA_ERR_INVALID_ARG, "num_q_heads and num_kv_heads must be >= 1");
+  if (p->num_q_heads % p->num_kv_heads)
+    return fail(XQA_ERR_INVALID_ARG, "num_q_heads (%d) must be a multiple of num_kv_heads (%d)",
+                p->num_q_heads, p->num_kv_heads);
+  if (p->page_size != 16 && p->page_size != 32 && p->page_size != 64 && p->page_size != 128)
+    return fail(XQA_ERR_INVALID_ARG, "page_size must be one of 16, 32, 64, 128; got %d", p->page_size);
+  if (p->pages_per_seq < 1) return fail(XQA_ERR_INVALID_ARG, "pages_per_seq must be >= 1");
+  if (p->num_pages < 1) return fail(XQA_ERR_INVALID_ARG, "num_pages must be >= 1");
+  if (p->q_seq_len < 1) return fail(XQA_ERR_INVALID_ARG, "q_seq_len must be >= 1");
+  if (p->q_seq_len > 32)
+    return fail(XQA_ERR_UNSUPPORTED, "q_seq_len > 32 is not supported (got %d)", p->q_seq_len);
+  if (p->sliding_win_size < 0) return fail(XQA_ERR_INVALID_ARG, "sliding_win_size must be >= 0");
+  if (!is_16bit(p->q_dtype)) return fail(XQA_ERR_INVALID_ARG, "q dtype must be float16 or bfloat16");
+  if (!(p->kv_dtype == p->q_dtype || p->kv_dtype == XQA_E4M3))
+    return fail(XQA_ERR_INVALID_ARG, "kv dtype must match q's dtype or be float8_e4m3fn");
+  if (p->out_dtype != p->q_dtype)
+    return fail(XQA_ERR_UNSUPPORTED, "output dtype must equal the query dtype (fp8 output is not built)");
+  if (p->head_dim < 1) return fail(XQA_ERR_INVALID_ARG, "head_dim must be >= 1");
+  const int64_t big = int64_t(1) << 31;
+  if (p->num_pages * std::max(p->page_size, p->num_kv_heads) >= big ||
+      int64_t(p->pages_per_seq) * p->page_size >= big)
+    return fail(XQA_ERR_UNSUPPORTED, "cache too large for 32-bit TMA coordinates");
+  if ((reinterpret_cast<uintptr_t>(p->k_cache) | reinterpret_cast<uintptr_t>(p->v_cache)) & 15)
+    return fail(XQA_ERR_INVALID_ARG, "k_cache and v_cache must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(p->q) | reinterpret_cast<uintptr_t>(p->output)) & 3)
+    return fail(XQA_ERR_INVALID_ARG, "q and output must be 4-byte aligned");
+  if (p->mask && (reinterpret_cast<uintptr_t>(p->mask) & 1))
+    return fail(XQA_ERR_INVALID_ARG, "mask must be 2-byte aligned");
+  return XQA_OK;
+}
+
+int resolve_sm_count(const xqa_params* p, int sm_count) {
+  if (sm_count > 0) return sm_count;
+  if (p && p->sm_count > 0) return p->sm_count;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  return device_sm_count(dev);
+}
+
+// Pages a CTA set may have to read for one sequence: the whole table, or
+// with a window the (window + q_seq_len - 1)-token span plus one page of
+// misalignment.
+int pages_bound(const xqa_params* p) {
+  int n = p->pages_per_seq;
+  if (p->sliding_win_size > 0) {
+    int64_t span = int64_t(p->sliding_win_size) + p->q_seq_len - 1;
+    n = int(std::min<int64_t>(n, (span + p->page_size - 1) / p->page_size + 1));
+  }
+  return n;
+}
+
+// Splits so that B * Hkv * row_groups * splits covers several waves of the
+// GPU (split count from B, the table bound and the SM count), in whole
+// 64-token stages and never below 256 tokens per split.
+void choose_splits(const xqa_params* p, Plan* pl, int sm_count, int ctas_per_sm, int stage_pages) {
+  const int64_t units = int64_t(p->batch_size) * p->num_kv_heads * pl->rg_count;
+  const int max_pages = pl->max_pages;
+  const int64_t target = int64_t(std::max(sm_count, 1)) * std::max(ctas_per_sm, 1) * 4;
+  int64_t ns = (target + units - 1) / units;
+  const int64_t by_stage = (max_pages + stage_pages - 1) / stage_pages;
+  const int64_t by_tokens = std::max<int64_t>(1, (int64_t(max_pages) * p->page_size) / 256);
+  ns = std::max<int64_t>(1, std::min(ns, std::min(by_stage, by_tokens)));
+  int sp = int((max_pages + ns - 1) / ns);
+  sp = ((sp + stage_pages - 1) / stage_pages) * stage_pages;
+  pl->split_pages = sp;
+  pl->nsplit = (max_pages + sp - 1) / sp;
+}
+
+xqa_status plan_gqa(const xqa_params* p, int sm_count_in, Plan* pl) {
+  xqa_status st = validate_common(p);
+  if (st != XQA_OK) return st;
+  const int D = p->head_dim;
+  if (p->kv_dtype == XQA_E4M3 ? D != 128 : (D != 64 && D != 128))
+    return fail(XQA_ERR_UNSUPPORTED, "head_dim %d is not built for this KV dtype (16-bit KV: 64 or 128; fp8 KV: 128)", D);
+  pl->D = pl->Dv = D;
+  pl->G = p->num_q_heads / p->num_kv_heads;
+  pl->R = p->q_seq_len * pl->G;
+  pl->row_blocks = (D == 64 && pl->R > 16) ? 2 : 1;
+  pl->rows = 16 * pl->row_blocks;
+  pl->rg_count = (pl->R + pl->rows - 1) / pl->rows;
+  pl->max_pages = pages_bound(p);
+  const int sm = resolve_sm_count(p, sm_count_in);
+  if (sm <= 0) return fail(XQA_ERR_CUDA, "cannot query the SM count of the current device");
+  int occ = 0;
+  cudaError_t e;
+  if (p->kv_dtype == XQA_E4M3)
+    e = xqa::gqa_launch_e4m3(D, pl->row_blocks, false, dim3(), nullptr, nullptr, nullptr, nullptr, &occ);
+  else if (p->kv_dtype == XQA_BF16)
+    e = xqa::gqa_launch_bf16(D, pl->row_blocks, false, dim3(), nullptr, nullptr, nullptr, nullptr, &occ);
+  else
+    e = xqa::gqa_launch_f16(D, pl->row_blocks, false, dim3(), nullptr, nullptr, nullptr, nullptr, &occ);
+  if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
+  const int stage_pages = p->page_size <= 64 ? 64 / p->page_size : 1;
+  choose_splits(p, pl, sm, occ, stage_pages);
+  const int64_t units = int64_t(p->batch_size) * p->num_kv_heads * pl->rg_count;
+  pl->nsems = size_t(units);
+  pl->ws_bytes = pl->nsplit > 1 ? size_t(units) * pl->nsplit * pl->rows * (D + 2) * sizeof(float) : 0;
+  return XQA_OK;
+}
+
+xqa_status make_maps(const xqa_params* p, int head_dim, int box_rows, CUtensorMap* tk, CUtensorMap* tv) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return fail(XQA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const int elt = elt_bytes(p->kv_dtype);
+  CUtensorMapDataType dt = p->kv_dtype == XQA_E4M3   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                           : p->kv_dtype == XQA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const uint64_t D = uint64_t(head_dim), H = uint64_t(p->num_kv_heads), ps = uint64_t(p->page_size);
+  cuuint64_t dims[3], strides[2];
+  cuuint32_t box[3], estr[3] = {1, 1, 1};
+  if (p->kv_layout == XQA_HND) {
+    dims[0] = D;
+    dims[1] = ps;
+    dims[2] = H * uint64_t(p->num_pages);
+    strides[0] = D * elt;
+    strides[1] = ps * D * elt;
+    box[0] = 128 / elt;
+    box[1] = box_rows;
+    box[2] = 1;
+  } else {
+    dims[0] = D;
+    dims[1] = H;
+    dims[2] = ps * uint64_t(p->num_pages);
+    strides[0] = D * elt;
+    strides[1] = H * D * elt;
+    box[0] = 128 / elt;
+    box[1] = 1;
+    box[2] = box_rows;
+  }
+  const void* ptrs[2] = {p->k_cache, p->v_cache};
+  CUtensorMap* maps[2] = {tk, tv};
+  for (int i = 0; i < 2; ++i) {
+    CUresult r = enc(maps[i], dt, 3, const_cast<void*>(ptrs[i]), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(XQA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+  }
+  return XQA_OK;
+}
+
+void fill_args(const xqa_params* p, const Plan& pl, void* ws, uint32_t* sems, xqa::DecodeArgs* a) {
+  memset(a, 0, sizeof *a);
+  a->q = p->q;
+  a->out = p->output;
+  a->page_table = p->page_table;
+  a->seq_lens = p->seq_lens;
+  a->sinks = p->sinks;
+  a->mask = p->mask;
+  a->q_scale_dev = p->q_scale_dev;
+  a->kv_scale_dev = p->kv_scale_dev;
+  a->ws = static_cast<float*>(ws);
+  a->sems = sems;
+  a->err = p->error_word;
+  a->num_pages = p->num_pages;
+  a->B = p->batch_size;
+  a->Hq = p->num_q_heads;
+  a->Hkv = p->num_kv_heads;
+  a->G = pl.G;
+  a->qs = p->q_seq_len;
+  a->R = pl.R;
+  a->ps = p->page_size;
+  a->pps = p->pages_per_seq;
+  a->win = p->sliding_win_size;
+  a->nsplit = pl.nsplit;
+  a->split_pages = pl.split_pages;
+  a->rg_count = pl.rg_count;
+  a->mask_words = ((p->q_seq_len + 31) / 32) * 2;
+  a->Dv = pl.Dv;
+  a->q_scale = p->q_scale;
+  a->kv_scale = p->kv_scale;
+  a->softmax_scale = p->softmax_scale != 0.f ? p->softmax_scale : 1.0f / sqrtf(float(pl.D));
+  a->rcp_out_scale = p->rcp_out_scale;
+  a->q_bf16 = p->q_dtype == XQA_BF16;
+  a->hnd = p->kv_layout == XQA_HND;
+}
+
+xqa_status check_buffers(const Plan& pl, void* ws, size_t ws_bytes, uint32_t* sems) {
+  if (pl.ws_bytes > 0) {
+    if (!ws || ws_bytes < pl.ws_bytes)
+      return fail(XQA_ERR_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes, got %zu", pl.ws_bytes,
+                  ws ? ws_bytes : size_t(0));
+    if (reinterpret_cast<uintptr_t>(ws) & 15)
+      return fail(XQA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    if (!sems) return fail(XQA_ERR_WORKSPACE_TOO_SMALL, "semaphores are required (%zu needed)", pl.nsems);
+  }
+  return XQA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* xqa_status_string(xqa_status s) {
+  switch (s) {
+    case XQA_OK: return "XQA_OK";
+    case XQA_ERR_INVALID_ARG: return "XQA_ERR_INVALID_ARG";
+    case XQA_ERR_UNSUPPORTED: return "XQA_ERR_UNSUPPORTED";
+    case XQA_ERR_WORKSPACE_TOO_SMALL: return "XQA_ERR_WORKSPACE_TOO_SMALL";
+    case XQA_ERR_CUDA: return "XQA_ERR_CUDA";
+  }
+  return "XQA_ERR_UNKNOWN";
+}
+
+const char* xqa_last_error(void) { return g_last_error; }
+
+size_t xqa_workspace_size(const xqa_params* p, int sm_count) {
+  Plan pl;
+  if (plan_gqa(p, sm_count, &pl) != XQA_OK) return size_t(-1);
+  return pl.ws_bytes;
+}
+
+size_t xqa_semaphore_count(const xqa_params* p) {
+  xqa_status st = validate_common(p);
+  if (st != XQA_OK) return size_t(-1);
+  const int G = p->num_q_heads / p->num_kv_heads;
+  const int R = p->q_seq_len * G;
+  const int rows = (p->head_dim == 64 && R > 16) ? 32 : 16;
+  return size_t(p->batch_size) * p->num_kv_heads * ((R + rows - 1) / rows);
+}
+
+xqa_status xqa_decode(const xqa_params* p, void* ws, size_t ws_bytes, uint32_t* sems,
+                      xqa_stream_t stream) {
+  g_last_error[0] = 0;
+  Plan pl;
+  xqa_status st = plan_gqa(p, 0, &pl);
+  if (st != XQA_OK) return st;
+  st = check_buffers(pl, ws, ws_bytes, sems);
+  if (st != XQA_OK) return st;
+  CUtensorMap tk, tv;
+  const int box_rows = std::min(p->page_size, 64);
+  st = make_maps(p, pl.D, box_rows, &tk, &tv);
+  if (st != XQA_OK) return st;
+  xqa::DecodeArgs a;
+  fill_args(p, pl, ws, sems, &a);
+  dim3 grid(pl.nsplit, p->num_kv_heads * pl.rg_count, p->batch_size);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (p->kv_dtype == XQA_E4M3)
+    e = xqa::gqa_launch_e4m3(pl.D, pl.row_blocks, true, grid, &tk, &tv, &a, s, nullptr);
+  else if (p->kv_dtype == XQA_BF16)
+    e = xqa::gqa_launch_bf16(pl.D, pl.row_blocks, true, grid, &tk, &tv, &a, s, nullptr);
+  else
+    e = xqa::gqa_launch_f16(pl.D, pl.row_blocks, true, grid, &tk, &tv, &a, s, nullptr);
+  if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+  return XQA_OK;
+}
+
+size_t xqa_mla_workspace_size(const xqa_params* p, int v_head_dim, int sm_count) {
+  return xqa::mla_workspace_size(p, v_head_dim, sm_count);
+}
+
+size_t xqa_mla_semaphore_count(const xqa_params* p, int v_head_dim) {
+  return xqa::mla_semaphore_count(p, v_head_dim);
+}
+
+xqa_status xqa_mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_bytes,
+                          uint32_t* sems, xqa_stream_t stream) {
+  g_last_error[0] = 0;
+  xqa_status st = validate_common(p);
+  if (st != XQA_OK) return st;
+  return xqa::mla_decode(p, v_head_dim, ws, ws_bytes, sems, reinterpret_cast<cudaStream_t>(stream),
+                         g_last_error, sizeof g_last_error);
+}
+
+}  // extern "C"

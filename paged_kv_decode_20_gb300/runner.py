@@ -1,0 +1,48 @@
+"""Buffers and launch for one decode problem, through the C ABI.
+
+``Decoder`` sizes the workspace and semaphores with the library's own queries,
+allocates them (zeroed) with torch once, and launches ``xqa_decode`` or
+``xqa_mla_decode`` on every ``run()``.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import xqa as X
+
+
+class Decoder:
+    def __init__(self, case, sm_count=None, error_word=True):
+        if not case.q.is_cuda:
+            raise ValueError("Decoder needs the problem on a CUDA device")
+        self.case = case
+        dev = case.q.device
+        B, qs, Hq, _ = case.q.shape
+        self.output = torch.empty((B, qs, Hq, case.dv), dtype=case.q.dtype, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev) if error_word else None
+        kw = case.kwargs()
+        v_head_dim = kw.pop("v_head_dim")
+        self.params = X.make_params(case.q, case.k_cache, case.v_cache, case.page_table,
+                                    case.seq_lens, self.output, q_seq_len=qs, sm_count=sm_count,
+                                    error_word=self.err, **kw)
+        self.mla = case.mla
+        self.v_head_dim = case.dv
+        if self.mla:
+            ws = X.xqa_mla_workspace_size(self.params, self.v_head_dim)
+            ns = X.xqa_mla_semaphore_count(self.params, self.v_head_dim)
+        else:
+            ws = X.xqa_workspace_size(self.params)
+            ns = X.xqa_semaphore_count(self.params)
+        self.workspace = torch.zeros(max(ws, 16), dtype=torch.uint8, device=dev)
+        self.semaphores = torch.zeros(max(ns, 1), dtype=torch.int32, device=dev)
+
+    def run(self, stream=None):
+        if self.mla:
+            X.xqa_mla_decode(self.params, self.v_head_dim, self.workspace, self.semaphores, stream)
+        else:
+            X.xqa_decode(self.params, self.workspace, self.semaphores, stream)
+        return self.output
+
+    def error_bits(self):
+        return 0 if self.err is None else int(self.err.item())

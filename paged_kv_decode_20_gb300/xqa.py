@@ -1,0 +1,293 @@
+"""ctypes binding of the C ABI in include/xqa.h (argument marshalling only).
+
+Every step of the computation runs in the CUDA library ``libxqa_gb300.so``;
+this module turns torch tensors into pointers, sizes and a stream handle, and
+raises on a non-OK status.  There is no fallback: if the library is missing
+or cannot load, the import of this module's entry points raises.
+
+``xqa`` follows the argument list of FlashInfer's ``flashinfer.xqa.xqa``
+(API page; beam_width fixed to 1) with one addition, ``softmax_scale``
+(default 1/sqrt(head_dim)); ``xqa_mla`` is the MLA latent variant (Kimi-K3
+MultiHeadLatentAttention page, ``forward_mqa``).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libxqa_gb300.so")
+
+XQA_OK, XQA_ERR_INVALID_ARG, XQA_ERR_UNSUPPORTED, XQA_ERR_WORKSPACE_TOO_SMALL, XQA_ERR_CUDA = range(5)
+XQA_F16, XQA_BF16, XQA_E4M3 = 0, 1, 2
+XQA_NHD, XQA_HND = 0, 1
+_DTYPES = {torch.float16: XQA_F16, torch.bfloat16: XQA_BF16, torch.float8_e4m3fn: XQA_E4M3}
+
+
+class XqaParams(ctypes.Structure):
+    """Mirror of ``struct xqa_params`` (field order and types as in xqa.h)."""
+
+    _fields_ = [
+        ("q", ctypes.c_void_p),
+        ("q_dtype", ctypes.c_int),
+        ("k_cache", ctypes.c_void_p),
+        ("v_cache", ctypes.c_void_p),
+        ("kv_dtype", ctypes.c_int),
+        ("kv_layout", ctypes.c_int),
+        ("num_pages", ctypes.c_int64),
+        ("page_table", ctypes.c_void_p),
+        ("pages_per_seq", ctypes.c_int32),
+        ("seq_lens", ctypes.c_void_p),
+        ("output", ctypes.c_void_p),
+        ("out_dtype", ctypes.c_int),
+        ("batch_size", ctypes.c_int32),
+        ("num_q_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("q_seq_len", ctypes.c_int32),
+        ("sinks", ctypes.c_void_p),
+        ("q_scale", ctypes.c_float),
+        ("kv_scale", ctypes.c_float),
+        ("q_scale_dev", ctypes.c_void_p),
+        ("kv_scale_dev", ctypes.c_void_p),
+        ("softmax_scale", ctypes.c_float),
+        ("sliding_win_size", ctypes.c_int32),
+        ("rcp_out_scale", ctypes.c_float),
+        ("mask", ctypes.c_void_p),
+        ("sm_count", ctypes.c_int32),
+        ("enable_pdl", ctypes.c_int32),
+        ("error_word", ctypes.c_void_p),
+    ]
+
+
+EXPORTS = ["xqa_workspace_size", "xqa_semaphore_count", "xqa_decode", "xqa_mla_workspace_size",
+           "xqa_mla_semaphore_count", "xqa_mla_decode", "xqa_status_string", "xqa_last_error"]
+
+_lock = threading.Lock()
+_lib = None
+
+
+class XqaError(RuntimeError):
+    def __init__(self, status, detail):
+        self.status = status
+        super().__init__(f"{status_name(status)}: {detail}")
+
+
+def load(path: str = LIB_PATH):
+    """Load libxqa_gb300.so (raises OSError if it is missing or broken)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise OSError(f"{path} is missing: build it with paged_kv_decode_20_gb300.build")
+            lib = ctypes.CDLL(path)
+            P = ctypes.POINTER(XqaParams)
+            lib.xqa_workspace_size.argtypes = [P, ctypes.c_int]
+            lib.xqa_workspace_size.restype = ctypes.c_size_t
+            lib.xqa_semaphore_count.argtypes = [P]
+            lib.xqa_semaphore_count.restype = ctypes.c_size_t
+            lib.xqa_decode.argtypes = [P, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                       ctypes.c_void_p]
+            lib.xqa_decode.restype = ctypes.c_int
+            lib.xqa_mla_workspace_size.argtypes = [P, ctypes.c_int, ctypes.c_int]
+            lib.xqa_mla_workspace_size.restype = ctypes.c_size_t
+            lib.xqa_mla_semaphore_count.argtypes = [P, ctypes.c_int]
+            lib.xqa_mla_semaphore_count.restype = ctypes.c_size_t
+            lib.xqa_mla_decode.argtypes = [P, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+                                           ctypes.c_void_p, ctypes.c_void_p]
+            lib.xqa_mla_decode.restype = ctypes.c_int
+            lib.xqa_status_string.argtypes = [ctypes.c_int]
+            lib.xqa_status_string.restype = ctypes.c_char_p
+            lib.xqa_last_error.argtypes = []
+            lib.xqa_last_error.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def status_name(status: int) -> str:
+    return load().xqa_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("every tensor argument must live on a CUDA device")
+    return t.data_ptr()
+
+
+def _q_view(q, q_seq_len):
+    """q as [B, q_seq_len, Hq, D]: accepts [B, Hq, D], [B, q_seq_len, Hq, D]
+    or [B, 1, q_seq_len, Hq, D] (beam width 1)."""
+    if q.dim() == 3:
+        q = q.unsqueeze(1)
+    elif q.dim() == 5:
+        if q.shape[1] != 1:
+            raise ValueError("only beam_width 1 is supported")
+        q = q[:, 0]
+    if q.dim() != 4:
+        raise ValueError(f"q must be 3-, 4- or 5-dimensional, got {tuple(q.shape)}")
+    if q.shape[1] != q_seq_len:
+        raise ValueError(f"q carries {q.shape[1]} tokens per sequence but q_seq_len={q_seq_len}")
+    return q
+
+
+def make_params(q, k_cache, v_cache, page_table, seq_lens, output, *, num_kv_heads, page_size,
+                sinks=None, q_scale=1.0, kv_scale=1.0, sliding_win_size=0, kv_layout="NHD",
+                sm_count=None, enable_pdl=None, rcp_out_scale=1.0, q_seq_len=1, mask=None,
+                softmax_scale=None, error_word=None):
+    """Build the C parameter struct; shapes are inferred as the API page
+    states (B from q, Hq from q.shape[-2], D from q.shape[-1], dtypes from q
+    and k_cache, max_seq_len = page_table.shape[-1] * page_size)."""
+    q4 = _q_view(q, q_seq_len)
+    for name, t in (("q", q4), ("k_cache", k_cache), ("v_cache", v_cache),
+                    ("page_table", page_table), ("seq_lens", seq_lens), ("output", output)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if q4.dtype not in _DTYPES or k_cache.dtype not in _DTYPES:
+        raise ValueError("unsupported dtype")
+    if page_table.dtype != torch.int32:
+        raise ValueError("page_table must be int32")
+    if seq_lens.dtype not in (torch.int32, torch.uint32):
+        raise ValueError("seq_lens must be uint32 (int32 storage accepted)")
+    if seq_lens.numel() != q4.shape[0]:
+        raise ValueError("seq_lens must hold one length per sequence (beam width 1)")
+    if sinks is not None and (sinks.dtype != torch.float32 or not sinks.is_contiguous()):
+        raise ValueError("sinks must be contiguous float32 [num_kv_heads, head_group_ratio]")
+    if sinks is not None and sinks.numel() != q4.shape[2]:
+        raise ValueError("sinks must hold num_kv_heads * head_group_ratio values")
+    if mask is not None:
+        words = ((q_seq_len + 31) // 32) * 2
+        if tuple(mask.shape) != (q4.shape[0], q_seq_len, words) or mask.element_size() != 2:
+            raise ValueError(f"mask must be 16-bit [{q4.shape[0]}, {q_seq_len}, {words}]")
+        if not mask.is_contiguous():
+            raise ValueError("mask must be contiguous")
+    p = XqaParams()
+    p.q = _ptr(q4)
+    p.q_dtype = _DTYPES[q4.dtype]
+    p.k_cache = _ptr(k_cache)
+    p.v_cache = _ptr(v_cache)
+    p.kv_dtype = _DTYPES[k_cache.dtype]
+    if v_cache.dtype != k_cache.dtype:
+        raise ValueError("k_cache and v_cache must share one dtype")
+    layout = kv_layout.upper()
+    if layout not in ("NHD", "HND"):
+        raise ValueError("kv_layout must be NHD or HND")
+    p.kv_layout = XQA_NHD if layout == "NHD" else XQA_HND
+    p.num_pages = k_cache.shape[0]
+    p.page_table = _ptr(page_table)
+    p.pages_per_seq = page_table.shape[-1]
+    p.seq_lens = _ptr(seq_lens)
+    p.output = _ptr(output)
+    p.out_dtype = _DTYPES.get(output.dtype, -1)
+    p.batch_size = q4.shape[0]
+    p.num_q_heads = q4.shape[-2]
+    p.num_kv_heads = int(num_kv_heads)
+    p.head_dim = q4.shape[-1]
+    p.page_size = int(page_size)
+    p.q_seq_len = int(q_seq_len)
+    p.sinks = _ptr(sinks)
+    if isinstance(q_scale, torch.Tensor):
+        p.q_scale, p.q_scale_dev = 1.0, _ptr(q_scale.to(torch.float32).contiguous())
+    else:
+        p.q_scale = float(q_scale)
+    if isinstance(kv_scale, torch.Tensor):
+        p.kv_scale, p.kv_scale_dev = 1.0, _ptr(kv_scale.to(torch.float32).contiguous())
+    else:
+        p.kv_scale = float(kv_scale)
+    p.softmax_scale = 0.0 if softmax_scale is None else float(softmax_scale)
+    p.sliding_win_size = int(sliding_win_size)
+    p.rcp_out_scale = float(rcp_out_scale)
+    p.mask = _ptr(mask)
+    p.sm_count = 0 if sm_count is None else int(sm_count)
+    p.enable_pdl = 1 if enable_pdl is None else int(bool(enable_pdl))
+    p.error_word = _ptr(error_word)
+    return p
+
+
+def _check(status):
+    if status != XQA_OK:
+        raise XqaError(status, load().xqa_last_error().decode())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def xqa_workspace_size(params: XqaParams, sm_count: int = 0) -> int:
+    n = load().xqa_workspace_size(ctypes.byref(params), int(sm_count))
+    if n == ctypes.c_size_t(-1).value:
+        raise XqaError(XQA_ERR_INVALID_ARG, load().xqa_last_error().decode())
+    return n
+
+
+def xqa_semaphore_count(params: XqaParams) -> int:
+    n = load().xqa_semaphore_count(ctypes.byref(params))
+    if n == ctypes.c_size_t(-1).value:
+        raise XqaError(XQA_ERR_INVALID_ARG, load().xqa_last_error().decode())
+    return n
+
+
+def xqa_mla_workspace_size(params: XqaParams, v_head_dim: int, sm_count: int = 0) -> int:
+    n = load().xqa_mla_workspace_size(ctypes.byref(params), int(v_head_dim), int(sm_count))
+    if n == ctypes.c_size_t(-1).value:
+        raise XqaError(XQA_ERR_UNSUPPORTED, load().xqa_last_error().decode())
+    return n
+
+
+def xqa_mla_semaphore_count(params: XqaParams, v_head_dim: int) -> int:
+    n = load().xqa_mla_semaphore_count(ctypes.byref(params), int(v_head_dim))
+    if n == ctypes.c_size_t(-1).value:
+        raise XqaError(XQA_ERR_UNSUPPORTED, load().xqa_last_error().decode())
+    return n
+
+
+def xqa_decode(params: XqaParams, workspace, semaphores, stream=None):
+    """Launch through the C ABI.  workspace: uint8 CUDA tensor or None."""
+    ws_ptr = None if workspace is None else _ptr(workspace)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().xqa_decode(ctypes.byref(params), ws_ptr, ws_bytes, _ptr(semaphores),
+                             _stream(stream)))
+
+
+def xqa_mla_decode(params: XqaParams, v_head_dim, workspace, semaphores, stream=None):
+    ws_ptr = None if workspace is None else _ptr(workspace)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().xqa_mla_decode(ctypes.byref(params), int(v_head_dim), ws_ptr, ws_bytes,
+                                 _ptr(semaphores), _stream(stream)))
+
+
+def xqa(q, k_cache, v_cache, page_table, seq_lens, output, workspace_buffer, semaphores,
+        num_kv_heads, page_size, sinks=None, q_scale=1.0, kv_scale=1.0, sliding_win_size=0,
+        kv_layout="NHD", sm_count=None, enable_pdl=None, rcp_out_scale=1.0, q_seq_len=1,
+        mask=None, softmax_scale=None, error_word=None, stream=None):
+    """Paged decode attention with the XQA API page's argument list; writes
+    ``output`` in place.  workspace_buffer: uint8, at least
+    ``xqa_workspace_size`` bytes; semaphores: uint32/int32, zeroed, at least
+    ``xqa_semaphore_count`` entries (left zeroed)."""
+    p = make_params(q, k_cache, v_cache, page_table, seq_lens, output, num_kv_heads=num_kv_heads,
+                    page_size=page_size, sinks=sinks, q_scale=q_scale, kv_scale=kv_scale,
+                    sliding_win_size=sliding_win_size, kv_layout=kv_layout, sm_count=sm_count,
+                    enable_pdl=enable_pdl, rcp_out_scale=rcp_out_scale, q_seq_len=q_seq_len,
+                    mask=mask, softmax_scale=softmax_scale, error_word=error_word)
+    xqa_decode(p, workspace_buffer, semaphores, stream)
+
+
+def xqa_mla(q, kv_cache, page_table, seq_lens, output, workspace_buffer, semaphores, page_size,
+            v_head_dim, softmax_scale, kv_layout="NHD", q_scale=1.0, kv_scale=1.0,
+            sm_count=None, rcp_out_scale=1.0, error_word=None, stream=None):
+    """MLA latent decode: q [B, Hq, Lr + rope] (absorbed), one latent kv head
+    ``kv_cache`` [num_pages, page_size, 1, Lr + rope]; output [B, Hq, Lr]."""
+    q_seq_len = 1 if q.dim() == 3 else q.shape[1]
+    p = make_params(q, kv_cache, kv_cache, page_table, seq_lens, output, num_kv_heads=1,
+                    page_size=page_size, q_scale=q_scale, kv_scale=kv_scale, kv_layout=kv_layout,
+                    sm_count=sm_count, rcp_out_scale=rcp_out_scale, q_seq_len=q_seq_len,
+                    softmax_scale=softmax_scale, error_word=error_word)
+    xqa_mla_decode(p, v_head_dim, workspace_buffer, semaphores, stream)

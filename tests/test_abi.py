@@ -1,0 +1,133 @@
+"""C ABI checks that need no GPU: the library loads, exports every function
+include/xqa.h declares, the ctypes struct matches the C layout, and host-side
+validation rejects malformed arguments before any CUDA call."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from paged_kv_decode_20_gb300 import build as B
+from paged_kv_decode_20_gb300 import xqa as X
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "xqa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return X.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(xqa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    assert declared_functions() == sorted(X.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", X.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (xqa_\w+)", out))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_params_struct_layout_matches_c(tmp_path):
+    fields = [f for f, _ in X.XqaParams._fields_]
+    prog = ["#include <stdio.h>", "#include <stddef.h>", '#include "xqa.h"', "int main(void){",
+            'printf("%zu\\n", sizeof(xqa_params));']
+    prog += [f'printf("%zu\\n", offsetof(xqa_params, {f}));' for f in fields]
+    prog += ["return 0;}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(prog))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I" + os.path.dirname(HEADER), str(src), "-o", str(exe)], check=True)
+    vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                           check=True).stdout.split()]
+    assert vals[0] == ctypes.sizeof(X.XqaParams)
+    for f, off in zip(fields, vals[1:]):
+        assert getattr(X.XqaParams, f).offset == off, f
+
+
+def test_status_strings(lib):
+    assert X.status_name(X.XQA_OK) == "XQA_OK"
+    assert X.status_name(X.XQA_ERR_WORKSPACE_TOO_SMALL) == "XQA_ERR_WORKSPACE_TOO_SMALL"
+    assert X.status_name(99) == "XQA_ERR_UNKNOWN"
+
+
+def fake_params(**over):
+    """A well-formed parameter block with fake (never dereferenced) pointers."""
+    p = X.XqaParams()
+    fake = 0x10000
+    p.q = p.k_cache = p.v_cache = p.page_table = p.seq_lens = p.output = fake
+    p.q_dtype = p.kv_dtype = p.out_dtype = X.XQA_BF16
+    p.kv_layout = X.XQA_NHD
+    p.num_pages = 128
+    p.pages_per_seq = 8
+    p.batch_size, p.num_q_heads, p.num_kv_heads = 4, 32, 8
+    p.head_dim, p.page_size, p.q_seq_len = 128, 64, 1
+    p.q_scale = p.kv_scale = p.rcp_out_scale = 1.0
+    for k, v in over.items():
+        setattr(p, k, v)
+    return p
+
+
+BAD = [
+    (dict(page_size=48), X.XQA_ERR_INVALID_ARG, "page_size"),
+    (dict(num_q_heads=30), X.XQA_ERR_INVALID_ARG, "multiple"),
+    (dict(batch_size=0), X.XQA_ERR_INVALID_ARG, "batch_size"),
+    (dict(q=0), X.XQA_ERR_INVALID_ARG, "required"),
+    (dict(q_seq_len=0), X.XQA_ERR_INVALID_ARG, "q_seq_len"),
+    (dict(q_seq_len=33), X.XQA_ERR_UNSUPPORTED, "q_seq_len"),
+    (dict(sliding_win_size=-1), X.XQA_ERR_INVALID_ARG, "sliding"),
+    (dict(q_dtype=X.XQA_E4M3, out_dtype=X.XQA_E4M3), X.XQA_ERR_INVALID_ARG, "q dtype"),
+    (dict(kv_dtype=X.XQA_F16), X.XQA_ERR_INVALID_ARG, "kv dtype"),
+    (dict(out_dtype=X.XQA_F16), X.XQA_ERR_UNSUPPORTED, "output dtype"),
+    (dict(head_dim=96), X.XQA_ERR_UNSUPPORTED, "head_dim"),
+    (dict(kv_dtype=X.XQA_E4M3, head_dim=64), X.XQA_ERR_UNSUPPORTED, "head_dim"),
+    (dict(k_cache=0x10008), X.XQA_ERR_INVALID_ARG, "16-byte"),
+    (dict(pages_per_seq=0), X.XQA_ERR_INVALID_ARG, "pages_per_seq"),
+    (dict(num_pages=1 << 28), X.XQA_ERR_UNSUPPORTED, "32-bit"),
+]
+
+
+@pytest.mark.parametrize("over,status,text", BAD, ids=[t for _, _, t in BAD])
+def test_validation_rejects_before_launch(lib, over, status, text):
+    p = fake_params(**over)
+    st = lib.xqa_decode(ctypes.byref(p), None, 0, None, None)
+    assert st == status
+    assert text in lib.xqa_last_error().decode()
+    assert lib.xqa_workspace_size(ctypes.byref(p), 152) == ctypes.c_size_t(-1).value
+
+
+def test_null_params_rejected(lib):
+    assert lib.xqa_decode(None, None, 0, None, None) == X.XQA_ERR_INVALID_ARG
+
+
+def test_semaphore_count_is_one_per_row_group(lib):
+    assert lib.xqa_semaphore_count(ctypes.byref(fake_params())) == 4 * 8
+    # 64 rows of D=128 per kv head -> four 16-row groups
+    p = fake_params(num_q_heads=64, q_seq_len=8)
+    assert lib.xqa_semaphore_count(ctypes.byref(p)) == 4 * 8 * 4
+    # D=64 uses 32-row groups
+    p = fake_params(head_dim=64, num_q_heads=64, q_seq_len=4)
+    assert lib.xqa_semaphore_count(ctypes.byref(p)) == 4 * 8 * 1
+
+
+def test_product_path_never_touches_the_oracle():
+    pkg = os.path.join(ROOT, "paged_kv_decode_20_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+                assert "xqa_oracle" not in text, f
