@@ -182,6 +182,7 @@ def run_gb300(args):
         dist.barrier()
     torch.cuda.synchronize(dev)
     with Clocks(local) as clk:
+        torch.cuda.nvtx.range_push("timed")
         t0.record(stream)
         for s in range(args.steps):
             ev[s][0].record(stream)
@@ -189,6 +190,7 @@ def run_gb300(args):
             ev[s][1].record(stream)
         t1.record(stream)
         torch.cuda.synchronize(dev)
+        torch.cuda.nvtx.range_pop()
     if world > 1:
         dist.barrier()
     total_ms = t0.elapsed_time(t1)

@@ -168,6 +168,7 @@ def make_params(q, k_cache, v_cache, page_table, seq_lens, output, *, num_kv_hea
         if not mask.is_contiguous():
             raise ValueError("mask must be contiguous")
     p = XqaParams()
+    keep = [q4, k_cache, v_cache, page_table, seq_lens, output, sinks, mask, error_word]
     p.q = _ptr(q4)
     p.q_dtype = _DTYPES[q4.dtype]
     p.k_cache = _ptr(k_cache)
@@ -193,11 +194,15 @@ def make_params(q, k_cache, v_cache, page_table, seq_lens, output, *, num_kv_hea
     p.q_seq_len = int(q_seq_len)
     p.sinks = _ptr(sinks)
     if isinstance(q_scale, torch.Tensor):
-        p.q_scale, p.q_scale_dev = 1.0, _ptr(q_scale.to(torch.float32).contiguous())
+        qs_t = q_scale.to(torch.float32).contiguous()
+        keep.append(qs_t)
+        p.q_scale, p.q_scale_dev = 1.0, _ptr(qs_t)
     else:
         p.q_scale = float(q_scale)
     if isinstance(kv_scale, torch.Tensor):
-        p.kv_scale, p.kv_scale_dev = 1.0, _ptr(kv_scale.to(torch.float32).contiguous())
+        kvs_t = kv_scale.to(torch.float32).contiguous()
+        keep.append(kvs_t)
+        p.kv_scale, p.kv_scale_dev = 1.0, _ptr(kvs_t)
     else:
         p.kv_scale = float(kv_scale)
     p.softmax_scale = 0.0 if softmax_scale is None else float(softmax_scale)
@@ -207,6 +212,8 @@ def make_params(q, k_cache, v_cache, page_table, seq_lens, output, *, num_kv_hea
     p.sm_count = 0 if sm_count is None else int(sm_count)
     p.enable_pdl = 1 if enable_pdl is None else int(bool(enable_pdl))
     p.error_word = _ptr(error_word)
+    # the struct holds raw pointers: keep every tensor it names alive with it
+    p._keep = keep
     return p
 
 
