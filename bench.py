@@ -67,12 +67,20 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash():
+KERNEL_FILES = {
+    "gqa_decode_kernel": ("gqa_", "ptx.cuh", "kernel_args.h"),
+    "mla_decode_kernel": ("mla_", "umma.cuh", "ptx.cuh", "kernel_args.h"),
+}
+
+
+def kernel_source_hash(kernel):
+    """Hash of the source files that make up one kernel."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_decode_20_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        h.update(f.encode())
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        if f.startswith(KERNEL_FILES[kernel]):
+            h.update(f.encode())
+            h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -84,7 +92,8 @@ def recorded_traffic(workload):
         d = json.load(open(path))[str(workload)]
     except Exception:
         return None
-    return d["dram_bytes_per_launch"] if d.get("kernel_hash") == kernel_source_hash() else None
+    same = d.get("kernel_hash") == kernel_source_hash(KERNEL_NAMES[workload])
+    return d["dram_bytes_per_launch"] if same else None
 
 
 class Clocks:
