@@ -42,9 +42,11 @@ KERNEL_NAMES = {1: "gqa_decode_kernel", 2: "gqa_decode_kernel", 3: "gqa_decode_k
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--batch", type=int, default=None,
+                    help="keep only the first B sequences (profiling a smaller case)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -111,7 +113,7 @@ class Clocks:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -150,9 +152,8 @@ class Clocks:
                 "samples": len(sm)}
 
 
-def build_case(idx, device, rank):
-    case = W.workload(idx, device=device, poison=False)
-    return case
+def build_case(idx, device, batch=None):
+    return W.workload(idx, device=device, poison=False, batch=batch)
 
 
 def run_gb300(args):
@@ -173,7 +174,7 @@ def run_gb300(args):
         dist.barrier()
     X.load()
 
-    case = build_case(args.workload, dev, rank)
+    case = build_case(args.workload, dev, args.batch)
     dec = Decoder(case, error_word=False)
     stream = torch.cuda.current_stream(dev)
     kv_bytes = case.kv_bytes()
@@ -302,7 +303,7 @@ def run_gb300(args):
         dist.destroy_process_group()
 
 
-def cpu_baseline(case, idx, max_rows=None):
+def cpu_baseline(case, idx, max_rows=None, min_seconds=10.0):
     """Time the float64 oracle on all rows of the workload (or a bounded
     sample of whole (b, kv head) units) with every host thread."""
     import oracle
@@ -335,10 +336,16 @@ def cpu_baseline(case, idx, max_rows=None):
     else:
         sample = f"all {rows} output rows of the workload, once"
     kw = case.kwargs()
+    reps = 0
     t = time.perf_counter()
-    oracle.xqa_attention(case.q, case.k_cache, case.v_cache, case.page_table, case.seq_lens,
-                         units=units, threads=threads, **kw)
-    dt = time.perf_counter() - t
+    while True:
+        oracle.xqa_attention(case.q, case.k_cache, case.v_cache, case.page_table, case.seq_lens,
+                             units=units, threads=threads, **kw)
+        reps += 1
+        if time.perf_counter() - t >= min_seconds or reps >= 500:
+            break
+    dt = (time.perf_counter() - t) / reps
+    sample += f" (mean of {reps} repetitions)"
     kv = case.kv_bytes() * frac
     return {"value": round(kv / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": sample, "seconds": round(dt, 3)}
@@ -350,16 +357,16 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    case = W.workload(args.workload, device="cpu", poison=False)
+    case = W.workload(args.workload, device="cpu", poison=False, batch=args.batch)
     B = case.batch
     # each step: a few whole (sequence, kv head) units
     rows_per_step = {1: 16, 2: 32, 3: 8, 4: 64, 5: 128}[args.workload]
     for _ in range(args.warmup):
-        cpu_baseline(case, args.workload, max_rows=rows_per_step)
+        cpu_baseline(case, args.workload, max_rows=rows_per_step, min_seconds=0.0)
     times, vals = [], []
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        r = cpu_baseline(case, args.workload, max_rows=rows_per_step)
+        r = cpu_baseline(case, args.workload, max_rows=rows_per_step, min_seconds=0.0)
         times.append(r["seconds"])
         vals.append(r["value"])
     total = time.perf_counter() - t0

@@ -1,18 +1,760 @@
-// MLA latent decode (vLLM Kimi-K3 MultiHeadLatentAttention page: forward_mqa
-// on the absorbed query; head_size = kv_lora_rank + qk_rope_head_dim).
+// MLA latent decode on the 5th-generation tensor cores (vLLM Kimi-K3
+// MultiHeadLatentAttention page: the absorbed query [ql_nope | q_pe] of width
+// kv_lora_rank + qk_rope_head_dim = 512 + 64 attends to one latent kv head of
+// the same width through forward_mqa; V is the first kv_lora_rank = 512
+// elements of each latent row; scale = qk_head_dim^-0.5 arrives as
+// softmax_scale).
+//
+// The 128 query rows (heads x speculative tokens) form one M = 128 UMMA tile.
+// Their fp32 output (128 x 512) alone fills a CTA's 512 tensor-memory
+// columns, so a cluster of two CTAs shares each (sequence, KV split):
+//
+//   CTA c = 0 owns latent dims [0, 256) plus the rope dims [512, 576);
+//   CTA c = 1 owns latent dims [256, 512).
+//   Each CTA streams only its dims of every latent row (TMA, 128-byte
+//   swizzle, multi-stage mbarrier ring), computes the partial logits
+//   S_c = Q_c K_c^T (tcgen05.mma, A = its latent query half held in tensor
+//   memory, B = K from shared memory; CTA 0 adds the rope part with A from
+//   shared memory), and sends S_c to its peer through distributed shared
+//   memory (st.async completing on the peer's mbarrier).  Both CTAs then hold
+//   the same S = S_0 + S_1 and run the same online softmax (128 threads, one
+//   row each), so their running maxima agree without further traffic.
+//   P (bf16) goes to shared memory and CTA c accumulates O_c += P V_c into
+//   its 256 tensor-memory columns, where V_c = latent dims [256c, 256c+256)
+//   are exactly the first four chunks of the K tile it already holds.
+//   Every latent byte is read from HBM once.
+//
+// Warp roles: 0 = TMA producer, 1 = MMA issuer, 2 = tensor-memory allocator,
+// 4..7 = softmax / exchange / epilogue (warp 4 + k reaches TMEM lanes 32k..).
+// Split-KV partials merge exactly as in the grouped-query kernel: the last
+// CTA of each column half to take a ticket merges every split.
+#include <cuda.h>
+#include <cuda_runtime.h>
 #include <stdio.h>
+#include <string.h>
 
+#include <algorithm>
+#include <mutex>
+
+#include "kernel_args.h"
 #include "mla_launch.h"
+#include "ptx.cuh"
+#include "umma.cuh"
 
 namespace xqa {
+namespace mla {
 
-size_t mla_workspace_size(const xqa_params*, int, int) { return size_t(-1); }
-size_t mla_semaphore_count(const xqa_params*, int) { return size_t(-1); }
+constexpr int kRows = 128;       // UMMA M: query rows (heads x spec tokens)
+constexpr int kLatent = 512;     // kv_lora_rank (= V width)
+constexpr int kRope = 64;        // qk_rope_head_dim
+constexpr int kDim = kLatent + kRope;
+constexpr int kHalf = kLatent / 2;  // V columns per CTA
+constexpr int kTok = 64;         // tokens per tile (UMMA N of QK, K of PV)
+constexpr int kChunkBytes = kTok * 128;  // one 64-element column chunk of a tile
+constexpr int kMaxChunks = 5;    // CTA 0: 4 latent + 1 rope chunk
+constexpr int kStageBytes = kMaxChunks * kChunkBytes;  // 40 KB
+constexpr int kStages = 4;
+constexpr int kThreads = 256;
 
-xqa_status mla_decode(const xqa_params*, int, void*, size_t, uint32_t*, cudaStream_t, char* err,
-                      size_t err_len) {
-  snprintf(err, err_len, "the MLA latent kernel is not built yet");
-  return XQA_ERR_UNSUPPORTED;
+// shared memory map (offsets from a 1024-aligned base)
+constexpr int kOffStages = 0;
+constexpr int kOffQRope = kOffStages + kStages * kStageBytes;  // 128 x 64 bf16
+constexpr int kOffP = kOffQRope + kRows * 128;                  // 128 x 64 bf16
+constexpr int kOffX = kOffP + kRows * 128;                      // 128 x 64 fp32 (peer partial)
+constexpr int kOffBar = kOffX + kRows * kTok * 4;
+constexpr int kNumBars = 2 * kStages + 9;
+constexpr int kSmem = 1024 + kOffBar + kNumBars * 8 + 32;
+
+// tensor memory columns
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 0;     // 256 fp32 columns: O half
+constexpr uint32_t kColQ = 256;   // 128 columns: latent query half, bf16 pairs
+constexpr uint32_t kColS = 384;   // 2 x 64 columns: logits double buffer
+
+constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by > 2^8
+
+struct MlaArgs {
+  const uint16_t* q;  // [B, qs, Hq, 576]
+  uint16_t* out;      // [B, qs, Hq, 512]
+  const int32_t* page_table;
+  const uint32_t* seq_lens;
+  const float* sinks;
+  const uint16_t* mask;
+  const float* q_scale_dev;
+  const float* kv_scale_dev;
+  float* ws;
+  uint32_t* sems;
+  uint32_t* err;
+  int64_t num_pages;
+  int B, Hq, qs, ps, pps, win, nsplit, split_pages, mask_words;
+  float q_scale, kv_scale, softmax_scale, rcp_out_scale;
+  int q_bf16;
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t map_peer(uint32_t saddr, uint32_t peer) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(peer));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+__device__ __forceinline__ void st_async_v4(uint32_t raddr, float a, float b, float c, float d,
+                                            uint32_t rbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1,%2,%3,%4}, [%5];" ::"r"(raddr),
+      "f"(a), "f"(b), "f"(c), "f"(d), "r"(rbar)
+      : "memory");
+}
+__device__ __forceinline__ void remote_arrive(uint32_t rbar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar) : "memory");
+}
+__device__ __forceinline__ bool wait_cluster(uint64_t* bar, uint32_t parity) {
+  auto try_once = [&]() {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+  };
+  if (try_once()) return true;
+  long long t0 = clock64();
+  while (!try_once()) {
+    if (clock64() - t0 > kWaitCycles) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ float ldscale(const float* dev, float host) { return dev ? __ldg(dev) : host; }
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    mla_decode_kernel(const __grid_constant__ CUtensorMap tmKV, const MlaArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* kv_full = bars;                 // [kStages]
+  uint64_t* kv_empty = bars + kStages;      // [kStages]
+  uint64_t* q_ready = bars + 2 * kStages;   // softmax warps stored the query
+  uint64_t* s_full = q_ready + 1;           // [2]
+  uint64_t* s_free = s_full + 2;            // [2]
+  uint64_t* p_full = s_free + 2;
+  uint64_t* pv_done = p_full + 1;
+  uint64_t* x_full = pv_done + 1;           // the peer's partial landed in my buffer
+  uint64_t* x_free = x_full + 1;            // the peer has read my previous partial
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  int* flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] abort, [1] last CTA
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t c = cluster_rank();
+  const uint32_t peer = c ^ 1u;
+  const int split = blockIdx.x >> 1;
+  const int b = blockIdx.z;
+
+  // ---- sequence geometry (identical in both CTAs and every split)
+  const int64_t max_len = int64_t(a.pps) * a.ps;
+  const int64_t len_raw = a.seq_lens[b];
+  const int L = int(len_raw < max_len ? len_raw : max_len);
+  if (len_raw > max_len && a.err && tid == 0 && blockIdx.x == 0) atomicOr(a.err, kErrClamped);
+  const int spec0 = L - a.qs;
+  const int t_lo_all = a.win > 0 ? max(0, spec0 - a.win + 1) : 0;
+  const int pg_first = t_lo_all / a.ps;
+  const int pg_last = (L + a.ps - 1) / a.ps;
+  const int npages = max(0, pg_last - pg_first);
+  const int nvalid = (npages + a.split_pages - 1) / a.split_pages;
+  if (split >= max(nvalid, 1)) return;  // both CTAs of the cluster leave together
+  const int pg_lo = pg_first + split * a.split_pages;
+  const int pg_hi = min(pg_lo + a.split_pages, pg_last);
+  const int t_begin = pg_lo * a.ps;
+  const int t_end = min(pg_hi * a.ps, L);
+  const int ntiles = (nvalid == 0 || t_end <= t_begin) ? 0 : (t_end - t_begin + kTok - 1) / kTok;
+  const int nchunks = c == 0 ? 5 : 4;
+
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    mbar_init(q_ready, 4);
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
+    mbar_init(&s_free[0], 4);
+    mbar_init(&s_free[1], 4);
+    mbar_init(p_full, 4);
+    mbar_init(pv_done, 1);
+    mbar_init(x_full, 1);
+    mbar_init(x_free, 4);
+    flags[0] = flags[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    umma::tmem_alloc(tmem_slot, kTmemCols);
+    umma::tmem_relinquish();
+  }
+  umma::fence_before_sync();
+  __syncthreads();
+  cluster_sync();  // the peer's barriers exist before any remote access
+  umma::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  const uint32_t stage0 = smem_u32(smem + kOffStages);
+  const uint32_t qrope = smem_u32(smem + kOffQRope);
+  const uint32_t pbuf = smem_u32(smem + kOffP);
+  float* xbuf = reinterpret_cast<float*>(smem + kOffX);
+
+  if (warp == 0) {
+    // ================= TMA producer =================
+    if (lane == 0 && ntiles > 0) {
+      prefetch_tensormap(&tmKV);
+      const int32_t* pt = a.page_table + int64_t(b) * a.pps;
+      const int box_rows = min(a.ps, kTok);
+      const uint32_t box_bytes = uint32_t(box_rows) * 128u;
+      bool bad_page = false;
+      int s = 0;
+      for (; s < ntiles; ++s) {
+        const int slot = s % kStages;
+        if (s >= kStages && !mbar_wait(&kv_empty[slot], ((s / kStages) & 1) ^ 1)) {
+          flags[0] = 1;
+          break;
+        }
+        const int tok0 = t_begin + s * kTok;
+        const int n_piece = a.ps <= kTok ? min(kTok / a.ps, pg_hi - tok0 / a.ps) : 1;
+        mbar_arrive_expect_tx(&kv_full[slot], uint32_t(n_piece) * box_bytes * nchunks);
+        uint8_t* dst = smem + kOffStages + slot * kStageBytes;
+        for (int j = 0; j < n_piece; ++j) {
+          const int lp = a.ps <= kTok ? tok0 / a.ps + j : tok0 / a.ps;
+          const int sub = a.ps <= kTok ? 0 : tok0 % a.ps;
+          int page = __ldg(pt + lp);
+          if (page < 0 || int64_t(page) >= a.num_pages) {
+            bad_page = true;
+            page = -1;
+          }
+          const int row_off = j * box_rows;
+          for (int k = 0; k < nchunks; ++k) {
+            // chunk slot k: latent dims 256c + 64k (k < 4) or the rope dims
+            const int x = k < 4 ? int(c) * kHalf + 64 * k : kLatent;
+            tma_load_3d(dst + k * kChunkBytes + row_off * 128, &tmKV, &kv_full[slot], x, 0,
+                        page * a.ps + sub);
+          }
+        }
+      }
+      if (bad_page && a.err) atomicOr(a.err, kErrClamped);
+      for (int t = max(0, s - kStages); t < s; ++t)
+        if (!mbar_wait(&kv_full[t % kStages], (t / kStages) & 1)) flags[0] = 1;
+    }
+  } else if (warp == 1) {
+    // ================= MMA issuer =================
+    if (lane == 0 && ntiles > 0) {
+      constexpr uint32_t kIdescQK = umma::idesc_f16(kRows, kTok, true, false, false);
+      constexpr uint32_t kIdescPV = umma::idesc_f16(kRows, kHalf, true, false, true);
+      bool ok = mbar_wait(q_ready, 0);
+      umma::fence_after_sync();
+      auto issue_qk = [&](int j) {
+        const int slot = j % kStages;
+        const uint32_t st = stage0 + slot * kStageBytes;
+        const uint32_t sd = tmem + kColS + 64u * uint32_t(j & 1);
+        for (int k = 0; k < 4; ++k)
+          for (int kk = 0; kk < 4; ++kk)
+            umma::mma_ts(sd, tmem + kColQ + 32u * k + 8u * kk,
+                         umma::smem_desc(st + k * kChunkBytes + 32 * kk, 16, 1024, umma::kSw128),
+                         kIdescQK, (k | kk) != 0);
+        if (c == 0)
+          for (int kk = 0; kk < 4; ++kk)
+            umma::mma_ss(sd, umma::smem_desc(qrope + 32 * kk, 16, 1024, umma::kSw128),
+                         umma::smem_desc(st + 4 * kChunkBytes + 32 * kk, 16, 1024, umma::kSw128),
+                         kIdescQK, 1u);
+        umma::commit(&s_full[j & 1]);
+      };
+      if (ok && mbar_wait(&kv_full[0], 0)) {
+        umma::fence_after_sync();
+        issue_qk(0);
+      } else {
+        ok = false;
+      }
+      for (int j = 0; ok && j < ntiles; ++j) {
+        const int jn = j + 1;
+        if (jn < ntiles) {
+          if (!mbar_wait(&kv_full[jn % kStages], (jn / kStages) & 1) ||
+              (jn >= 2 && !mbar_wait(&s_free[jn & 1], ((jn >> 1) - 1) & 1))) {
+            ok = false;
+            break;
+          }
+          umma::fence_after_sync();
+          issue_qk(jn);
+        }
+        if (!mbar_wait(p_full, j & 1)) {
+          ok = false;
+          break;
+        }
+        umma::fence_after_sync();
+        const uint32_t st = stage0 + (j % kStages) * kStageBytes;
+        for (int kk = 0; kk < 4; ++kk)
+          umma::mma_ss(tmem + kColO, umma::smem_desc(pbuf + 32 * kk, 16, 1024, umma::kSw128),
+                       umma::smem_desc(st + 2048 * kk, kChunkBytes, 1024, umma::kSw128), kIdescPV,
+                       (j | kk) != 0);
+        umma::commit(&kv_empty[j % kStages]);
+        umma::commit(pv_done);
+      }
+      if (!ok) flags[0] = 1;
+    }
+  } else if (warp >= 4) {
+    // ================= softmax / exchange / epilogue =================
+    const int t = tid - 128;  // row = TMEM lane
+    const uint32_t lane_base = uint32_t(32 * (warp - 4)) << 16;
+    const int i = t / a.Hq, h = t % a.Hq;  // row t = (spec token i, head h)
+    const float q_scale = ldscale(a.q_scale_dev, a.q_scale);
+    const float kv_scale = ldscale(a.kv_scale_dev, a.kv_scale);
+    const float lscale = a.softmax_scale * q_scale * kv_scale * kLog2e;
+    const bool qbf = a.q_bf16 != 0;
+
+    // ---- query: latent half into tensor memory, rope into shared memory (CTA 0)
+    {
+      const uint16_t* qrow = a.q + (int64_t(b) * a.qs * a.Hq + t) * kDim;
+      const uint4* src = reinterpret_cast<const uint4*>(qrow + c * kHalf);
+      for (int part = 0; part < 4; ++part) {  // 4 x 32 columns = 256 bf16
+        uint32_t w[32];
+        for (int v = 0; v < 8; ++v) {
+          const uint4 x = __ldg(src + part * 8 + v);
+          w[4 * v + 0] = x.x;
+          w[4 * v + 1] = x.y;
+          w[4 * v + 2] = x.z;
+          w[4 * v + 3] = x.w;
+        }
+        umma::tmem_st32(tmem + lane_base + kColQ + 32u * part, w);
+      }
+      if (c == 0) {
+        const uint4* rsrc = reinterpret_cast<const uint4*>(qrow + kLatent);
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(smem + kOffQRope + umma::sw128(t, u)) = __ldg(rsrc + u);
+      }
+      umma::tmem_st_wait();
+      umma::fence_proxy_async_smem();
+      umma::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_ready);
+    }
+    (void)qbf;
+
+    // per-row visibility
+    const int row_lb = a.win > 0 ? spec0 + i - a.win + 1 : INT_MIN;
+    uint32_t row_mw = 0xffffffffu;
+    if (a.mask) {
+      const uint16_t* mrow = a.mask + (int64_t(b) * a.qs + i) * a.mask_words;
+      row_mw = uint32_t(__ldg(mrow)) | (uint32_t(__ldg(mrow + 1)) << 16);
+    }
+
+    const uint32_t x_full_peer = map_peer(smem_u32(x_full), peer);
+    const uint32_t x_free_peer = map_peer(smem_u32(x_free), peer);
+    const uint32_t xrow_peer = map_peer(smem_u32(xbuf + t * kTok), peer);
+    float m_ref = -INFINITY, l_run = 0.f;
+    bool ok = true;
+
+    for (int j = 0; j < ntiles; ++j) {
+      const int sb = j & 1;
+      float s[kTok];
+      if (!mbar_wait(&s_full[sb], (j >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      umma::fence_after_sync();
+      umma::tmem_ld32(tmem + lane_base + kColS + 64u * sb, s);
+      umma::tmem_ld32(tmem + lane_base + kColS + 64u * sb + 32u, s + 32);
+      umma::tmem_ld_wait();
+      umma::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[sb]);
+
+      // ---- exchange partial logits with the peer
+      if (j > 0 && !wait_cluster(x_free, (j - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      for (int v = 0; v < kTok / 4; ++v) {
+        // 16-byte unit v of the row, XOR-swizzled by row to spread banks
+        const uint32_t off = uint32_t(((v ^ (t & 15)) & 15) * 16);
+        st_async_v4(xrow_peer + off, s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3], x_full_peer);
+      }
+      if (t == 0) mbar_arrive_expect_tx(x_full, uint32_t(kRows * kTok * 4));
+      if (!wait_cluster(x_full, j & 1)) {
+        ok = false;
+        break;
+      }
+      {
+        const float* xr = xbuf + t * kTok;
+        for (int v = 0; v < kTok / 4; ++v) {
+          const float4 p4 = *reinterpret_cast<const float4*>(xr + (((v ^ (t & 15)) & 15) * 4));
+          s[4 * v] += p4.x;
+          s[4 * v + 1] += p4.y;
+          s[4 * v + 2] += p4.z;
+          s[4 * v + 3] += p4.w;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) remote_arrive(x_free_peer);
+
+      // ---- scale, mask, online softmax (log2 domain, lazy rescale)
+      const int tile0 = t_begin + j * kTok;
+      const bool edge = tile0 + kTok > t_end || tile0 <= row_lb || (a.mask && tile0 + kTok > spec0);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < kTok; ++k) {
+        float x = s[k] * lscale;
+        if (edge) {
+          const int tt = tile0 + k;
+          bool vis = tt < t_end && tt >= row_lb;
+          if (a.mask && tt >= spec0) vis = vis && ((row_mw >> (tt - spec0)) & 1u);
+          x = vis ? x : -INFINITY;
+        }
+        s[k] = x;
+        mx = fmaxf(mx, x);
+      }
+      // P and O may be touched only once the previous P.V is done
+      if (j > 0 && !mbar_wait(pv_done, (j - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      umma::fence_after_sync();
+      const float m_new = fmaxf(m_ref, mx);
+      if (m_new > m_ref + kRescaleLog2 || (m_ref == -INFINITY && m_new != -INFINITY)) {
+        if (m_ref != -INFINITY) {
+          const float f = exp2f(m_ref - m_new);
+          l_run *= f;
+          for (int part = 0; part < kHalf / 32; ++part) {
+            float o[32];
+            umma::tmem_ld32(tmem + lane_base + kColO + 32u * part, o);
+            umma::tmem_ld_wait();
+            uint32_t w[32];
+            for (int k = 0; k < 32; ++k) w[k] = __float_as_uint(o[k] * f);
+            umma::tmem_st32(tmem + lane_base + kColO + 32u * part, w);
+          }
+          umma::tmem_st_wait();
+        }
+        m_ref = m_new;
+      }
+      // P row t (bf16) into the swizzled K-major P tile
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        uint32_t w4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float p0 = m_ref == -INFINITY ? 0.f : exp2f(s[8 * u + 2 * e] - m_ref);
+          const float p1 = m_ref == -INFINITY ? 0.f : exp2f(s[8 * u + 2 * e + 1] - m_ref);
+          l_run += p0 + p1;
+          w4[e] = pack_f32x2(p0, p1, true);
+        }
+        *reinterpret_cast<uint4*>(smem + kOffP + umma::sw128(t, u)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      }
+      // V rows past this split's last token hold stale or foreign data: zero them
+      if (tile0 + kTok > t_end) {
+        const int r0 = max(0, t_end - tile0);
+        uint8_t* st = smem + kOffStages + (j % kStages) * kStageBytes;
+        for (int idx = t; idx < (kTok - r0) * 4 * 8; idx += kRows) {
+          const int r = r0 + idx / 32, k = (idx / 8) % 4, u = idx % 8;
+          *reinterpret_cast<uint4*>(st + k * kChunkBytes + r * 128 + u * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      umma::fence_proxy_async_smem();
+      umma::fence_before_sync();
+      named_bar(1, kRows);  // every softmax thread finished P (and the V tail)
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    if (!ok) flags[0] = 1;
+
+    // ---- epilogue: wait for the last P.V, then finalise or write the partial
+    bool have_o = ntiles > 0;
+    if (have_o && ok && !mbar_wait(pv_done, (ntiles - 1) & 1)) {
+      flags[0] = 1;
+      ok = false;
+    }
+    umma::fence_after_sync();
+    if (ok) {
+      const bool single = nvalid <= 1;
+      float mul = 0.f;
+      if (single) {
+        const float sig = a.sinks ? __ldg(a.sinks + h) * kLog2e : -INFINITY;
+        const float Mf = fmaxf(m_ref, sig);
+        if (Mf != -INFINITY) {
+          const float f = m_ref == -INFINITY ? 0.f : exp2f(m_ref - Mf);
+          const float den = l_run * f + (sig == -INFINITY ? 0.f : exp2f(sig - Mf));
+          mul = f * kv_scale * a.rcp_out_scale / den;
+        }
+      }
+      const int64_t row_g = (int64_t(b) * a.qs + i) * a.Hq + h;
+      float* wrow = a.ws + ((int64_t(b) * a.nsplit + split) * kRows + t) * (kLatent + 4);
+      for (int part = 0; part < kHalf / 32; ++part) {
+        float o[32];
+        if (have_o) {
+          umma::tmem_ld32(tmem + lane_base + kColO + 32u * part, o);
+          umma::tmem_ld_wait();
+        } else {
+          for (int k = 0; k < 32; ++k) o[k] = 0.f;
+        }
+        const int col = int(c) * kHalf + 32 * part;
+        if (single) {
+          uint4* dst = reinterpret_cast<uint4*>(a.out + row_g * kLatent + col);
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(pack_f32x2(o[8 * v] * mul, o[8 * v + 1] * mul, true),
+                                pack_f32x2(o[8 * v + 2] * mul, o[8 * v + 3] * mul, true),
+                                pack_f32x2(o[8 * v + 4] * mul, o[8 * v + 5] * mul, true),
+                                pack_f32x2(o[8 * v + 6] * mul, o[8 * v + 7] * mul, true));
+        } else {
+          float4* dst = reinterpret_cast<float4*>(wrow + col);
+          for (int v = 0; v < 8; ++v) dst[v] = make_float4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+        }
+      }
+      if (!single) {
+        wrow[kLatent + 2 * c] = m_ref;
+        wrow[kLatent + 2 * c + 1] = l_run;
+      }
+    }
+  }
+
+  // ---- teardown: no tensor-memory or peer traffic may outlive this point
+  umma::fence_before_sync();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 2) {
+    umma::fence_after_sync();
+    umma::tmem_dealloc(tmem, kTmemCols);
+  }
+  if (flags[0]) {
+    if (tid == 0 && a.err) atomicOr(a.err, kErrTimeout);
+    return;
+  }
+  if (nvalid <= 1) return;
+
+  // ---- split-KV: the last CTA of this column half merges every split
+  __threadfence();
+  __syncthreads();
+  const int unit = b * 2 + int(c);
+  if (tid == 0) {
+    const uint32_t prev = atomicAdd(a.sems + unit, 1u);
+    flags[1] = prev == uint32_t(nvalid - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!flags[1]) return;
+  __threadfence();
+  const float kv_scale = ldscale(a.kv_scale_dev, a.kv_scale);
+  const int64_t ws_b = int64_t(b) * a.nsplit * kRows * (kLatent + 4);
+  for (int idx = tid; idx < kRows * (kHalf / 2); idx += kThreads) {
+    const int row = idx / (kHalf / 2);
+    const int col = int(c) * kHalf + 2 * (idx % (kHalf / 2));
+    float M = -INFINITY;
+    for (int sp = 0; sp < nvalid; ++sp)
+      M = fmaxf(M, __ldcg(a.ws + ws_b + (int64_t(sp) * kRows + row) * (kLatent + 4) + kLatent + 2 * c));
+    float o0 = 0.f, o1 = 0.f, l = 0.f;
+    for (int sp = 0; sp < nvalid; ++sp) {
+      const float* src = a.ws + ws_b + (int64_t(sp) * kRows + row) * (kLatent + 4);
+      const float ms = __ldcg(src + kLatent + 2 * c);
+      const float f = ms == -INFINITY ? 0.f : exp2f(ms - M);
+      o0 += f * __ldcg(src + col);
+      o1 += f * __ldcg(src + col + 1);
+      l += f * __ldcg(src + kLatent + 2 * c + 1);
+    }
+    const int ii = row / a.Hq, hh = row % a.Hq;
+    const float sig = a.sinks ? __ldg(a.sinks + hh) * kLog2e : -INFINITY;
+    const float Mf = fmaxf(M, sig);
+    float v0 = 0.f, v1 = 0.f;
+    if (Mf != -INFINITY) {
+      const float f = M == -INFINITY ? 0.f : exp2f(M - Mf);
+      const float den = l * f + (sig == -INFINITY ? 0.f : exp2f(sig - Mf));
+      const float mul = f * kv_scale * a.rcp_out_scale / den;
+      v0 = o0 * mul;
+      v1 = o1 * mul;
+    }
+    const int64_t oi = ((int64_t(b) * a.qs + ii) * a.Hq + hh) * kLatent + col;
+    *reinterpret_cast<uint32_t*>(a.out + oi) = pack_f32x2(v0, v1, true);
+  }
+  if (tid == 0) a.sems[unit] = 0u;
+}
+
+// ---------------------------------------------------------------- host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+struct Plan {
+  int nsplit = 1, split_pages = 1;
+  size_t ws_bytes = 0, nsems = 0;
+};
+
+const char* check_shape(const xqa_params* p, int v_head_dim) {
+  if (p->num_kv_heads != 1) return "the MLA variant has one latent kv head (num_kv_heads must be 1)";
+  if (p->head_dim != kDim || v_head_dim != kLatent)
+    return "the MLA kernel is built for a 576-wide latent row (512 latent + 64 rope) with v_head_dim 512";
+  if (p->num_q_heads * p->q_seq_len != kRows)
+    return "the MLA kernel needs num_q_heads * q_seq_len == 128 (one UMMA tile of query rows)";
+  if (p->q_dtype != XQA_BF16 || p->kv_dtype != XQA_BF16)
+    return "the MLA kernel is built for bf16 query and latent cache";
+  if (p->kv_layout != XQA_NHD && p->kv_layout != XQA_HND) return "bad kv_layout";
+  return nullptr;
+}
+
+int sm_count_of(const xqa_params* p, int sm_count) {
+  if (sm_count > 0) return sm_count;
+  if (p->sm_count > 0) return p->sm_count;
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+bool plan(const xqa_params* p, int sm_count, Plan* pl) {
+  int max_pages = p->pages_per_seq;
+  if (p->sliding_win_size > 0) {
+    const int64_t span = int64_t(p->sliding_win_size) + p->q_seq_len - 1;
+    max_pages = int(std::min<int64_t>(max_pages, (span + p->page_size - 1) / p->page_size + 1));
+  }
+  const int sm = sm_count_of(p, sm_count);
+  if (sm <= 0) return false;
+  const int stage_pages = p->page_size <= kTok ? kTok / p->page_size : 1;
+  // one cluster (2 CTAs, one per SM) per (sequence, split); aim for ~8 waves
+  const int64_t pairs = int64_t(sm / 2) * 8;
+  int64_t ns = (pairs + p->batch_size - 1) / p->batch_size;
+  const int64_t by_tiles = (max_pages + stage_pages - 1) / stage_pages;
+  const int64_t by_tokens = std::max<int64_t>(1, int64_t(max_pages) * p->page_size / 1024);
+  ns = std::max<int64_t>(1, std::min(ns, std::min(by_tiles, by_tokens)));
+  int sp = int((max_pages + ns - 1) / ns);
+  sp = ((sp + stage_pages - 1) / stage_pages) * stage_pages;
+  pl->split_pages = sp;
+  pl->nsplit = (max_pages + sp - 1) / sp;
+  pl->nsems = size_t(p->batch_size) * 2;
+  pl->ws_bytes = pl->nsplit > 1 ? size_t(p->batch_size) * pl->nsplit * kRows * (kLatent + 4) * sizeof(float) : 0;
+  return true;
+}
+
+}  // namespace mla
+
+size_t mla_workspace_size(const xqa_params* p, int v_head_dim, int sm_count) {
+  if (!p || mla::check_shape(p, v_head_dim)) return size_t(-1);
+  mla::Plan pl;
+  if (!mla::plan(p, sm_count, &pl)) return size_t(-1);
+  return pl.ws_bytes;
+}
+
+size_t mla_semaphore_count(const xqa_params* p, int v_head_dim) {
+  if (!p || mla::check_shape(p, v_head_dim)) return size_t(-1);
+  return size_t(p->batch_size) * 2;
+}
+
+xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_bytes, uint32_t* sems,
+                      cudaStream_t stream, char* err, size_t err_len) {
+  using namespace mla;
+  if (const char* why = check_shape(p, v_head_dim)) {
+    snprintf(err, err_len, "%s", why);
+    return XQA_ERR_UNSUPPORTED;
+  }
+  if (p->q_seq_len > 32) {
+    snprintf(err, err_len, "q_seq_len > 32 is not supported");
+    return XQA_ERR_UNSUPPORTED;
+  }
+  if ((reinterpret_cast<uintptr_t>(p->q) | reinterpret_cast<uintptr_t>(p->output)) & 15) {
+    snprintf(err, err_len, "q and output must be 16-byte aligned for the MLA kernel");
+    return XQA_ERR_INVALID_ARG;
+  }
+  Plan pl;
+  if (!plan(p, 0, &pl)) {
+    snprintf(err, err_len, "cannot query the SM count of the current device");
+    return XQA_ERR_CUDA;
+  }
+  if (pl.ws_bytes > 0) {
+    if (!ws || ws_bytes < pl.ws_bytes) {
+      snprintf(err, err_len, "workspace needs %zu bytes, got %zu", pl.ws_bytes, ws ? ws_bytes : size_t(0));
+      return XQA_ERR_WORKSPACE_TOO_SMALL;
+    }
+    if (!sems) {
+      snprintf(err, err_len, "semaphores are required (%zu needed)", pl.nsems);
+      return XQA_ERR_WORKSPACE_TOO_SMALL;
+    }
+    if (reinterpret_cast<uintptr_t>(ws) & 15) {
+      snprintf(err, err_len, "workspace must be 16-byte aligned");
+      return XQA_ERR_INVALID_ARG;
+    }
+  }
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) {
+    snprintf(err, err_len, "cuTensorMapEncodeTiled is unavailable");
+    return XQA_ERR_CUDA;
+  }
+  // NHD and HND coincide for one kv head: rows of 576 elements, token-major.
+  CUtensorMap tm;
+  cuuint64_t dims[3] = {cuuint64_t(kDim), 1, cuuint64_t(p->page_size) * cuuint64_t(p->num_pages)};
+  cuuint64_t strides[2] = {cuuint64_t(kDim) * 2, cuuint64_t(kDim) * 2};
+  cuuint32_t box[3] = {64, 1, cuuint32_t(std::min(p->page_size, kTok))};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p->k_cache), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(err, err_len, "cuTensorMapEncodeTiled failed (%d)", int(r));
+    return XQA_ERR_CUDA;
+  }
+  MlaArgs a;
+  memset(&a, 0, sizeof a);
+  a.q = static_cast<const uint16_t*>(p->q);
+  a.out = static_cast<uint16_t*>(p->output);
+  a.page_table = p->page_table;
+  a.seq_lens = p->seq_lens;
+  a.sinks = p->sinks;
+  a.mask = p->mask;
+  a.q_scale_dev = p->q_scale_dev;
+  a.kv_scale_dev = p->kv_scale_dev;
+  a.ws = static_cast<float*>(ws);
+  a.sems = sems;
+  a.err = p->error_word;
+  a.num_pages = p->num_pages;
+  a.B = p->batch_size;
+  a.Hq = p->num_q_heads;
+  a.qs = p->q_seq_len;
+  a.ps = p->page_size;
+  a.pps = p->pages_per_seq;
+  a.win = p->sliding_win_size;
+  a.nsplit = pl.nsplit;
+  a.split_pages = pl.split_pages;
+  a.mask_words = ((p->q_seq_len + 31) / 32) * 2;
+  a.q_scale = p->q_scale;
+  a.kv_scale = p->kv_scale;
+  a.softmax_scale = p->softmax_scale != 0.f ? p->softmax_scale : 1.0f / sqrtf(float(kDim));
+  a.rcp_out_scale = p->rcp_out_scale;
+  a.q_bf16 = 1;
+  cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) {
+    snprintf(err, err_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    return XQA_ERR_CUDA;
+  }
+  dim3 grid(2 * pl.nsplit, 1, p->batch_size);
+  mla_decode_kernel<<<grid, kThreads, kSmem, stream>>>(tm, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    snprintf(err, err_len, "MLA kernel launch: %s", cudaGetErrorString(e));
+    return XQA_ERR_CUDA;
+  }
+  return XQA_OK;
 }
 
 }  // namespace xqa

@@ -1,0 +1,80 @@
+"""GPU parity of the MLA latent decode kernel (one 576-wide latent kv head, V =
+its first 512 elements; vLLM Kimi-K3 MultiHeadLatentAttention page) against
+the float64 oracle on identical seeded inputs.  Tolerance: max-abs 1e-2 and
+relative L2 1e-2 (bf16 output; P rounded to bf16 before P.V)."""
+
+import pytest
+import torch
+
+import oracle
+from paged_kv_decode_20_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2
+SCALE = (128 + 64) ** -0.5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_decode_20_gb300 import build as B
+    B.build()
+
+
+def mla_case(lens, ps=64, seed=0, heads=128, qs=1, **kw):
+    return W.make_case(batch=len(lens), num_q_heads=heads, num_kv_heads=1, head_dim=576,
+                       v_head_dim=512, mla=True, page_size=ps, seq_lens=lens, kv_layout="NHD",
+                       q_seq_len=qs, softmax_scale=SCALE, seed=seed, **kw)
+
+
+def run_and_compare(c, tol=TOL, runs=2, **kw):
+    from paged_kv_decode_20_gb300.runner import Decoder
+    dec = Decoder(c.to("cuda"), **kw)
+    outs = []
+    for _ in range(runs):
+        dec.output.fill_(float("nan"))
+        outs.append(dec.run().clone())
+    torch.cuda.synchronize()
+    assert dec.error_bits() == 0, f"error word {dec.error_bits()}"
+    assert int(dec.semaphores.abs().sum()) == 0
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    got = outs[0].cpu().to(torch.float64)
+    ref = oracle.xqa_attention(c.q, c.k_cache, c.v_cache, c.page_table, c.seq_lens, **c.kwargs())
+    assert not torch.isnan(got).any()
+    err = (got - ref).abs().max().item()
+    l2 = ((got - ref).norm() / ref.norm().clamp_min(1e-30)).item()
+    assert err <= tol, f"max abs {err:.3e}"
+    assert l2 <= 1e-2, f"rel L2 {l2:.3e}"
+    return err, l2
+
+
+def test_mla_workload_first_sequences():
+    run_and_compare(W.workload(5, batch=2))
+
+
+@pytest.mark.parametrize("ps", [16, 32, 64, 128])
+def test_mla_page_sizes(ps):
+    run_and_compare(mla_case([1, 63, 64, 65, 700], ps=ps, seed=ps))
+
+
+@pytest.mark.parametrize("sm_count", [2, 40, 1000])
+def test_mla_split_counts(sm_count):
+    run_and_compare(mla_case([5000, 130], seed=3), sm_count=sm_count)
+
+
+def test_mla_peaked_rows_force_rescales():
+    run_and_compare(mla_case([3000, 77], seed=4, q_mult=4.0))
+
+
+def test_mla_sinks_window_and_spec_tokens():
+    c = mla_case([900, 300], seed=5, heads=64, qs=2, sinks=True, sliding_win_size=200,
+                 mask="causal")
+    run_and_compare(c)
+
+
+def test_mla_empty_and_nan_poison():
+    c = mla_case([0, 1, 129], seed=6, pool_pages=12, poison=True)
+    run_and_compare(c)
