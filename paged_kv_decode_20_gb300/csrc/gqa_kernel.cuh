@@ -6,11 +6,13 @@
 // the GQA group stacked), padded to 16-row MMA blocks.
 //
 //   warp 4 (producer, one lane): walks page_table and issues one TMA tile load
-//     per (page, 128-byte column chunk) for K and for V into a ring of 64-token
-//     stages, each guarded by a full/empty mbarrier pair.  NHD and HND differ
-//     only in the tensor map and the coordinates.  TMA writes the rows with the
-//     128-byte swizzle, so ldmatrix reads are bank-conflict free.
-//   warps 0-3 (consumers): each takes 16 tokens of every stage.
+//     per (page, 128-byte column chunk) for K and for V into a ring of stages
+//     (128 tokens when a row is one 128-byte chunk, else 64), each guarded by
+//     a full/empty mbarrier pair.  NHD and HND differ only in the tensor map
+//     and the coordinates.  TMA writes the rows with the 128-byte swizzle, so
+//     ldmatrix reads are bank-conflict free.
+//   warps 0-3 (consumers): each takes a quarter of every stage (16 or 32
+//     tokens, i.e. two or four independent 8-token MMA chains).
 //     S = Q K^T with mma.sync m16n8k16 (rows on M, tokens on N), fp32 online
 //     softmax in the exp2 domain with window / spec-mask / tail masking by
 //     select, then O += P V (P re-used from the S accumulator registers).
@@ -40,10 +42,12 @@ struct GqaCfg {
   static constexpr int kRowBytes = D * kElt;  // 128 or 256
   static_assert(kRowBytes == 128 || kRowBytes == 256, "row must be 1 or 2 swizzle chunks");
   static constexpr int kChunks = kRowBytes / 128;
-  static constexpr int kTok = 64;                          // tokens per stage
+  // tokens per stage: 128 when a row is one 128-byte chunk and one 16-row
+  // block suffices (four MMA chains per warp), else 64 (register budget)
+  static constexpr int kTok = (kRowBytes == 128 && RB == 1) ? 128 : 64;
   static constexpr int kTile = kTok * kRowBytes;           // K (or V) bytes per stage
   static constexpr int kStage = 2 * kTile;
-  static constexpr int kNumStages = kStage >= 32768 ? 3 : 5;
+  static constexpr int kNumStages = kStage >= 32768 ? 3 : 5;  // 96 KB or 80 KB per CTA
   static constexpr int kRows = 16 * RB;
   static constexpr int kThreads = 160;
   static constexpr int kScratch = 4 * kRows * D * 4 + 2 * 4 * kRows * 4;
@@ -280,6 +284,10 @@ __global__ void __launch_bounds__(160, 2)
       for (int j = 0; j < kDvTiles; ++j) o[rb][j][0] = o[rb][j][1] = o[rb][j][2] = o[rb][j][3] = 0.f;
     }
 
+    constexpr int KB = C::kTok / 64;  // 16-token blocks per warp and stage
+    constexpr int NT = 2 * KB;        // 8-token MMA n-tiles per warp and stage
+    const int wt0 = 16 * KB * warp;   // this warp's first row of every stage
+    const int mat = lane >> 3;
     for (int s = 0; s < nst; ++s) {
       const int slot = s % C::kNumStages;
       if (!mbar_wait(&full[slot], (s / C::kNumStages) & 1)) {
@@ -287,61 +295,68 @@ __global__ void __launch_bounds__(160, 2)
         if (a.err && lane == 0) atomicOr(a.err, kErrTimeout);
         break;
       }
-      const int ta = t_begin + s * C::kTok + 16 * warp;  // this warp's first token
+      const int ta = t_begin + s * C::kTok + wt0;  // this warp's first token
       if (ta < t_end) {
         const uint32_t kt = smem_u32(smem + slot * C::kStage);
         const uint32_t vt = kt + C::kTile;
-        const bool edge = (ta + 16 > t_end) || (ta < lb_max) || (a.mask && ta + 16 > spec0);
+        const bool edge = (ta + 16 * KB > t_end) || (ta < lb_max) || (a.mask && ta + 16 * KB > spec0);
 
-        // ---- S = Q K^T over this warp's 16 tokens (two n-tiles of 8)
-        float sacc[RB][2][4];
+        // ---- S = Q K^T over this warp's tokens (NT independent n-tile chains)
+        float sacc[RB][NT][4];
 #pragma unroll
         for (int rb = 0; rb < RB; ++rb)
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) sacc[rb][nt][0] = sacc[rb][nt][1] = sacc[rb][nt][2] = sacc[rb][nt][3] = 0.f;
-        const int mat = lane >> 3;
+          for (int nt = 0; nt < NT; ++nt)
+            sacc[rb][nt][0] = sacc[rb][nt][1] = sacc[rb][nt][2] = sacc[rb][nt][3] = 0.f;
         if constexpr (!kF8) {
-          const int tr = 16 * warp + (mat >> 1) * 8 + (lane & 7);
 #pragma unroll
           for (int kc = 0; kc < kKSteps; ++kc) {
-            const int u = 2 * kc + (mat & 1);
-            const uint32_t addr = kt + (u >> 3) * (C::kTok * 128) + tr * 128 + (((u & 7) ^ (tr & 7)) << 4);
-            uint32_t r0, r1, r2, r3;
-            ldsm_x4(addr, r0, r1, r2, r3);
 #pragma unroll
-            for (int rb = 0; rb < RB; ++rb) {
-              mma16816<kMmaBf16>(sacc[rb][0], qa[rb][kc], r0, r1);
-              mma16816<kMmaBf16>(sacc[rb][1], qa[rb][kc], r2, r3);
+            for (int kb = 0; kb < KB; ++kb) {
+              const int tr = wt0 + 16 * kb + (mat >> 1) * 8 + (lane & 7);
+              const int u = 2 * kc + (mat & 1);
+              const uint32_t addr =
+                  kt + (u >> 3) * (C::kTok * 128) + tr * 128 + (((u & 7) ^ (tr & 7)) << 4);
+              uint32_t r0, r1, r2, r3;
+              ldsm_x4(addr, r0, r1, r2, r3);
+#pragma unroll
+              for (int rb = 0; rb < RB; ++rb) {
+                mma16816<kMmaBf16>(sacc[rb][2 * kb], qa[rb][kc], r0, r1);
+                mma16816<kMmaBf16>(sacc[rb][2 * kb + 1], qa[rb][kc], r2, r3);
+              }
             }
           }
         } else {
-          const int tr = 16 * warp + (mat & 1) * 8 + (lane & 7);
 #pragma unroll
           for (int kc2 = 0; kc2 < kKSteps / 2; ++kc2) {
-            const int u = 2 * kc2 + (mat >> 1);
-            const uint32_t addr = kt + tr * 128 + (((u & 7) ^ (tr & 7)) << 4);
-            uint32_t r[4];
-            ldsm_x4(addr, r[0], r[1], r[2], r[3]);
 #pragma unroll
-            for (int x = 0; x < 4; ++x) {
-              const int nt = x & 1, kc = 2 * kc2 + (x >> 1);
-              const uint32_t b01 = e4m3x2_to_f16x2(r[x] & 0xffffu);
-              const uint32_t b23 = e4m3x2_to_f16x2(r[x] >> 16);
+            for (int kb = 0; kb < KB; ++kb) {
+              const int tr = wt0 + 16 * kb + (mat & 1) * 8 + (lane & 7);
+              const int u = 2 * kc2 + (mat >> 1);
+              const uint32_t addr = kt + tr * 128 + (((u & 7) ^ (tr & 7)) << 4);
+              uint32_t r[4];
+              ldsm_x4(addr, r[0], r[1], r[2], r[3]);
 #pragma unroll
-              for (int rb = 0; rb < RB; ++rb) mma16816<false>(sacc[rb][nt], qa[rb][kc], b01, b23);
+              for (int x = 0; x < 4; ++x) {
+                const int nt = 2 * kb + (x & 1), kc = 2 * kc2 + (x >> 1);
+                const uint32_t b01 = e4m3x2_to_f16x2(r[x] & 0xffffu);
+                const uint32_t b23 = e4m3x2_to_f16x2(r[x] >> 16);
+#pragma unroll
+                for (int rb = 0; rb < RB; ++rb) mma16816<false>(sacc[rb][nt], qa[rb][kc], b01, b23);
+              }
             }
           }
         }
 
         // ---- scale, mask, online softmax (exp2 domain)
-        uint32_t pa[RB][4];
+        uint32_t pa[RB][KB][4];
         bool any_rescale = false;
         float corr[RB][2];
 #pragma unroll
         for (int rb = 0; rb < RB; ++rb) {
           float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
+          for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               float x = sacc[rb][nt][e] * lscale;
@@ -364,24 +379,31 @@ __global__ void __launch_bounds__(160, 2)
             any_rescale |= corr[rb][hh] != 1.f;
             m_run[rb][hh] = m_new;
           }
-          float p[2][4];
+          // P rounded to the MMA's 16-bit type; the row sums use the rounded
+          // values so that the output stays a convex combination of V.
           float rs[2] = {0.f, 0.f};
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
+          for (int kb = 0; kb < KB; ++kb) {
+            float p[2][4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float mm = m_run[rb][e >> 1];
-              const float v = (mm == -INFINITY) ? 0.f : exp2f(sacc[rb][nt][e] - mm);
-              p[nt][e] = v;
-              rs[e >> 1] += v;
+            for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float mm = m_run[rb][e >> 1];
+                p[h2][e] = (mm == -INFINITY) ? 0.f : exp2f(sacc[rb][2 * kb + h2][e] - mm);
+              }
+            pa[rb][kb][0] = pack_f32x2(p[0][0], p[0][1], kMmaBf16);
+            pa[rb][kb][1] = pack_f32x2(p[0][2], p[0][3], kMmaBf16);
+            pa[rb][kb][2] = pack_f32x2(p[1][0], p[1][1], kMmaBf16);
+            pa[rb][kb][3] = pack_f32x2(p[1][2], p[1][3], kMmaBf16);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float2 f = unpack_16x2(pa[rb][kb][k], kMmaBf16);
+              rs[k & 1] += f.x + f.y;
             }
+          }
           l_run[rb][0] = l_run[rb][0] * corr[rb][0] + rs[0];
           l_run[rb][1] = l_run[rb][1] * corr[rb][1] + rs[1];
-          constexpr bool kPBf16 = kMmaBf16;
-          pa[rb][0] = pack_f32x2(p[0][0], p[0][1], kPBf16);
-          pa[rb][1] = pack_f32x2(p[0][2], p[0][3], kPBf16);
-          pa[rb][2] = pack_f32x2(p[1][0], p[1][1], kPBf16);
-          pa[rb][3] = pack_f32x2(p[1][2], p[1][3], kPBf16);
         }
         if (__any_sync(0xffffffffu, any_rescale)) {
 #pragma unroll
@@ -396,62 +418,67 @@ __global__ void __launch_bounds__(160, 2)
         }
 
         // ---- O += P V
-        if constexpr (!kF8) {
-          // V tokens held by this lane: (ta+2qd, +1) in r0/r2 and (ta+8+2qd, +1) in r1/r3
-          uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
-          if (edge) {
-            const int t0 = ta + 2 * qd, t1 = ta + 8 + 2 * qd;
-            vm0 = ((t0 < t_end && t0 >= t_lo_all) ? 0x0000ffffu : 0u) |
-                  ((t0 + 1 < t_end && t0 + 1 >= t_lo_all) ? 0xffff0000u : 0u);
-            vm1 = ((t1 < t_end && t1 >= t_lo_all) ? 0x0000ffffu : 0u) |
-                  ((t1 + 1 < t_end && t1 + 1 >= t_lo_all) ? 0xffff0000u : 0u);
-          }
-          const int tr = 16 * warp + (mat & 1) * 8 + (lane & 7);
 #pragma unroll
-          for (int j2 = 0; j2 < kDvTiles / 2; ++j2) {
-            const int u = 2 * j2 + (mat >> 1);
-            const uint32_t addr = vt + (u >> 3) * (C::kTok * 128) + tr * 128 + (((u & 7) ^ (tr & 7)) << 4);
-            uint32_t r0, r1, r2, r3;
-            ldsm_x4_t(addr, r0, r1, r2, r3);
-            r0 &= vm0;
-            r1 &= vm1;
-            r2 &= vm0;
-            r3 &= vm1;
-#pragma unroll
-            for (int rb = 0; rb < RB; ++rb) {
-              mma16816<kMmaBf16>(o[rb][2 * j2], pa[rb], r0, r1);
-              mma16816<kMmaBf16>(o[rb][2 * j2 + 1], pa[rb], r2, r3);
+        for (int kb = 0; kb < KB; ++kb) {
+          const int tb = ta + 16 * kb;  // first token of this 16-token block
+          if constexpr (!kF8) {
+            // V tokens held by this lane: (tb+2qd, +1) in r0/r2, (tb+8+2qd, +1) in r1/r3
+            uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+            if (edge) {
+              const int t0 = tb + 2 * qd, t1 = tb + 8 + 2 * qd;
+              vm0 = ((t0 < t_end && t0 >= t_lo_all) ? 0x0000ffffu : 0u) |
+                    ((t0 + 1 < t_end && t0 + 1 >= t_lo_all) ? 0xffff0000u : 0u);
+              vm1 = ((t1 < t_end && t1 >= t_lo_all) ? 0x0000ffffu : 0u) |
+                    ((t1 + 1 < t_end && t1 + 1 >= t_lo_all) ? 0xffff0000u : 0u);
             }
-          }
-        } else {
-          const int tl[4] = {16 * warp + 2 * qd, 16 * warp + 2 * qd + 1, 16 * warp + 8 + 2 * qd,
-                             16 * warp + 9 + 2 * qd};
-          bool tv[4] = {true, true, true, true};
-          if (edge) {
+            const int tr = wt0 + 16 * kb + (mat & 1) * 8 + (lane & 7);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int t = t_begin + s * C::kTok + tl[k];
-              tv[k] = t < t_end && t >= t_lo_all;
+            for (int j2 = 0; j2 < kDvTiles / 2; ++j2) {
+              const int u = 2 * j2 + (mat >> 1);
+              const uint32_t addr =
+                  vt + (u >> 3) * (C::kTok * 128) + tr * 128 + (((u & 7) ^ (tr & 7)) << 4);
+              uint32_t r0, r1, r2, r3;
+              ldsm_x4_t(addr, r0, r1, r2, r3);
+              r0 &= vm0;
+              r1 &= vm1;
+              r2 &= vm0;
+              r3 &= vm1;
+#pragma unroll
+              for (int rb = 0; rb < RB; ++rb) {
+                mma16816<kMmaBf16>(o[rb][2 * j2], pa[rb][kb], r0, r1);
+                mma16816<kMmaBf16>(o[rb][2 * j2 + 1], pa[rb][kb], r2, r3);
+              }
             }
-          }
+          } else {
+            const int r0w = wt0 + 16 * kb;
+            const int tl[4] = {r0w + 2 * qd, r0w + 2 * qd + 1, r0w + 8 + 2 * qd, r0w + 9 + 2 * qd};
+            bool tv[4] = {true, true, true, true};
+            if (edge) {
 #pragma unroll
-          for (int j4 = 0; j4 < D / 32; ++j4) {
-            const int u = 2 * j4 + (g >> 2);
-            uint32_t w[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint32_t addr = vt + tl[k] * 128 + (((u & 7) ^ (tl[k] & 7)) << 4) + 4 * (g & 3);
-              uint32_t x;
-              asm volatile("ld.shared.b32 %0, [%1];" : "=r"(x) : "r"(addr));
-              w[k] = tv[k] ? x : 0u;
+              for (int k = 0; k < 4; ++k) {
+                const int t = t_begin + s * C::kTok + tl[k];
+                tv[k] = t < t_end && t >= t_lo_all;
+              }
             }
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const uint32_t sel = uint32_t(c) | (uint32_t(c + 4) << 4);
-              const uint32_t b01 = e4m3x2_to_f16x2(prmt(w[0], w[1], sel) & 0xffffu);
-              const uint32_t b23 = e4m3x2_to_f16x2(prmt(w[2], w[3], sel) & 0xffffu);
+            for (int j4 = 0; j4 < D / 32; ++j4) {
+              const int u = 2 * j4 + (g >> 2);
+              uint32_t w[4];
 #pragma unroll
-              for (int rb = 0; rb < RB; ++rb) mma16816<false>(o[rb][4 * j4 + c], pa[rb], b01, b23);
+              for (int k = 0; k < 4; ++k) {
+                const uint32_t addr = vt + tl[k] * 128 + (((u & 7) ^ (tl[k] & 7)) << 4) + 4 * (g & 3);
+                uint32_t x;
+                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(x) : "r"(addr));
+                w[k] = tv[k] ? x : 0u;
+              }
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                const uint32_t sel = uint32_t(c) | (uint32_t(c + 4) << 4);
+                const uint32_t b01 = e4m3x2_to_f16x2(prmt(w[0], w[1], sel) & 0xffffu);
+                const uint32_t b23 = e4m3x2_to_f16x2(prmt(w[2], w[3], sel) & 0xffffu);
+#pragma unroll
+                for (int rb = 0; rb < RB; ++rb) mma16816<false>(o[rb][4 * j4 + c], pa[rb][kb], b01, b23);
+              }
             }
           }
         }

@@ -449,8 +449,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 4; ++e) {
           const float p0 = m_ref == -INFINITY ? 0.f : exp2f(s[8 * u + 2 * e] - m_ref);
           const float p1 = m_ref == -INFINITY ? 0.f : exp2f(s[8 * u + 2 * e + 1] - m_ref);
-          l_run += p0 + p1;
           w4[e] = pack_f32x2(p0, p1, true);
+          // the row sum takes the rounded weights, so O / l stays a convex
+          // combination of V rows
+          const float2 r = unpack_16x2(w4[e], true);
+          l_run += r.x + r.y;
         }
         *reinterpret_cast<uint4*>(smem + kOffP + umma::sw128(t, u)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
       }

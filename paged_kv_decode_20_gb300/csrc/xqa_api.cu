@@ -142,7 +142,7 @@ int pages_bound(const xqa_params* p) {
 
 // Splits so that B * Hkv * row_groups * splits covers several waves of the
 // GPU (split count from B, the table bound and the SM count), in whole
-// 64-token stages and never below 256 tokens per split.
+// pipeline stages and never below 256 tokens per split.
 void choose_splits(const xqa_params* p, Plan* pl, int sm_count, int ctas_per_sm, int stage_pages) {
   const int64_t units = int64_t(p->batch_size) * p->num_kv_heads * pl->rg_count;
   const int max_pages = pl->max_pages;
@@ -155,6 +155,13 @@ void choose_splits(const xqa_params* p, Plan* pl, int sm_count, int ctas_per_sm,
   sp = ((sp + stage_pages - 1) / stage_pages) * stage_pages;
   pl->split_pages = sp;
   pl->nsplit = (max_pages + sp - 1) / sp;
+}
+
+// Tokens per pipeline stage of the GQA kernel: 128 when a K row is one
+// 128-byte swizzle chunk (fp8 D=128, 16-bit D=64) and one 16-row block holds
+// the rows, else 64.  Must match GqaCfg::kTok.
+int stage_tokens(const xqa_params* p, int row_blocks) {
+  return (p->head_dim * elt_bytes(p->kv_dtype) == 128 && row_blocks == 1) ? 128 : 64;
 }
 
 xqa_status plan_gqa(const xqa_params* p, int sm_count_in, Plan* pl) {
@@ -181,7 +188,8 @@ xqa_status plan_gqa(const xqa_params* p, int sm_count_in, Plan* pl) {
   else
     e = xqa::gqa_launch_f16(D, pl->row_blocks, false, dim3(), nullptr, nullptr, nullptr, nullptr, &occ);
   if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
-  const int stage_pages = p->page_size <= 64 ? 64 / p->page_size : 1;
+  const int tok = stage_tokens(p, pl->row_blocks);
+  const int stage_pages = p->page_size <= tok ? tok / p->page_size : 1;
   choose_splits(p, pl, sm, occ, stage_pages);
   const int64_t units = int64_t(p->batch_size) * p->num_kv_heads * pl->rg_count;
   pl->nsems = size_t(units);
@@ -318,7 +326,7 @@ xqa_status xqa_decode(const xqa_params* p, void* ws, size_t ws_bytes, uint32_t* 
   st = check_buffers(pl, ws, ws_bytes, sems);
   if (st != XQA_OK) return st;
   CUtensorMap tk, tv;
-  const int box_rows = std::min(p->page_size, 64);
+  const int box_rows = std::min(p->page_size, stage_tokens(p, pl.row_blocks));
   st = make_maps(p, pl.D, box_rows, &tk, &tv);
   if (st != XQA_OK) return st;
   xqa::DecodeArgs a;
