@@ -119,70 +119,77 @@ __global__ void __launch_bounds__(160, 2)
   float* sc_l = sc_m + 4 * C::kRows;
 
   if (warp == 4) {
-    // ================= producer =================
-    if (lane == 0 && nst > 0) {
-      prefetch_tensormap(&tmK);
-      prefetch_tensormap(&tmV);
+    // ================= producer (whole warp fetches page indices, lane 0 issues TMA)
+    if (nst > 0) {
+      if (lane == 0) {
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+      }
       const int32_t* pt = a.page_table + int64_t(b) * a.pps;
       const int box_rows = a.ps < C::kTok ? a.ps : C::kTok;
       const uint32_t box_bytes = uint32_t(box_rows) * 128u;
       constexpr int kChunkElems = 128 / C::kElt;
+      // 32 consecutive page indices, one per lane, starting at win_base
+      int win_base = pg_lo;
+      auto fetch = [&](int base) {
+        int pg = 0;
+        if (base + lane < pg_hi) {
+          pg = __ldg(pt + base + lane);
+          if (pg < 0 || int64_t(pg) >= a.num_pages) pg = -1;  // out of the pool: TMA fills zeros
+        }
+        return pg;
+      };
+      int my_page = fetch(win_base);
       bool bad_page = false;
       int s = 0;
       for (; s < nst; ++s) {
         const int slot = s % C::kNumStages;
         const int round = s / C::kNumStages;
-        if (s >= C::kNumStages && !mbar_wait(&empty[slot], (round & 1) ^ 1)) {
-          flags[0] = 1;
+        int ok = 1;
+        if (lane == 0 && s >= C::kNumStages) ok = mbar_wait(&empty[slot], (round & 1) ^ 1);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          if (lane == 0) flags[0] = 1;
           break;
         }
         uint8_t* kdst = smem + slot * C::kStage;
         uint8_t* vdst = kdst + C::kTile;
         const int tok0 = t_begin + s * C::kTok;
-        // pieces of this stage: (logical page, first slot, destination row)
-        int n_piece = 0;
-        if (a.ps <= C::kTok) {
-          const int per = C::kTok / a.ps;
-          const int lp0 = tok0 / a.ps;
-          n_piece = min(per, pg_hi - lp0);
-        } else {
-          n_piece = 1;
+        const int lp0 = tok0 / a.ps;
+        const int sub = a.ps <= C::kTok ? 0 : tok0 % a.ps;
+        const int n_piece = a.ps <= C::kTok ? min(C::kTok / a.ps, pg_hi - lp0) : 1;
+        if (lp0 + n_piece > win_base + 32) {
+          win_base = lp0;
+          my_page = fetch(win_base);
         }
-        mbar_arrive_expect_tx(&full[slot], uint32_t(n_piece) * box_bytes * 2u * C::kChunks);
+        if (lane == 0)
+          mbar_arrive_expect_tx(&full[slot], uint32_t(n_piece) * box_bytes * 2u * C::kChunks);
         for (int j = 0; j < n_piece; ++j) {
-          int lp, sub;
-          if (a.ps <= C::kTok) {
-            lp = tok0 / a.ps + j;
-            sub = 0;
-          } else {
-            lp = tok0 / a.ps;
-            sub = tok0 % a.ps;
-          }
-          int page = __ldg(pt + lp);
-          if (page < 0 || int64_t(page) >= a.num_pages) {
-            bad_page = true;
-            page = -1;  // every coordinate out of bounds: TMA fills zeros
-          }
-          const int row_off = j * box_rows;
-          for (int c = 0; c < C::kChunks; ++c) {
-            const int off = c * C::kTok * 128 + row_off * 128;
-            if (a.hnd) {
-              tma_load_3d(kdst + off, &tmK, &full[slot], c * kChunkElems, sub, page * a.Hkv + kvh);
-              tma_load_3d(vdst + off, &tmV, &full[slot], c * kChunkElems, sub, page * a.Hkv + kvh);
-            } else {
-              tma_load_3d(kdst + off, &tmK, &full[slot], c * kChunkElems, kvh, page * a.ps + sub);
-              tma_load_3d(vdst + off, &tmV, &full[slot], c * kChunkElems, kvh, page * a.ps + sub);
+          const int page = __shfl_sync(0xffffffffu, my_page, lp0 + j - win_base);
+          if (lane == 0) {
+            bad_page |= page < 0;
+            const int row_off = j * box_rows;
+            for (int c = 0; c < C::kChunks; ++c) {
+              const int off = c * C::kTok * 128 + row_off * 128;
+              if (a.hnd) {
+                tma_load_3d(kdst + off, &tmK, &full[slot], c * kChunkElems, sub, page * a.Hkv + kvh);
+                tma_load_3d(vdst + off, &tmV, &full[slot], c * kChunkElems, sub, page * a.Hkv + kvh);
+              } else {
+                tma_load_3d(kdst + off, &tmK, &full[slot], c * kChunkElems, kvh, page * a.ps + sub);
+                tma_load_3d(vdst + off, &tmV, &full[slot], c * kChunkElems, kvh, page * a.ps + sub);
+              }
             }
           }
         }
       }
-      if (bad_page && a.err) atomicOr(a.err, kErrClamped);
-      // Leave no copy in flight: wait (bounded) for the last stages issued.
-      const int first = max(0, s - C::kNumStages);
-      for (int t = first; t < s; ++t) {
-        if (!mbar_wait(&full[t % C::kNumStages], (t / C::kNumStages) & 1)) flags[0] = 1;
+      if (lane == 0) {
+        if (bad_page && a.err) atomicOr(a.err, kErrClamped);
+        // Leave no copy in flight: wait (bounded) for the last stages issued.
+        const int first = max(0, s - C::kNumStages);
+        for (int t = first; t < s; ++t) {
+          if (!mbar_wait(&full[t % C::kNumStages], (t / C::kNumStages) & 1)) flags[0] = 1;
+        }
+        if (flags[0] && a.err) atomicOr(a.err, kErrTimeout);
       }
-      if (flags[0] && a.err) atomicOr(a.err, kErrTimeout);
     }
   } else {
     // ================= consumers =================
@@ -290,7 +297,8 @@ __global__ void __launch_bounds__(160, 2)
     const int mat = lane >> 3;
     for (int s = 0; s < nst; ++s) {
       const int slot = s % C::kNumStages;
-      if (!mbar_wait(&full[slot], (s / C::kNumStages) & 1)) {
+      // voted, so the warp leaves together (its shuffles and ldmatrix are collective)
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], (s / C::kNumStages) & 1))) {
         flags[0] = 1;
         if (a.err && lane == 0) atomicOr(a.err, kErrTimeout);
         break;

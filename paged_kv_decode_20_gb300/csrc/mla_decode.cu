@@ -62,7 +62,7 @@ constexpr int kOffQRope = kOffStages + kStages * kStageBytes;  // 128 x 64 bf16
 constexpr int kOffP = kOffQRope + kRows * 128;                  // 128 x 64 bf16
 constexpr int kOffX = kOffP + kRows * 128;                      // 128 x 64 fp32 (peer partial)
 constexpr int kOffBar = kOffX + kRows * kTok * 4;
-constexpr int kNumBars = 2 * kStages + 9;
+constexpr int kNumBars = 2 * kStages + 10;
 constexpr int kSmem = 1024 + kOffBar + kNumBars * 8 + 32;
 
 // tensor memory columns
@@ -152,6 +152,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* pv_done = p_full + 1;
   uint64_t* x_full = pv_done + 1;           // the peer's partial landed in my buffer
   uint64_t* x_free = x_full + 1;            // the peer has read my previous partial
+  uint64_t* mma_drain = x_free + 1;         // every MMA this CTA issued has finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
   int* flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] abort, [1] last CTA
 
@@ -194,6 +195,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(pv_done, 1);
     mbar_init(x_full, 1);
     mbar_init(x_free, 4);
+    mbar_init(mma_drain, 1);
     flags[0] = flags[1] = 0;
     fence_mbar_init();
   }
@@ -213,44 +215,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   float* xbuf = reinterpret_cast<float*>(smem + kOffX);
 
   if (warp == 0) {
-    // ================= TMA producer =================
-    if (lane == 0 && ntiles > 0) {
-      prefetch_tensormap(&tmKV);
+    // ================= TMA producer (warp fetches page indices, lane 0 issues)
+    if (ntiles > 0) {
+      if (lane == 0) prefetch_tensormap(&tmKV);
       const int32_t* pt = a.page_table + int64_t(b) * a.pps;
       const int box_rows = min(a.ps, kTok);
       const uint32_t box_bytes = uint32_t(box_rows) * 128u;
+      int win_base = pg_lo;
+      auto fetch = [&](int base) {
+        int pg = 0;
+        if (base + lane < pg_hi) {
+          pg = __ldg(pt + base + lane);
+          if (pg < 0 || int64_t(pg) >= a.num_pages) pg = -1;  // TMA fills zeros
+        }
+        return pg;
+      };
+      int my_page = fetch(win_base);
       bool bad_page = false;
       int s = 0;
       for (; s < ntiles; ++s) {
         const int slot = s % kStages;
-        if (s >= kStages && !mbar_wait(&kv_empty[slot], ((s / kStages) & 1) ^ 1)) {
-          flags[0] = 1;
+        int ok = 1;
+        if (lane == 0 && s >= kStages) ok = mbar_wait(&kv_empty[slot], ((s / kStages) & 1) ^ 1);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          if (lane == 0) flags[0] = 1;
           break;
         }
         const int tok0 = t_begin + s * kTok;
-        const int n_piece = a.ps <= kTok ? min(kTok / a.ps, pg_hi - tok0 / a.ps) : 1;
-        mbar_arrive_expect_tx(&kv_full[slot], uint32_t(n_piece) * box_bytes * nchunks);
+        const int lp0 = tok0 / a.ps;
+        const int sub = a.ps <= kTok ? 0 : tok0 % a.ps;
+        const int n_piece = a.ps <= kTok ? min(kTok / a.ps, pg_hi - lp0) : 1;
+        if (lp0 + n_piece > win_base + 32) {
+          win_base = lp0;
+          my_page = fetch(win_base);
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&kv_full[slot], uint32_t(n_piece) * box_bytes * nchunks);
         uint8_t* dst = smem + kOffStages + slot * kStageBytes;
         for (int j = 0; j < n_piece; ++j) {
-          const int lp = a.ps <= kTok ? tok0 / a.ps + j : tok0 / a.ps;
-          const int sub = a.ps <= kTok ? 0 : tok0 % a.ps;
-          int page = __ldg(pt + lp);
-          if (page < 0 || int64_t(page) >= a.num_pages) {
-            bad_page = true;
-            page = -1;
-          }
-          const int row_off = j * box_rows;
-          for (int k = 0; k < nchunks; ++k) {
-            // chunk slot k: latent dims 256c + 64k (k < 4) or the rope dims
-            const int x = k < 4 ? int(c) * kHalf + 64 * k : kLatent;
-            tma_load_3d(dst + k * kChunkBytes + row_off * 128, &tmKV, &kv_full[slot], x, 0,
-                        page * a.ps + sub);
+          const int page = __shfl_sync(0xffffffffu, my_page, lp0 + j - win_base);
+          if (lane == 0) {
+            bad_page |= page < 0;
+            const int row_off = j * box_rows;
+            for (int k = 0; k < nchunks; ++k) {
+              // chunk slot k: latent dims 256c + 64k (k < 4) or the rope dims
+              const int x = k < 4 ? int(c) * kHalf + 64 * k : kLatent;
+              tma_load_3d(dst + k * kChunkBytes + row_off * 128, &tmKV, &kv_full[slot], x, 0,
+                          page * a.ps + sub);
+            }
           }
         }
       }
-      if (bad_page && a.err) atomicOr(a.err, kErrClamped);
-      for (int t = max(0, s - kStages); t < s; ++t)
-        if (!mbar_wait(&kv_full[t % kStages], (t / kStages) & 1)) flags[0] = 1;
+      if (lane == 0) {
+        if (bad_page && a.err) atomicOr(a.err, kErrClamped);
+        for (int t = max(0, s - kStages); t < s; ++t)
+          if (!mbar_wait(&kv_full[t % kStages], (t / kStages) & 1)) flags[0] = 1;
+      }
     }
   } else if (warp == 1) {
     // ================= MMA issuer =================
@@ -306,6 +325,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         umma::commit(pv_done);
       }
       if (!ok) flags[0] = 1;
+      // nothing this thread issued may still run when tensor memory is freed
+      umma::commit(mma_drain);
+      if (!mbar_wait(mma_drain, 0)) flags[0] = 1;
     }
   } else if (warp >= 4) {
     // ================= softmax / exchange / epilogue =================
@@ -358,38 +380,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t xrow_peer = map_peer(smem_u32(xbuf + t * kTok), peer);
     float m_ref = -INFINITY, l_run = 0.f;
     bool ok = true;
+    constexpr unsigned kAll = 0xffffffffu;
 
+    // Control flow below stays uniform across each warp (tcgen05.ld / st are
+    // warp-collective) and across the four softmax warps (named barrier):
+    // waits are voted with __all_sync and the loop is left collectively.
     for (int j = 0; j < ntiles; ++j) {
       const int sb = j & 1;
       float s[kTok];
-      if (!mbar_wait(&s_full[sb], (j >> 1) & 1)) {
-        ok = false;
-        break;
+      ok = __all_sync(kAll, mbar_wait(&s_full[sb], (j >> 1) & 1));
+      if (ok) {
+        umma::fence_after_sync();
+        umma::tmem_ld32(tmem + lane_base + kColS + 64u * sb, s);
+        umma::tmem_ld32(tmem + lane_base + kColS + 64u * sb + 32u, s + 32);
+        umma::tmem_ld_wait();
+        umma::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[sb]);
+        // ---- exchange partial logits with the peer
+        if (j > 0) ok = __all_sync(kAll, wait_cluster(x_free, (j - 1) & 1));
       }
-      umma::fence_after_sync();
-      umma::tmem_ld32(tmem + lane_base + kColS + 64u * sb, s);
-      umma::tmem_ld32(tmem + lane_base + kColS + 64u * sb + 32u, s + 32);
-      umma::tmem_ld_wait();
-      umma::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[sb]);
-
-      // ---- exchange partial logits with the peer
-      if (j > 0 && !wait_cluster(x_free, (j - 1) & 1)) {
-        ok = false;
-        break;
+      if (ok) {
+        for (int v = 0; v < kTok / 4; ++v) {
+          // 16-byte unit v of the row, XOR-swizzled by row to spread banks
+          const uint32_t off = uint32_t(((v ^ (t & 15)) & 15) * 16);
+          st_async_v4(xrow_peer + off, s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3], x_full_peer);
+        }
+        if (t == 0) mbar_arrive_expect_tx(x_full, uint32_t(kRows * kTok * 4));
+        ok = __all_sync(kAll, wait_cluster(x_full, j & 1));
       }
-      for (int v = 0; v < kTok / 4; ++v) {
-        // 16-byte unit v of the row, XOR-swizzled by row to spread banks
-        const uint32_t off = uint32_t(((v ^ (t & 15)) & 15) * 16);
-        st_async_v4(xrow_peer + off, s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3], x_full_peer);
-      }
-      if (t == 0) mbar_arrive_expect_tx(x_full, uint32_t(kRows * kTok * 4));
-      if (!wait_cluster(x_full, j & 1)) {
-        ok = false;
-        break;
-      }
-      {
+      const int tile0 = t_begin + j * kTok;
+      float mx = -INFINITY;
+      if (ok) {
         const float* xr = xbuf + t * kTok;
         for (int v = 0; v < kTok / 4; ++v) {
           const float4 p4 = *reinterpret_cast<const float4*>(xr + (((v ^ (t & 15)) & 15) * 4));
@@ -398,37 +420,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           s[4 * v + 2] += p4.z;
           s[4 * v + 3] += p4.w;
         }
-      }
-      __syncwarp();
-      if (lane == 0) remote_arrive(x_free_peer);
+        __syncwarp();
+        if (lane == 0) remote_arrive(x_free_peer);
 
-      // ---- scale, mask, online softmax (log2 domain, lazy rescale)
-      const int tile0 = t_begin + j * kTok;
-      const bool edge = tile0 + kTok > t_end || tile0 <= row_lb || (a.mask && tile0 + kTok > spec0);
-      float mx = -INFINITY;
+        // ---- scale, mask, online softmax (log2 domain, lazy rescale)
+        const bool edge = tile0 + kTok > t_end || tile0 <= row_lb || (a.mask && tile0 + kTok > spec0);
 #pragma unroll
-      for (int k = 0; k < kTok; ++k) {
-        float x = s[k] * lscale;
-        if (edge) {
-          const int tt = tile0 + k;
-          bool vis = tt < t_end && tt >= row_lb;
-          if (a.mask && tt >= spec0) vis = vis && ((row_mw >> (tt - spec0)) & 1u);
-          x = vis ? x : -INFINITY;
+        for (int k = 0; k < kTok; ++k) {
+          float x = s[k] * lscale;
+          if (edge) {
+            const int tt = tile0 + k;
+            bool vis = tt < t_end && tt >= row_lb;
+            if (a.mask && tt >= spec0) vis = vis && ((row_mw >> (tt - spec0)) & 1u);
+            x = vis ? x : -INFINITY;
+          }
+          s[k] = x;
+          mx = fmaxf(mx, x);
         }
-        s[k] = x;
-        mx = fmaxf(mx, x);
+        // P and O may be touched only once the previous P.V is done
+        if (j > 0) ok = __all_sync(kAll, mbar_wait(pv_done, (j - 1) & 1));
       }
-      // P and O may be touched only once the previous P.V is done
-      if (j > 0 && !mbar_wait(pv_done, (j - 1) & 1)) {
-        ok = false;
-        break;
-      }
-      umma::fence_after_sync();
-      const float m_new = fmaxf(m_ref, mx);
-      if (m_new > m_ref + kRescaleLog2 || (m_ref == -INFINITY && m_new != -INFINITY)) {
-        if (m_ref != -INFINITY) {
-          const float f = exp2f(m_ref - m_new);
-          l_run *= f;
+      if (ok) {
+        umma::fence_after_sync();
+        const float m_new = fmaxf(m_ref, mx);
+        const bool need = m_new > m_ref + kRescaleLog2 || (m_ref == -INFINITY && m_new != -INFINITY);
+        const float f = (need && m_ref != -INFINITY) ? exp2f(m_ref - m_new) : 1.f;
+        if (__any_sync(kAll, f != 1.f)) {
+          // whole warp rescales its 32 rows of O (factor 1 for rows that keep theirs)
           for (int part = 0; part < kHalf / 32; ++part) {
             float o[32];
             umma::tmem_ld32(tmem + lane_base + kColO + 32u * part, o);
@@ -439,43 +457,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           umma::tmem_st_wait();
         }
-        m_ref = m_new;
-      }
-      // P row t (bf16) into the swizzled K-major P tile
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        uint32_t w4[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = m_ref == -INFINITY ? 0.f : exp2f(s[8 * u + 2 * e] - m_ref);
-          const float p1 = m_ref == -INFINITY ? 0.f : exp2f(s[8 * u + 2 * e + 1] - m_ref);
-          w4[e] = pack_f32x2(p0, p1, true);
-          // the row sum takes the rounded weights, so O / l stays a convex
-          // combination of V rows
-          const float2 r = unpack_16x2(w4[e], true);
-          l_run += r.x + r.y;
+        if (need) {
+          l_run *= f;
+          m_ref = m_new;
         }
-        *reinterpret_cast<uint4*>(smem + kOffP + umma::sw128(t, u)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-      }
-      // V rows past this split's last token hold stale or foreign data: zero them
-      if (tile0 + kTok > t_end) {
-        const int r0 = max(0, t_end - tile0);
-        uint8_t* st = smem + kOffStages + (j % kStages) * kStageBytes;
-        for (int idx = t; idx < (kTok - r0) * 4 * 8; idx += kRows) {
-          const int r = r0 + idx / 32, k = (idx / 8) % 4, u = idx % 8;
-          *reinterpret_cast<uint4*>(st + k * kChunkBytes + r * 128 + u * 16) = make_uint4(0, 0, 0, 0);
+        // P row t (bf16) into the swizzled K-major P tile
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float p0 = m_ref == -INFINITY ? 0.f : exp2f(s[8 * u + 2 * e] - m_ref);
+            const float p1 = m_ref == -INFINITY ? 0.f : exp2f(s[8 * u + 2 * e + 1] - m_ref);
+            w4[e] = pack_f32x2(p0, p1, true);
+            // the row sum takes the rounded weights, so O / l stays a convex
+            // combination of V rows
+            const float2 r = unpack_16x2(w4[e], true);
+            l_run += r.x + r.y;
+          }
+          *reinterpret_cast<uint4*>(smem + kOffP + umma::sw128(t, u)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
+        // V rows past this split's last token hold stale or foreign data: zero them
+        if (tile0 + kTok > t_end) {
+          const int r0 = max(0, t_end - tile0);
+          uint8_t* st = smem + kOffStages + (j % kStages) * kStageBytes;
+          for (int idx = t; idx < (kTok - r0) * 4 * 8; idx += kRows) {
+            const int r = r0 + idx / 32, k = (idx / 8) % 4, u = idx % 8;
+            *reinterpret_cast<uint4*>(st + k * kChunkBytes + r * 128 + u * 16) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        umma::fence_proxy_async_smem();
+        umma::fence_before_sync();
       }
-      umma::fence_proxy_async_smem();
-      umma::fence_before_sync();
-      named_bar(1, kRows);  // every softmax thread finished P (and the V tail)
+      // every softmax thread finished P (and the V tail), or someone gave up
+      if (named_bar_or(1, kRows, !ok)) {
+        ok = false;
+        break;
+      }
       if (lane == 0) mbar_arrive(p_full);
     }
     if (!ok) flags[0] = 1;
 
     // ---- epilogue: wait for the last P.V, then finalise or write the partial
-    bool have_o = ntiles > 0;
-    if (have_o && ok && !mbar_wait(pv_done, (ntiles - 1) & 1)) {
+    const bool have_o = ntiles > 0;
+    if (have_o && ok && !__all_sync(kAll, mbar_wait(pv_done, (ntiles - 1) & 1))) {
       flags[0] = 1;
       ok = false;
     }

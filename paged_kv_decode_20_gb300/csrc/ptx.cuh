@@ -132,5 +132,19 @@ __device__ __forceinline__ float2 unpack_16x2(uint32_t v, bool bf16) {
 __device__ __forceinline__ void named_bar(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
+// Named barrier that also returns the OR of `v` over the participating threads
+// (the same value in every thread, so a loop can be left collectively).
+__device__ __forceinline__ bool named_bar_or(int id, int threads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %3, 0;\n\t"
+      "bar.red.or.pred po, %1, %2, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"(id), "r"(threads), "r"(uint32_t(v))
+      : "memory");
+  return r != 0;
+}
 
 }  // namespace xqa
