@@ -60,6 +60,16 @@ def dist_env():
     return ws, rank, local
 
 
+def reduce_max(x, device=None):
+    """Max of a float over all ranks (identity without torch.distributed)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -203,12 +213,8 @@ def run_gb300(args):
         torch.cuda.nvtx.range_pop()
     if world > 1:
         dist.barrier()
-    total_ms = t0.elapsed_time(t1)
+    total_ms = reduce_max(t0.elapsed_time(t1), dev)
     launch_ms = [a.elapsed_time(b) for a, b in ev]
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
     ms_per_step = total_ms / args.steps
     avg_launch_ms = sum(launch_ms) / len(launch_ms)
 
@@ -242,11 +248,7 @@ def run_gb300(args):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        e_ms = e0.elapsed_time(e1) / e_steps
-        if world > 1:
-            tt = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e_ms = float(tt.item())
+        e_ms = reduce_max(e0.elapsed_time(e1) / e_steps, dev)
         e2e = {"value": round(kv_bytes * world / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "ms_per_step": round(e_ms, 4), "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h}
