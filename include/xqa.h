@@ -133,6 +133,26 @@ size_t xqa_mla_semaphore_count(const xqa_params* params, int v_head_dim);
 xqa_status xqa_mla_decode(const xqa_params* params, int v_head_dim, void* workspace,
                           size_t workspace_bytes, uint32_t* semaphores, xqa_stream_t stream);
 
+/* xqa_decode without caller-provided scratch.  The pages have no counterpart:
+   the XQA call always takes workspace_buffer and semaphores from its caller.
+   This variant is for callers that may not allocate device memory where they
+   call decode attention (for example a runtime that has reserved the device's
+   memory for its own KV-cache pool, or code whose allocator lives elsewhere):
+   it uses a scratch array built into the library instead -- 64 MiB of split
+   workspace and 16384 tickets, held on every GPU that loads the library until
+   the process exits.  It never calls cudaMalloc or cudaFree.
+   - The first call on a device looks up that device's scratch address
+     (cudaGetSymbolAddress); make that first call before any stream capture.
+   - Problems whose workspace or ticket count exceed the built-in sizes are
+     rejected with XQA_ERR_WORKSPACE_TOO_SMALL (see xqa_last_error) before
+     anything is launched; use xqa_decode with your own buffers for them.
+   - Every call on a device shares the one array.  Calls whose executions
+     overlap on the GPU (different streams, different threads) race on it and
+     produce wrong results; serialise them.  Each call clears the tickets it
+     needs on `stream` before launching; the workspace keeps the last call's
+     contents, which no call reads before writing. */
+xqa_status xqa_decode_noalloc(const xqa_params* params, xqa_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* xqa_status_string(xqa_status status);
 

@@ -19,6 +19,7 @@
 #include "kernel_args.h"
 #include "mla_launch.h"
 #include "xqa.h"
+#include "xqa_internal.h"
 
 namespace {
 
@@ -286,6 +287,10 @@ xqa_status check_buffers(const Plan& pl, void* ws, size_t ws_bytes, uint32_t* se
 }
 
 }  // namespace
+
+namespace xqa {
+void set_last_error(const char* msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+}  // namespace xqa
 
 extern "C" {
 

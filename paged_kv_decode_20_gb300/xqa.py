@@ -66,7 +66,8 @@ class XqaParams(ctypes.Structure):
 
 
 EXPORTS = ["xqa_workspace_size", "xqa_semaphore_count", "xqa_decode", "xqa_mla_workspace_size",
-           "xqa_mla_semaphore_count", "xqa_mla_decode", "xqa_status_string", "xqa_last_error"]
+           "xqa_mla_semaphore_count", "xqa_mla_decode", "xqa_decode_noalloc", "xqa_status_string",
+           "xqa_last_error"]
 
 _lock = threading.Lock()
 _lib = None
