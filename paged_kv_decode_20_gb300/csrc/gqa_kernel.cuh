@@ -347,8 +347,8 @@ __global__ void __launch_bounds__(160, 2)
 #pragma unroll
               for (int x = 0; x < 4; ++x) {
                 const int nt = 2 * kb + (x & 1), kc = 2 * kc2 + (x >> 1);
-                const uint32_t b01 = e4m3x2_to_f16x2(r[x] & 0xffffu);
-                const uint32_t b23 = e4m3x2_to_f16x2(r[x] >> 16);
+                uint32_t b01, b23;
+                e4m3x4_to_f16x2x2(r[x], b01, b23);
 #pragma unroll
                 for (int rb = 0; rb < RB; ++rb) mma16816<false>(sacc[rb][nt], qa[rb][kc], b01, b23);
               }
@@ -480,12 +480,19 @@ __global__ void __launch_bounds__(160, 2)
                 w[k] = tv[k] ? x : 0u;
               }
 #pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                const uint32_t sel = uint32_t(c) | (uint32_t(c + 4) << 4);
-                const uint32_t b01 = e4m3x2_to_f16x2(prmt(w[0], w[1], sel) & 0xffffu);
-                const uint32_t b23 = e4m3x2_to_f16x2(prmt(w[2], w[3], sel) & 0xffffu);
+              for (int cp = 0; cp < 2; ++cp) {
+                // bytes (c, c) of tokens (0, 1) and of tokens (2, 3) for columns
+                // c = 2cp and 2cp + 1: one permute feeds two conversions
+                const uint32_t c0 = 2 * cp, c1 = 2 * cp + 1;
+                const uint32_t sel = c0 | ((c0 + 4) << 4) | (c1 << 8) | ((c1 + 4) << 12);
+                uint32_t b01_c0, b01_c1, b23_c0, b23_c1;
+                e4m3x4_to_f16x2x2(prmt(w[0], w[1], sel), b01_c0, b01_c1);
+                e4m3x4_to_f16x2x2(prmt(w[2], w[3], sel), b23_c0, b23_c1);
 #pragma unroll
-                for (int rb = 0; rb < RB; ++rb) mma16816<false>(o[rb][4 * j4 + c], pa[rb][kb], b01, b23);
+                for (int rb = 0; rb < RB; ++rb) {
+                  mma16816<false>(o[rb][4 * j4 + c0], pa[rb][kb], b01_c0, b23_c0);
+                  mma16816<false>(o[rb][4 * j4 + c1], pa[rb][kb], b01_c1, b23_c1);
+                }
               }
             }
           }

@@ -16,7 +16,8 @@
 //   S_c = Q_c K_c^T (tcgen05.mma, A = its latent query half held in tensor
 //   memory, B = K from shared memory; CTA 0 adds the rope part with A from
 //   shared memory), and sends S_c to its peer through distributed shared
-//   memory (st.async completing on the peer's mbarrier).  Both CTAs then hold
+//   memory (remote stores, then one release-arrive per warp on the peer's
+//   mbarrier).  Both CTAs then hold
 //   the same S = S_0 + S_1 and run the same online softmax (128 threads, one
 //   row each), so their running maxima agree without further traffic.
 //   P (bf16) goes to shared memory and CTA c accumulates O_c += P V_c into
@@ -105,12 +106,14 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
 }
-__device__ __forceinline__ void st_async_v4(uint32_t raddr, float a, float b, float c, float d,
-                                            uint32_t rbar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1,%2,%3,%4}, [%5];" ::"r"(raddr),
-      "f"(a), "f"(b), "f"(c), "f"(d), "r"(rbar)
-      : "memory");
+// Plain store into the peer CTA's shared memory (no per-store barrier traffic).
+__device__ __forceinline__ void st_remote_v4(uint32_t raddr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(raddr), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+__device__ __forceinline__ void fence_cluster() {
+  asm volatile("fence.acq_rel.cluster;" ::: "memory");
 }
 __device__ __forceinline__ void remote_arrive(uint32_t rbar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar) : "memory");
@@ -150,7 +153,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* s_free = s_full + 2;            // [2]
   uint64_t* p_full = s_free + 2;
   uint64_t* pv_done = p_full + 1;
-  uint64_t* x_full = pv_done + 1;           // the peer's partial landed in my buffer
+  uint64_t* x_full = pv_done + 1;           // the peer's partial is in my buffer
   uint64_t* x_free = x_full + 1;            // the peer has read my previous partial
   uint64_t* mma_drain = x_free + 1;         // every MMA this CTA issued has finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
@@ -193,7 +196,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&s_free[1], 4);
     mbar_init(p_full, 4);
     mbar_init(pv_done, 1);
-    mbar_init(x_full, 1);
+    mbar_init(x_full, 4);  // the peer's four softmax warps
     mbar_init(x_free, 4);
     mbar_init(mma_drain, 1);
     flags[0] = flags[1] = 0;
@@ -404,9 +407,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int v = 0; v < kTok / 4; ++v) {
           // 16-byte unit v of the row, XOR-swizzled by row to spread banks
           const uint32_t off = uint32_t(((v ^ (t & 15)) & 15) * 16);
-          st_async_v4(xrow_peer + off, s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3], x_full_peer);
+          st_remote_v4(xrow_peer + off, s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3]);
         }
-        if (t == 0) mbar_arrive_expect_tx(x_full, uint32_t(kRows * kTok * 4));
+        // publish this warp's rows to the peer: one release-arrive per warp
+        fence_cluster();
+        __syncwarp();
+        if (lane == 0) remote_arrive(x_full_peer);
         ok = __all_sync(kAll, wait_cluster(x_full, j & 1));
       }
       const int tile0 = t_begin + j * kTok;
