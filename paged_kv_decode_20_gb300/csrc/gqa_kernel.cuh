@@ -83,6 +83,11 @@ __global__ void __launch_bounds__(160, 2)
   const int kvh = blockIdx.y / a.rg_count, rg = blockIdx.y % a.rg_count;
   const int b = blockIdx.z;
 
+  // Inputs may come from the previous kernel in the stream: wait for it before
+  // the first global access, then let the next decode call start launching.
+  pdl_wait();
+  pdl_launch_dependents();
+
   // ---- sequence geometry (identical in every CTA of this (b, kvh, rg))
   const int64_t max_len = int64_t(a.pps) * a.ps;
   const int64_t len_raw = a.seq_lens[b];
@@ -542,7 +547,7 @@ __global__ void __launch_bounds__(160, 2)
   const float out_mul = kv_scale * a.rcp_out_scale;
   const bool single = nvalid <= 1;
   const int rows_here = min(C::kRows, a.R - rg * C::kRows);
-  const int row_stride = D + 2;
+  const int row_stride = D + 4;  // O, then m and l; padded so rows stay 16-byte aligned
   float* ws_unit = a.ws + (int64_t(unit) * a.nsplit) * C::kRows * row_stride;
   uint16_t* out16 = static_cast<uint16_t*>(a.out);
   const bool obf = a.q_bf16 != 0;
@@ -601,35 +606,69 @@ __global__ void __launch_bounds__(160, 2)
   __syncthreads();
   if (!flags[1]) return;
   __threadfence();
-  for (int idx = tid; idx < rows_here * (D / 2); idx += C::kThreads) {
-    const int row = idx / (D / 2);
-    const int dv = 2 * (idx % (D / 2));
+  // phase 1: one thread per row folds the split maxima, the sink and the
+  // output scales into one weight per (row, split), staged in shared memory
+  // (the stage ring is free again)
+  float* wts = reinterpret_cast<float*>(smem);  // [rows][nvalid]
+  if (tid < rows_here) {
+    const int row = tid;
     float M = -INFINITY;
     for (int sp = 0; sp < nvalid; ++sp)
       M = fmaxf(M, __ldcg(ws_unit + (int64_t(sp) * C::kRows + row) * row_stride + D));
-    float o0 = 0.f, o1 = 0.f, l = 0.f;
+    float l = 0.f;
     for (int sp = 0; sp < nvalid; ++sp) {
-      const float* src = ws_unit + (int64_t(sp) * C::kRows + row) * row_stride;
-      const float ms = __ldcg(src + D);
+      const float* src = ws_unit + (int64_t(sp) * C::kRows + row) * row_stride + D;
+      const float ms = __ldcg(src);
       const float f = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-      o0 += f * __ldcg(src + dv);
-      o1 += f * __ldcg(src + dv + 1);
-      l += f * __ldcg(src + D + 1);
+      wts[row * nvalid + sp] = f;
+      l += f * __ldcg(src + 1);
+    }
+    const int r = rg * C::kRows + row;
+    const float sig = a.sinks ? __ldg(a.sinks + kvh * a.G + r % a.G) * kLog2e : -INFINITY;
+    const float Mf = fmaxf(M, sig);
+    float mul = 0.f;
+    if (Mf != -INFINITY) {
+      const float f = (M == -INFINITY) ? 0.f : exp2f(M - Mf);
+      mul = f * out_mul / (l * f + ((sig == -INFINITY) ? 0.f : exp2f(sig - Mf)));
+    }
+    for (int sp = 0; sp < nvalid; ++sp) wts[row * nvalid + sp] *= mul;
+  }
+  __syncthreads();
+  // phase 2: every (row, 4-column group) sums the weighted partials
+  const int64_t sstride = int64_t(C::kRows) * row_stride;
+  for (int item = tid; item < rows_here * (D / 4); item += C::kThreads) {
+    const int row = item / (D / 4);
+    const int dv = 4 * (item % (D / 4));
+    const float* w = wts + row * nvalid;
+    const float* src = ws_unit + int64_t(row) * row_stride + dv;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int sp = 0;
+    for (; sp + 4 <= nvalid; sp += 4) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = __ldcg(reinterpret_cast<const float4*>(src + (sp + u) * sstride));
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float f = w[sp + u];
+        acc.x += f * v[u].x;
+        acc.y += f * v[u].y;
+        acc.z += f * v[u].z;
+        acc.w += f * v[u].w;
+      }
+    }
+    for (; sp < nvalid; ++sp) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(src + sp * sstride));
+      const float f = w[sp];
+      acc.x += f * v.x;
+      acc.y += f * v.y;
+      acc.z += f * v.z;
+      acc.w += f * v.w;
     }
     const int r = rg * C::kRows + row;
     const int i = r / a.G, gg = r % a.G;
-    const float sig = a.sinks ? __ldg(a.sinks + kvh * a.G + gg) * kLog2e : -INFINITY;
-    const float Mf = fmaxf(M, sig);
-    float v0 = 0.f, v1 = 0.f;
-    if (Mf != -INFINITY) {
-      const float f = (M == -INFINITY) ? 0.f : exp2f(M - Mf);
-      const float den = l * f + ((sig == -INFINITY) ? 0.f : exp2f(sig - Mf));
-      const float mul = f * out_mul / den;
-      v0 = o0 * mul;
-      v1 = o1 * mul;
-    }
     const int64_t oi = ((int64_t(b) * a.qs + i) * a.Hq + int64_t(kvh) * a.G + gg) * a.Dv + dv;
-    *reinterpret_cast<uint32_t*>(out16 + oi) = pack_f32x2(v0, v1, obf);
+    *reinterpret_cast<uint2*>(out16 + oi) =
+        make_uint2(pack_f32x2(acc.x, acc.y, obf), pack_f32x2(acc.z, acc.w, obf));
   }
   if (tid == 0) a.sems[unit] = 0u;
 }

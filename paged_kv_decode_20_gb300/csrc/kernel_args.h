@@ -29,6 +29,7 @@ struct DecodeArgs {
   float q_scale, kv_scale, softmax_scale, rcp_out_scale;
   int q_bf16;                  // q and out are bf16 (else f16)
   int hnd;                     // cache layout HND (else NHD)
+  int pdl;                     // launched with programmatic stream serialization
 };
 
 }  // namespace xqa

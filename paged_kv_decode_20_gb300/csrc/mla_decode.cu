@@ -73,6 +73,7 @@ constexpr uint32_t kColQ = 256;   // 128 columns: latent query half, bf16 pairs
 constexpr uint32_t kColS = 384;   // 2 x 64 columns: logits double buffer
 
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by > 2^8
+constexpr int kMaxSplits = 64;       // merge weights [128][splits] fit in shared memory
 
 struct MlaArgs {
   const uint16_t* q;  // [B, qs, Hq, 576]
@@ -164,6 +165,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t peer = c ^ 1u;
   const int split = blockIdx.x >> 1;
   const int b = blockIdx.z;
+
+  // wait for the producer of our inputs, then let the next call start launching
+  pdl_wait();
+  pdl_launch_dependents();
 
   // ---- sequence geometry (identical in both CTAs and every split)
   const int64_t max_len = int64_t(a.pps) * a.ps;
@@ -579,35 +584,68 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (!flags[1]) return;
   __threadfence();
   const float kv_scale = ldscale(a.kv_scale_dev, a.kv_scale);
-  const int64_t ws_b = int64_t(b) * a.nsplit * kRows * (kLatent + 4);
-  for (int idx = tid; idx < kRows * (kHalf / 2); idx += kThreads) {
-    const int row = idx / (kHalf / 2);
-    const int col = int(c) * kHalf + 2 * (idx % (kHalf / 2));
+  constexpr int kStride = kLatent + 4;
+  const float* ws_b = a.ws + int64_t(b) * a.nsplit * kRows * kStride;
+  // phase 1: one thread per row folds the split maxima, the sink and the
+  // output scales into one weight per (row, split), staged in shared memory
+  float* wts = reinterpret_cast<float*>(smem);  // [kRows][nvalid]
+  if (tid < kRows) {
+    const int row = tid;
     float M = -INFINITY;
     for (int sp = 0; sp < nvalid; ++sp)
-      M = fmaxf(M, __ldcg(a.ws + ws_b + (int64_t(sp) * kRows + row) * (kLatent + 4) + kLatent + 2 * c));
-    float o0 = 0.f, o1 = 0.f, l = 0.f;
+      M = fmaxf(M, __ldcg(ws_b + (int64_t(sp) * kRows + row) * kStride + kLatent + 2 * c));
+    float l = 0.f;
     for (int sp = 0; sp < nvalid; ++sp) {
-      const float* src = a.ws + ws_b + (int64_t(sp) * kRows + row) * (kLatent + 4);
-      const float ms = __ldcg(src + kLatent + 2 * c);
+      const float* src = ws_b + (int64_t(sp) * kRows + row) * kStride + kLatent + 2 * c;
+      const float ms = __ldcg(src);
       const float f = ms == -INFINITY ? 0.f : exp2f(ms - M);
-      o0 += f * __ldcg(src + col);
-      o1 += f * __ldcg(src + col + 1);
-      l += f * __ldcg(src + kLatent + 2 * c + 1);
+      wts[row * nvalid + sp] = f;
+      l += f * __ldcg(src + 1);
     }
-    const int ii = row / a.Hq, hh = row % a.Hq;
-    const float sig = a.sinks ? __ldg(a.sinks + hh) * kLog2e : -INFINITY;
+    const float sig = a.sinks ? __ldg(a.sinks + row % a.Hq) * kLog2e : -INFINITY;
     const float Mf = fmaxf(M, sig);
-    float v0 = 0.f, v1 = 0.f;
+    float mul = 0.f;
     if (Mf != -INFINITY) {
       const float f = M == -INFINITY ? 0.f : exp2f(M - Mf);
-      const float den = l * f + (sig == -INFINITY ? 0.f : exp2f(sig - Mf));
-      const float mul = f * kv_scale * a.rcp_out_scale / den;
-      v0 = o0 * mul;
-      v1 = o1 * mul;
+      mul = f * kv_scale * a.rcp_out_scale / (l * f + (sig == -INFINITY ? 0.f : exp2f(sig - Mf)));
     }
+    for (int sp = 0; sp < nvalid; ++sp) wts[row * nvalid + sp] *= mul;
+  }
+  __syncthreads();
+  // phase 2: every (row, 4-column group) sums the weighted partials
+  for (int item = tid; item < kRows * (kHalf / 4); item += kThreads) {
+    const int row = item / (kHalf / 4);
+    const int col = int(c) * kHalf + 4 * (item % (kHalf / 4));
+    const float* w = wts + row * nvalid;
+    const float* src = ws_b + int64_t(row) * kStride + col;
+    const int64_t sstride = int64_t(kRows) * kStride;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int sp = 0;
+    for (; sp + 4 <= nvalid; sp += 4) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = __ldcg(reinterpret_cast<const float4*>(src + (sp + u) * sstride));
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float f = w[sp + u];
+        acc.x += f * v[u].x;
+        acc.y += f * v[u].y;
+        acc.z += f * v[u].z;
+        acc.w += f * v[u].w;
+      }
+    }
+    for (; sp < nvalid; ++sp) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(src + sp * sstride));
+      const float f = w[sp];
+      acc.x += f * v.x;
+      acc.y += f * v.y;
+      acc.z += f * v.z;
+      acc.w += f * v.w;
+    }
+    const int ii = row / a.Hq, hh = row % a.Hq;
     const int64_t oi = ((int64_t(b) * a.qs + ii) * a.Hq + hh) * kLatent + col;
-    *reinterpret_cast<uint32_t*>(a.out + oi) = pack_f32x2(v0, v1, true);
+    *reinterpret_cast<uint2*>(a.out + oi) =
+        make_uint2(pack_f32x2(acc.x, acc.y, true), pack_f32x2(acc.z, acc.w, true));
   }
   if (tid == 0) a.sems[unit] = 0u;
 }
@@ -673,6 +711,7 @@ bool plan(const xqa_params* p, int sm_count, Plan* pl) {
   const int64_t by_tiles = (max_pages + stage_pages - 1) / stage_pages;
   const int64_t by_tokens = std::max<int64_t>(1, int64_t(max_pages) * p->page_size / 1024);
   ns = std::max<int64_t>(1, std::min(ns, std::min(by_tiles, by_tokens)));
+  ns = std::min<int64_t>(ns, kMaxSplits);
   int sp = int((max_pages + ns - 1) / ns);
   sp = ((sp + stage_pages - 1) / stage_pages) * stage_pages;
   pl->split_pages = sp;
@@ -781,9 +820,17 @@ xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_b
     snprintf(err, err_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     return XQA_ERR_CUDA;
   }
-  dim3 grid(2 * pl.nsplit, 1, p->batch_size);
-  mla_decode_kernel<<<grid, kThreads, kSmem, stream>>>(tm, a);
-  e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pl.nsplit, 1, p->batch_size);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = p->enable_pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, mla_decode_kernel, tm, a);
   if (e != cudaSuccess) {
     snprintf(err, err_len, "MLA kernel launch: %s", cudaGetErrorString(e));
     return XQA_ERR_CUDA;

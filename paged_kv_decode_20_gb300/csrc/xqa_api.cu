@@ -59,6 +59,7 @@ EncodeTiledFn encode_tiled() {
 
 // ---------------------------------------------------------------- device facts
 constexpr int kMaxDevices = 64;
+constexpr int kMaxSplits = 64;  // merge weights [rows][splits] fit in the kernel's shared memory
 
 int device_sm_count(int dev) {
   static int cache[kMaxDevices] = {0};
@@ -152,6 +153,7 @@ void choose_splits(const xqa_params* p, Plan* pl, int sm_count, int ctas_per_sm,
   const int64_t by_stage = (max_pages + stage_pages - 1) / stage_pages;
   const int64_t by_tokens = std::max<int64_t>(1, (int64_t(max_pages) * p->page_size) / 256);
   ns = std::max<int64_t>(1, std::min(ns, std::min(by_stage, by_tokens)));
+  ns = std::min<int64_t>(ns, kMaxSplits);
   int sp = int((max_pages + ns - 1) / ns);
   sp = ((sp + stage_pages - 1) / stage_pages) * stage_pages;
   pl->split_pages = sp;
@@ -194,7 +196,7 @@ xqa_status plan_gqa(const xqa_params* p, int sm_count_in, Plan* pl) {
   choose_splits(p, pl, sm, occ, stage_pages);
   const int64_t units = int64_t(p->batch_size) * p->num_kv_heads * pl->rg_count;
   pl->nsems = size_t(units);
-  pl->ws_bytes = pl->nsplit > 1 ? size_t(units) * pl->nsplit * pl->rows * (D + 2) * sizeof(float) : 0;
+  pl->ws_bytes = pl->nsplit > 1 ? size_t(units) * pl->nsplit * pl->rows * (D + 4) * sizeof(float) : 0;
   return XQA_OK;
 }
 
@@ -272,6 +274,7 @@ void fill_args(const xqa_params* p, const Plan& pl, void* ws, uint32_t* sems, xq
   a->rcp_out_scale = p->rcp_out_scale;
   a->q_bf16 = p->q_dtype == XQA_BF16;
   a->hnd = p->kv_layout == XQA_HND;
+  a->pdl = p->enable_pdl != 0;
 }
 
 xqa_status check_buffers(const Plan& pl, void* ws, size_t ws_bytes, uint32_t* sems) {
