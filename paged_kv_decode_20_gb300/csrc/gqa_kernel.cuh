@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(160, 2)
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const float mm = m_run[rb][e >> 1];
-                p[h2][e] = (mm == -INFINITY) ? 0.f : exp2f(sacc[rb][2 * kb + h2][e] - mm);
+                p[h2][e] = (mm == -INFINITY) ? 0.f : ex2(sacc[rb][2 * kb + h2][e] - mm);
               }
             pa[rb][kb][0] = pack_f32x2(p[0][0], p[0][1], kMmaBf16);
             pa[rb][kb][1] = pack_f32x2(p[0][2], p[0][3], kMmaBf16);

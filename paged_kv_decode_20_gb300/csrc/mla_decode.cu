@@ -54,17 +54,22 @@ constexpr int kTok = 64;         // tokens per tile (UMMA N of QK, K of PV)
 constexpr int kChunkBytes = kTok * 128;  // one 64-element column chunk of a tile
 constexpr int kMaxChunks = 5;    // CTA 0: 4 latent + 1 rope chunk
 constexpr int kStageBytes = kMaxChunks * kChunkBytes;  // 40 KB
-constexpr int kStages = 4;
-constexpr int kThreads = 256;
+constexpr int kStages = 3;
+constexpr int kSoftWarps = 8;    // two threads per query row, 32 logit columns each
+constexpr int kSoft = 32 * kSoftWarps;
+constexpr int kThreads = 128 + kSoft;
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int kOffStages = 0;
 constexpr int kOffQRope = kOffStages + kStages * kStageBytes;  // 128 x 64 bf16
 constexpr int kOffP = kOffQRope + kRows * 128;                  // 128 x 64 bf16
-constexpr int kOffX = kOffP + kRows * 128;                      // 128 x 64 fp32 (peer partial)
-constexpr int kOffBar = kOffX + kRows * kTok * 4;
+constexpr int kOffRecv = kOffP + kRows * 128;                   // 128 x 64 fp32: peer's partial
+constexpr int kOffSend = kOffRecv + kRows * kTok * 4;           // 128 x 64 fp32: own partial
+constexpr int kOffRowX = kOffSend + kRows * kTok * 4;           // [2][128] fp32: row max / sum halves
+constexpr int kOffBar = kOffRowX + 2 * kRows * 4;
 constexpr int kNumBars = 2 * kStages + 10;
 constexpr int kSmem = 1024 + kOffBar + kNumBars * 8 + 32;
+static_assert(kSmem <= 232448, "shared memory budget");
 
 // tensor memory columns
 constexpr uint32_t kTmemCols = 512;
@@ -107,14 +112,15 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
 }
-// Plain store into the peer CTA's shared memory (no per-store barrier traffic).
-__device__ __forceinline__ void st_remote_v4(uint32_t raddr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(raddr), "f"(a), "f"(b), "f"(c),
-               "f"(d)
-               : "memory");
-}
-__device__ __forceinline__ void fence_cluster() {
-  asm volatile("fence.acq_rel.cluster;" ::: "memory");
+// One bulk copy of `bytes` from this CTA's shared memory into the peer's,
+// completing that many transaction bytes on the peer's mbarrier.
+__device__ __forceinline__ void bulk_to_peer(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                             uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_cluster),
+      "r"(src_cta), "r"(bytes), "r"(bar_cluster)
+      : "memory");
 }
 __device__ __forceinline__ void remote_arrive(uint32_t rbar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar) : "memory");
@@ -141,6 +147,9 @@ __device__ __forceinline__ bool wait_cluster(uint64_t* bar, uint32_t parity) {
 
 __device__ __forceinline__ float ldscale(const float* dev, float host) { return dev ? __ldg(dev) : host; }
 
+// 16-byte unit u (0..15) of row t of a 128 x 64 fp32 buffer, XOR-swizzled by row.
+__device__ __forceinline__ int xunit(int t, int u) { return t * kTok + ((u ^ (t & 15)) & 15) * 4; }
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tmKV, const MlaArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -154,7 +163,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* s_free = s_full + 2;            // [2]
   uint64_t* p_full = s_free + 2;
   uint64_t* pv_done = p_full + 1;
-  uint64_t* x_full = pv_done + 1;           // the peer's partial is in my buffer
+  uint64_t* x_full = pv_done + 1;           // the peer's partial is in my receive buffer
   uint64_t* x_free = x_full + 1;            // the peer has read my previous partial
   uint64_t* mma_drain = x_free + 1;         // every MMA this CTA issued has finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
@@ -194,15 +203,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
-    mbar_init(q_ready, 4);
+    mbar_init(q_ready, kSoftWarps);
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
-    mbar_init(&s_free[0], 4);
-    mbar_init(&s_free[1], 4);
-    mbar_init(p_full, 4);
+    mbar_init(&s_free[0], kSoftWarps);
+    mbar_init(&s_free[1], kSoftWarps);
+    mbar_init(p_full, kSoftWarps);
     mbar_init(pv_done, 1);
-    mbar_init(x_full, 4);  // the peer's four softmax warps
-    mbar_init(x_free, 4);
+    mbar_init(x_full, 1);  // own expect-tx arrival + the peer's bulk copy bytes
+    mbar_init(x_free, 1);  // one remote arrival from the peer per tile
     mbar_init(mma_drain, 1);
     flags[0] = flags[1] = 0;
     fence_mbar_init();
@@ -220,7 +229,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t stage0 = smem_u32(smem + kOffStages);
   const uint32_t qrope = smem_u32(smem + kOffQRope);
   const uint32_t pbuf = smem_u32(smem + kOffP);
-  float* xbuf = reinterpret_cast<float*>(smem + kOffX);
 
   if (warp == 0) {
     // ================= TMA producer (warp fetches page indices, lane 0 issues)
@@ -339,19 +347,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ================= softmax / exchange / epilogue =================
-    const int t = tid - 128;  // row = TMEM lane
-    const uint32_t lane_base = uint32_t(32 * (warp - 4)) << 16;
-    const int i = t / a.Hq, h = t % a.Hq;  // row t = (spec token i, head h)
+    // Warp 4 + 4h + q reaches TMEM lanes 32q..32q+31 (query rows) and handles
+    // logit columns [32h, 32h + 32) of every tile and O columns [128h, 128h+128).
+    const int q4 = (warp - 4) & 3, h = (warp - 4) >> 2;
+    const int t = 32 * q4 + lane;  // query row = TMEM lane
+    const int st = tid - 128;      // 0 .. kSoft - 1
+    const uint32_t lane_base = uint32_t(32 * q4) << 16;
+    const int i = t / a.Hq, hd = t % a.Hq;  // row t = (spec token i, head hd)
     const float q_scale = ldscale(a.q_scale_dev, a.q_scale);
     const float kv_scale = ldscale(a.kv_scale_dev, a.kv_scale);
     const float lscale = a.softmax_scale * q_scale * kv_scale * kLog2e;
-    const bool qbf = a.q_bf16 != 0;
+    float* recv = reinterpret_cast<float*>(smem + kOffRecv);
+    float* send = reinterpret_cast<float*>(smem + kOffSend);
+    float* rowx = reinterpret_cast<float*>(smem + kOffRowX);  // [2][128]
 
-    // ---- query: latent half into tensor memory, rope into shared memory (CTA 0)
+    // ---- query: this thread's half of the row's latent half into tensor
+    // memory; the rope part into shared memory (CTA 0)
     {
       const uint16_t* qrow = a.q + (int64_t(b) * a.qs * a.Hq + t) * kDim;
-      const uint4* src = reinterpret_cast<const uint4*>(qrow + c * kHalf);
-      for (int part = 0; part < 4; ++part) {  // 4 x 32 columns = 256 bf16
+      const uint4* src = reinterpret_cast<const uint4*>(qrow + c * kHalf + 128 * h);
+      for (int part = 0; part < 2; ++part) {  // 2 x 32 columns = 128 bf16
         uint32_t w[32];
         for (int v = 0; v < 8; ++v) {
           const uint4 x = __ldg(src + part * 8 + v);
@@ -360,11 +375,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           w[4 * v + 2] = x.z;
           w[4 * v + 3] = x.w;
         }
-        umma::tmem_st32(tmem + lane_base + kColQ + 32u * part, w);
+        umma::tmem_st32(tmem + lane_base + kColQ + 64u * h + 32u * part, w);
       }
       if (c == 0) {
         const uint4* rsrc = reinterpret_cast<const uint4*>(qrow + kLatent);
-        for (int u = 0; u < 8; ++u)
+        for (int u = 4 * h; u < 4 * h + 4; ++u)
           *reinterpret_cast<uint4*>(smem + kOffQRope + umma::sw128(t, u)) = __ldg(rsrc + u);
       }
       umma::tmem_st_wait();
@@ -373,7 +388,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(q_ready);
     }
-    (void)qbf;
 
     // per-row visibility
     const int row_lb = a.win > 0 ? spec0 + i - a.win + 1 : INT_MIN;
@@ -385,62 +399,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     const uint32_t x_full_peer = map_peer(smem_u32(x_full), peer);
     const uint32_t x_free_peer = map_peer(smem_u32(x_free), peer);
-    const uint32_t xrow_peer = map_peer(smem_u32(xbuf + t * kTok), peer);
-    float m_ref = -INFINITY, l_run = 0.f;
+    const uint32_t recv_peer = map_peer(smem_u32(recv), peer);
+    const uint32_t send_cta = smem_u32(send);
+    float m_ref = -INFINITY, l_half = 0.f;
     bool ok = true;
     constexpr unsigned kAll = 0xffffffffu;
+    constexpr int kC = kTok / 2;  // logit columns per thread
 
-    // Control flow below stays uniform across each warp (tcgen05.ld / st are
-    // warp-collective) and across the four softmax warps (named barrier):
-    // waits are voted with __all_sync and the loop is left collectively.
+    // Control flow stays uniform across each warp (tcgen05.ld / st are
+    // warp-collective) and across the eight softmax warps (named barrier 1):
+    // waits are voted and the loop is left collectively.
     for (int j = 0; j < ntiles; ++j) {
       const int sb = j & 1;
-      float s[kTok];
+      float s[kC];
       ok = __all_sync(kAll, mbar_wait(&s_full[sb], (j >> 1) & 1));
       if (ok) {
         umma::fence_after_sync();
-        umma::tmem_ld32(tmem + lane_base + kColS + 64u * sb, s);
-        umma::tmem_ld32(tmem + lane_base + kColS + 64u * sb + 32u, s + 32);
+        umma::tmem_ld32(tmem + lane_base + kColS + 64u * sb + 32u * h, s);
         umma::tmem_ld_wait();
         umma::fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_free[sb]);
-        // ---- exchange partial logits with the peer
-        if (j > 0) ok = __all_sync(kAll, wait_cluster(x_free, (j - 1) & 1));
+        // my send buffer and the peer's receive buffer are free once the peer
+        // has read my previous partial
+        if (j > 0 && st == 0) ok = wait_cluster(x_free, (j - 1) & 1);
       }
-      if (ok) {
-        for (int v = 0; v < kTok / 4; ++v) {
-          // 16-byte unit v of the row, XOR-swizzled by row to spread banks
-          const uint32_t off = uint32_t(((v ^ (t & 15)) & 15) * 16);
-          st_remote_v4(xrow_peer + off, s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3]);
-        }
-        // publish this warp's rows to the peer: one release-arrive per warp
-        fence_cluster();
-        __syncwarp();
-        if (lane == 0) remote_arrive(x_full_peer);
-        ok = __all_sync(kAll, wait_cluster(x_full, j & 1));
+      if (named_bar_or(1, kSoft, !ok)) {
+        ok = false;
+        break;
       }
+      // ---- exchange partial logits: stage mine, one bulk copy to the peer
+      for (int v = 0; v < kC / 4; ++v)
+        *reinterpret_cast<float4*>(send + xunit(t, 8 * h + v)) =
+            make_float4(s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3]);
+      umma::fence_proxy_async_smem();
+      named_bar(1, kSoft);
+      if (st == 0) {
+        mbar_arrive_expect_tx(x_full, uint32_t(kRows * kTok * 4));
+        bulk_to_peer(recv_peer, send_cta, uint32_t(kRows * kTok * 4), x_full_peer);
+      }
+      ok = __all_sync(kAll, wait_cluster(x_full, j & 1));
       const int tile0 = t_begin + j * kTok;
       float mx = -INFINITY;
       if (ok) {
-        const float* xr = xbuf + t * kTok;
-        for (int v = 0; v < kTok / 4; ++v) {
-          const float4 p4 = *reinterpret_cast<const float4*>(xr + (((v ^ (t & 15)) & 15) * 4));
+        const bool edge = tile0 + kTok > t_end || tile0 <= row_lb || (a.mask && tile0 + kTok > spec0);
+#pragma unroll
+        for (int v = 0; v < kC / 4; ++v) {
+          const float4 p4 = *reinterpret_cast<const float4*>(recv + xunit(t, 8 * h + v));
           s[4 * v] += p4.x;
           s[4 * v + 1] += p4.y;
           s[4 * v + 2] += p4.z;
           s[4 * v + 3] += p4.w;
         }
-        __syncwarp();
-        if (lane == 0) remote_arrive(x_free_peer);
-
-        // ---- scale, mask, online softmax (log2 domain, lazy rescale)
-        const bool edge = tile0 + kTok > t_end || tile0 <= row_lb || (a.mask && tile0 + kTok > spec0);
 #pragma unroll
-        for (int k = 0; k < kTok; ++k) {
+        for (int k = 0; k < kC; ++k) {
           float x = s[k] * lscale;
           if (edge) {
-            const int tt = tile0 + k;
+            const int tt = tile0 + 32 * h + k;
             bool vis = tt < t_end && tt >= row_lb;
             if (a.mask && tt >= spec0) vis = vis && ((row_mw >> (tt - spec0)) & 1u);
             x = vis ? x : -INFINITY;
@@ -448,60 +463,69 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           s[k] = x;
           mx = fmaxf(mx, x);
         }
-        // P and O may be touched only once the previous P.V is done
-        if (j > 0) ok = __all_sync(kAll, mbar_wait(pv_done, (j - 1) & 1));
+        rowx[h * kRows + t] = mx;
       }
+      // both halves of every row published their maxima; the receive buffer is read
+      if (named_bar_or(1, kSoft, !ok)) {
+        ok = false;
+        break;
+      }
+      if (st == 0) remote_arrive(x_free_peer);
+      mx = fmaxf(mx, rowx[(1 - h) * kRows + t]);
+      // P and O may be touched only once the previous P.V is done
+      if (j > 0) ok = __all_sync(kAll, mbar_wait(pv_done, (j - 1) & 1));
       if (ok) {
         umma::fence_after_sync();
         const float m_new = fmaxf(m_ref, mx);
         const bool need = m_new > m_ref + kRescaleLog2 || (m_ref == -INFINITY && m_new != -INFINITY);
         const float f = (need && m_ref != -INFINITY) ? exp2f(m_ref - m_new) : 1.f;
         if (__any_sync(kAll, f != 1.f)) {
-          // whole warp rescales its 32 rows of O (factor 1 for rows that keep theirs)
-          for (int part = 0; part < kHalf / 32; ++part) {
+          // whole warp rescales its rows' O half-columns (factor 1 where unchanged)
+          for (int part = 0; part < kHalf / 64; ++part) {
             float o[32];
-            umma::tmem_ld32(tmem + lane_base + kColO + 32u * part, o);
+            const uint32_t col = kColO + 128u * h + 32u * part;
+            umma::tmem_ld32(tmem + lane_base + col, o);
             umma::tmem_ld_wait();
             uint32_t w[32];
             for (int k = 0; k < 32; ++k) w[k] = __float_as_uint(o[k] * f);
-            umma::tmem_st32(tmem + lane_base + kColO + 32u * part, w);
+            umma::tmem_st32(tmem + lane_base + col, w);
           }
           umma::tmem_st_wait();
         }
         if (need) {
-          l_run *= f;
+          l_half *= f;
           m_ref = m_new;
         }
-        // P row t (bf16) into the swizzled K-major P tile
+        // P (bf16) for this thread's 32 columns: units 4h..4h+3 of row t; the
+        // row sum takes the rounded weights so O / l stays a convex combination
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 4; ++u) {
           uint32_t w4[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float p0 = m_ref == -INFINITY ? 0.f : exp2f(s[8 * u + 2 * e] - m_ref);
-            const float p1 = m_ref == -INFINITY ? 0.f : exp2f(s[8 * u + 2 * e + 1] - m_ref);
+            const float p0 = m_ref == -INFINITY ? 0.f : ex2(s[8 * u + 2 * e] - m_ref);
+            const float p1 = m_ref == -INFINITY ? 0.f : ex2(s[8 * u + 2 * e + 1] - m_ref);
             w4[e] = pack_f32x2(p0, p1, true);
-            // the row sum takes the rounded weights, so O / l stays a convex
-            // combination of V rows
             const float2 r = unpack_16x2(w4[e], true);
-            l_run += r.x + r.y;
+            l_half += r.x + r.y;
           }
-          *reinterpret_cast<uint4*>(smem + kOffP + umma::sw128(t, u)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          *reinterpret_cast<uint4*>(smem + kOffP + umma::sw128(t, 4 * h + u)) =
+              make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
         // V rows past this split's last token hold stale or foreign data: zero them
         if (tile0 + kTok > t_end) {
           const int r0 = max(0, t_end - tile0);
-          uint8_t* st = smem + kOffStages + (j % kStages) * kStageBytes;
-          for (int idx = t; idx < (kTok - r0) * 4 * 8; idx += kRows) {
+          uint8_t* stg = smem + kOffStages + (j % kStages) * kStageBytes;
+          for (int idx = st; idx < (kTok - r0) * 4 * 8; idx += kSoft) {
             const int r = r0 + idx / 32, k = (idx / 8) % 4, u = idx % 8;
-            *reinterpret_cast<uint4*>(st + k * kChunkBytes + r * 128 + u * 16) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(stg + k * kChunkBytes + r * 128 + u * 16) = make_uint4(0, 0, 0, 0);
           }
         }
         umma::fence_proxy_async_smem();
         umma::fence_before_sync();
       }
       // every softmax thread finished P (and the V tail), or someone gave up
-      if (named_bar_or(1, kRows, !ok)) {
+      if (named_bar_or(1, kSoft, !ok)) {
         ok = false;
         break;
       }
@@ -516,11 +540,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ok = false;
     }
     umma::fence_after_sync();
+    rowx[h * kRows + t] = l_half;
+    named_bar(1, kSoft);
+    const float l_run = rowx[t] + rowx[kRows + t];
     if (ok) {
       const bool single = nvalid <= 1;
       float mul = 0.f;
       if (single) {
-        const float sig = a.sinks ? __ldg(a.sinks + h) * kLog2e : -INFINITY;
+        const float sig = a.sinks ? __ldg(a.sinks + hd) * kLog2e : -INFINITY;
         const float Mf = fmaxf(m_ref, sig);
         if (Mf != -INFINITY) {
           const float f = m_ref == -INFINITY ? 0.f : exp2f(m_ref - Mf);
@@ -528,17 +555,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           mul = f * kv_scale * a.rcp_out_scale / den;
         }
       }
-      const int64_t row_g = (int64_t(b) * a.qs + i) * a.Hq + h;
+      const int64_t row_g = (int64_t(b) * a.qs + i) * a.Hq + hd;
       float* wrow = a.ws + ((int64_t(b) * a.nsplit + split) * kRows + t) * (kLatent + 4);
-      for (int part = 0; part < kHalf / 32; ++part) {
+      for (int part = 0; part < kHalf / 64; ++part) {
         float o[32];
+        const uint32_t col_t = kColO + 128u * h + 32u * part;
         if (have_o) {
-          umma::tmem_ld32(tmem + lane_base + kColO + 32u * part, o);
+          umma::tmem_ld32(tmem + lane_base + col_t, o);
           umma::tmem_ld_wait();
         } else {
           for (int k = 0; k < 32; ++k) o[k] = 0.f;
         }
-        const int col = int(c) * kHalf + 32 * part;
+        const int col = int(c) * kHalf + 128 * h + 32 * part;
         if (single) {
           uint4* dst = reinterpret_cast<uint4*>(a.out + row_g * kLatent + col);
           for (int v = 0; v < 4; ++v)
@@ -551,7 +579,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int v = 0; v < 8; ++v) dst[v] = make_float4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
         }
       }
-      if (!single) {
+      if (!single && h == 0) {
         wrow[kLatent + 2 * c] = m_ref;
         wrow[kLatent + 2 * c + 1] = l_run;
       }

@@ -147,6 +147,13 @@ __device__ __forceinline__ float2 unpack_16x2(uint32_t v, bool bf16) {
   return __half22float2(*reinterpret_cast<__half2*>(&v));
 }
 
+// 2^x with the hardware approximation (relative error ~2^-22; -inf -> +0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Named barrier over `threads` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
