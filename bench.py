@@ -336,7 +336,7 @@ def cpu_baseline(case, idx, max_rows=None, min_seconds=10.0):
                      (per_b.sum() * case.num_kv_heads))
         sample = f"{len(sel)} of {B * case.num_kv_heads} (sequence, kv head) units, all their rows"
     else:
-        sample = f"all {rows} output rows of the workload, once"
+        sample = f"all {rows} output rows of the workload"
     kw = case.kwargs()
     reps = 0
     t = time.perf_counter()
