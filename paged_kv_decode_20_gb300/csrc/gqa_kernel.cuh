@@ -50,7 +50,9 @@ struct GqaCfg {
   static constexpr int kNumStages = kStage >= 32768 ? 3 : 5;  // 96 KB or 80 KB per CTA
   static constexpr int kRows = 16 * RB;
   static constexpr int kThreads = 160;
-  static constexpr int kScratch = 4 * kRows * D * 4 + 2 * 4 * kRows * 4;
+  // epilogue scratch: per-warp O [4][rows][D], m and l [4][rows], then per-row
+  // weights [rows][4] and the row's (max, sum) for a partial
+  static constexpr int kScratch = 4 * kRows * D * 4 + 2 * 4 * kRows * 4 + 6 * kRows * 4;
   static constexpr int kRing = kNumStages * kStage;
   static_assert(kScratch <= kRing, "epilogue scratch reuses the stage ring");
   static constexpr int kBarOff = kRing;
@@ -122,6 +124,8 @@ __global__ void __launch_bounds__(160, 2)
   float* scratch = reinterpret_cast<float*>(smem);  // epilogue: [4][rows][D] O, then m, l
   float* sc_m = scratch + 4 * C::kRows * D;
   float* sc_l = sc_m + 4 * C::kRows;
+  float* sc_w = sc_l + 4 * C::kRows;  // [rows][4] per-warp weights (scales folded in)
+  float* sc_ml = sc_w + 4 * C::kRows;  // [rows][2] merged (max, sum) of a split partial
 
   if (warp == 4) {
     // ================= producer (whole warp fetches page indices, lane 0 issues TMA)
@@ -168,24 +172,25 @@ __global__ void __launch_bounds__(160, 2)
         }
         if (lane == 0)
           mbar_arrive_expect_tx(&full[slot], uint32_t(n_piece) * box_bytes * 2u * C::kChunks);
-        for (int j = 0; j < n_piece; ++j) {
-          const int page = __shfl_sync(0xffffffffu, my_page, lp0 + j - win_base);
-          if (lane == 0) {
-            bad_page |= page < 0;
-            const int row_off = j * box_rows;
-            for (int c = 0; c < C::kChunks; ++c) {
-              const int off = c * C::kTok * 128 + row_off * 128;
-              if (a.hnd) {
-                tma_load_3d(kdst + off, &tmK, &full[slot], c * kChunkElems, sub, page * a.Hkv + kvh);
-                tma_load_3d(vdst + off, &tmV, &full[slot], c * kChunkElems, sub, page * a.Hkv + kvh);
-              } else {
-                tma_load_3d(kdst + off, &tmK, &full[slot], c * kChunkElems, kvh, page * a.ps + sub);
-                tma_load_3d(vdst + off, &tmV, &full[slot], c * kChunkElems, kvh, page * a.ps + sub);
-              }
+        __syncwarp();
+        // lane j issues the tile loads of page piece j (pieces are independent)
+        const int page = __shfl_sync(0xffffffffu, my_page, (lp0 + lane - win_base) & 31);
+        if (lane < n_piece) {
+          bad_page |= page < 0;
+          const int row_off = lane * box_rows;
+          for (int c = 0; c < C::kChunks; ++c) {
+            const int off = c * C::kTok * 128 + row_off * 128;
+            if (a.hnd) {
+              tma_load_3d(kdst + off, &tmK, &full[slot], c * kChunkElems, sub, page * a.Hkv + kvh);
+              tma_load_3d(vdst + off, &tmV, &full[slot], c * kChunkElems, sub, page * a.Hkv + kvh);
+            } else {
+              tma_load_3d(kdst + off, &tmK, &full[slot], c * kChunkElems, kvh, page * a.ps + sub);
+              tma_load_3d(vdst + off, &tmV, &full[slot], c * kChunkElems, kvh, page * a.ps + sub);
             }
           }
         }
       }
+      bad_page = __any_sync(0xffffffffu, bad_page);
       if (lane == 0) {
         if (bad_page && a.err) atomicOr(a.err, kErrClamped);
         // Leave no copy in flight: wait (bounded) for the last stages issued.
@@ -552,45 +557,66 @@ __global__ void __launch_bounds__(160, 2)
   uint16_t* out16 = static_cast<uint16_t*>(a.out);
   const bool obf = a.q_bf16 != 0;
 
-  for (int idx = tid; idx < rows_here * (D / 2); idx += C::kThreads) {
-    const int row = idx / (D / 2);
-    const int dv = 2 * (idx % (D / 2));
+  // phase 1: one thread per row folds the four warps' maxima (and, with one
+  // split, the sink and the output scales) into one weight per warp
+  if (tid < rows_here) {
+    const int row = tid;
     float mw[4], M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
       mw[w] = sc_m[w * C::kRows + row];
       M = fmaxf(M, mw[w]);
     }
-    float o0 = 0.f, o1 = 0.f, l = 0.f;
+    float f[4], l = 0.f;
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-      const float f = (mw[w] == -INFINITY) ? 0.f : exp2f(mw[w] - M);
-      o0 += f * scratch[(w * C::kRows + row) * D + dv];
-      o1 += f * scratch[(w * C::kRows + row) * D + dv + 1];
-      l += f * sc_l[w * C::kRows + row];
+      f[w] = (mw[w] == -INFINITY) ? 0.f : exp2f(mw[w] - M);
+      l += f[w] * sc_l[w * C::kRows + row];
     }
-    const int r = rg * C::kRows + row;
-    const int i = r / a.G, gg = r % a.G;
+    float mul = 1.f;
     if (single) {
-      const float sig = a.sinks ? __ldg(a.sinks + kvh * a.G + gg) * kLog2e : -INFINITY;
+      const int r = rg * C::kRows + row;
+      const float sig = a.sinks ? __ldg(a.sinks + kvh * a.G + r % a.G) * kLog2e : -INFINITY;
       const float Mf = fmaxf(M, sig);
-      float v0 = 0.f, v1 = 0.f;
+      mul = 0.f;
       if (Mf != -INFINITY) {
-        const float f = (M == -INFINITY) ? 0.f : exp2f(M - Mf);
-        const float den = l * f + ((sig == -INFINITY) ? 0.f : exp2f(sig - Mf));
-        const float mul = f * out_mul / den;
-        v0 = o0 * mul;
-        v1 = o1 * mul;
+        const float fm = (M == -INFINITY) ? 0.f : exp2f(M - Mf);
+        mul = fm * out_mul / (l * fm + ((sig == -INFINITY) ? 0.f : exp2f(sig - Mf)));
       }
+    } else {
+      sc_ml[2 * row] = M;
+      sc_ml[2 * row + 1] = l;
+    }
+#pragma unroll
+    for (int w = 0; w < 4; ++w) sc_w[4 * row + w] = f[w] * mul;
+  }
+  __syncthreads();
+  // phase 2: every (row, 4 columns) combines the warps' partial O
+  for (int item = tid; item < rows_here * (D / 4); item += C::kThreads) {
+    const int row = item / (D / 4);
+    const int dv = 4 * (item % (D / 4));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float f = sc_w[4 * row + w];
+      const float4 v = *reinterpret_cast<const float4*>(scratch + (w * C::kRows + row) * D + dv);
+      acc.x += f * v.x;
+      acc.y += f * v.y;
+      acc.z += f * v.z;
+      acc.w += f * v.w;
+    }
+    if (single) {
+      const int r = rg * C::kRows + row;
+      const int i = r / a.G, gg = r % a.G;
       const int64_t oi = ((int64_t(b) * a.qs + i) * a.Hq + int64_t(kvh) * a.G + gg) * a.Dv + dv;
-      *reinterpret_cast<uint32_t*>(out16 + oi) = pack_f32x2(v0, v1, obf);
+      *reinterpret_cast<uint2*>(out16 + oi) =
+          make_uint2(pack_f32x2(acc.x, acc.y, obf), pack_f32x2(acc.z, acc.w, obf));
     } else {
       float* dst = ws_unit + (int64_t(split) * C::kRows + row) * row_stride;
-      dst[dv] = o0;
-      dst[dv + 1] = o1;
+      *reinterpret_cast<float4*>(dst + dv) = acc;
       if (dv == 0) {
-        dst[D] = M;
-        dst[D + 1] = l;
+        dst[D] = sc_ml[2 * row];
+        dst[D + 1] = sc_ml[2 * row + 1];
       }
     }
   }

@@ -266,21 +266,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           my_page = fetch(win_base);
         }
         if (lane == 0) mbar_arrive_expect_tx(&kv_full[slot], uint32_t(n_piece) * box_bytes * nchunks);
+        __syncwarp();
         uint8_t* dst = smem + kOffStages + slot * kStageBytes;
-        for (int j = 0; j < n_piece; ++j) {
-          const int page = __shfl_sync(0xffffffffu, my_page, lp0 + j - win_base);
-          if (lane == 0) {
-            bad_page |= page < 0;
-            const int row_off = j * box_rows;
-            for (int k = 0; k < nchunks; ++k) {
-              // chunk slot k: latent dims 256c + 64k (k < 4) or the rope dims
-              const int x = k < 4 ? int(c) * kHalf + 64 * k : kLatent;
-              tma_load_3d(dst + k * kChunkBytes + row_off * 128, &tmKV, &kv_full[slot], x, 0,
-                          page * a.ps + sub);
-            }
+        // lane j issues the tile loads of page piece j (pieces are independent)
+        const int page = __shfl_sync(0xffffffffu, my_page, (lp0 + lane - win_base) & 31);
+        if (lane < n_piece) {
+          bad_page |= page < 0;
+          const int row_off = lane * box_rows;
+          for (int k = 0; k < nchunks; ++k) {
+            // chunk slot k: latent dims 256c + 64k (k < 4) or the rope dims
+            const int x = k < 4 ? int(c) * kHalf + 64 * k : kLatent;
+            tma_load_3d(dst + k * kChunkBytes + row_off * 128, &tmKV, &kv_full[slot], x, 0,
+                        page * a.ps + sub);
           }
         }
       }
+      bad_page = __any_sync(0xffffffffu, bad_page);
       if (lane == 0) {
         if (bad_page && a.err) atomicOr(a.err, kErrClamped);
         for (int t = max(0, s - kStages); t < s; ++t)
