@@ -25,8 +25,8 @@
 //   are exactly the first four chunks of the K tile it already holds.
 //   Every latent byte is read from HBM once.
 //
-// Warp roles: 0 = TMA producer, 1 = MMA issuer, 2 = tensor-memory allocator,
-// 4..7 = softmax / exchange / epilogue (warp 4 + k reaches TMEM lanes 32k..).
+// Warp roles: 0 = TMA producer and tensor-memory allocator, 1 = MMA issuer,
+// 2..9 = softmax / exchange / epilogue (warp w reaches TMEM lanes 32 (w % 4)..).
 // Split-KV partials merge exactly as in the grouped-query kernel: the last
 // CTA of each column half to take a ticket merges every split.
 #include <cuda.h>
@@ -57,7 +57,8 @@ constexpr int kStageBytes = kMaxChunks * kChunkBytes;  // 40 KB
 constexpr int kStages = 3;
 constexpr int kSoftWarps = 8;    // two threads per query row, 32 logit columns each
 constexpr int kSoft = 32 * kSoftWarps;
-constexpr int kThreads = 128 + kSoft;
+constexpr int kSoftWarp0 = 2;    // softmax warps are 2..9: two per TMEM sub-partition
+constexpr int kThreads = 32 * kSoftWarp0 + kSoft;
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int kOffStages = 0;
@@ -216,7 +217,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     flags[0] = flags[1] = 0;
     fence_mbar_init();
   }
-  if (warp == 2) {
+  if (warp == 0) {
     umma::tmem_alloc(tmem_slot, kTmemCols);
     umma::tmem_relinquish();
   }
@@ -346,13 +347,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       umma::commit(mma_drain);
       if (!mbar_wait(mma_drain, 0)) flags[0] = 1;
     }
-  } else if (warp >= 4) {
+  } else {
     // ================= softmax / exchange / epilogue =================
-    // Warp 4 + 4h + q reaches TMEM lanes 32q..32q+31 (query rows) and handles
-    // logit columns [32h, 32h + 32) of every tile and O columns [128h, 128h+128).
-    const int q4 = (warp - 4) & 3, h = (warp - 4) >> 2;
-    const int t = 32 * q4 + lane;  // query row = TMEM lane
-    const int st = tid - 128;      // 0 .. kSoft - 1
+    // Warp w (2..9) reaches TMEM lanes 32 (w % 4) .. +31 (query rows); h = (w - 2) / 4
+    // picks logit columns [32h, 32h + 32) of every tile and O columns [128h, 128h+128).
+    const int q4 = warp & 3, h = (warp - kSoftWarp0) >> 2;
+    const int t = 32 * q4 + lane;            // query row = TMEM lane
+    const int st = tid - 32 * kSoftWarp0;    // 0 .. kSoft - 1
     const uint32_t lane_base = uint32_t(32 * q4) << 16;
     const int i = t / a.Hq, hd = t % a.Hq;  // row t = (spec token i, head hd)
     const float q_scale = ldscale(a.q_scale_dev, a.q_scale);
@@ -367,8 +368,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     {
       const uint16_t* qrow = a.q + (int64_t(b) * a.qs * a.Hq + t) * kDim;
       const uint4* src = reinterpret_cast<const uint4*>(qrow + c * kHalf + 128 * h);
+      #pragma unroll
       for (int part = 0; part < 2; ++part) {  // 2 x 32 columns = 128 bf16
         uint32_t w[32];
+        #pragma unroll
         for (int v = 0; v < 8; ++v) {
           const uint4 x = __ldg(src + part * 8 + v);
           w[4 * v + 0] = x.x;
@@ -430,6 +433,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         break;
       }
       // ---- exchange partial logits: stage mine, one bulk copy to the peer
+      #pragma unroll
       for (int v = 0; v < kC / 4; ++v)
         *reinterpret_cast<float4*>(send + xunit(t, 8 * h + v)) =
             make_float4(s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3]);
@@ -480,19 +484,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const float m_new = fmaxf(m_ref, mx);
         const bool need = m_new > m_ref + kRescaleLog2 || (m_ref == -INFINITY && m_new != -INFINITY);
         const float f = (need && m_ref != -INFINITY) ? exp2f(m_ref - m_new) : 1.f;
-        if (__any_sync(kAll, f != 1.f)) {
-          // whole warp rescales its rows' O half-columns (factor 1 where unchanged)
-          for (int part = 0; part < kHalf / 64; ++part) {
-            float o[32];
-            const uint32_t col = kColO + 128u * h + 32u * part;
-            umma::tmem_ld32(tmem + lane_base + col, o);
-            umma::tmem_ld_wait();
-            uint32_t w[32];
-            for (int k = 0; k < 32; ++k) w[k] = __float_as_uint(o[k] * f);
-            umma::tmem_st32(tmem + lane_base + col, w);
-          }
-          umma::tmem_st_wait();
-        }
         if (need) {
           l_half *= f;
           m_ref = m_new;
@@ -521,6 +512,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int r = r0 + idx / 32, k = (idx / 8) % 4, u = idx % 8;
             *reinterpret_cast<uint4*>(stg + k * kChunkBytes + r * 128 + u * 16) = make_uint4(0, 0, 0, 0);
           }
+        }
+        if (__any_sync(kAll, f != 1.f)) {
+          // whole warp rescales its rows' O half-columns (factor 1 where unchanged);
+          // done after P so that the logits are no longer live
+          #pragma unroll
+          for (int part = 0; part < kHalf / 64; ++part) {
+            float o[32];
+            const uint32_t col = kColO + 128u * h + 32u * part;
+            umma::tmem_ld32(tmem + lane_base + col, o);
+            umma::tmem_ld_wait();
+            #pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] *= f;
+            umma::tmem_st32(tmem + lane_base + col, reinterpret_cast<const uint32_t*>(o));
+          }
+          umma::tmem_st_wait();
         }
         umma::fence_proxy_async_smem();
         umma::fence_before_sync();
@@ -558,6 +564,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       const int64_t row_g = (int64_t(b) * a.qs + i) * a.Hq + hd;
       float* wrow = a.ws + ((int64_t(b) * a.nsplit + split) * kRows + t) * (kLatent + 4);
+      #pragma unroll
       for (int part = 0; part < kHalf / 64; ++part) {
         float o[32];
         const uint32_t col_t = kColO + 128u * h + 32u * part;
@@ -565,11 +572,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           umma::tmem_ld32(tmem + lane_base + col_t, o);
           umma::tmem_ld_wait();
         } else {
+          #pragma unroll
           for (int k = 0; k < 32; ++k) o[k] = 0.f;
         }
         const int col = int(c) * kHalf + 128 * h + 32 * part;
         if (single) {
           uint4* dst = reinterpret_cast<uint4*>(a.out + row_g * kLatent + col);
+          #pragma unroll
           for (int v = 0; v < 4; ++v)
             dst[v] = make_uint4(pack_f32x2(o[8 * v] * mul, o[8 * v + 1] * mul, true),
                                 pack_f32x2(o[8 * v + 2] * mul, o[8 * v + 3] * mul, true),
@@ -577,6 +586,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 pack_f32x2(o[8 * v + 6] * mul, o[8 * v + 7] * mul, true));
         } else {
           float4* dst = reinterpret_cast<float4*>(wrow + col);
+          #pragma unroll
           for (int v = 0; v < 8; ++v) dst[v] = make_float4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
         }
       }
@@ -591,7 +601,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   umma::fence_before_sync();
   __syncthreads();
   cluster_sync();
-  if (warp == 2) {
+  if (warp == 0) {
     umma::fence_after_sync();
     umma::tmem_dealloc(tmem, kTmemCols);
   }
