@@ -123,27 +123,11 @@ __device__ __forceinline__ void bulk_to_peer(uint32_t dst_cluster, uint32_t src_
       "r"(src_cta), "r"(bytes), "r"(bar_cluster)
       : "memory");
 }
+// Tells the peer that this CTA has consumed its receive buffer.  The arrive
+// carries no data: the loads it orders were consumed before the arrive is
+// issued, so relaxed ordering suffices and avoids a cluster-scope release.
 __device__ __forceinline__ void remote_arrive(uint32_t rbar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar) : "memory");
-}
-__device__ __forceinline__ bool wait_cluster(uint64_t* bar, uint32_t parity) {
-  auto try_once = [&]() {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-  };
-  if (try_once()) return true;
-  long long t0 = clock64();
-  while (!try_once()) {
-    if (clock64() - t0 > kWaitCycles) return false;
-  }
-  return true;
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar) : "memory");
 }
 
 __device__ __forceinline__ float ldscale(const float* dev, float host) { return dev ? __ldg(dev) : host; }
@@ -426,7 +410,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&s_free[sb]);
         // my send buffer and the peer's receive buffer are free once the peer
         // has read my previous partial
-        if (j > 0 && st == 0) ok = wait_cluster(x_free, (j - 1) & 1);
+        if (j > 0 && st == 0) ok = mbar_wait(x_free, (j - 1) & 1);
       }
       if (named_bar_or(1, kSoft, !ok)) {
         ok = false;
@@ -443,7 +427,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(x_full, uint32_t(kRows * kTok * 4));
         bulk_to_peer(recv_peer, send_cta, uint32_t(kRows * kTok * 4), x_full_peer);
       }
-      ok = __all_sync(kAll, wait_cluster(x_full, j & 1));
+      // the peer's bytes complete on this CTA's own barrier, as a tile load does
+      ok = __all_sync(kAll, mbar_wait(x_full, j & 1));
       const int tile0 = t_begin + j * kTok;
       float mx = -INFINITY;
       if (ok) {
