@@ -441,15 +441,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           s[4 * v + 2] += p4.z;
           s[4 * v + 3] += p4.w;
         }
+        // visibility of this thread's 32 columns as one bit each (all set
+        // away from the split's end, the window start and the spec tokens)
+        uint32_t vis = 0xffffffffu;
+        if (edge) {
+          vis = 0u;
+#pragma unroll 1
+          for (int k = 0; k < kC; ++k) {
+            const int tt = tile0 + 32 * h + k;
+            bool v = tt < t_end && tt >= row_lb;
+            if (a.mask && tt >= spec0) v = v && ((row_mw >> (tt - spec0)) & 1u);
+            vis |= uint32_t(v) << k;
+          }
+        }
 #pragma unroll
         for (int k = 0; k < kC; ++k) {
-          float x = s[k] * lscale;
-          if (edge) {
-            const int tt = tile0 + 32 * h + k;
-            bool vis = tt < t_end && tt >= row_lb;
-            if (a.mask && tt >= spec0) vis = vis && ((row_mw >> (tt - spec0)) & 1u);
-            x = vis ? x : -INFINITY;
-          }
+          const float x = (vis >> k) & 1u ? s[k] * lscale : -INFINITY;
           s[k] = x;
           mx = fmaxf(mx, x);
         }
