@@ -7,28 +7,29 @@
 //
 // The 128 query rows (heads x speculative tokens) form one M = 128 UMMA tile.
 // Their fp32 output (128 x 512) alone fills a CTA's 512 tensor-memory
-// columns, so a cluster of two CTAs shares each (sequence, KV split):
+// columns, so a cluster of two CTAs shares each (sequence, KV split), each
+// CTA holding half of the output columns:
 //
-//   CTA c = 0 owns latent dims [0, 256) plus the rope dims [512, 576);
-//   CTA c = 1 owns latent dims [256, 512).
+//   CTA 0 ("master") owns latent dims [0, 256);
+//   CTA 1 ("feeder") owns latent dims [256, 512) plus the rope dims [512, 576).
 //   Each CTA streams only its dims of every latent row (TMA, 128-byte
-//   swizzle, multi-stage mbarrier ring), computes the partial logits
-//   S_c = Q_c K_c^T (tcgen05.mma, A = its latent query half held in tensor
-//   memory, B = K from shared memory; CTA 0 adds the rope part with A from
-//   shared memory), and sends S_c to its peer through distributed shared
-//   memory (remote stores, then one release-arrive per warp on the peer's
-//   mbarrier).  Both CTAs then hold
-//   the same S = S_0 + S_1 and run the same online softmax (128 threads, one
-//   row each), so their running maxima agree without further traffic.
-//   P (bf16) goes to shared memory and CTA c accumulates O_c += P V_c into
-//   its 256 tensor-memory columns, where V_c = latent dims [256c, 256c+256)
-//   are exactly the first four chunks of the K tile it already holds.
-//   Every latent byte is read from HBM once.
+//   swizzle, three-stage mbarrier ring) and computes the partial logits
+//   S_c = Q_c K_c^T with tcgen05.mma (A = its latent query half held in
+//   tensor memory, B = K from shared memory; CTA 1 adds the rope part with A
+//   from shared memory).  CTA 1 ships S_1 (fp32) to CTA 0 with one bulk copy
+//   into distributed shared memory, a tile ahead of CTA 0's softmax.  CTA 0
+//   adds it to S_0, runs the only online softmax, and ships P (bf16, already
+//   in UMMA operand layout) with the per-row rescale factors back.  Both CTAs
+//   accumulate O_c += P V_c in their own 256 tensor-memory columns, V_c being
+//   the first four chunks of the K tile the CTA already holds.  Every latent
+//   byte is read from HBM once, and no tile waits on a round trip between the
+//   two CTAs.
 //
 // Warp roles: 0 = TMA producer and tensor-memory allocator, 1 = MMA issuer,
-// 2..9 = softmax / exchange / epilogue (warp w reaches TMEM lanes 32 (w % 4)..).
-// Split-KV partials merge exactly as in the grouped-query kernel: the last
-// CTA of each column half to take a ticket merges every split.
+// 2..9 = softmax (CTA 0) or logit shipping and O rescale (CTA 1), then the
+// epilogue; warp w reaches TMEM lanes 32 (w % 4).. and two threads share a
+// query row.  Split-KV partials merge exactly as in the grouped-query kernel:
+// the last CTA of each column half to take a ticket merges every split.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdio.h>
@@ -52,25 +53,57 @@ constexpr int kDim = kLatent + kRope;
 constexpr int kHalf = kLatent / 2;  // V columns per CTA
 constexpr int kTok = 64;         // tokens per tile (UMMA N of QK, K of PV)
 constexpr int kChunkBytes = kTok * 128;  // one 64-element column chunk of a tile
-constexpr int kMaxChunks = 5;    // CTA 0: 4 latent + 1 rope chunk
-constexpr int kStageBytes = kMaxChunks * kChunkBytes;  // 40 KB
 constexpr int kStages = 3;
 constexpr int kSoftWarps = 8;    // two threads per query row, 32 logit columns each
 constexpr int kSoft = 32 * kSoftWarps;
 constexpr int kSoftWarp0 = 2;    // softmax warps are 2..9: two per TMEM sub-partition
 constexpr int kThreads = 32 * kSoftWarp0 + kSoft;
 
-// shared memory map (offsets from a 1024-aligned base)
-constexpr int kOffStages = 0;
-constexpr int kOffQRope = kOffStages + kStages * kStageBytes;  // 128 x 64 bf16
-constexpr int kOffP = kOffQRope + kRows * 128;                  // 128 x 64 bf16
-constexpr int kOffRecv = kOffP + kRows * 128;                   // 128 x 64 fp32: peer's partial
-constexpr int kOffSend = kOffRecv + kRows * kTok * 4;           // 128 x 64 fp32: own partial
-constexpr int kOffRowX = kOffSend + kRows * kTok * 4;           // [2][128] fp32: row max / sum halves
+// ---- shared memory (offsets from a 1024-aligned base).  The two CTAs lay out
+// their buffers differently; the barrier block sits at the same offset in
+// both because each CTA signals barriers of its peer.
+constexpr int kXBytes = kRows * kTok * 4;  // one fp32 logit tile
+constexpr int kPBytes = kRows * kTok * 2;  // one bf16 P tile
+constexpr int kPMsg = kPBytes + kRows * 4; // P followed by one rescale factor per row
+constexpr int kPSlot = 17 * 1024;
+constexpr int kStride0 = 4 * kChunkBytes;  // CTA 0 stage: 4 latent chunks
+constexpr int kStride1 = 5 * kChunkBytes;  // CTA 1 stage: 4 latent chunks + rope
+// CTA 0: stages | P slots x2 | logit receive slots x2
+constexpr int kOffPSlot0 = kStages * kStride0;
+constexpr int kOffRecv = kOffPSlot0 + 2 * kPSlot;
+// CTA 1: stages | rope query (128 x 64 bf16) | P slots x2 | logit send buffer
+constexpr int kOffQRope = kStages * kStride1;
+constexpr int kOffPSlot1 = kOffQRope + kRows * 128;
+constexpr int kOffSend = kOffPSlot1 + 2 * kPSlot;
+// both: [2][128] floats (CTA 0: row maxima / sums; CTA 1: the final m and l)
+constexpr int kOffRowX = (kOffRecv + 2 * kXBytes) > (kOffSend + kXBytes) ? (kOffRecv + 2 * kXBytes)
+                                                                         : (kOffSend + kXBytes);
 constexpr int kOffBar = kOffRowX + 2 * kRows * 4;
-constexpr int kNumBars = 2 * kStages + 10;
+
+enum BarIdx {
+  kKvFull = 0,                  // [kStages] TMA bytes landed
+  kKvEmpty = kKvFull + kStages, // [kStages] the P.V reading the stage is done
+  kQReady = kKvEmpty + kStages, // the query is in tensor / shared memory
+  kSFull = kQReady + 1,         // [2] S tile computed
+  kSFree = kSFull + 2,          // [2] S tile read out of tensor memory
+  kPFull = kSFree + 2,          // P (and any O rescale) ready for the P.V
+  kPvDone = kPFull + 1,         // the last P.V issued is done
+  kDrain = kPvDone + 1,         // every MMA this CTA issued is done
+  kXFull = kDrain + 1,          // CTA 0 [2]: the peer's logit tile landed
+  kXFree = kXFull + 2,          // CTA 1: CTA 0 received the previous logit tile
+  kPIn = kXFree + 1,            // CTA 1 [2]: a P message landed
+  kPSlotFree = kPIn + 2,        // CTA 0 [2]: CTA 1's P.V on that P slot is done
+  kFin = kPSlotFree + 2,        // CTA 1: the final (m, l) rows landed
+  kNumBars = kFin + 1
+};
 constexpr int kSmem = 1024 + kOffBar + kNumBars * 8 + 32;
 static_assert(kSmem <= 232448, "shared memory budget");
+static_assert(kOffPSlot0 % 1024 == 0 && kOffPSlot1 % 1024 == 0 && kPSlot % 1024 == 0 &&
+                  kOffQRope % 1024 == 0 && kOffRecv % 16 == 0 && kOffSend % 16 == 0,
+              "UMMA operands need 1024-byte alignment, bulk copies 16");
+static_assert(kPMsg <= kPSlot && kPMsg % 16 == 0, "P message");
+constexpr int kCopyPieces = 4;  // each message travels as this many bulk copies
+static_assert(kPMsg % (16 * kCopyPieces) == 0 && kXBytes % (16 * kCopyPieces) == 0, "copy pieces");
 
 // tensor memory columns
 constexpr uint32_t kTmemCols = 512;
@@ -123,11 +156,20 @@ __device__ __forceinline__ void bulk_to_peer(uint32_t dst_cluster, uint32_t src_
       "r"(src_cta), "r"(bytes), "r"(bar_cluster)
       : "memory");
 }
-// Tells the peer that this CTA has consumed its receive buffer.  The arrive
-// carries no data: the loads it orders were consumed before the arrive is
-// issued, so relaxed ordering suffices and avoids a cluster-scope release.
+// Tells the peer that this CTA has received what the peer sent.  The arrive
+// carries no data of its own, so relaxed ordering suffices and avoids a
+// cluster-scope release.
 __device__ __forceinline__ void remote_arrive(uint32_t rbar) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar) : "memory");
+}
+// Arrives once on the barrier at the same offset in every CTA of `mask` when
+// every MMA this thread issued so far is done.
+__device__ __forceinline__ void commit_to(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(mask)
+      : "memory");
 }
 
 __device__ __forceinline__ float ldscale(const float* dev, float host) { return dev ? __ldg(dev) : host; }
@@ -135,22 +177,36 @@ __device__ __forceinline__ float ldscale(const float* dev, float host) { return 
 // 16-byte unit u (0..15) of row t of a 128 x 64 fp32 buffer, XOR-swizzled by row.
 __device__ __forceinline__ int xunit(int t, int u) { return t * kTok + ((u ^ (t & 15)) & 15) * 4; }
 
+// Multiplies this warp's 32 rows of O columns [128h, 128h + 128) by f.
+__device__ __forceinline__ void rescale_o(uint32_t taddr, float f) {
+#pragma unroll 1
+  for (int part = 0; part < kHalf / 64; ++part) {
+    float o[32];
+    umma::tmem_ld32(taddr + 32u * part, o);
+    umma::tmem_ld_wait();
+#pragma unroll
+    for (int k = 0; k < 32; ++k) o[k] *= f;
+    umma::tmem_st32(taddr + 32u * part, reinterpret_cast<const uint32_t*>(o));
+  }
+  umma::tmem_st_wait();
+}
+
+// Zeroes V rows [r0, kTok) of a stage's four latent chunks: past a split's
+// last token the rows hold stale or foreign data (possibly NaN), and P = 0
+// there must not meet it in the P.V.
+__device__ __forceinline__ void zero_v_tail(uint8_t* stage, int r0, int st) {
+  for (int idx = st; idx < (kTok - r0) * 4 * 8; idx += kSoft) {
+    const int r = r0 + idx / 32, k = (idx / 8) % 4, u = idx % 8;
+    *reinterpret_cast<uint4*>(stage + k * kChunkBytes + r * 128 + u * 16) = make_uint4(0, 0, 0, 0);
+  }
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tmKV, const MlaArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* kv_full = bars;                 // [kStages]
-  uint64_t* kv_empty = bars + kStages;      // [kStages]
-  uint64_t* q_ready = bars + 2 * kStages;   // softmax warps stored the query
-  uint64_t* s_full = q_ready + 1;           // [2]
-  uint64_t* s_free = s_full + 2;            // [2]
-  uint64_t* p_full = s_free + 2;
-  uint64_t* pv_done = p_full + 1;
-  uint64_t* x_full = pv_done + 1;           // the peer's partial is in my receive buffer
-  uint64_t* x_free = x_full + 1;            // the peer has read my previous partial
-  uint64_t* mma_drain = x_free + 1;         // every MMA this CTA issued has finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
   int* flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] abort, [1] last CTA
 
@@ -181,24 +237,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int t_begin = pg_lo * a.ps;
   const int t_end = min(pg_hi * a.ps, L);
   const int ntiles = (nvalid == 0 || t_end <= t_begin) ? 0 : (t_end - t_begin + kTok - 1) / kTok;
-  const int nchunks = c == 0 ? 5 : 4;
+  const int nchunks = c == 0 ? 4 : 5;
+  const int stride = c == 0 ? kStride0 : kStride1;
+  const int off_p = c == 0 ? kOffPSlot0 : kOffPSlot1;
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&bars[kKvFull + i], 1);
+      mbar_init(&bars[kKvEmpty + i], 1);
     }
-    mbar_init(q_ready, kSoftWarps);
-    mbar_init(&s_full[0], 1);
-    mbar_init(&s_full[1], 1);
-    mbar_init(&s_free[0], kSoftWarps);
-    mbar_init(&s_free[1], kSoftWarps);
-    mbar_init(p_full, kSoftWarps);
-    mbar_init(pv_done, 1);
-    mbar_init(x_full, 1);  // own expect-tx arrival + the peer's bulk copy bytes
-    mbar_init(x_free, 1);  // one remote arrival from the peer per tile
-    mbar_init(mma_drain, 1);
+    mbar_init(&bars[kQReady], kSoftWarps);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&bars[kSFull + k], 1);
+      mbar_init(&bars[kSFree + k], kSoftWarps);
+      mbar_init(&bars[kXFull + k], 1);      // own expect-tx arrival + the peer's bytes
+      mbar_init(&bars[kPIn + k], 1);        // own expect-tx arrival + the peer's bytes
+      mbar_init(&bars[kPSlotFree + k], 1);  // the peer's MMA completion
+    }
+    mbar_init(&bars[kPFull], kSoftWarps);
+    mbar_init(&bars[kPvDone], 1);
+    mbar_init(&bars[kDrain], 1);
+    mbar_init(&bars[kXFree], 1);
+    mbar_init(&bars[kFin], 1);
     flags[0] = flags[1] = 0;
+    // the first two receive slots and the final rows are expected up front
+    for (int k = 0; k < min(2, ntiles); ++k)
+      mbar_arrive_expect_tx(&bars[c == 0 ? kXFull + k : kPIn + k], c == 0 ? kXBytes : kPMsg);
+    if (c == 1) mbar_arrive_expect_tx(&bars[kFin], 2 * kRows * 4);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -210,13 +275,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();  // the peer's barriers exist before any remote access
   umma::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-
-  const uint32_t stage0 = smem_u32(smem + kOffStages);
-  const uint32_t qrope = smem_u32(smem + kOffQRope);
-  const uint32_t pbuf = smem_u32(smem + kOffP);
+  const uint32_t peer_bars = map_peer(smem_u32(bars), peer);
 
   if (warp == 0) {
-    // ================= TMA producer (warp fetches page indices, lane 0 issues)
+    // ================= TMA producer (warp fetches page indices, lanes issue)
     if (ntiles > 0) {
       if (lane == 0) prefetch_tensormap(&tmKV);
       const int32_t* pt = a.page_table + int64_t(b) * a.pps;
@@ -237,7 +299,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (; s < ntiles; ++s) {
         const int slot = s % kStages;
         int ok = 1;
-        if (lane == 0 && s >= kStages) ok = mbar_wait(&kv_empty[slot], ((s / kStages) & 1) ^ 1);
+        if (lane == 0 && s >= kStages) ok = mbar_wait(&bars[kKvEmpty + slot], ((s / kStages) & 1) ^ 1);
         if (!__shfl_sync(0xffffffffu, ok, 0)) {
           if (lane == 0) flags[0] = 1;
           break;
@@ -250,9 +312,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           win_base = lp0;
           my_page = fetch(win_base);
         }
-        if (lane == 0) mbar_arrive_expect_tx(&kv_full[slot], uint32_t(n_piece) * box_bytes * nchunks);
+        if (lane == 0)
+          mbar_arrive_expect_tx(&bars[kKvFull + slot], uint32_t(n_piece) * box_bytes * nchunks);
         __syncwarp();
-        uint8_t* dst = smem + kOffStages + slot * kStageBytes;
+        uint8_t* dst = smem + slot * stride;
         // lane j issues the tile loads of page piece j (pieces are independent)
         const int page = __shfl_sync(0xffffffffu, my_page, (lp0 + lane - win_base) & 31);
         if (lane < n_piece) {
@@ -261,8 +324,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int k = 0; k < nchunks; ++k) {
             // chunk slot k: latent dims 256c + 64k (k < 4) or the rope dims
             const int x = k < 4 ? int(c) * kHalf + 64 * k : kLatent;
-            tma_load_3d(dst + k * kChunkBytes + row_off * 128, &tmKV, &kv_full[slot], x, 0,
+            tma_load_3d(dst + k * kChunkBytes + row_off * 128, &tmKV, &bars[kKvFull + slot], x, 0,
                         page * a.ps + sub);
+          }
+        }
+        // the tile that will reuse this stage next: into L2 now, so that its
+        // load (issued only when the stage frees) does not pay HBM latency
+        const int sp = s + kStages;
+        if (sp < ntiles) {
+          const int ptok = t_begin + sp * kTok;
+          const int plp = ptok / a.ps;
+          const int psub = a.ps <= kTok ? 0 : ptok % a.ps;
+          const int pn = a.ps <= kTok ? min(kTok / a.ps, pg_hi - plp) : 1;
+          if (lane < pn) {
+            const int pg = __ldg(pt + plp + lane);
+            if (pg >= 0 && int64_t(pg) < a.num_pages)
+              for (int k = 0; k < nchunks; ++k)
+                tma_prefetch_l2_3d(&tmKV, k < 4 ? int(c) * kHalf + 64 * k : kLatent, 0, pg * a.ps + psub);
           }
         }
       }
@@ -270,7 +348,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         if (bad_page && a.err) atomicOr(a.err, kErrClamped);
         for (int t = max(0, s - kStages); t < s; ++t)
-          if (!mbar_wait(&kv_full[t % kStages], (t / kStages) & 1)) flags[0] = 1;
+          if (!mbar_wait(&bars[kKvFull + t % kStages], (t / kStages) & 1)) flags[0] = 1;
       }
     }
   } else if (warp == 1) {
@@ -278,84 +356,95 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t kIdescQK = umma::idesc_f16(kRows, kTok, true, false, false);
       constexpr uint32_t kIdescPV = umma::idesc_f16(kRows, kHalf, true, false, true);
-      bool ok = mbar_wait(q_ready, 0);
+      const uint32_t stage0 = smem_u32(smem);
+      const uint32_t pslot = smem_u32(smem + off_p);
+      const uint32_t qrope = smem_u32(smem + kOffQRope);
+      bool ok = mbar_wait(&bars[kQReady], 0);
       umma::fence_after_sync();
       auto issue_qk = [&](int j) {
-        const int slot = j % kStages;
-        const uint32_t st = stage0 + slot * kStageBytes;
+        const uint32_t st = stage0 + (j % kStages) * stride;
         const uint32_t sd = tmem + kColS + 64u * uint32_t(j & 1);
         for (int k = 0; k < 4; ++k)
           for (int kk = 0; kk < 4; ++kk)
             umma::mma_ts(sd, tmem + kColQ + 32u * k + 8u * kk,
                          umma::smem_desc(st + k * kChunkBytes + 32 * kk, 16, 1024, umma::kSw128),
                          kIdescQK, (k | kk) != 0);
-        if (c == 0)
+        if (c == 1)
           for (int kk = 0; kk < 4; ++kk)
             umma::mma_ss(sd, umma::smem_desc(qrope + 32 * kk, 16, 1024, umma::kSw128),
                          umma::smem_desc(st + 4 * kChunkBytes + 32 * kk, 16, 1024, umma::kSw128),
                          kIdescQK, 1u);
-        umma::commit(&s_full[j & 1]);
+        umma::commit(&bars[kSFull + (j & 1)]);
       };
-      if (ok && mbar_wait(&kv_full[0], 0)) {
-        umma::fence_after_sync();
-        issue_qk(0);
-      } else {
-        ok = false;
-      }
-      for (int j = 0; ok && j < ntiles; ++j) {
-        const int jn = j + 1;
-        if (jn < ntiles) {
-          if (!mbar_wait(&kv_full[jn % kStages], (jn / kStages) & 1) ||
-              (jn >= 2 && !mbar_wait(&s_free[jn & 1], ((jn >> 1) - 1) & 1))) {
-            ok = false;
-            break;
-          }
-          umma::fence_after_sync();
-          issue_qk(jn);
-        }
-        if (!mbar_wait(p_full, j & 1)) {
-          ok = false;
-          break;
-        }
-        umma::fence_after_sync();
-        const uint32_t st = stage0 + (j % kStages) * kStageBytes;
+      auto issue_pv = [&](int j) {
+        const uint32_t st = stage0 + (j % kStages) * stride;
+        const uint32_t pa = pslot + (j & 1) * kPSlot;
         for (int kk = 0; kk < 4; ++kk)
-          umma::mma_ss(tmem + kColO, umma::smem_desc(pbuf + 32 * kk, 16, 1024, umma::kSw128),
+          umma::mma_ss(tmem + kColO, umma::smem_desc(pa + 32 * kk, 16, 1024, umma::kSw128),
                        umma::smem_desc(st + 2048 * kk, kChunkBytes, 1024, umma::kSw128), kIdescPV,
                        (j | kk) != 0);
-        umma::commit(&kv_empty[j % kStages]);
-        umma::commit(pv_done);
+        umma::commit(&bars[kKvEmpty + j % kStages]);
+        umma::commit(&bars[kPvDone]);
+        // the P slot may take CTA 0's next message once this P.V has read it
+        if (c == 1) commit_to(&bars[kPSlotFree + (j & 1)], uint16_t(1u));
+      };
+      // Issue whichever is ready: the P.V of the oldest tile (it frees a
+      // stage) or the logits of the next one, so QK runs ahead of the round
+      // trip that P takes.  Tests never block; the loop gives up after
+      // kWaitCycles without progress.
+      int nq = 0, np = 0;
+      long long t_idle = clock64();
+      while (ok && np < ntiles) {
+        bool moved = false;
+        // CTA 1's P arrives from the peer; CTA 0 wrote its own
+        if (np < nq && mbar_test(&bars[kPFull], np & 1) &&
+            (c == 0 || mbar_test(&bars[kPIn + (np & 1)], (np >> 1) & 1))) {
+          umma::fence_after_sync();
+          issue_pv(np++);
+          moved = true;
+        }
+        if (nq < ntiles && mbar_test(&bars[kKvFull + nq % kStages], (nq / kStages) & 1) &&
+            (nq < 2 || mbar_test(&bars[kSFree + (nq & 1)], ((nq >> 1) - 1) & 1))) {
+          umma::fence_after_sync();
+          issue_qk(nq++);
+          moved = true;
+        }
+        if (moved)
+          t_idle = clock64();
+        else if (clock64() - t_idle > kWaitCycles)
+          ok = false;
       }
       if (!ok) flags[0] = 1;
       // nothing this thread issued may still run when tensor memory is freed
-      umma::commit(mma_drain);
-      if (!mbar_wait(mma_drain, 0)) flags[0] = 1;
+      umma::commit(&bars[kDrain]);
+      if (!mbar_wait(&bars[kDrain], 0)) flags[0] = 1;
     }
   } else {
-    // ================= softmax / exchange / epilogue =================
+    // ================= softmax / logit shipping / epilogue =================
     // Warp w (2..9) reaches TMEM lanes 32 (w % 4) .. +31 (query rows); h = (w - 2) / 4
     // picks logit columns [32h, 32h + 32) of every tile and O columns [128h, 128h+128).
     const int q4 = warp & 3, h = (warp - kSoftWarp0) >> 2;
     const int t = 32 * q4 + lane;            // query row = TMEM lane
     const int st = tid - 32 * kSoftWarp0;    // 0 .. kSoft - 1
     const uint32_t lane_base = uint32_t(32 * q4) << 16;
+    const uint32_t o_cols = tmem + lane_base + kColO + 128u * h;
     const int i = t / a.Hq, hd = t % a.Hq;  // row t = (spec token i, head hd)
     const float q_scale = ldscale(a.q_scale_dev, a.q_scale);
     const float kv_scale = ldscale(a.kv_scale_dev, a.kv_scale);
     const float lscale = a.softmax_scale * q_scale * kv_scale * kLog2e;
-    float* recv = reinterpret_cast<float*>(smem + kOffRecv);
-    float* send = reinterpret_cast<float*>(smem + kOffSend);
     float* rowx = reinterpret_cast<float*>(smem + kOffRowX);  // [2][128]
+    constexpr unsigned kAll = 0xffffffffu;
+    constexpr int kC = kTok / 2;  // logit columns per thread
 
     // ---- query: this thread's half of the row's latent half into tensor
-    // memory; the rope part into shared memory (CTA 0)
+    // memory; the rope part into shared memory (CTA 1)
     {
       const uint16_t* qrow = a.q + (int64_t(b) * a.qs * a.Hq + t) * kDim;
       const uint4* src = reinterpret_cast<const uint4*>(qrow + c * kHalf + 128 * h);
-      #pragma unroll
+#pragma unroll
       for (int part = 0; part < 2; ++part) {  // 2 x 32 columns = 128 bf16
         uint32_t w[32];
-        #pragma unroll
+#pragma unroll
         for (int v = 0; v < 8; ++v) {
           const uint4 x = __ldg(src + part * 8 + v);
           w[4 * v + 0] = x.x;
@@ -365,7 +454,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         umma::tmem_st32(tmem + lane_base + kColQ + 64u * h + 32u * part, w);
       }
-      if (c == 0) {
+      if (c == 1) {
         const uint4* rsrc = reinterpret_cast<const uint4*>(qrow + kLatent);
         for (int u = 4 * h; u < 4 * h + 4; ++u)
           *reinterpret_cast<uint4*>(smem + kOffQRope + umma::sw128(t, u)) = __ldg(rsrc + u);
@@ -374,174 +463,230 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       umma::fence_proxy_async_smem();
       umma::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(q_ready);
+      if (lane == 0) mbar_arrive(&bars[kQReady]);
     }
 
-    // per-row visibility
-    const int row_lb = a.win > 0 ? spec0 + i - a.win + 1 : INT_MIN;
-    uint32_t row_mw = 0xffffffffu;
-    if (a.mask) {
-      const uint16_t* mrow = a.mask + (int64_t(b) * a.qs + i) * a.mask_words;
-      row_mw = uint32_t(__ldg(mrow)) | (uint32_t(__ldg(mrow + 1)) << 16);
-    }
-
-    const uint32_t x_full_peer = map_peer(smem_u32(x_full), peer);
-    const uint32_t x_free_peer = map_peer(smem_u32(x_free), peer);
-    const uint32_t recv_peer = map_peer(smem_u32(recv), peer);
-    const uint32_t send_cta = smem_u32(send);
     float m_ref = -INFINITY, l_half = 0.f;
     bool ok = true;
-    constexpr unsigned kAll = 0xffffffffu;
-    constexpr int kC = kTok / 2;  // logit columns per thread
-
     // Control flow stays uniform across each warp (tcgen05.ld / st are
     // warp-collective) and across the eight softmax warps (named barrier 1):
-    // waits are voted and the loop is left collectively.
-    for (int j = 0; j < ntiles; ++j) {
-      const int sb = j & 1;
-      float s[kC];
-      ok = __all_sync(kAll, mbar_wait(&s_full[sb], (j >> 1) & 1));
-      if (ok) {
-        umma::fence_after_sync();
-        umma::tmem_ld32(tmem + lane_base + kColS + 64u * sb + 32u * h, s);
-        umma::tmem_ld_wait();
-        umma::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_free[sb]);
-        // my send buffer and the peer's receive buffer are free once the peer
-        // has read my previous partial
-        if (j > 0 && st == 0) ok = mbar_wait(x_free, (j - 1) & 1);
+    // waits are voted and loops are left collectively.
+    if (c == 0) {
+      // ---------------- CTA 0: full logits, online softmax, P for both CTAs
+      const float* recv = reinterpret_cast<const float*>(smem + kOffRecv);
+      const uint32_t pslot_peer = map_peer(smem_u32(smem + kOffPSlot1), peer);
+      const int row_lb = a.win > 0 ? spec0 + i - a.win + 1 : INT_MIN;
+      uint32_t row_mw = 0xffffffffu;
+      if (a.mask) {
+        const uint16_t* mrow = a.mask + (int64_t(b) * a.qs + i) * a.mask_words;
+        row_mw = uint32_t(__ldg(mrow)) | (uint32_t(__ldg(mrow + 1)) << 16);
       }
-      if (named_bar_or(1, kSoft, !ok)) {
-        ok = false;
-        break;
-      }
-      // ---- exchange partial logits: stage mine, one bulk copy to the peer
-      #pragma unroll
-      for (int v = 0; v < kC / 4; ++v)
-        *reinterpret_cast<float4*>(send + xunit(t, 8 * h + v)) =
-            make_float4(s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3]);
-      umma::fence_proxy_async_smem();
-      named_bar(1, kSoft);
-      if (st == 0) {
-        mbar_arrive_expect_tx(x_full, uint32_t(kRows * kTok * 4));
-        bulk_to_peer(recv_peer, send_cta, uint32_t(kRows * kTok * 4), x_full_peer);
-      }
-      // the peer's bytes complete on this CTA's own barrier, as a tile load does
-      ok = __all_sync(kAll, mbar_wait(x_full, j & 1));
-      const int tile0 = t_begin + j * kTok;
-      float mx = -INFINITY;
-      if (ok) {
-        const bool edge = tile0 + kTok > t_end || tile0 <= row_lb || (a.mask && tile0 + kTok > spec0);
-#pragma unroll
-        for (int v = 0; v < kC / 4; ++v) {
-          const float4 p4 = *reinterpret_cast<const float4*>(recv + xunit(t, 8 * h + v));
-          s[4 * v] += p4.x;
-          s[4 * v + 1] += p4.y;
-          s[4 * v + 2] += p4.z;
-          s[4 * v + 3] += p4.w;
+      for (int j = 0; j < ntiles; ++j) {
+        const int sb = j & 1;
+        const uint32_t par = (j >> 1) & 1;
+        float s[kC];
+        ok = __all_sync(kAll, mbar_wait(&bars[kSFull + sb], par));
+        if (ok) {
+          umma::fence_after_sync();
+          umma::tmem_ld32(tmem + lane_base + kColS + 64u * sb + 32u * h, s);
+          umma::tmem_ld_wait();
+          umma::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[kSFree + sb]);
+          // the peer's partial logits of this tile
+          ok = __all_sync(kAll, mbar_wait(&bars[kXFull + sb], par));
         }
-        // visibility of this thread's 32 columns as one bit each (all set
-        // away from the split's end, the window start and the spec tokens)
-        uint32_t vis = 0xffffffffu;
-        if (edge) {
-          vis = 0u;
+        // received: the peer may refill its send buffer (and so this CTA's other
+        // slot); after the last tile nobody waits for the signal, so none is sent
+        if (ok && st == 0 && j + 1 < ntiles) remote_arrive(peer_bars + 8u * kXFree);
+        const int tile0 = t_begin + j * kTok;
+        float mx = -INFINITY;
+        if (ok) {
+          const float* rx = recv + sb * (kXBytes / 4);
+#pragma unroll
+          for (int v = 0; v < kC / 4; ++v) {
+            const float4 p4 = *reinterpret_cast<const float4*>(rx + xunit(t, 8 * h + v));
+            s[4 * v] += p4.x;
+            s[4 * v + 1] += p4.y;
+            s[4 * v + 2] += p4.z;
+            s[4 * v + 3] += p4.w;
+          }
+          // visibility of this thread's 32 columns as one bit each (all set
+          // away from the split's end, the window start and the spec tokens)
+          const bool edge = tile0 + kTok > t_end || tile0 <= row_lb || (a.mask && tile0 + kTok > spec0);
+          uint32_t vis = 0xffffffffu;
+          if (edge) {
+            vis = 0u;
 #pragma unroll 1
+            for (int k = 0; k < kC; ++k) {
+              const int tt = tile0 + 32 * h + k;
+              bool v = tt < t_end && tt >= row_lb;
+              if (a.mask && tt >= spec0) v = v && ((row_mw >> (tt - spec0)) & 1u);
+              vis |= uint32_t(v) << k;
+            }
+          }
+#pragma unroll
           for (int k = 0; k < kC; ++k) {
-            const int tt = tile0 + 32 * h + k;
-            bool v = tt < t_end && tt >= row_lb;
-            if (a.mask && tt >= spec0) v = v && ((row_mw >> (tt - spec0)) & 1u);
-            vis |= uint32_t(v) << k;
+            const float x = (vis >> k) & 1u ? s[k] * lscale : -INFINITY;
+            s[k] = x;
+            mx = fmaxf(mx, x);
           }
+          rowx[h * kRows + t] = mx;
         }
+        // both halves of every row published their maxima; the slot is consumed
+        if (named_bar_or(1, kSoft, !ok)) {
+          ok = false;
+          break;
+        }
+        if (st == 0 && j + 2 < ntiles) mbar_arrive_expect_tx(&bars[kXFull + sb], kXBytes);
+        mx = fmaxf(mx, rowx[(1 - h) * kRows + t]);
+        // O may be rescaled once the previous P.V is done; P slot sb is free
+        // once both CTAs' P.V of tile j - 2 are done (which also means its
+        // copy to the peer has landed)
+        if (j > 0) ok = __all_sync(kAll, mbar_wait(&bars[kPvDone], (j - 1) & 1));
+        if (ok && j >= 2) ok = __all_sync(kAll, mbar_wait(&bars[kPSlotFree + sb], ((j >> 1) - 1) & 1));
+        uint8_t* pbuf = smem + kOffPSlot0 + sb * kPSlot;
+        if (ok) {
+          umma::fence_after_sync();
+          const float m_new = fmaxf(m_ref, mx);
+          const bool need = m_new > m_ref + kRescaleLog2 || (m_ref == -INFINITY && m_new != -INFINITY);
+          const float f = (need && m_ref != -INFINITY) ? exp2f(m_ref - m_new) : 1.f;
+          if (need) {
+            l_half *= f;
+            m_ref = m_new;
+          }
+          // P (bf16) for this thread's 32 columns: units 4h..4h+3 of row t; the
+          // row sum takes the rounded weights so O / l stays a convex combination
 #pragma unroll
-        for (int k = 0; k < kC; ++k) {
-          const float x = (vis >> k) & 1u ? s[k] * lscale : -INFINITY;
-          s[k] = x;
-          mx = fmaxf(mx, x);
+          for (int u = 0; u < 4; ++u) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float p0 = m_ref == -INFINITY ? 0.f : ex2(s[8 * u + 2 * e] - m_ref);
+              const float p1 = m_ref == -INFINITY ? 0.f : ex2(s[8 * u + 2 * e + 1] - m_ref);
+              w4[e] = pack_f32x2(p0, p1, true);
+              const float2 r = unpack_16x2(w4[e], true);
+              l_half += r.x + r.y;
+            }
+            *reinterpret_cast<uint4*>(pbuf + umma::sw128(t, 4 * h + u)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+          if (h == 0) reinterpret_cast<float*>(pbuf + kPBytes)[t] = f;
+          if (tile0 + kTok > t_end) zero_v_tail(smem + (j % kStages) * kStride0, max(0, t_end - tile0), st);
+          // whole warp rescales its rows' O half-columns (factor 1 where unchanged)
+          if (__any_sync(kAll, f != 1.f)) rescale_o(o_cols, f);
+          umma::fence_proxy_async_smem();
+          umma::fence_before_sync();
         }
-        rowx[h * kRows + t] = mx;
+        // every thread finished P, the factors and the V tail, or someone gave up
+        if (named_bar_or(1, kSoft, !ok)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) mbar_arrive(&bars[kPFull]);
+        // four copies from four warps: one long copy moves slower than pieces in flight together
+        if ((st & 31) == 0 && st < 32 * kCopyPieces) {
+          const uint32_t off = uint32_t(st >> 5) * (kPMsg / kCopyPieces);
+          bulk_to_peer(pslot_peer + sb * kPSlot + off, smem_u32(pbuf) + off, kPMsg / kCopyPieces,
+                       peer_bars + 8u * (kPIn + sb));
+        }
       }
-      // both halves of every row published their maxima; the receive buffer is read
-      if (named_bar_or(1, kSoft, !ok)) {
-        ok = false;
-        break;
-      }
-      if (st == 0) remote_arrive(x_free_peer);
-      mx = fmaxf(mx, rowx[(1 - h) * kRows + t]);
-      // P and O may be touched only once the previous P.V is done
-      if (j > 0) ok = __all_sync(kAll, mbar_wait(pv_done, (j - 1) & 1));
-      if (ok) {
-        umma::fence_after_sync();
-        const float m_new = fmaxf(m_ref, mx);
-        const bool need = m_new > m_ref + kRescaleLog2 || (m_ref == -INFINITY && m_new != -INFINITY);
-        const float f = (need && m_ref != -INFINITY) ? exp2f(m_ref - m_new) : 1.f;
-        if (need) {
-          l_half *= f;
-          m_ref = m_new;
-        }
-        // P (bf16) for this thread's 32 columns: units 4h..4h+3 of row t; the
-        // row sum takes the rounded weights so O / l stays a convex combination
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          uint32_t w4[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float p0 = m_ref == -INFINITY ? 0.f : ex2(s[8 * u + 2 * e] - m_ref);
-            const float p1 = m_ref == -INFINITY ? 0.f : ex2(s[8 * u + 2 * e + 1] - m_ref);
-            w4[e] = pack_f32x2(p0, p1, true);
-            const float2 r = unpack_16x2(w4[e], true);
-            l_half += r.x + r.y;
-          }
-          *reinterpret_cast<uint4*>(smem + kOffP + umma::sw128(t, 4 * h + u)) =
-              make_uint4(w4[0], w4[1], w4[2], w4[3]);
-        }
-        // V rows past this split's last token hold stale or foreign data: zero them
-        if (tile0 + kTok > t_end) {
-          const int r0 = max(0, t_end - tile0);
-          uint8_t* stg = smem + kOffStages + (j % kStages) * kStageBytes;
-          for (int idx = st; idx < (kTok - r0) * 4 * 8; idx += kSoft) {
-            const int r = r0 + idx / 32, k = (idx / 8) % 4, u = idx % 8;
-            *reinterpret_cast<uint4*>(stg + k * kChunkBytes + r * 128 + u * 16) = make_uint4(0, 0, 0, 0);
-          }
-        }
-        if (__any_sync(kAll, f != 1.f)) {
-          // whole warp rescales its rows' O half-columns (factor 1 where unchanged);
-          // done after P so that the logits are no longer live
-          #pragma unroll
-          for (int part = 0; part < kHalf / 64; ++part) {
-            float o[32];
-            const uint32_t col = kColO + 128u * h + 32u * part;
-            umma::tmem_ld32(tmem + lane_base + col, o);
+    } else {
+      // ---------------- CTA 1: ship partial logits a tile ahead, apply P
+      float* send = reinterpret_cast<float*>(smem + kOffSend);
+      const uint32_t recv_peer = map_peer(smem_u32(smem + kOffRecv), peer);
+      for (int j = 0; j <= ntiles; ++j) {
+        if (j < ntiles) {
+          const int sb = j & 1;
+          float s[kC];
+          ok = __all_sync(kAll, mbar_wait(&bars[kSFull + sb], (j >> 1) & 1));
+          if (ok) {
+            umma::fence_after_sync();
+            umma::tmem_ld32(tmem + lane_base + kColS + 64u * sb + 32u * h, s);
             umma::tmem_ld_wait();
-            #pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] *= f;
-            umma::tmem_st32(tmem + lane_base + col, reinterpret_cast<const uint32_t*>(o));
+            umma::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kSFree + sb]);
+            // the send buffer and the peer's slot sb are free once the peer
+            // has received the previous tile
+            if (j > 0 && st == 0) ok = mbar_wait(&bars[kXFree], (j - 1) & 1);
           }
-          umma::tmem_st_wait();
+          if (named_bar_or(1, kSoft, !ok)) {
+            ok = false;
+            break;
+          }
+#pragma unroll
+          for (int v = 0; v < kC / 4; ++v)
+            *reinterpret_cast<float4*>(send + xunit(t, 8 * h + v)) =
+                make_float4(s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3]);
+          umma::fence_proxy_async_smem();
+          named_bar(1, kSoft);
+          if ((st & 31) == 0 && st < 32 * kCopyPieces) {
+            const uint32_t off = uint32_t(st >> 5) * (kXBytes / kCopyPieces);
+            bulk_to_peer(recv_peer + sb * kXBytes + off, smem_u32(send) + off, kXBytes / kCopyPieces,
+                         peer_bars + 8u * (kXFull + sb));
+          }
         }
-        umma::fence_proxy_async_smem();
-        umma::fence_before_sync();
+        if (j > 0) {
+          // P of the previous tile: rescale O as the master did, then release the P.V
+          const int jp = j - 1, kp = jp & 1;
+          ok = __all_sync(kAll, mbar_wait(&bars[kPIn + kp], (jp >> 1) & 1));
+          if (ok && jp > 0) ok = __all_sync(kAll, mbar_wait(&bars[kPvDone], (jp - 1) & 1));
+          if (ok) {
+            umma::fence_after_sync();
+            const float f = reinterpret_cast<const float*>(smem + kOffPSlot1 + kp * kPSlot + kPBytes)[t];
+            if (__any_sync(kAll, f != 1.f)) rescale_o(o_cols, f);
+            const int tile0 = t_begin + jp * kTok;
+            if (tile0 + kTok > t_end) zero_v_tail(smem + (jp % kStages) * kStride1, max(0, t_end - tile0), st);
+            umma::fence_proxy_async_smem();
+            umma::fence_before_sync();
+          }
+          // the slot's next message (tile jp + 2) is expected before its P.V frees it
+          if (st == 0 && jp + 2 < ntiles) mbar_arrive_expect_tx(&bars[kPIn + kp], kPMsg);
+          if (named_bar_or(1, kSoft, !ok)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) mbar_arrive(&bars[kPFull]);
+        }
       }
-      // every softmax thread finished P (and the V tail), or someone gave up
-      if (named_bar_or(1, kSoft, !ok)) {
-        ok = false;
-        break;
-      }
-      if (lane == 0) mbar_arrive(p_full);
     }
     if (!ok) flags[0] = 1;
 
-    // ---- epilogue: wait for the last P.V, then finalise or write the partial
+    // ---- epilogue: wait for the last P.V, agree on (m, l), then finalise or
+    // write the partial
     const bool have_o = ntiles > 0;
-    if (have_o && ok && !__all_sync(kAll, mbar_wait(pv_done, (ntiles - 1) & 1))) {
+    if (have_o && ok && !__all_sync(kAll, mbar_wait(&bars[kPvDone], (ntiles - 1) & 1))) {
       flags[0] = 1;
       ok = false;
     }
     umma::fence_after_sync();
-    rowx[h * kRows + t] = l_half;
-    named_bar(1, kSoft);
-    const float l_run = rowx[t] + rowx[kRows + t];
+    float l_run;
+    if (c == 0) {
+      // the peer's completion signals for the last two P slots must land
+      // before this CTA may exit
+      for (int j = max(0, ntiles - 2); ok && j < ntiles; ++j)
+        ok = __all_sync(kAll, mbar_wait(&bars[kPSlotFree + (j & 1)], (j >> 1) & 1));
+      if (!ok) flags[0] = 1;
+      rowx[h * kRows + t] = l_half;
+      named_bar(1, kSoft);
+      l_run = rowx[t] + rowx[kRows + t];
+      named_bar(1, kSoft);
+      if (h == 0) {
+        rowx[t] = m_ref;
+        rowx[kRows + t] = l_run;
+      }
+      umma::fence_proxy_async_smem();
+      named_bar(1, kSoft);
+      if (st == 0)
+        bulk_to_peer(map_peer(smem_u32(rowx), peer), smem_u32(rowx), 2 * kRows * 4, peer_bars + 8u * kFin);
+    } else {
+      if (!__all_sync(kAll, mbar_wait(&bars[kFin], 0))) {
+        flags[0] = 1;
+        ok = false;
+      }
+      m_ref = rowx[t];
+      l_run = rowx[kRows + t];
+    }
     if (ok) {
       const bool single = nvalid <= 1;
       float mul = 0.f;
@@ -556,21 +701,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       const int64_t row_g = (int64_t(b) * a.qs + i) * a.Hq + hd;
       float* wrow = a.ws + ((int64_t(b) * a.nsplit + split) * kRows + t) * (kLatent + 4);
-      #pragma unroll
+#pragma unroll
       for (int part = 0; part < kHalf / 64; ++part) {
         float o[32];
-        const uint32_t col_t = kColO + 128u * h + 32u * part;
         if (have_o) {
-          umma::tmem_ld32(tmem + lane_base + col_t, o);
+          umma::tmem_ld32(o_cols + 32u * part, o);
           umma::tmem_ld_wait();
         } else {
-          #pragma unroll
+#pragma unroll
           for (int k = 0; k < 32; ++k) o[k] = 0.f;
         }
         const int col = int(c) * kHalf + 128 * h + 32 * part;
         if (single) {
           uint4* dst = reinterpret_cast<uint4*>(a.out + row_g * kLatent + col);
-          #pragma unroll
+#pragma unroll
           for (int v = 0; v < 4; ++v)
             dst[v] = make_uint4(pack_f32x2(o[8 * v] * mul, o[8 * v + 1] * mul, true),
                                 pack_f32x2(o[8 * v + 2] * mul, o[8 * v + 3] * mul, true),
@@ -578,7 +722,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 pack_f32x2(o[8 * v + 6] * mul, o[8 * v + 7] * mul, true));
         } else {
           float4* dst = reinterpret_cast<float4*>(wrow + col);
-          #pragma unroll
+#pragma unroll
           for (int v = 0; v < 8; ++v) dst[v] = make_float4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
         }
       }
