@@ -16,7 +16,7 @@
 //   swizzle, three-stage mbarrier ring) and computes the partial logits
 //   S_c = Q_c K_c^T with tcgen05.mma (A = its latent query half held in
 //   tensor memory, B = K from shared memory; CTA 1 adds the rope part with A
-//   from shared memory).  CTA 1 ships S_1 (fp32) to CTA 0 with one bulk copy
+//   from shared memory).  CTA 1 ships S_1 (fp32) to CTA 0 with bulk copies
 //   into distributed shared memory, a tile ahead of CTA 0's softmax.  CTA 0
 //   adds it to S_0, runs the only online softmax, and ships P (bf16, already
 //   in UMMA operand layout) with the per-row rescale factors back.  Both CTAs
