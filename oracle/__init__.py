@@ -59,8 +59,13 @@ def _load():
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, ctypes.c_void_p, ctypes.c_double, ctypes.c_double, ctypes.c_double,
                 ctypes.c_int, ctypes.c_double, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
-                ctypes.c_void_p, ctypes.c_int,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
             ]
+            lib.oracle_merge_attn_states.restype = None
+            lib.oracle_merge_attn_states.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 4 + [
+                ctypes.c_void_p, ctypes.c_void_p]
+            lib.oracle_encode_e4m3.restype = ctypes.c_uint32
+            lib.oracle_encode_e4m3.argtypes = [ctypes.c_double]
             lib.oracle_decode.restype = ctypes.c_double
             lib.oracle_decode.argtypes = [ctypes.c_int, ctypes.c_uint32]
             _lib = lib
@@ -90,7 +95,7 @@ def _cpu_contig(t, dtype=None):
 def xqa_attention(q, k_cache, v_cache, page_table, seq_lens, *, num_kv_heads, page_size,
                   kv_layout="NHD", v_head_dim=None, sinks=None, q_scale=1.0, kv_scale=1.0,
                   softmax_scale=None, sliding_win_size=0, rcp_out_scale=1.0, q_seq_len=None,
-                  mask=None, units=None, threads=0):
+                  mask=None, units=None, threads=0, return_lse=False):
     """Exact float64 paged decode attention.
 
     q: [B, q_seq_len, Hq, D] (or [B, Hq, D]) fp16/bf16.  k_cache, v_cache:
@@ -100,6 +105,9 @@ def xqa_attention(q, k_cache, v_cache, page_table, seq_lens, *, num_kv_heads, pa
     seq_lens: [B] (uint32 semantics).  softmax_scale None means 1/sqrt(D).
     units: optional flat row ids (b * q_seq_len + i) * Hq + h; the result is
     then [len(units), Dv], otherwise [B, q_seq_len, Hq, Dv].  float64 tensor.
+    return_lse: also return each row's log-sum-exp (natural log of the
+    normaliser the output was divided by, sink included; -inf for an empty
+    row), shaped [len(units)] or [B, q_seq_len, Hq].
     """
     q = _cpu_contig(q)
     if q.dim() == 3:
@@ -133,19 +141,48 @@ def xqa_attention(q, k_cache, v_cache, page_table, seq_lens, *, num_kv_heads, pa
     if units is not None:
         units = _cpu_contig(units, torch.int64)
         out = torch.empty((units.numel(), Dv), dtype=torch.float64)
+        lse = torch.empty((units.numel(),), dtype=torch.float64)
         n_units = units.numel()
     else:
         out = torch.empty((B, qs, Hq, Dv), dtype=torch.float64)
+        lse = torch.empty((B, qs, Hq), dtype=torch.float64)
         n_units = 0
     rc = _load().oracle_xqa_attention(
         _ptr(q_bits), _DTYPE_CODE[q.dtype], _ptr(k_bits), _ptr(v_bits), kv_code, layout_hnd,
         k_cache.shape[0], _ptr(page_table), page_table.shape[1], _ptr(seq_lens), B, Hq,
         int(num_kv_heads), D, Dv, int(page_size), qs, _ptr(sinks), float(q_scale),
         float(kv_scale), float(softmax_scale), int(sliding_win_size), float(rcp_out_scale),
-        _ptr(mask), _ptr(units), n_units, _ptr(out), int(threads))
+        _ptr(mask), _ptr(units), n_units, _ptr(out), _ptr(lse), int(threads))
     if rc != 0:
         raise ValueError(f"oracle rejected the problem (code {rc})")
-    return out
+    return (out, lse) if return_lse else out
+
+
+def merge_attn_states(prefix_out, prefix_lse, suffix_out, suffix_lse, n_with_prefix=None):
+    """merge_attn_states (Kimi-K3 MultiHeadLatentAttention page, prefill with
+    chunked context) in float64: outputs [T, H, D] with log-sum-exps [T, H];
+    rows t >= n_with_prefix take the suffix unchanged.  Returns (out, lse)."""
+    po = _cpu_contig(prefix_out, torch.float64)
+    so = _cpu_contig(suffix_out, torch.float64)
+    pl = _cpu_contig(prefix_lse, torch.float64)
+    sl = _cpu_contig(suffix_lse, torch.float64)
+    T, H, D = so.shape
+    if tuple(po.shape) != (T, H, D) or tuple(pl.shape) != (T, H) or tuple(sl.shape) != (T, H):
+        raise ValueError("outputs must be [T, H, D] and lse [T, H]")
+    n = T if n_with_prefix is None else int(n_with_prefix)
+    out = torch.empty((T, H, D), dtype=torch.float64)
+    lse = torch.empty((T, H), dtype=torch.float64)
+    _load().oracle_merge_attn_states(_ptr(po), _ptr(pl), _ptr(so), _ptr(sl), T, H, D, n, _ptr(out),
+                                     _ptr(lse))
+    return out, lse
+
+
+def encode_e4m3(x) -> torch.Tensor:
+    """OCP E4M3FN codes (uint8) of float64 values: round to nearest even,
+    saturating at +-448 (the oracle's rounding of an fp8 output)."""
+    x = _cpu_contig(x, torch.float64).reshape(-1)
+    enc = _load().oracle_encode_e4m3
+    return torch.tensor([enc(float(v)) for v in x.tolist()], dtype=torch.uint8)
 
 
 def unit_ids(batch_idx, q_idx, head_idx, q_seq_len, num_q_heads):

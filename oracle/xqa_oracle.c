@@ -137,7 +137,8 @@ static int orc_mask_bit(const orc_problem* P, int b, int i, int64_t j) {
 
 /* One output row: unit = (b * q_seq_len + i) * Hq + h.  Returns 0, or -1 for
  * an out-of-range page, or -2 for a sequence longer than the page table. */
-static int orc_one_row(const orc_problem* P, int64_t unit, double* out_row, double* logits) {
+static int orc_one_row(const orc_problem* P, int64_t unit, double* out_row, double* logits,
+                       double* lse) {
   int Hq = P->num_q_heads, G = P->num_q_heads / P->num_kv_heads;
   int h = (int)(unit % Hq);
   int i = (int)((unit / Hq) % P->q_seq_len);
@@ -173,6 +174,7 @@ static int orc_one_row(const orc_problem* P, int64_t unit, double* out_row, doub
 
   /* step 2: normaliser and weighted sum of values */
   for (int d = 0; d < P->v_head_dim; ++d) out_row[d] = 0.0;
+  *lse = -INFINITY;
   if (m == -INFINITY) return 0; /* nothing visible and no sink */
   double z = exp(sigma - m);
   for (int64_t t = 0; t < L; ++t) {
@@ -183,6 +185,9 @@ static int orc_one_row(const orc_problem* P, int64_t unit, double* out_row, doub
     for (int d = 0; d < P->v_head_dim; ++d) out_row[d] += w * orc_load(P->v_cache, P->kv_dtype, off + d);
   }
   for (int d = 0; d < P->v_head_dim; ++d) out_row[d] = P->rcp_out_scale * P->kv_scale * out_row[d] / z;
+  /* log-sum-exp of the row's logits (natural log), the sink included: the
+   * normaliser that the output was divided by, as merge_attn_states takes it */
+  *lse = m + log(z);
   return 0;
 }
 
@@ -198,7 +203,7 @@ int oracle_xqa_attention(const void* q, int q_dtype, const void* k_cache, const 
                          int q_seq_len, const float* sinks, double q_scale, double kv_scale,
                          double softmax_scale, int sliding_win_size, double rcp_out_scale,
                          const uint16_t* mask, const int64_t* units, int64_t n_units, double* out,
-                         int n_threads) {
+                         double* lse, int n_threads) {
   if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return -3;
   if (head_dim <= 0 || v_head_dim <= 0 || v_head_dim > head_dim || page_size <= 0) return -3;
   if (q_seq_len <= 0 || pages_per_seq <= 0 || sliding_win_size < 0) return -3;
@@ -221,7 +226,10 @@ int oracle_xqa_attention(const void* q, int q_dtype, const void* k_cache, const 
 #endif
     for (int64_t k = 0; k < n; ++k) {
       int64_t unit = units ? units[k] : k;
-      int rc = (unit < 0 || unit >= total) ? -3 : orc_one_row(&P, unit, out + k * v_head_dim, logits);
+      double row_lse = -INFINITY;
+      int rc = (unit < 0 || unit >= total) ? -3
+                                           : orc_one_row(&P, unit, out + k * v_head_dim, logits, &row_lse);
+      if (lse) lse[k] = row_lse;
       if (rc) {
 #ifdef _OPENMP
 #pragma omp critical
@@ -232,4 +240,64 @@ int oracle_xqa_attention(const void* q, int q_dtype, const void* k_cache, const 
     free(logits);
   }
   return status;
+}
+
+/*
+ * merge_attn_states (vLLM Kimi-K3 MultiHeadLatentAttention page, the prefill
+ * path with chunked context): two attention results over disjoint key sets,
+ * each normalised by its own sum, with their log-sum-exps, combine into the
+ * result over the union:
+ *   M = max(lse_p, lse_s),  w_p = exp(lse_p - M),  w_s = exp(lse_s - M),
+ *   out = (w_p * out_p + w_s * out_s) / (w_p + w_s),  lse = M + log(w_p + w_s).
+ * Rows t >= n_with_prefix have no prefix: they take the suffix unchanged.  A
+ * side whose lse is -inf (no visible key) gets weight 0; both -inf gives 0.
+ * Layout: out_*[T][H][D], lse_*[T][H]; all float64.
+ */
+void oracle_merge_attn_states(const double* out_p, const double* lse_p, const double* out_s,
+                              const double* lse_s, int64_t T, int64_t H, int64_t D,
+                              int64_t n_with_prefix, double* out, double* lse) {
+  for (int64_t t = 0; t < T; ++t)
+    for (int64_t h = 0; h < H; ++h) {
+      const int64_t r = t * H + h;
+      double wp = 0.0, ws = 1.0, M = lse_s[r];
+      if (t < n_with_prefix) {
+        M = lse_p[r] > lse_s[r] ? lse_p[r] : lse_s[r];
+        wp = M == -INFINITY ? 0.0 : exp(lse_p[r] - M);
+        ws = M == -INFINITY ? 0.0 : exp(lse_s[r] - M);
+      }
+      const double z = wp + ws;
+      for (int64_t d = 0; d < D; ++d)
+        out[r * D + d] = z == 0.0 ? 0.0 : (wp * out_p[r * D + d] + ws * out_s[r * D + d]) / z;
+      lse[r] = z == 0.0 ? -INFINITY : M + log(z);
+    }
+}
+
+/*
+ * OCP FP8 E4M3FN encoding of x (sign, 4 exponent bits with bias 7, 3 mantissa
+ * bits; no infinities, S.1111.111 is NaN): round to nearest, ties to even, and
+ * saturate finite values beyond the largest magnitude 448 to +-448.  NaN maps
+ * to 0x7f.
+ */
+uint32_t oracle_encode_e4m3(double x) {
+  if (isnan(x)) return 0x7fu;
+  uint32_t sign = signbit(x) ? 0x80u : 0u;
+  double a = fabs(x);
+  if (a >= 448.0) return sign | 0x7eu;
+  /* the representable magnitudes are k * 2^(e-3) for normals (e >= -6, k in
+   * 8..15) and k * 2^-9 for subnormals (k in 0..7): scale to the spacing and
+   * round the integer k, ties to even */
+  int ex = 0;
+  if (a > 0.0) frexp(a, &ex); /* a = f * 2^ex, f in [0.5, 1): floor(log2 a) = ex - 1 */
+  int e = a > 0.0 ? ex - 1 : -7;
+  if (e < -6) e = -6;
+  double q = ldexp(a, 3 - e); /* position in units of the spacing at exponent e */
+  double k = floor(q);
+  double rem = q - k;
+  if (rem > 0.5 || (rem == 0.5 && fmod(k, 2.0) != 0.0)) k += 1.0;
+  if (k >= 16.0) { k = 8.0; e += 1; } /* carried into the next binade */
+  if (e > 8 || (e == 8 && k > 14.0)) return sign | 0x7eu;
+  uint32_t code;
+  if (k < 8.0) code = (uint32_t)k; /* subnormal (only possible at e = -6) */
+  else code = ((uint32_t)(e + 7) << 3) | ((uint32_t)k - 8u);
+  return sign | code;
 }
