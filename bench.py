@@ -80,8 +80,8 @@ def peaks():
 
 
 KERNEL_FILES = {
-    "gqa_decode_kernel": ("gqa_", "ptx.cuh", "kernel_args.h"),
-    "mla_decode_kernel": ("mla_", "umma.cuh", "ptx.cuh", "kernel_args.h"),
+    "gqa_decode_kernel": ("gqa_", "ptx.cuh", "kernel_args.h", "finalize.cuh"),
+    "mla_decode_kernel": ("mla_", "umma.cuh", "ptx.cuh", "kernel_args.h", "finalize.cuh"),
 }
 
 

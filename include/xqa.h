@@ -104,6 +104,13 @@ typedef struct xqa_params {
   int32_t sm_count;   /* SMs to plan for; 0 = the current device's count */
   int32_t enable_pdl; /* programmatic dependent launch; accepted, no numeric effect */
   uint32_t* error_word; /* optional device word; bit 0 = clamped length or bad page index */
+  /* Optional fp32 [batch, q_seq_len, num_q_heads], or NULL: each row's
+     log-sum-exp, the natural log of the normaliser its output was divided by
+     (visible logits and the sink; -inf for a row with neither).  It is the
+     `lse` that forward_mqa returns next to the latent output (vLLM Kimi-K3
+     MultiHeadLatentAttention page, forward), in the units merge_attn_states
+     takes (same page, the prefill path with chunked context). */
+  float* lse;
 } xqa_params;
 
 /* Bytes of workspace xqa_decode needs for these parameters when planning for
@@ -152,6 +159,43 @@ xqa_status xqa_mla_decode(const xqa_params* params, int v_head_dim, void* worksp
      needs on `stream` before launching; the workspace keeps the last call's
      contents, which no call reads before writing. */
 xqa_status xqa_decode_noalloc(const xqa_params* params, xqa_stream_t stream);
+
+/* merge_attn_states (vLLM Kimi-K3 MultiHeadLatentAttention page, the prefill
+   path with chunked context): two attention results over disjoint key sets of
+   the same query rows, each normalised by its own sum, combine into the result
+   over the union of the keys:
+     M = max(lse_p, lse_s), w_p = e^(lse_p - M), w_s = e^(lse_s - M),
+     out = (w_p out_p + w_s out_s) / (w_p + w_s), lse = M + ln(w_p + w_s).
+   A side whose lse is -inf (no visible key) weighs 0; both -inf gives 0 and
+   -inf.  Rows of tokens t >= tokens_with_prefix have no prefix and take the
+   suffix unchanged (the page's prefill_tokens_with_context).
+   Outputs are fp16 or bf16 [num_tokens, num_heads, head_dim] with element
+   strides between tokens and between heads (head_dim contiguous; strides and
+   pointers 16-byte aligned, head_dim a multiple of 8), so a prefix result wider
+   than head_dim (a latent slice) is read in place.  lse arrays are fp32 with
+   their own token and head strides, shared by the three of them.  output_lse
+   may be NULL.  All memory is caller-owned device memory; the call is
+   asynchronous on `stream`.  Returns XQA_ERR_INVALID_ARG for bad shapes,
+   strides or alignment, before any launch. */
+typedef struct xqa_merge_params {
+  void* output;
+  const void* prefix_output;
+  const void* suffix_output;
+  xqa_dtype dtype;            /* of all three outputs: XQA_F16 or XQA_BF16 */
+  float* output_lse;          /* NULL: not written */
+  const float* prefix_lse;
+  const float* suffix_lse;
+  int64_t num_tokens;
+  int32_t num_heads;
+  int32_t head_dim;
+  int64_t tokens_with_prefix; /* 0 .. num_tokens */
+  int64_t out_stride_token, out_stride_head;       /* elements */
+  int64_t prefix_stride_token, prefix_stride_head; /* elements */
+  int64_t suffix_stride_token, suffix_stride_head; /* elements */
+  int64_t lse_stride_token, lse_stride_head;       /* floats */
+} xqa_merge_params;
+
+xqa_status xqa_merge_attn_states(const xqa_merge_params* params, xqa_stream_t stream);
 
 /* Human-readable name of a status code (static string). */
 const char* xqa_status_string(xqa_status status);

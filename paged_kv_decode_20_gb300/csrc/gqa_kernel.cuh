@@ -28,6 +28,7 @@
 //     the output and resets the semaphore to zero.  No CTA ever waits on
 //     another.
 #pragma once
+#include "finalize.cuh"
 #include "kernel_args.h"
 #include "ptx.cuh"
 
@@ -554,8 +555,6 @@ __global__ void __launch_bounds__(160, 2)
   const int rows_here = min(C::kRows, a.R - rg * C::kRows);
   const int row_stride = D + 4;  // O, then m and l; padded so rows stay 16-byte aligned
   float* ws_unit = a.ws + (int64_t(unit) * a.nsplit) * C::kRows * row_stride;
-  uint16_t* out16 = static_cast<uint16_t*>(a.out);
-  const bool obf = a.q_bf16 != 0;
 
   // phase 1: one thread per row folds the four warps' maxima (and, with one
   // split, the sink and the output scales) into one weight per warp
@@ -577,12 +576,7 @@ __global__ void __launch_bounds__(160, 2)
     if (single) {
       const int r = rg * C::kRows + row;
       const float sig = a.sinks ? __ldg(a.sinks + kvh * a.G + r % a.G) * kLog2e : -INFINITY;
-      const float Mf = fmaxf(M, sig);
-      mul = 0.f;
-      if (Mf != -INFINITY) {
-        const float fm = (M == -INFINITY) ? 0.f : exp2f(M - Mf);
-        mul = fm * out_mul / (l * fm + ((sig == -INFINITY) ? 0.f : exp2f(sig - Mf)));
-      }
+      mul = finalize_row(M, l, sig, out_mul, a.lse ? a.lse + lse_index(a, b, kvh, r) : nullptr);
     } else {
       sc_ml[2 * row] = M;
       sc_ml[2 * row + 1] = l;
@@ -609,8 +603,7 @@ __global__ void __launch_bounds__(160, 2)
       const int r = rg * C::kRows + row;
       const int i = r / a.G, gg = r % a.G;
       const int64_t oi = ((int64_t(b) * a.qs + i) * a.Hq + int64_t(kvh) * a.G + gg) * a.Dv + dv;
-      *reinterpret_cast<uint2*>(out16 + oi) =
-          make_uint2(pack_f32x2(acc.x, acc.y, obf), pack_f32x2(acc.z, acc.w, obf));
+      store_out4(a, oi, acc);
     } else {
       float* dst = ws_unit + (int64_t(split) * C::kRows + row) * row_stride;
       *reinterpret_cast<float4*>(dst + dv) = acc;
@@ -651,12 +644,7 @@ __global__ void __launch_bounds__(160, 2)
     }
     const int r = rg * C::kRows + row;
     const float sig = a.sinks ? __ldg(a.sinks + kvh * a.G + r % a.G) * kLog2e : -INFINITY;
-    const float Mf = fmaxf(M, sig);
-    float mul = 0.f;
-    if (Mf != -INFINITY) {
-      const float f = (M == -INFINITY) ? 0.f : exp2f(M - Mf);
-      mul = f * out_mul / (l * f + ((sig == -INFINITY) ? 0.f : exp2f(sig - Mf)));
-    }
+    const float mul = finalize_row(M, l, sig, out_mul, a.lse ? a.lse + lse_index(a, b, kvh, r) : nullptr);
     for (int sp = 0; sp < nvalid; ++sp) wts[row * nvalid + sp] *= mul;
   }
   __syncthreads();
@@ -693,8 +681,7 @@ __global__ void __launch_bounds__(160, 2)
     const int r = rg * C::kRows + row;
     const int i = r / a.G, gg = r % a.G;
     const int64_t oi = ((int64_t(b) * a.qs + i) * a.Hq + int64_t(kvh) * a.G + gg) * a.Dv + dv;
-    *reinterpret_cast<uint2*>(out16 + oi) =
-        make_uint2(pack_f32x2(acc.x, acc.y, obf), pack_f32x2(acc.z, acc.w, obf));
+    store_out4(a, oi, acc);
   }
   if (tid == 0) a.sems[unit] = 0u;
 }

@@ -18,6 +18,7 @@ struct DecodeArgs {
   float* ws;                   // split partials
   uint32_t* sems;              // one ticket counter per (b, kvh, row group)
   uint32_t* err;               // optional error word
+  float* lse;                  // optional [B, qs, Hq] natural-log log-sum-exp per row
   int64_t num_pages;
   int B, Hq, Hkv, G, qs, R;    // R = qs * G rows per kv head
   int ps, pps, win;            // page size, pages per sequence, sliding window
@@ -27,7 +28,8 @@ struct DecodeArgs {
   int mask_words;              // uint16 per mask row
   int Dv;
   float q_scale, kv_scale, softmax_scale, rcp_out_scale;
-  int q_bf16;                  // q and out are bf16 (else f16)
+  int q_bf16;                  // q (and a 16-bit out) are bf16 (else f16)
+  int out_e4m3;                // out is float8_e4m3fn (rounded to nearest, saturated at +-448)
   int hnd;                     // cache layout HND (else NHD)
   int pdl;                     // launched with programmatic stream serialization
 };

@@ -38,6 +38,7 @@
 #include <algorithm>
 #include <mutex>
 
+#include "finalize.cuh"
 #include "kernel_args.h"
 #include "mla_launch.h"
 #include "ptx.cuh"
@@ -126,6 +127,7 @@ struct MlaArgs {
   float* ws;
   uint32_t* sems;
   uint32_t* err;
+  float* lse;  // optional [B, qs, Hq] natural-log log-sum-exp per row
   int64_t num_pages;
   int B, Hq, qs, ps, pps, win, nsplit, split_pages, mask_words;
   float q_scale, kv_scale, softmax_scale, rcp_out_scale;
@@ -690,16 +692,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (ok) {
       const bool single = nvalid <= 1;
       float mul = 0.f;
+      const int64_t row_g = (int64_t(b) * a.qs + i) * a.Hq + hd;
       if (single) {
         const float sig = a.sinks ? __ldg(a.sinks + hd) * kLog2e : -INFINITY;
-        const float Mf = fmaxf(m_ref, sig);
-        if (Mf != -INFINITY) {
-          const float f = m_ref == -INFINITY ? 0.f : exp2f(m_ref - Mf);
-          const float den = l_run * f + (sig == -INFINITY ? 0.f : exp2f(sig - Mf));
-          mul = f * kv_scale * a.rcp_out_scale / den;
-        }
+        mul = finalize_row(m_ref, l_run, sig, kv_scale * a.rcp_out_scale,
+                           (a.lse && c == 0 && h == 0) ? a.lse + row_g : nullptr);
       }
-      const int64_t row_g = (int64_t(b) * a.qs + i) * a.Hq + hd;
       float* wrow = a.ws + ((int64_t(b) * a.nsplit + split) * kRows + t) * (kLatent + 4);
 #pragma unroll
       for (int part = 0; part < kHalf / 64; ++part) {
@@ -778,12 +776,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       l += f * __ldcg(src + 1);
     }
     const float sig = a.sinks ? __ldg(a.sinks + row % a.Hq) * kLog2e : -INFINITY;
-    const float Mf = fmaxf(M, sig);
-    float mul = 0.f;
-    if (Mf != -INFINITY) {
-      const float f = M == -INFINITY ? 0.f : exp2f(M - Mf);
-      mul = f * kv_scale * a.rcp_out_scale / (l * f + (sig == -INFINITY ? 0.f : exp2f(sig - Mf)));
-    }
+    const int64_t row_g = (int64_t(b) * a.qs + row / a.Hq) * a.Hq + row % a.Hq;
+    const float mul = finalize_row(M, l, sig, kv_scale * a.rcp_out_scale,
+                                   (a.lse && c == 0) ? a.lse + row_g : nullptr);
     for (int sp = 0; sp < nvalid; ++sp) wts[row * nvalid + sp] *= mul;
   }
   __syncthreads();
@@ -975,6 +970,7 @@ xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_b
   a.ws = static_cast<float*>(ws);
   a.sems = sems;
   a.err = p->error_word;
+  a.lse = p->lse;
   a.num_pages = p->num_pages;
   a.B = p->batch_size;
   a.Hq = p->num_q_heads;

@@ -90,6 +90,7 @@ xqa_status validate_common(const xqa_params* p) {
   if (!p->q || !p->k_cache || !p->v_cache || !p->page_table || !p->seq_lens || !p->output)
     return fail(XQA_ERR_INVALID_ARG, "q, k_cache, v_cache, page_table, seq_lens and output are required");
   if (p->batch_size < 1) return fail(XQA_ERR_INVALID_ARG, "batch_size must be >= 1, got %d", p->batch_size);
+  if (reinterpret_cast<uintptr_t>(p->lse) & 3) return fail(XQA_ERR_INVALID_ARG, "lse must be 4-byte aligned");
   if (p->num_q_heads < 1 || p->num_kv_heads < 1)
     return fail(XQA_ERR_INVALID_ARG, "num_q_heads and num_kv_heads must be >= 1");
   if (p->num_q_heads % p->num_kv_heads)
@@ -106,8 +107,9 @@ xqa_status validate_common(const xqa_params* p) {
   if (!is_16bit(p->q_dtype)) return fail(XQA_ERR_INVALID_ARG, "q dtype must be float16 or bfloat16");
   if (!(p->kv_dtype == p->q_dtype || p->kv_dtype == XQA_E4M3))
     return fail(XQA_ERR_INVALID_ARG, "kv dtype must match q's dtype or be float8_e4m3fn");
-  if (p->out_dtype != p->q_dtype)
-    return fail(XQA_ERR_UNSUPPORTED, "output dtype must equal the query dtype (fp8 output is not built)");
+  // the output dtype matches the query, or the fp8 cache (API page, `output`)
+  if (!(p->out_dtype == p->q_dtype || (p->out_dtype == XQA_E4M3 && p->kv_dtype == XQA_E4M3)))
+    return fail(XQA_ERR_UNSUPPORTED, "output dtype must equal the query dtype, or be float8_e4m3fn with an fp8 cache");
   if (p->head_dim < 1) return fail(XQA_ERR_INVALID_ARG, "head_dim must be >= 1");
   const int64_t big = int64_t(1) << 31;
   if (p->num_pages * std::max(p->page_size, p->num_kv_heads) >= big ||
@@ -253,6 +255,7 @@ void fill_args(const xqa_params* p, const Plan& pl, void* ws, uint32_t* sems, xq
   a->ws = static_cast<float*>(ws);
   a->sems = sems;
   a->err = p->error_word;
+  a->lse = p->lse;
   a->num_pages = p->num_pages;
   a->B = p->batch_size;
   a->Hq = p->num_q_heads;
@@ -273,6 +276,7 @@ void fill_args(const xqa_params* p, const Plan& pl, void* ws, uint32_t* sems, xq
   a->softmax_scale = p->softmax_scale != 0.f ? p->softmax_scale : 1.0f / sqrtf(float(pl.D));
   a->rcp_out_scale = p->rcp_out_scale;
   a->q_bf16 = p->q_dtype == XQA_BF16;
+  a->out_e4m3 = p->out_dtype == XQA_E4M3;
   a->hnd = p->kv_layout == XQA_HND;
   a->pdl = p->enable_pdl != 0;
 }

@@ -13,19 +13,20 @@ from . import xqa as X
 
 
 class Decoder:
-    def __init__(self, case, sm_count=None, error_word=True):
+    def __init__(self, case, sm_count=None, error_word=True, lse=False, out_dtype=None):
         if not case.q.is_cuda:
             raise ValueError("Decoder needs the problem on a CUDA device")
         self.case = case
         dev = case.q.device
         B, qs, Hq, _ = case.q.shape
-        self.output = torch.empty((B, qs, Hq, case.dv), dtype=case.q.dtype, device=dev)
+        self.output = torch.empty((B, qs, Hq, case.dv), dtype=out_dtype or case.q.dtype, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev) if error_word else None
+        self.lse = torch.empty((B, qs, Hq), dtype=torch.float32, device=dev) if lse else None
         kw = case.kwargs()
         v_head_dim = kw.pop("v_head_dim")
         self.params = X.make_params(case.q, case.k_cache, case.v_cache, case.page_table,
                                     case.seq_lens, self.output, q_seq_len=qs, sm_count=sm_count,
-                                    error_word=self.err, **kw)
+                                    error_word=self.err, lse=self.lse, **kw)
         self.mla = case.mla
         self.v_head_dim = case.dv
         if self.mla:

@@ -62,12 +62,39 @@ class XqaParams(ctypes.Structure):
         ("sm_count", ctypes.c_int32),
         ("enable_pdl", ctypes.c_int32),
         ("error_word", ctypes.c_void_p),
+        ("lse", ctypes.c_void_p),
+    ]
+
+
+class XqaMergeParams(ctypes.Structure):
+    """Mirror of ``struct xqa_merge_params``."""
+
+    _fields_ = [
+        ("output", ctypes.c_void_p),
+        ("prefix_output", ctypes.c_void_p),
+        ("suffix_output", ctypes.c_void_p),
+        ("dtype", ctypes.c_int),
+        ("output_lse", ctypes.c_void_p),
+        ("prefix_lse", ctypes.c_void_p),
+        ("suffix_lse", ctypes.c_void_p),
+        ("num_tokens", ctypes.c_int64),
+        ("num_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("tokens_with_prefix", ctypes.c_int64),
+        ("out_stride_token", ctypes.c_int64),
+        ("out_stride_head", ctypes.c_int64),
+        ("prefix_stride_token", ctypes.c_int64),
+        ("prefix_stride_head", ctypes.c_int64),
+        ("suffix_stride_token", ctypes.c_int64),
+        ("suffix_stride_head", ctypes.c_int64),
+        ("lse_stride_token", ctypes.c_int64),
+        ("lse_stride_head", ctypes.c_int64),
     ]
 
 
 EXPORTS = ["xqa_workspace_size", "xqa_semaphore_count", "xqa_decode", "xqa_mla_workspace_size",
-           "xqa_mla_semaphore_count", "xqa_mla_decode", "xqa_decode_noalloc", "xqa_status_string",
-           "xqa_last_error"]
+           "xqa_mla_semaphore_count", "xqa_mla_decode", "xqa_decode_noalloc", "xqa_merge_attn_states",
+           "xqa_status_string", "xqa_last_error"]
 
 _lock = threading.Lock()
 _lib = None
@@ -102,6 +129,8 @@ def load(path: str = LIB_PATH):
             lib.xqa_mla_decode.argtypes = [P, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
                                            ctypes.c_void_p, ctypes.c_void_p]
             lib.xqa_mla_decode.restype = ctypes.c_int
+            lib.xqa_merge_attn_states.argtypes = [ctypes.POINTER(XqaMergeParams), ctypes.c_void_p]
+            lib.xqa_merge_attn_states.restype = ctypes.c_int
             lib.xqa_status_string.argtypes = [ctypes.c_int]
             lib.xqa_status_string.restype = ctypes.c_char_p
             lib.xqa_last_error.argtypes = []
@@ -141,7 +170,7 @@ def _q_view(q, q_seq_len):
 def make_params(q, k_cache, v_cache, page_table, seq_lens, output, *, num_kv_heads, page_size,
                 sinks=None, q_scale=1.0, kv_scale=1.0, sliding_win_size=0, kv_layout="NHD",
                 sm_count=None, enable_pdl=None, rcp_out_scale=1.0, q_seq_len=1, mask=None,
-                softmax_scale=None, error_word=None):
+                softmax_scale=None, error_word=None, lse=None):
     """Build the C parameter struct; shapes are inferred as the API page
     states (B from q, Hq from q.shape[-2], D from q.shape[-1], dtypes from q
     and k_cache, max_seq_len = page_table.shape[-1] * page_size)."""
@@ -168,8 +197,11 @@ def make_params(q, k_cache, v_cache, page_table, seq_lens, output, *, num_kv_hea
             raise ValueError(f"mask must be 16-bit [{q4.shape[0]}, {q_seq_len}, {words}]")
         if not mask.is_contiguous():
             raise ValueError("mask must be contiguous")
+    if lse is not None:
+        if lse.dtype != torch.float32 or tuple(lse.shape) != tuple(q4.shape[:3]) or not lse.is_contiguous():
+            raise ValueError(f"lse must be contiguous float32 {tuple(q4.shape[:3])}")
     p = XqaParams()
-    keep = [q4, k_cache, v_cache, page_table, seq_lens, output, sinks, mask, error_word]
+    keep = [q4, k_cache, v_cache, page_table, seq_lens, output, sinks, mask, error_word, lse]
     p.q = _ptr(q4)
     p.q_dtype = _DTYPES[q4.dtype]
     p.k_cache = _ptr(k_cache)
@@ -213,6 +245,7 @@ def make_params(q, k_cache, v_cache, page_table, seq_lens, output, *, num_kv_hea
     p.sm_count = 0 if sm_count is None else int(sm_count)
     p.enable_pdl = 1 if enable_pdl is None else int(bool(enable_pdl))
     p.error_word = _ptr(error_word)
+    p.lse = _ptr(lse)
     # the struct holds raw pointers: keep every tensor it names alive with it
     p._keep = keep
     return p
@@ -275,27 +308,61 @@ def xqa_mla_decode(params: XqaParams, v_head_dim, workspace, semaphores, stream=
 def xqa(q, k_cache, v_cache, page_table, seq_lens, output, workspace_buffer, semaphores,
         num_kv_heads, page_size, sinks=None, q_scale=1.0, kv_scale=1.0, sliding_win_size=0,
         kv_layout="NHD", sm_count=None, enable_pdl=None, rcp_out_scale=1.0, q_seq_len=1,
-        mask=None, softmax_scale=None, error_word=None, stream=None):
+        mask=None, softmax_scale=None, error_word=None, lse=None, stream=None):
     """Paged decode attention with the XQA API page's argument list; writes
-    ``output`` in place.  workspace_buffer: uint8, at least
+    ``output`` in place (and, when given, each row's log-sum-exp into ``lse``,
+    float32 [B, q_seq_len, Hq]).  workspace_buffer: uint8, at least
     ``xqa_workspace_size`` bytes; semaphores: uint32/int32, zeroed, at least
     ``xqa_semaphore_count`` entries (left zeroed)."""
     p = make_params(q, k_cache, v_cache, page_table, seq_lens, output, num_kv_heads=num_kv_heads,
                     page_size=page_size, sinks=sinks, q_scale=q_scale, kv_scale=kv_scale,
                     sliding_win_size=sliding_win_size, kv_layout=kv_layout, sm_count=sm_count,
                     enable_pdl=enable_pdl, rcp_out_scale=rcp_out_scale, q_seq_len=q_seq_len,
-                    mask=mask, softmax_scale=softmax_scale, error_word=error_word)
+                    mask=mask, softmax_scale=softmax_scale, error_word=error_word, lse=lse)
     xqa_decode(p, workspace_buffer, semaphores, stream)
 
 
 def xqa_mla(q, kv_cache, page_table, seq_lens, output, workspace_buffer, semaphores, page_size,
             v_head_dim, softmax_scale, kv_layout="NHD", q_scale=1.0, kv_scale=1.0,
-            sm_count=None, rcp_out_scale=1.0, error_word=None, stream=None):
+            sm_count=None, rcp_out_scale=1.0, error_word=None, lse=None, stream=None):
     """MLA latent decode: q [B, Hq, Lr + rope] (absorbed), one latent kv head
     ``kv_cache`` [num_pages, page_size, 1, Lr + rope]; output [B, Hq, Lr]."""
     q_seq_len = 1 if q.dim() == 3 else q.shape[1]
     p = make_params(q, kv_cache, kv_cache, page_table, seq_lens, output, num_kv_heads=1,
                     page_size=page_size, q_scale=q_scale, kv_scale=kv_scale, kv_layout=kv_layout,
                     sm_count=sm_count, rcp_out_scale=rcp_out_scale, q_seq_len=q_seq_len,
-                    softmax_scale=softmax_scale, error_word=error_word)
+                    softmax_scale=softmax_scale, error_word=error_word, lse=lse)
     xqa_mla_decode(p, v_head_dim, workspace_buffer, semaphores, stream)
+
+
+def merge_attn_states(output, prefix_output, prefix_lse, suffix_output, suffix_lse,
+                      tokens_with_prefix=None, output_lse=None, stream=None):
+    """merge_attn_states (Kimi-K3 MultiHeadLatentAttention page, prefill with
+    chunked context) through the C ABI.  Outputs are [T, H, D] fp16/bf16 views
+    with a contiguous last dim (a prefix wider than D may be a slice); lse
+    tensors are float32 [T, H] sharing one stride pattern.  Rows of tokens
+    t >= tokens_with_prefix (default T) take the suffix unchanged."""
+    T, H, D = suffix_output.shape
+    for name, t in (("output", output), ("prefix_output", prefix_output)):
+        if tuple(t.shape) != (T, H, D):
+            raise ValueError(f"{name} must be [{T}, {H}, {D}]")
+    for t in (output, prefix_output, suffix_output):
+        if t.stride(-1) != 1 or t.dtype != suffix_output.dtype:
+            raise ValueError("outputs must share one dtype and have a contiguous last dim")
+    lses = [x for x in (prefix_lse, suffix_lse, output_lse) if x is not None]
+    for x in lses:
+        if x.dtype != torch.float32 or tuple(x.shape) != (T, H) or x.stride() != suffix_lse.stride():
+            raise ValueError(f"lse tensors must be float32 [{T}, {H}] with identical strides")
+    if suffix_output.dtype not in (torch.float16, torch.bfloat16):
+        raise ValueError("merge works on fp16 or bf16 outputs")
+    p = XqaMergeParams()
+    p.output, p.prefix_output, p.suffix_output = _ptr(output), _ptr(prefix_output), _ptr(suffix_output)
+    p.dtype = _DTYPES[suffix_output.dtype]
+    p.output_lse, p.prefix_lse, p.suffix_lse = _ptr(output_lse), _ptr(prefix_lse), _ptr(suffix_lse)
+    p.num_tokens, p.num_heads, p.head_dim = T, H, D
+    p.tokens_with_prefix = T if tokens_with_prefix is None else int(tokens_with_prefix)
+    p.out_stride_token, p.out_stride_head = output.stride(0), output.stride(1)
+    p.prefix_stride_token, p.prefix_stride_head = prefix_output.stride(0), prefix_output.stride(1)
+    p.suffix_stride_token, p.suffix_stride_head = suffix_output.stride(0), suffix_output.stride(1)
+    p.lse_stride_token, p.lse_stride_head = suffix_lse.stride(0), suffix_lse.stride(1)
+    _check(load().xqa_merge_attn_states(ctypes.byref(p), _stream(stream)))

@@ -92,6 +92,7 @@ BAD = [
     (dict(q_dtype=X.XQA_E4M3, out_dtype=X.XQA_E4M3), X.XQA_ERR_INVALID_ARG, "q dtype"),
     (dict(kv_dtype=X.XQA_F16), X.XQA_ERR_INVALID_ARG, "kv dtype"),
     (dict(out_dtype=X.XQA_F16), X.XQA_ERR_UNSUPPORTED, "output dtype"),
+    (dict(out_dtype=X.XQA_E4M3), X.XQA_ERR_UNSUPPORTED, "fp8 cache"),
     (dict(head_dim=96), X.XQA_ERR_UNSUPPORTED, "head_dim"),
     (dict(kv_dtype=X.XQA_E4M3, head_dim=64), X.XQA_ERR_UNSUPPORTED, "head_dim"),
     (dict(k_cache=0x10008), X.XQA_ERR_INVALID_ARG, "16-byte"),
@@ -131,3 +132,64 @@ def test_product_path_never_touches_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
                 assert "xqa_oracle" not in text, f
+
+
+def test_merge_params_struct_layout_matches_c(tmp_path):
+    fields = [f for f, _ in X.XqaMergeParams._fields_]
+    prog = ["#include <stdio.h>", "#include <stddef.h>", '#include "xqa.h"', "int main(void){",
+            'printf("%zu\\n", sizeof(xqa_merge_params));']
+    prog += [f'printf("%zu\\n", offsetof(xqa_merge_params, {f}));' for f in fields]
+    prog += ["return 0;}"]
+    src = tmp_path / "mlayout.c"
+    src.write_text("\n".join(prog))
+    exe = tmp_path / "mlayout"
+    subprocess.run(["gcc", "-I" + os.path.dirname(HEADER), str(src), "-o", str(exe)], check=True)
+    vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                           check=True).stdout.split()]
+    assert vals[0] == ctypes.sizeof(X.XqaMergeParams)
+    for f, off in zip(fields, vals[1:]):
+        assert getattr(X.XqaMergeParams, f).offset == off, f
+
+
+def fake_merge(**over):
+    """A well-formed merge parameter block with fake (never dereferenced) pointers."""
+    p = X.XqaMergeParams()
+    p.output = p.prefix_output = p.suffix_output = 0x10000
+    p.output_lse = p.prefix_lse = p.suffix_lse = 0x20000
+    p.dtype = X.XQA_BF16
+    p.num_tokens, p.num_heads, p.head_dim, p.tokens_with_prefix = 4, 2, 64, 4
+    p.out_stride_token = p.prefix_stride_token = p.suffix_stride_token = 128
+    p.out_stride_head = p.prefix_stride_head = p.suffix_stride_head = 64
+    p.lse_stride_token, p.lse_stride_head = 2, 1
+    for k, v in over.items():
+        setattr(p, k, v)
+    return p
+
+
+MERGE_BAD = [
+    (dict(dtype=X.XQA_E4M3), "dtype"),
+    (dict(head_dim=12), "head_dim"),
+    (dict(tokens_with_prefix=5), "tokens_with_prefix"),
+    (dict(prefix_output=0), "NULL"),
+    (dict(suffix_output=0x10004), "aligned"),
+    (dict(prefix_stride_head=60), "strides"),
+    (dict(lse_stride_token=-1), "lse strides"),
+]
+
+
+@pytest.mark.parametrize("over,text", MERGE_BAD, ids=[t for _, t in MERGE_BAD])
+def test_merge_validation_rejects_before_launch(lib, over, text):
+    st = lib.xqa_merge_attn_states(ctypes.byref(fake_merge(**over)), None)
+    assert st == X.XQA_ERR_INVALID_ARG
+    assert text in lib.xqa_last_error().decode()
+
+
+def test_merge_of_zero_tokens_is_a_no_op(lib):
+    assert lib.xqa_merge_attn_states(ctypes.byref(fake_merge(num_tokens=0, tokens_with_prefix=0)),
+                                     None) == X.XQA_OK
+
+
+def test_misaligned_lse_rejected(lib):
+    p = fake_params(lse=0x10002)
+    assert lib.xqa_decode(ctypes.byref(p), None, 0, None, None) == X.XQA_ERR_INVALID_ARG
+    assert "lse" in lib.xqa_last_error().decode()
