@@ -9,6 +9,8 @@ than L2, so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5]
   python bench.py --impl reference ...   (the float64 CPU oracle, bounded sample)
+  python bench.py --op merge ...         (merge_attn_states on a chunked-prefill shape)
+  python bench.py --workload 3 --out-dtype e4m3   (fp8 output with the fp8 cache)
 
 Multi-GPU: one process per GPU (torchrun); decode sequences are independent,
 so every rank runs its own replica of the workload with no collective on the
@@ -50,6 +52,9 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="decode", choices=["decode", "merge"])
+    ap.add_argument("--out-dtype", default=None, choices=["e4m3"],
+                    help="fp8 output (workloads with an fp8 cache)")
     return ap.parse_args()
 
 
@@ -185,7 +190,8 @@ def run_gb300(args):
     X.load()
 
     case = build_case(args.workload, dev, args.batch)
-    dec = Decoder(case, error_word=False)
+    dec = Decoder(case, error_word=False,
+                  out_dtype=torch.float8_e4m3fn if args.out_dtype == "e4m3" else None)
     stream = torch.cuda.current_stream(dev)
     kv_bytes = case.kv_bytes()
     q_bytes = case.q_bytes()
@@ -281,7 +287,8 @@ def run_gb300(args):
         "dtype": {torch.bfloat16: "bf16", torch.float16: "f16",
                   torch.float8_e4m3fn: "e4m3 kv, bf16 q"}[case.k_cache.dtype],
         "data": "synthetic (seeded N(0,1) q/K/V, shuffled page pool)",
-        "config": {"workload": W.WORKLOADS[args.workload], "global_batch": case.batch * world,
+        "config": {"workload": W.WORKLOADS[args.workload] + (", fp8 output" if args.out_dtype else ""),
+                   "global_batch": case.batch * world,
                    "kv_bytes_per_step": kv_bytes * world, "q_bytes_per_step": q_bytes * world,
                    "l2": "inputs larger than L2 (no flush)" if kv_bytes > 129e6
                    else "KV fits in L2: numbers are L2-assisted",
@@ -397,9 +404,125 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# merge_attn_states on the shape of Kimi-K3's prefill with chunked context (vLLM
+# MultiHeadLatentAttention page): 8192 new tokens, 128 heads, v_head_dim 128.
+MERGE_SHAPE = (8192, 128, 128)
+MERGE_METRIC = "merge_attn_states: GB/s moved (two results + lse in, one out) & % of HBM peak"
+
+
+def merge_inputs(device, T, H, D):
+    g = torch.Generator(device="cpu").manual_seed(12)
+    po = torch.randn((T, H, D), generator=g).to(torch.bfloat16)
+    so = torch.randn((T, H, D), generator=g).to(torch.bfloat16)
+    pl = torch.randn((T, H), generator=g) * 3
+    sl = torch.randn((T, H), generator=g) * 3
+    return [x.to(device) for x in (po, pl, so, sl)]
+
+
+def run_merge(args):
+    """One step = one merge_attn_states call over MERGE_SHAPE (bf16)."""
+    T, H, D = MERGE_SHAPE
+    moved = 3 * T * H * D * 2 + 3 * T * H * 4
+    cfg = {"workload": f"merge_attn_states T{T} H{H} D{D} bf16 (chunked-context prefill)",
+           "global_batch": T, "bytes_per_step": moved,
+           "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas x1 (no collective)"}
+    world, rank, local = dist_env()
+    if rank != 0:
+        return
+    if args.impl == "reference":
+        import oracle
+        n = 64  # tokens per sample
+        po, pl, so, sl = [x[:n].to(torch.float64) for x in merge_inputs("cpu", T, H, D)]
+        for _ in range(args.warmup):
+            oracle.merge_attn_states(po, pl, so, sl)
+        t = time.perf_counter()
+        for _ in range(args.steps):
+            oracle.merge_attn_states(po, pl, so, sl)
+        dt = (time.perf_counter() - t) / args.steps * (T / n)  # scaled to a full step
+        v = moved / dt / 1e9
+        print(json.dumps({"metric": MERGE_METRIC, "value": round(v, 3), "unit": "GB/s", "n_gpus": world,
+                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                          "dtype": "f64", "data": "synthetic (seeded N(0,1))", "config": cfg,
+                          "impl": "reference",
+                          "cpu_baseline": {"value": round(v, 3), "unit": "GB/s", "cores": 1,
+                                           "kind": "oracle", "sample": f"{n} of {T} tokens per step"},
+                          "e2e": {"value": round(v, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return
+    from paged_kv_decode_20_gb300 import build as B
+    from paged_kv_decode_20_gb300 import xqa as X
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    B.build()
+    po, pl, so, sl = merge_inputs(dev, T, H, D)
+    out = torch.empty_like(so)
+    out_lse = torch.empty_like(sl)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        X.merge_attn_states(out, po, pl, so, sl, output_lse=out_lse, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    with Clocks(local) as clk:
+        t0.record(stream)
+        for s_ in range(args.steps):
+            ev[s_][0].record(stream)
+            step()
+            ev[s_][1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    ms = t0.elapsed_time(t1) / args.steps
+    launch = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    # end to end: inputs from pinned host memory, result and lse back
+    hosts = [x.cpu().pin_memory() for x in (po, pl, so, sl)]
+    oh, lh = torch.empty(out.shape, dtype=out.dtype).pin_memory(), torch.empty(sl.shape).pin_memory()
+
+    def e2e_step():
+        for d_, h_ in zip((po, pl, so, sl), hosts):
+            d_.copy_(h_, non_blocking=True)
+        step()
+        oh.copy_(out, non_blocking=True)
+        lh.copy_(out_lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ne = max(3, args.steps // 10)
+    e0.record(stream)
+    for _ in range(ne):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e_ms = e0.elapsed_time(e1) / ne
+    peak, kind = peaks()
+    achieved = moved / (launch * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": MERGE_METRIC, "value": round(moved / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1))", "config": cfg,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": kind, "traffic": None,
+                     "kernel": "merge_kernel", "algorithmic_bytes_per_launch": moved,
+                     "avg_launch_ms": round(launch, 5)},
+        "gpu_launches": args.steps,
+        "e2e": {"value": round(moved / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s", "ms_per_step": round(e_ms, 4),
+                "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in hosts),
+                "d2h_bytes_per_step": oh.numel() * 2 + lh.numel() * 4},
+        "cpu_baseline": None, "clocks": clk.summary()}), flush=True)
+
+
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.op == "merge":
+        run_merge(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gb300(args)

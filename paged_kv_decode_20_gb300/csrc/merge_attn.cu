@@ -2,8 +2,8 @@
 // path with chunked context): two attention results over disjoint key sets of
 // the same query rows, each normalised by its own sum and carrying its
 // log-sum-exp, combine into the result over the union of the keys.  A pure
-// streaming op (two rows in, one row out per (token, head)): one warp per row,
-// 16-byte loads and stores, fp32 arithmetic.
+// streaming op (two rows in, one row out per (token, head)): 16-byte loads and
+// stores, fp32 arithmetic.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdarg.h>
@@ -18,7 +18,7 @@
 namespace xqa {
 namespace merge {
 
-constexpr int kWarps = 8;  // rows per 256-thread block
+constexpr int kThreads = 256;
 
 struct MergeArgs {
   uint16_t* out;
@@ -27,26 +27,34 @@ struct MergeArgs {
   float* out_lse;
   const float* pre_lse;
   const float* suf_lse;
-  int64_t T, n_pre;
+  int64_t T, n_pre, chunks;  // chunks = T * H * (D / 8)
   int H, D;
   int64_t o_st, o_sh, p_st, p_sh, s_st, s_sh, l_st, l_sh;
 };
 
+// One thread per 8-element (16-byte) chunk of a row: the two log-sum-exps and
+// both chunks are loaded together, so each thread keeps one round of DRAM
+// latency in flight rather than two in a row.
 template <bool kBf16>
-__global__ void __launch_bounds__(32 * kWarps) merge_kernel(const MergeArgs a) {
-  const int64_t row = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-  if (row >= a.T * a.H) return;
-  const int lane = threadIdx.x & 31;
+__global__ void __launch_bounds__(kThreads) merge_kernel(const MergeArgs a) {
+  const int64_t idx = int64_t(blockIdx.x) * kThreads + threadIdx.x;
+  if (idx >= a.chunks) return;
+  const int cpr = a.D >> 3;
+  const int64_t row = idx / cpr;
+  const int d = int(idx - row * cpr) << 3;
   const int64_t t = row / a.H;
-  const int h = int(row % a.H);
+  const int h = int(row - t * a.H);
   const int64_t li = t * a.l_st + h * a.l_sh;
-  // weights of the two sides relative to the larger log-sum-exp; a side
-  // with no visible key (-inf) weighs 0, and a token without a prefix keeps
-  // its suffix exactly (weight 1, factor 1)
+  const bool has_pre = t < a.n_pre;
   const float ls = __ldg(a.suf_lse + li);
+  const float lp = has_pre ? __ldg(a.pre_lse + li) : -INFINITY;
+  const uint4 sv = __ldg(reinterpret_cast<const uint4*>(a.suf + t * a.s_st + h * a.s_sh + d));
+  const uint4 pv = has_pre ? __ldg(reinterpret_cast<const uint4*>(a.pre + t * a.p_st + h * a.p_sh + d))
+                           : make_uint4(0, 0, 0, 0);
+  // weights of the two sides relative to the larger log-sum-exp; a side
+  // with no visible key (-inf) weighs 0
   float wp = 0.f, ws = 1.f, M = ls;
-  if (t < a.n_pre) {
-    const float lp = __ldg(a.pre_lse + li);
+  if (has_pre) {
     M = fmaxf(lp, ls);
     wp = M == -INFINITY ? 0.f : expf(lp - M);
     ws = M == -INFINITY ? 0.f : expf(ls - M);
@@ -54,27 +62,19 @@ __global__ void __launch_bounds__(32 * kWarps) merge_kernel(const MergeArgs a) {
   const float z = wp + ws;
   const float fp = z == 0.f ? 0.f : wp / z;
   const float fs = z == 0.f ? 0.f : ws / z;
-  const uint16_t* sp = a.suf + t * a.s_st + h * a.s_sh;
-  const uint16_t* pp = a.pre + t * a.p_st + h * a.p_sh;
-  uint16_t* op = a.out + t * a.o_st + h * a.o_sh;
-  for (int d = lane * 8; d < a.D; d += 32 * 8) {
-    const uint4 sv = __ldg(reinterpret_cast<const uint4*>(sp + d));
-    uint4 pv = make_uint4(0, 0, 0, 0);
-    if (fp != 0.f) pv = __ldg(reinterpret_cast<const uint4*>(pp + d));
+  uint32_t o4[4] = {sv.x, sv.y, sv.z, sv.w};  // bit-exact copy when the suffix stands alone
+  if (fp != 0.f || fs != 1.f) {
     const uint32_t s4[4] = {sv.x, sv.y, sv.z, sv.w};
     const uint32_t p4[4] = {pv.x, pv.y, pv.z, pv.w};
-    uint32_t o4[4] = {sv.x, sv.y, sv.z, sv.w};  // bit-exact copy when the suffix stands alone
-    if (fp != 0.f || fs != 1.f) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 s2 = unpack_16x2(s4[k], kBf16);
-        const float2 p2 = unpack_16x2(p4[k], kBf16);
-        o4[k] = pack_f32x2(fs * s2.x + fp * p2.x, fs * s2.y + fp * p2.y, kBf16);
-      }
+    for (int k = 0; k < 4; ++k) {
+      const float2 s2 = unpack_16x2(s4[k], kBf16);
+      const float2 p2 = fp != 0.f ? unpack_16x2(p4[k], kBf16) : make_float2(0.f, 0.f);
+      o4[k] = pack_f32x2(fs * s2.x + fp * p2.x, fs * s2.y + fp * p2.y, kBf16);
     }
-    *reinterpret_cast<uint4*>(op + d) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
   }
-  if (a.out_lse && lane == 0) a.out_lse[li] = z == 0.f ? -INFINITY : M + logf(z);
+  *reinterpret_cast<uint4*>(a.out + t * a.o_st + h * a.o_sh + d) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+  if (a.out_lse && d == 0) a.out_lse[li] = z == 0.f ? -INFINITY : M + logf(z);
 }
 
 }  // namespace merge
@@ -137,14 +137,14 @@ extern "C" xqa_status xqa_merge_attn_states(const xqa_merge_params* p, xqa_strea
   a.s_sh = p->suffix_stride_head;
   a.l_st = p->lse_stride_token;
   a.l_sh = p->lse_stride_head;
-  const int64_t rows = a.T * a.H;
-  const int64_t blocks = (rows + kWarps - 1) / kWarps;
+  a.chunks = a.T * a.H * (a.D / 8);
+  const int64_t blocks = (a.chunks + kThreads - 1) / kThreads;
   if (blocks > 0x7fffffffLL) return merge_fail(XQA_ERR_UNSUPPORTED, "too many rows for one launch");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (p->dtype == XQA_BF16)
-    merge_kernel<true><<<unsigned(blocks), 32 * kWarps, 0, s>>>(a);
+    merge_kernel<true><<<unsigned(blocks), kThreads, 0, s>>>(a);
   else
-    merge_kernel<false><<<unsigned(blocks), 32 * kWarps, 0, s>>>(a);
+    merge_kernel<false><<<unsigned(blocks), kThreads, 0, s>>>(a);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return merge_fail(XQA_ERR_CUDA, "merge kernel launch: %s", cudaGetErrorString(e));
   return XQA_OK;
