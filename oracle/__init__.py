@@ -191,3 +191,49 @@ def unit_ids(batch_idx, q_idx, head_idx, q_seq_len, num_q_heads):
     i = torch.as_tensor(q_idx, dtype=torch.int64)
     h = torch.as_tensor(head_idx, dtype=torch.int64)
     return (b * q_seq_len + i) * num_q_heads + h
+
+
+def rope_pairs(x, cos, sin):
+    """GPT-J (non-neox) rotary embedding of the last dim of x: element pairs
+    (2i, 2i+1) rotate by angle i (Kimi-K3 MultiHeadLatentAttention page,
+    `get_rope(..., is_neox_style=False)`): out_2i = x_2i cos_i - x_2i+1 sin_i,
+    out_2i+1 = x_2i+1 cos_i + x_2i sin_i.  cos, sin broadcast over the pairs."""
+    x0, x1 = x[..., 0::2], x[..., 1::2]
+    out = torch.empty_like(x)
+    out[..., 0::2] = x0 * cos - x1 * sin
+    out[..., 1::2] = x1 * cos + x0 * sin
+    return out
+
+
+def mla_decode_prep(ql_nope, q_pe, kv_c, k_pe, positions, cos_sin_cache, slot_mapping, kv_cache):
+    """The fused decode query-concat + latent cache insert (Kimi-K3
+    MultiHeadLatentAttention page, `_decode_concat_cache`), in float64.
+
+    ql_nope [T, H, Lr], q_pe [T, H, R], kv_c [T, Lr], k_pe [T, R]; positions
+    [T] (None: no rotation); cos_sin_cache fp32 [max_pos, R] holding cos then
+    sin of the R/2 angles; slot_mapping [T] (a negative slot is skipped);
+    kv_cache [num_slots, Lr + R] (any float dtype, not modified).
+
+    Returns (q [T, H, Lr + R] float64, cache float64 copy of kv_cache with the
+    rows [kv_c | rope(k_pe)] written at their slots)."""
+    ql = _cpu_contig(ql_nope).to(torch.float64)
+    qp = _cpu_contig(q_pe).to(torch.float64)
+    kc = _cpu_contig(kv_c).to(torch.float64)
+    kp = _cpu_contig(k_pe).to(torch.float64)
+    cache = _cpu_contig(kv_cache).to(torch.float64).clone()
+    T, H, Lr = ql.shape
+    R = qp.shape[-1]
+    q = torch.empty((T, H, Lr + R), dtype=torch.float64)
+    for t in range(T):
+        if positions is None:
+            c, s = torch.ones(R // 2, dtype=torch.float64), torch.zeros(R // 2, dtype=torch.float64)
+        else:
+            row = _cpu_contig(cos_sin_cache)[int(positions[t])].to(torch.float64)
+            c, s = row[: R // 2], row[R // 2:]
+        q[t, :, :Lr] = ql[t]
+        q[t, :, Lr:] = rope_pairs(qp[t], c, s)
+        slot = int(slot_mapping[t])
+        if slot >= 0:
+            cache[slot, :Lr] = kc[t]
+            cache[slot, Lr:] = rope_pairs(kp[t], c, s)
+    return q, cache
