@@ -10,6 +10,7 @@ than L2, so no flush is needed between steps.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5]
   python bench.py --impl reference ...   (the float64 CPU oracle, bounded sample)
   python bench.py --op merge ...         (merge_attn_states on a chunked-prefill shape)
+  python bench.py --op prep ...          (fused MLA decode prep on the MLA decode step)
   python bench.py --workload 3 --out-dtype e4m3   (fp8 output with the fp8 cache)
 
 Multi-GPU: one process per GPU (torchrun); decode sequences are independent,
@@ -52,7 +53,7 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="decode", choices=["decode", "merge"])
+    ap.add_argument("--op", default="decode", choices=["decode", "merge", "prep"])
     ap.add_argument("--out-dtype", default=None, choices=["e4m3"],
                     help="fp8 output (workloads with an fp8 cache)")
     return ap.parse_args()
@@ -518,10 +519,121 @@ def run_merge(args):
         "cpu_baseline": None, "clocks": clk.summary()}), flush=True)
 
 
+# the fused MLA decode prep on the MLA latent workload's decode step: 64 tokens,
+# 128 heads, kv_lora_rank 512, rope 64 (Kimi-K3 MultiHeadLatentAttention page)
+PREP_SHAPE = (64, 128, 512, 64)
+PREP_METRIC = "MLA decode prep (q concat + RoPE + latent cache insert): GB/s moved & % of HBM peak"
+
+
+def run_prep(args):
+    """One step = one xqa_mla_decode_prep call; L2 is flushed (a 256 MB write)
+    before every timed launch because the step's bytes fit in L2."""
+    T, H, Lr, R = PREP_SHAPE
+    moved = 2 * T * H * (Lr + R) * 2 + 2 * T * (Lr + R) * 2 + T * 16 + T * R * 4
+    cfg = {"workload": f"MLA decode prep T{T} H{H} latent {Lr} rope {R} bf16",
+           "global_batch": T, "bytes_per_step": moved, "l2": "flushed before every launch (256 MB write)",
+           "parallelism": "replicas x1 (no collective)"}
+    world, rank, local = dist_env()
+    if rank != 0:
+        return
+    g = torch.Generator().manual_seed(13)
+    P = 32768
+    inv = 10000.0 ** (-torch.arange(0, R, 2, dtype=torch.float64) / R)
+    ang = torch.arange(P, dtype=torch.float64)[:, None] * inv[None, :]
+    cs = torch.cat([ang.cos(), ang.sin()], dim=1).to(torch.float32)
+    ql = torch.randn(T, H, Lr, generator=g).to(torch.bfloat16)
+    qp = torch.randn(T, H, R, generator=g).to(torch.bfloat16)
+    kc = torch.randn(T, Lr, generator=g).to(torch.bfloat16)
+    kp = torch.randn(T, R, generator=g).to(torch.bfloat16)
+    pos = torch.randint(0, P, (T,), generator=g)
+    slots = torch.randperm(64 * 512, generator=g)[:T]
+    if args.impl == "reference":
+        import oracle
+        cache = torch.zeros(64 * 512, Lr + R, dtype=torch.bfloat16)
+        t0 = time.perf_counter()
+        n = max(1, args.steps)
+        for _ in range(n):
+            oracle.mla_decode_prep(ql, qp, kc, kp, pos, cs, slots, cache)
+        dt = (time.perf_counter() - t0) / n
+        v = moved / dt / 1e9
+        print(json.dumps({"metric": PREP_METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": world,
+                          "steps": n, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic (seeded N(0,1))", "config": cfg, "impl": "reference",
+                          "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                           "sample": "the whole step"},
+                          "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return
+    from paged_kv_decode_20_gb300 import build as B
+    from paged_kv_decode_20_gb300 import xqa as X
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    B.build()
+    d = [x.to(dev) for x in (ql, qp, kc, kp, pos, cs, slots)]
+    cache = torch.zeros(64, 512, 1, Lr + R, dtype=torch.bfloat16, device=dev)
+    q_out = torch.empty(T, H, Lr + R, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        X.mla_decode_prep(d[0], d[1], d[2], d[3], d[4], d[5], d[6], cache, q_out=q_out, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    with Clocks(local) as clk:
+        for s_ in range(args.steps):
+            flush.fill_(float(s_))
+            ev[s_][0].record(stream)
+            step()
+            ev[s_][1].record(stream)
+        torch.cuda.synchronize(dev)
+    launch = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    hosts = [x.cpu().pin_memory() for x in d]
+    qh = torch.empty(q_out.shape, dtype=q_out.dtype).pin_memory()
+
+    def e2e_step():
+        for dd, hh in zip(d, hosts):
+            dd.copy_(hh, non_blocking=True)
+        step()
+        qh.copy_(q_out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ne = max(3, args.steps // 10)
+    e0.record(stream)
+    for _ in range(ne):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e_ms = e0.elapsed_time(e1) / ne
+    peak, kind = peaks()
+    achieved = moved / (launch * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": PREP_METRIC, "value": round(achieved, 2), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(launch, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1))", "config": cfg,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": kind, "traffic": None,
+                     "kernel": "prep_kernel", "algorithmic_bytes_per_launch": moved,
+                     "avg_launch_ms": round(launch, 5)},
+        "gpu_launches": args.steps,
+        "e2e": {"value": round(moved / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s", "ms_per_step": round(e_ms, 4),
+                "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in hosts),
+                "d2h_bytes_per_step": qh.numel() * 2},
+        "cpu_baseline": None, "clocks": clk.summary()}), flush=True)
+
+
 def main():
     args = parse()
     if args.op == "merge":
         run_merge(args)
+    elif args.op == "prep":
+        run_prep(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -197,6 +197,47 @@ typedef struct xqa_merge_params {
 
 xqa_status xqa_merge_attn_states(const xqa_merge_params* params, xqa_stream_t stream);
 
+/* Fused MLA decode prep (vLLM Kimi-K3 MultiHeadLatentAttention page,
+   `_decode_concat_cache`, the launch right before forward_mqa), bf16:
+     q_out[t, h] = [ql_nope[t, h] | rope(q_pe[t, h], positions[t])]
+     kv_cache[slot_mapping[t]] = [kv_c[t] | rope(k_pe[t], positions[t])]
+   rope is the GPT-J (non-neox) rotation: pair (2i, 2i+1) turns by angle i, with
+   cos and sin read in fp32 from cos_sin_cache[positions[t]] = [cos_0..cos_{R/2-1} |
+   sin_0..sin_{R/2-1}]; positions NULL means no rotation.  A negative slot is a
+   padding token and inserts nothing.  A position outside [0, max_position) is
+   not rotated and a slot >= num_slots is not written; both set bit 0 of
+   error_word when one is given.
+   Layouts: ql_nope [T, H, Lr], q_pe [T, H, R] with element strides per token and
+   per head; kv_c [T, Lr], k_pe [T, R] with a token stride; kv_cache
+   [num_slots, Lr + R] (num_pages * page_size rows of the latent cache, NHD);
+   q_out [T, H, Lr + R] contiguous.  Lr and R multiples of 8, strides multiples
+   of 8 elements, tensors 16-byte aligned.  Asynchronous on `stream`; returns
+   XQA_ERR_INVALID_ARG before any launch for malformed arguments. */
+typedef struct xqa_mla_prep_params {
+  const void* ql_nope;
+  int64_t ql_stride_token, ql_stride_head;
+  const void* q_pe;
+  int64_t qpe_stride_token, qpe_stride_head;
+  const void* kv_c;
+  int64_t kvc_stride_token;
+  const void* k_pe;
+  int64_t kpe_stride_token;
+  const int64_t* positions;    /* [T] or NULL */
+  const float* cos_sin_cache;  /* fp32 [max_position, R] */
+  int64_t max_position;
+  const int64_t* slot_mapping; /* [T] */
+  void* kv_cache;
+  int64_t num_slots;
+  void* q_out;
+  int64_t num_tokens;
+  int32_t num_heads;
+  int32_t kv_lora_rank;        /* Lr */
+  int32_t rope_dim;            /* R */
+  uint32_t* error_word;        /* optional */
+} xqa_mla_prep_params;
+
+xqa_status xqa_mla_decode_prep(const xqa_mla_prep_params* params, xqa_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* xqa_status_string(xqa_status status);
 

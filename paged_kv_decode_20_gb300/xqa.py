@@ -92,8 +92,37 @@ class XqaMergeParams(ctypes.Structure):
     ]
 
 
+class XqaMlaPrepParams(ctypes.Structure):
+    """Mirror of ``struct xqa_mla_prep_params``."""
+
+    _fields_ = [
+        ("ql_nope", ctypes.c_void_p),
+        ("ql_stride_token", ctypes.c_int64),
+        ("ql_stride_head", ctypes.c_int64),
+        ("q_pe", ctypes.c_void_p),
+        ("qpe_stride_token", ctypes.c_int64),
+        ("qpe_stride_head", ctypes.c_int64),
+        ("kv_c", ctypes.c_void_p),
+        ("kvc_stride_token", ctypes.c_int64),
+        ("k_pe", ctypes.c_void_p),
+        ("kpe_stride_token", ctypes.c_int64),
+        ("positions", ctypes.c_void_p),
+        ("cos_sin_cache", ctypes.c_void_p),
+        ("max_position", ctypes.c_int64),
+        ("slot_mapping", ctypes.c_void_p),
+        ("kv_cache", ctypes.c_void_p),
+        ("num_slots", ctypes.c_int64),
+        ("q_out", ctypes.c_void_p),
+        ("num_tokens", ctypes.c_int64),
+        ("num_heads", ctypes.c_int32),
+        ("kv_lora_rank", ctypes.c_int32),
+        ("rope_dim", ctypes.c_int32),
+        ("error_word", ctypes.c_void_p),
+    ]
+
+
 EXPORTS = ["xqa_workspace_size", "xqa_semaphore_count", "xqa_decode", "xqa_mla_workspace_size",
-           "xqa_mla_semaphore_count", "xqa_mla_decode", "xqa_decode_noalloc", "xqa_merge_attn_states",
+           "xqa_mla_semaphore_count", "xqa_mla_decode", "xqa_decode_noalloc", "xqa_merge_attn_states", "xqa_mla_decode_prep",
            "xqa_status_string", "xqa_last_error"]
 
 _lock = threading.Lock()
@@ -131,6 +160,8 @@ def load(path: str = LIB_PATH):
             lib.xqa_mla_decode.restype = ctypes.c_int
             lib.xqa_merge_attn_states.argtypes = [ctypes.POINTER(XqaMergeParams), ctypes.c_void_p]
             lib.xqa_merge_attn_states.restype = ctypes.c_int
+            lib.xqa_mla_decode_prep.argtypes = [ctypes.POINTER(XqaMlaPrepParams), ctypes.c_void_p]
+            lib.xqa_mla_decode_prep.restype = ctypes.c_int
             lib.xqa_status_string.argtypes = [ctypes.c_int]
             lib.xqa_status_string.restype = ctypes.c_char_p
             lib.xqa_last_error.argtypes = []
@@ -366,3 +397,45 @@ def merge_attn_states(output, prefix_output, prefix_lse, suffix_output, suffix_l
     p.suffix_stride_token, p.suffix_stride_head = suffix_output.stride(0), suffix_output.stride(1)
     p.lse_stride_token, p.lse_stride_head = suffix_lse.stride(0), suffix_lse.stride(1)
     _check(load().xqa_merge_attn_states(ctypes.byref(p), _stream(stream)))
+
+
+def mla_decode_prep(ql_nope, q_pe, kv_c, k_pe, positions, cos_sin_cache, slot_mapping, kv_cache,
+                    q_out=None, error_word=None, stream=None):
+    """Fused MLA decode prep through the C ABI (Kimi-K3 MultiHeadLatentAttention
+    page, `_decode_concat_cache`): returns q_out [T, H, Lr + R] = [ql_nope |
+    rope(q_pe)] and writes [kv_c | rope(k_pe)] into kv_cache at slot_mapping.
+    bf16 tensors with a contiguous last dim; kv_cache [num_pages, page_size,
+    (1,) Lr + R] contiguous; positions and slot_mapping int64 [T]."""
+    T, H, Lr = ql_nope.shape
+    R = q_pe.shape[-1]
+    kc = kv_c.reshape(T, Lr)
+    kp = k_pe.reshape(T, R)
+    for name, t in (("ql_nope", ql_nope), ("q_pe", q_pe), ("kv_c", kc), ("k_pe", kp)):
+        if t.dtype != torch.bfloat16 or t.stride(-1) != 1:
+            raise ValueError(f"{name} must be bf16 with a contiguous last dim")
+    if kv_cache.dtype != torch.bfloat16 or not kv_cache.is_contiguous() or kv_cache.shape[-1] != Lr + R:
+        raise ValueError(f"kv_cache must be contiguous bf16 with rows of {Lr + R}")
+    for name, t in (("slot_mapping", slot_mapping), ("positions", positions)):
+        if t is not None and (t.dtype != torch.int64 or not t.is_contiguous() or t.numel() != T):
+            raise ValueError(f"{name} must be contiguous int64 [{T}]")
+    if cos_sin_cache is not None and (cos_sin_cache.dtype != torch.float32 or not cos_sin_cache.is_contiguous()
+                                      or cos_sin_cache.shape[-1] != R):
+        raise ValueError(f"cos_sin_cache must be contiguous fp32 [max_position, {R}]")
+    if q_out is None:
+        q_out = torch.empty((T, H, Lr + R), dtype=torch.bfloat16, device=ql_nope.device)
+    p = XqaMlaPrepParams()
+    p.ql_nope, p.ql_stride_token, p.ql_stride_head = _ptr(ql_nope), ql_nope.stride(0), ql_nope.stride(1)
+    p.q_pe, p.qpe_stride_token, p.qpe_stride_head = _ptr(q_pe), q_pe.stride(0), q_pe.stride(1)
+    p.kv_c, p.kvc_stride_token = _ptr(kc), kc.stride(0)
+    p.k_pe, p.kpe_stride_token = _ptr(kp), kp.stride(0)
+    p.positions = _ptr(positions)
+    p.cos_sin_cache = _ptr(cos_sin_cache)
+    p.max_position = 0 if cos_sin_cache is None else cos_sin_cache.shape[0]
+    p.slot_mapping = _ptr(slot_mapping)
+    p.kv_cache = _ptr(kv_cache)
+    p.num_slots = kv_cache.numel() // (Lr + R)
+    p.q_out = _ptr(q_out)
+    p.num_tokens, p.num_heads, p.kv_lora_rank, p.rope_dim = T, H, Lr, R
+    p.error_word = _ptr(error_word)
+    _check(load().xqa_mla_decode_prep(ctypes.byref(p), _stream(stream)))
+    return q_out

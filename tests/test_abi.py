@@ -193,3 +193,51 @@ def test_misaligned_lse_rejected(lib):
     p = fake_params(lse=0x10002)
     assert lib.xqa_decode(ctypes.byref(p), None, 0, None, None) == X.XQA_ERR_INVALID_ARG
     assert "lse" in lib.xqa_last_error().decode()
+
+
+def test_prep_params_struct_layout_matches_c(tmp_path):
+    fields = [f for f, _ in X.XqaMlaPrepParams._fields_]
+    prog = ["#include <stdio.h>", "#include <stddef.h>", '#include "xqa.h"', "int main(void){",
+            'printf("%zu\\n", sizeof(xqa_mla_prep_params));']
+    prog += [f'printf("%zu\\n", offsetof(xqa_mla_prep_params, {f}));' for f in fields]
+    prog += ["return 0;}"]
+    src = tmp_path / "playout.c"
+    src.write_text("\n".join(prog))
+    exe = tmp_path / "playout"
+    subprocess.run(["gcc", "-I" + os.path.dirname(HEADER), str(src), "-o", str(exe)], check=True)
+    vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                           check=True).stdout.split()]
+    assert vals[0] == ctypes.sizeof(X.XqaMlaPrepParams)
+    for f, off in zip(fields, vals[1:]):
+        assert getattr(X.XqaMlaPrepParams, f).offset == off, f
+
+
+def fake_prep(**over):
+    p = X.XqaMlaPrepParams()
+    p.ql_nope = p.q_pe = p.kv_c = p.k_pe = p.kv_cache = p.q_out = 0x10000
+    p.positions = p.slot_mapping = 0x20000
+    p.cos_sin_cache = 0x30000
+    p.max_position = 4096
+    p.ql_stride_token, p.ql_stride_head = 128 * 512, 512
+    p.qpe_stride_token, p.qpe_stride_head = 128 * 64, 64
+    p.kvc_stride_token, p.kpe_stride_token = 512, 64
+    p.num_slots, p.num_tokens, p.num_heads, p.kv_lora_rank, p.rope_dim = 640, 4, 128, 512, 64
+    for k, v in over.items():
+        setattr(p, k, v)
+    return p
+
+
+PREP_BAD = [
+    (dict(rope_dim=60), "multiples of 8"),
+    (dict(num_heads=0), "num_heads"),
+    (dict(kv_cache=0), "NULL"),
+    (dict(q_out=0x10008), "aligned"),
+    (dict(qpe_stride_head=65), "strides"),
+    (dict(cos_sin_cache=0), "cos_sin_cache"),
+]
+
+
+@pytest.mark.parametrize("over,text", PREP_BAD, ids=[t for _, t in PREP_BAD])
+def test_prep_validation_rejects_before_launch(lib, over, text):
+    assert lib.xqa_mla_decode_prep(ctypes.byref(fake_prep(**over)), None) == X.XQA_ERR_INVALID_ARG
+    assert text in lib.xqa_last_error().decode()
