@@ -76,6 +76,15 @@ def reduce_max(x, device=None):
     return float(t.item())
 
 
+def tensor_peak():
+    """Measured dense bf16 TFLOP/s (burst: the kernel is timed alone)."""
+    try:
+        d = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        return float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -308,6 +317,16 @@ def run_gb300(args):
         "cpu_baseline": cpu,
         "clocks": clk.summary(),
     }
+    if case.mla:
+        # the latent workload sits near the ridge: report the tensor pipe too
+        # (QK over 576 dims and P.V over 512, 2 flops per multiply-add, per
+        # visible token and query row)
+        flops = case.visible_tokens() * case.q_seq_len * case.q.shape[2] * 2 * (case.q.shape[3] + case.dv)
+        tf = flops / (avg_launch_ms * 1e-3) / 1e12
+        tpeak, tkind = tensor_peak()
+        line["roofline_tensor"] = {"bound": "tensor", "achieved": round(tf, 2), "peak": tpeak,
+                                   "unit": "TFLOP/s", "frac": round(tf / tpeak, 4), "peak_source": tkind,
+                                   "flops_per_launch": flops}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

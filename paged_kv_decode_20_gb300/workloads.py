@@ -85,15 +85,20 @@ class Case:
             out.v_cache = out.k_cache
         return out
 
-    def kv_bytes(self):
-        """Algorithmic KV bytes: every visible token's K row and V row once
-        (the MLA latent row once, since V is its prefix)."""
+    def visible_tokens(self):
+        """Tokens a query row of each sequence reads, summed over the batch
+        (the window bounds them when one is set)."""
         lens = self.seq_lens.to(torch.int64).cpu()
         if self.sliding_win_size > 0:
             lens = torch.clamp(lens, max=self.sliding_win_size + self.q_seq_len - 1)
+        return int(lens.sum())
+
+    def kv_bytes(self):
+        """Algorithmic KV bytes: every visible token's K row and V row once
+        (the MLA latent row once, since V is its prefix)."""
         elt = self.k_cache.element_size()
         per_tok = self.head_dim * elt * self.num_kv_heads * (1 if self.mla else 2)
-        return int(lens.sum()) * per_tok
+        return self.visible_tokens() * per_tok
 
     def q_bytes(self):
         return self.q.numel() * self.q.element_size()
