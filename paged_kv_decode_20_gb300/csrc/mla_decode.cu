@@ -22,8 +22,9 @@
 //   in UMMA operand layout) with the per-row rescale factors back.  Both CTAs
 //   accumulate O_c += P V_c in their own 256 tensor-memory columns, V_c being
 //   the first four chunks of the K tile the CTA already holds.  Every latent
-//   byte is read from HBM once, and no tile waits on a round trip between the
-//   two CTAs.
+//   byte is read from HBM once; CTA 0's softmax waits on no round trip (the
+//   feeder ships a tile's logits before the master needs them), while CTA 1's
+//   P.V of a tile waits for one message back.
 //
 // Warp roles: 0 = TMA producer and tensor-memory allocator, 1 = MMA issuer,
 // 2..9 = softmax (CTA 0) or logit shipping and O rescale (CTA 1), then the
@@ -54,37 +55,47 @@ constexpr int kDim = kLatent + kRope;
 constexpr int kHalf = kLatent / 2;  // V columns per CTA
 constexpr int kTok = 64;         // tokens per tile (UMMA N of QK, K of PV)
 constexpr int kChunkBytes = kTok * 128;  // one 64-element column chunk of a tile
-constexpr int kStages = 3;
 constexpr int kSoftWarps = 8;    // two threads per query row, 32 logit columns each
 constexpr int kSoft = 32 * kSoftWarps;
 constexpr int kSoftWarp0 = 2;    // softmax warps are 2..9: two per TMEM sub-partition
 constexpr int kThreads = 32 * kSoftWarp0 + kSoft;
 
-// ---- shared memory (offsets from a 1024-aligned base).  The two CTAs lay out
-// their buffers differently; the barrier block sits at the same offset in
-// both because each CTA signals barriers of its peer.
+// ---- shared memory (offsets from the dynamic base, which is 1024-aligned:
+// checked at run time).  Each CTA keeps two rings: K slots hold a tile's
+// chunks until its QK is done; V slots hold the same latent chunks, fetched
+// again (from L2, right after the QK) until its P.V is done.  Holding a stage
+// only as long as its own use needs lets two slots of each kind cover the
+// tile's whole exchange.  The barrier block sits at the same offset in both
+// CTAs because each CTA signals barriers of its peer.
 constexpr int kXBytes = kRows * kTok * 4;  // one fp32 logit tile
 constexpr int kPBytes = kRows * kTok * 2;  // one bf16 P tile
-constexpr int kPMsg = kPBytes + kRows * 4; // P followed by one rescale factor per row
-constexpr int kPSlot = 17 * 1024;
-constexpr int kStride0 = 4 * kChunkBytes;  // CTA 0 stage: 4 latent chunks
-constexpr int kStride1 = 5 * kChunkBytes;  // CTA 1 stage: 4 latent chunks + rope
-// CTA 0: stages | P slots x2 | logit receive slots x2
-constexpr int kOffPSlot0 = kStages * kStride0;
-constexpr int kOffRecv = kOffPSlot0 + 2 * kPSlot;
-// CTA 1: stages | rope query (128 x 64 bf16) | P slots x2 | logit send buffer
-constexpr int kOffQRope = kStages * kStride1;
-constexpr int kOffPSlot1 = kOffQRope + kRows * 128;
-constexpr int kOffSend = kOffPSlot1 + 2 * kPSlot;
+constexpr int kFBytes = kRows * 4;         // one rescale factor per row
+constexpr int kPMsg = kPBytes + kFBytes;   // P, then its factors (two copies)
+constexpr int kVBytes = 4 * kChunkBytes;   // the four latent chunks of a tile
+constexpr int kKBytes0 = 4 * kChunkBytes;  // CTA 0 K slot: 4 latent chunks
+constexpr int kKBytes1 = 5 * kChunkBytes;  // CTA 1 K slot: 4 latent chunks + rope
+// CTA 0: K x2 | V x2 | P x2 | factors x2 | logit receive slots x2
+constexpr int kOffV0 = 2 * kKBytes0;
+constexpr int kOffP0 = kOffV0 + 2 * kVBytes;
+constexpr int kOffF0 = kOffP0 + 2 * kPBytes;
+constexpr int kOffRecv = kOffF0 + 2 * kFBytes;
+// CTA 1: K x2 | V x2 | rope query (128 x 64 bf16) | P x2 | factors x2 | send buffer
+constexpr int kOffV1 = 2 * kKBytes1;
+constexpr int kOffQRope = kOffV1 + 2 * kVBytes;
+constexpr int kOffP1 = kOffQRope + kRows * 128;
+constexpr int kOffF1 = kOffP1 + 2 * kPBytes;
+constexpr int kOffSend = kOffF1 + 2 * kFBytes;
 // both: [2][128] floats (CTA 0: row maxima / sums; CTA 1: the final m and l)
 constexpr int kOffRowX = (kOffRecv + 2 * kXBytes) > (kOffSend + kXBytes) ? (kOffRecv + 2 * kXBytes)
                                                                          : (kOffSend + kXBytes);
 constexpr int kOffBar = kOffRowX + 2 * kRows * 4;
 
 enum BarIdx {
-  kKvFull = 0,                  // [kStages] TMA bytes landed
-  kKvEmpty = kKvFull + kStages, // [kStages] the P.V reading the stage is done
-  kQReady = kKvEmpty + kStages, // the query is in tensor / shared memory
+  kKFull = 0,                   // [2] a K slot's bytes landed
+  kKEmpty = kKFull + 2,         // [2] the QK reading a K slot is done
+  kVFull = kKEmpty + 2,         // [2] a V slot's bytes landed
+  kVEmpty = kVFull + 2,         // [2] the P.V reading a V slot is done
+  kQReady = kVEmpty + 2,        // the query is in tensor / shared memory
   kSFull = kQReady + 1,         // [2] S tile computed
   kSFree = kSFull + 2,          // [2] S tile read out of tensor memory
   kPFull = kSFree + 2,          // P (and any O rescale) ready for the P.V
@@ -97,14 +108,14 @@ enum BarIdx {
   kFin = kPSlotFree + 2,        // CTA 1: the final (m, l) rows landed
   kNumBars = kFin + 1
 };
-constexpr int kSmem = 1024 + kOffBar + kNumBars * 8 + 32;
+constexpr int kSmem = kOffBar + kNumBars * 8 + 32;
 static_assert(kSmem <= 232448, "shared memory budget");
-static_assert(kOffPSlot0 % 1024 == 0 && kOffPSlot1 % 1024 == 0 && kPSlot % 1024 == 0 &&
-                  kOffQRope % 1024 == 0 && kOffRecv % 16 == 0 && kOffSend % 16 == 0,
+static_assert(kOffV0 % 1024 == 0 && kOffP0 % 1024 == 0 && kOffV1 % 1024 == 0 && kOffP1 % 1024 == 0 &&
+                  kOffQRope % 1024 == 0 && kOffRecv % 16 == 0 && kOffSend % 16 == 0 && kOffF0 % 16 == 0 &&
+                  kOffF1 % 16 == 0,
               "UMMA operands need 1024-byte alignment, bulk copies 16");
-static_assert(kPMsg <= kPSlot && kPMsg % 16 == 0, "P message");
-constexpr int kCopyPieces = 4;  // each message travels as this many bulk copies
-static_assert(kPMsg % (16 * kCopyPieces) == 0 && kXBytes % (16 * kCopyPieces) == 0, "copy pieces");
+constexpr int kCopyPieces = 4;  // the logit tile and the P tile travel as this many bulk copies
+static_assert(kPBytes % (16 * kCopyPieces) == 0 && kXBytes % (16 * kCopyPieces) == 0, "copy pieces");
 
 // tensor memory columns
 constexpr uint32_t kTmemCols = 512;
@@ -205,9 +216,8 @@ __device__ __forceinline__ void zero_v_tail(uint8_t* stage, int r0, int st) {
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tmKV, const MlaArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
   int* flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] abort, [1] last CTA
@@ -239,14 +249,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int t_begin = pg_lo * a.ps;
   const int t_end = min(pg_hi * a.ps, L);
   const int ntiles = (nvalid == 0 || t_end <= t_begin) ? 0 : (t_end - t_begin + kTok - 1) / kTok;
-  const int nchunks = c == 0 ? 4 : 5;
-  const int stride = c == 0 ? kStride0 : kStride1;
-  const int off_p = c == 0 ? kOffPSlot0 : kOffPSlot1;
+  const int nchunks = c == 0 ? 4 : 5;  // chunks of a K slot
+  const int kbytes = c == 0 ? kKBytes0 : kKBytes1;
+  const int off_v = c == 0 ? kOffV0 : kOffV1;
+  const int off_p = c == 0 ? kOffP0 : kOffP1;
+  // the layout assumes a 1024-aligned dynamic base (the 128-byte swizzle
+  // atoms of the UMMA operands); both CTAs see the same base and leave together
+  if (smem_u32(smem_raw) & 1023u) {
+    if (tid == 0 && a.err) atomicOr(a.err, kErrTimeout);
+    return;
+  }
 
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&bars[kKvFull + i], 1);
-      mbar_init(&bars[kKvEmpty + i], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[kKFull + i], 1);
+      mbar_init(&bars[kKEmpty + i], 1);
+      mbar_init(&bars[kVFull + i], 1);
+      mbar_init(&bars[kVEmpty + i], 1);
     }
     mbar_init(&bars[kQReady], kSoftWarps);
     for (int k = 0; k < 2; ++k) {
@@ -280,77 +299,95 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t peer_bars = map_peer(smem_u32(bars), peer);
 
   if (warp == 0) {
-    // ================= TMA producer (warp fetches page indices, lanes issue)
+    // ================= TMA producer (lane 0 decides, lane j loads page piece j)
+    // K(j) may load once the QK of tile j - 2 is done (its slot is free); V(j)
+    // once the QK of tile j is done and the P.V of tile j - 2 has freed its V
+    // slot.  Tests never block; the loop gives up after kWaitCycles idle.
     if (ntiles > 0) {
       if (lane == 0) prefetch_tensormap(&tmKV);
       const int32_t* pt = a.page_table + int64_t(b) * a.pps;
       const int box_rows = min(a.ps, kTok);
       const uint32_t box_bytes = uint32_t(box_rows) * 128u;
-      int win_base = pg_lo;
-      auto fetch = [&](int base) {
-        int pg = 0;
-        if (base + lane < pg_hi) {
-          pg = __ldg(pt + base + lane);
-          if (pg < 0 || int64_t(pg) >= a.num_pages) pg = -1;  // TMA fills zeros
-        }
-        return pg;
-      };
-      int my_page = fetch(win_base);
       bool bad_page = false;
-      int s = 0;
-      for (; s < ntiles; ++s) {
-        const int slot = s % kStages;
-        int ok = 1;
-        if (lane == 0 && s >= kStages) ok = mbar_wait(&bars[kKvEmpty + slot], ((s / kStages) & 1) ^ 1);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) {
-          if (lane == 0) flags[0] = 1;
-          break;
-        }
-        const int tok0 = t_begin + s * kTok;
+      // all tile loads of tile j (nck chunks per page piece) into dst, on bar
+      auto issue = [&](int j, uint8_t* dst, uint64_t* bar, int nck) {
+        const int tok0 = t_begin + j * kTok;
         const int lp0 = tok0 / a.ps;
         const int sub = a.ps <= kTok ? 0 : tok0 % a.ps;
         const int n_piece = a.ps <= kTok ? min(kTok / a.ps, pg_hi - lp0) : 1;
-        if (lp0 + n_piece > win_base + 32) {
-          win_base = lp0;
-          my_page = fetch(win_base);
-        }
-        if (lane == 0)
-          mbar_arrive_expect_tx(&bars[kKvFull + slot], uint32_t(n_piece) * box_bytes * nchunks);
+        if (lane == 0) mbar_arrive_expect_tx(bar, uint32_t(n_piece) * box_bytes * nck);
         __syncwarp();
-        uint8_t* dst = smem + slot * stride;
-        // lane j issues the tile loads of page piece j (pieces are independent)
-        const int page = __shfl_sync(0xffffffffu, my_page, (lp0 + lane - win_base) & 31);
         if (lane < n_piece) {
-          bad_page |= page < 0;
-          const int row_off = lane * box_rows;
-          for (int k = 0; k < nchunks; ++k) {
-            // chunk slot k: latent dims 256c + 64k (k < 4) or the rope dims
+          int page = __ldg(pt + lp0 + lane);
+          if (page < 0 || int64_t(page) >= a.num_pages) {
+            page = -1;  // the TMA fills zeros
+            bad_page = true;
+          }
+          for (int k = 0; k < nck; ++k) {
+            // chunk k: latent dims 256c + 64k (k < 4) or the rope dims
             const int x = k < 4 ? int(c) * kHalf + 64 * k : kLatent;
-            tma_load_3d(dst + k * kChunkBytes + row_off * 128, &tmKV, &bars[kKvFull + slot], x, 0,
-                        page * a.ps + sub);
+            tma_load_3d(dst + k * kChunkBytes + lane * box_rows * 128, &tmKV, bar, x, 0, page * a.ps + sub);
           }
         }
-        // the tile that will reuse this stage next: into L2 now, so that its
-        // load (issued only when the stage frees) does not pay HBM latency
-        const int sp = s + kStages;
-        if (sp < ntiles) {
-          const int ptok = t_begin + sp * kTok;
-          const int plp = ptok / a.ps;
-          const int psub = a.ps <= kTok ? 0 : ptok % a.ps;
-          const int pn = a.ps <= kTok ? min(kTok / a.ps, pg_hi - plp) : 1;
-          if (lane < pn) {
-            const int pg = __ldg(pt + plp + lane);
-            if (pg >= 0 && int64_t(pg) < a.num_pages)
-              for (int k = 0; k < nchunks; ++k)
-                tma_prefetch_l2_3d(&tmKV, k < 4 ? int(c) * kHalf + 64 * k : kLatent, 0, pg * a.ps + psub);
-          }
+        __syncwarp();
+      };
+      // the tile two K loads ahead goes into L2 early, so that its own load
+      // (issued only when a K slot frees) does not pay HBM latency
+      auto prefetch = [&](int j) {
+        if (j >= ntiles) return;
+        const int tok0 = t_begin + j * kTok;
+        const int lp0 = tok0 / a.ps;
+        const int sub = a.ps <= kTok ? 0 : tok0 % a.ps;
+        const int n_piece = a.ps <= kTok ? min(kTok / a.ps, pg_hi - lp0) : 1;
+        if (lane < n_piece) {
+          const int pg = __ldg(pt + lp0 + lane);
+          if (pg >= 0 && int64_t(pg) < a.num_pages)
+            for (int k = 0; k < nchunks; ++k)
+              tma_prefetch_l2_3d(&tmKV, k < 4 ? int(c) * kHalf + 64 * k : kLatent, 0, pg * a.ps + sub);
         }
+      };
+      int nk = 0, nv = 0, seen = 0;  // K loads, V loads issued; QKs seen done (lane 0)
+      long long t_idle = clock64();
+      while (true) {
+        int dec = 0;  // 1: load K(nk), 2: load V(nv), 3: finished, 4: gave up
+        if (lane == 0) {
+          if (seen < nk && mbar_test(&bars[kKEmpty + (seen & 1)], (seen >> 1) & 1)) {
+            ++seen;
+            t_idle = clock64();
+          }
+          if (nv >= ntiles)
+            dec = 3;
+          else if (nk < ntiles && nk < seen + 2)
+            dec = 1;
+          else if (nv < seen && (nv < 2 || mbar_test(&bars[kVEmpty + (nv & 1)], ((nv >> 1) - 1) & 1)))
+            dec = 2;
+          else if (clock64() - t_idle > kWaitCycles)
+            dec = 4;
+        }
+        dec = __shfl_sync(0xffffffffu, dec, 0);
+        if (dec == 3) break;
+        if (dec == 4) {
+          if (lane == 0) flags[0] = 1;
+          break;
+        }
+        if (dec == 1) {
+          issue(nk, smem + (nk & 1) * kbytes, &bars[kKFull + (nk & 1)], nchunks);
+          prefetch(nk + 2);
+          ++nk;
+        } else if (dec == 2) {
+          issue(nv, smem + off_v + (nv & 1) * kVBytes, &bars[kVFull + (nv & 1)], 4);
+          ++nv;
+        }
+        if (dec && lane == 0) t_idle = clock64();
       }
       bad_page = __any_sync(0xffffffffu, bad_page);
       if (lane == 0) {
         if (bad_page && a.err) atomicOr(a.err, kErrClamped);
-        for (int t = max(0, s - kStages); t < s; ++t)
-          if (!mbar_wait(&bars[kKvFull + t % kStages], (t / kStages) & 1)) flags[0] = 1;
+        // no load of this CTA may land after it exits
+        for (int t = max(0, nk - 2); t < nk; ++t)
+          if (!mbar_wait(&bars[kKFull + (t & 1)], (t >> 1) & 1)) flags[0] = 1;
+        for (int t = max(0, nv - 2); t < nv; ++t)
+          if (!mbar_wait(&bars[kVFull + (t & 1)], (t >> 1) & 1)) flags[0] = 1;
       }
     }
   } else if (warp == 1) {
@@ -358,13 +395,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t kIdescQK = umma::idesc_f16(kRows, kTok, true, false, false);
       constexpr uint32_t kIdescPV = umma::idesc_f16(kRows, kHalf, true, false, true);
-      const uint32_t stage0 = smem_u32(smem);
+      const uint32_t kbase = smem_u32(smem);
+      const uint32_t vbase = smem_u32(smem + off_v);
       const uint32_t pslot = smem_u32(smem + off_p);
       const uint32_t qrope = smem_u32(smem + kOffQRope);
       bool ok = mbar_wait(&bars[kQReady], 0);
       umma::fence_after_sync();
       auto issue_qk = [&](int j) {
-        const uint32_t st = stage0 + (j % kStages) * stride;
+        const uint32_t st = kbase + (j & 1) * kbytes;
         const uint32_t sd = tmem + kColS + 64u * uint32_t(j & 1);
         for (int k = 0; k < 4; ++k)
           for (int kk = 0; kk < 4; ++kk)
@@ -377,21 +415,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                          umma::smem_desc(st + 4 * kChunkBytes + 32 * kk, 16, 1024, umma::kSw128),
                          kIdescQK, 1u);
         umma::commit(&bars[kSFull + (j & 1)]);
+        umma::commit(&bars[kKEmpty + (j & 1)]);  // the K slot may refill
       };
       auto issue_pv = [&](int j) {
-        const uint32_t st = stage0 + (j % kStages) * stride;
-        const uint32_t pa = pslot + (j & 1) * kPSlot;
+        const uint32_t st = vbase + (j & 1) * kVBytes;
+        const uint32_t pa = pslot + (j & 1) * kPBytes;
         for (int kk = 0; kk < 4; ++kk)
           umma::mma_ss(tmem + kColO, umma::smem_desc(pa + 32 * kk, 16, 1024, umma::kSw128),
                        umma::smem_desc(st + 2048 * kk, kChunkBytes, 1024, umma::kSw128), kIdescPV,
                        (j | kk) != 0);
-        umma::commit(&bars[kKvEmpty + j % kStages]);
+        umma::commit(&bars[kVEmpty + (j & 1)]);
         umma::commit(&bars[kPvDone]);
         // the P slot may take CTA 0's next message once this P.V has read it
         if (c == 1) commit_to(&bars[kPSlotFree + (j & 1)], uint16_t(1u));
       };
-      // Issue whichever is ready: the P.V of the oldest tile (it frees a
-      // stage) or the logits of the next one, so QK runs ahead of the round
+      // Issue whichever is ready: the P.V of the oldest tile (it frees a V
+      // slot) or the logits of the next one, so QK runs ahead of the round
       // trip that P takes.  Tests never block; the loop gives up after
       // kWaitCycles without progress.
       int nq = 0, np = 0;
@@ -400,12 +439,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         bool moved = false;
         // CTA 1's P arrives from the peer; CTA 0 wrote its own
         if (np < nq && mbar_test(&bars[kPFull], np & 1) &&
+            mbar_test(&bars[kVFull + (np & 1)], (np >> 1) & 1) &&
             (c == 0 || mbar_test(&bars[kPIn + (np & 1)], (np >> 1) & 1))) {
           umma::fence_after_sync();
           issue_pv(np++);
           moved = true;
         }
-        if (nq < ntiles && mbar_test(&bars[kKvFull + nq % kStages], (nq / kStages) & 1) &&
+        if (nq < ntiles && mbar_test(&bars[kKFull + (nq & 1)], (nq >> 1) & 1) &&
             (nq < 2 || mbar_test(&bars[kSFree + (nq & 1)], ((nq >> 1) - 1) & 1))) {
           umma::fence_after_sync();
           issue_qk(nq++);
@@ -476,7 +516,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (c == 0) {
       // ---------------- CTA 0: full logits, online softmax, P for both CTAs
       const float* recv = reinterpret_cast<const float*>(smem + kOffRecv);
-      const uint32_t pslot_peer = map_peer(smem_u32(smem + kOffPSlot1), peer);
+      const uint32_t pslot_peer = map_peer(smem_u32(smem + kOffP1), peer);
+      const uint32_t fslot_peer = map_peer(smem_u32(smem + kOffF1), peer);
       const int row_lb = a.win > 0 ? spec0 + i - a.win + 1 : INT_MIN;
       uint32_t row_mw = 0xffffffffu;
       if (a.mask) {
@@ -547,7 +588,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // copy to the peer has landed)
         if (j > 0) ok = __all_sync(kAll, mbar_wait(&bars[kPvDone], (j - 1) & 1));
         if (ok && j >= 2) ok = __all_sync(kAll, mbar_wait(&bars[kPSlotFree + sb], ((j >> 1) - 1) & 1));
-        uint8_t* pbuf = smem + kOffPSlot0 + sb * kPSlot;
+        uint8_t* pbuf = smem + kOffP0 + sb * kPBytes;
+        float* fbuf = reinterpret_cast<float*>(smem + kOffF0 + sb * kFBytes);
         if (ok) {
           umma::fence_after_sync();
           const float m_new = fmaxf(m_ref, mx);
@@ -572,8 +614,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             *reinterpret_cast<uint4*>(pbuf + umma::sw128(t, 4 * h + u)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
-          if (h == 0) reinterpret_cast<float*>(pbuf + kPBytes)[t] = f;
-          if (tile0 + kTok > t_end) zero_v_tail(smem + (j % kStages) * kStride0, max(0, t_end - tile0), st);
+          if (h == 0) fbuf[t] = f;
+          // the split's last tile: its V slot must have landed before the tail is cleared
+          if (tile0 + kTok > t_end) {
+            ok = __all_sync(kAll, mbar_wait(&bars[kVFull + sb], (j >> 1) & 1));
+            if (ok) zero_v_tail(smem + kOffV0 + sb * kVBytes, max(0, t_end - tile0), st);
+          }
           // whole warp rescales its rows' O half-columns (factor 1 where unchanged)
           if (__any_sync(kAll, f != 1.f)) rescale_o(o_cols, f);
           umma::fence_proxy_async_smem();
@@ -585,11 +631,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         }
         if (lane == 0) mbar_arrive(&bars[kPFull]);
-        // four copies from four warps: one long copy moves slower than pieces in flight together
+        // P in four copies from four warps, the factors in a fifth
         if ((st & 31) == 0 && st < 32 * kCopyPieces) {
-          const uint32_t off = uint32_t(st >> 5) * (kPMsg / kCopyPieces);
-          bulk_to_peer(pslot_peer + sb * kPSlot + off, smem_u32(pbuf) + off, kPMsg / kCopyPieces,
+          const uint32_t off = uint32_t(st >> 5) * (kPBytes / kCopyPieces);
+          bulk_to_peer(pslot_peer + sb * kPBytes + off, smem_u32(pbuf) + off, kPBytes / kCopyPieces,
                        peer_bars + 8u * (kPIn + sb));
+        } else if (st == 32 * kCopyPieces) {
+          bulk_to_peer(fslot_peer + sb * kFBytes, smem_u32(fbuf), kFBytes, peer_bars + 8u * (kPIn + sb));
         }
       }
     } else {
@@ -635,10 +683,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (ok && jp > 0) ok = __all_sync(kAll, mbar_wait(&bars[kPvDone], (jp - 1) & 1));
           if (ok) {
             umma::fence_after_sync();
-            const float f = reinterpret_cast<const float*>(smem + kOffPSlot1 + kp * kPSlot + kPBytes)[t];
+            const float f = reinterpret_cast<const float*>(smem + kOffF1 + kp * kFBytes)[t];
             if (__any_sync(kAll, f != 1.f)) rescale_o(o_cols, f);
             const int tile0 = t_begin + jp * kTok;
-            if (tile0 + kTok > t_end) zero_v_tail(smem + (jp % kStages) * kStride1, max(0, t_end - tile0), st);
+            if (tile0 + kTok > t_end) {
+              ok = __all_sync(kAll, mbar_wait(&bars[kVFull + kp], (jp >> 1) & 1));
+              if (ok) zero_v_tail(smem + kOffV1 + kp * kVBytes, max(0, t_end - tile0), st);
+            }
             umma::fence_proxy_async_smem();
             umma::fence_before_sync();
           }
