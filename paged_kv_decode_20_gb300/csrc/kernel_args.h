@@ -32,6 +32,7 @@ struct DecodeArgs {
   int out_e4m3;                // out is float8_e4m3fn (rounded to nearest, saturated at +-448)
   int hnd;                     // cache layout HND (else NHD)
   int pdl;                     // launched with programmatic stream serialization
+  int sort_b;                  // map grid slots to sequences longest first (B <= 160)
 };
 
 }  // namespace xqa

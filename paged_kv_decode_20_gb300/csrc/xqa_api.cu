@@ -279,6 +279,7 @@ void fill_args(const xqa_params* p, const Plan& pl, void* ws, uint32_t* sems, xq
   a->out_e4m3 = p->out_dtype == XQA_E4M3;
   a->hnd = p->kv_layout == XQA_HND;
   a->pdl = p->enable_pdl != 0;
+  a->sort_b = p->batch_size > 1 && p->batch_size <= 160;
 }
 
 xqa_status check_buffers(const Plan& pl, void* ws, size_t ws_bytes, uint32_t* sems) {
