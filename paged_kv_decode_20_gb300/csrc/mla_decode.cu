@@ -7,30 +7,28 @@
 //
 // The 128 query rows (heads x speculative tokens) form one M = 128 UMMA tile.
 // Their fp32 output (128 x 512) alone fills a CTA's 512 tensor-memory
-// columns, so a cluster of two CTAs shares each (sequence, KV split), each
-// CTA holding half of the output columns:
+// columns, so a cluster of two CTAs shares each (sequence, KV split) and the
+// two split the work by stage:
 //
-//   CTA 0 ("master") owns latent dims [0, 256);
-//   CTA 1 ("feeder") owns latent dims [256, 512) plus the rope dims [512, 576).
-//   Each CTA streams only its dims of every latent row (TMA, 128-byte
-//   swizzle, three-stage mbarrier ring) and computes the partial logits
-//   S_c = Q_c K_c^T with tcgen05.mma (A = its latent query half held in
-//   tensor memory, B = K from shared memory; CTA 1 adds the rope part with A
-//   from shared memory).  CTA 1 ships S_1 (fp32) to CTA 0 with bulk copies
-//   into distributed shared memory, a tile ahead of CTA 0's softmax.  CTA 0
-//   adds it to S_0, runs the only online softmax, and ships P (bf16, already
-//   in UMMA operand layout) with the per-row rescale factors back.  Both CTAs
-//   accumulate O_c += P V_c in their own 256 tensor-memory columns, V_c being
-//   the first four chunks of the K tile the CTA already holds.  Every latent
-//   byte is read from HBM once; CTA 0's softmax waits on no round trip (the
-//   feeder ships a tile's logits before the master needs them), while CTA 1's
-//   P.V of a tile waits for one message back.
+//   CTA 1 (the logit CTA) holds the whole query: the latent part in tensor
+//   memory, the rope part in shared memory.  It streams each 576-wide latent
+//   row of the split through a ring of 64-token x 64-dim chunks (TMA, 128-byte
+//   swizzle).  It computes the logits S = Q K^T with tcgen05.mma and runs the
+//   online softmax.  P (bf16, already in UMMA operand layout) and one rescale
+//   factor per row travel into CTA 0's shared memory by bulk copy.
+//   CTA 0 (the output CTA) holds the whole fp32 output in tensor memory.  It
+//   fetches the first 512 dims of each tile (V) again, from L2, and
+//   accumulates O += P V with two N = 256 MMAs per 16 tokens.  Its eight spare
+//   warps rescale O when the softmax raised a row maximum by more than 2^8,
+//   clear V rows past the split's end, and run the epilogue.
 //
-// Warp roles: 0 = TMA producer and tensor-memory allocator, 1 = MMA issuer,
-// 2..9 = softmax (CTA 0) or logit shipping and O rescale (CTA 1), then the
-// epilogue; warp w reaches TMEM lanes 32 (w % 4).. and two threads share a
-// query row.  Split-KV partials merge exactly as in the grouped-query kernel:
-// the last CTA of each column half to take a ticket merges every split.
+// Only P crosses the cluster (16.5 KB per 64 tokens, one way), and every
+// latent byte is read from HBM once.  Warp roles in both CTAs: 0 = TMA
+// producer and tensor-memory allocator, 1 = MMA issuer, 2..9 = softmax
+// (logit CTA) or rescale / epilogue (output CTA); warp w reaches TMEM lanes
+// 32 (w % 4).., so two threads share each query row.  Split-KV partials merge
+// as in the grouped-query kernel: the last CTA of each column half to take a
+// ticket merges every split.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdio.h>
@@ -52,76 +50,86 @@ constexpr int kRows = 128;       // UMMA M: query rows (heads x spec tokens)
 constexpr int kLatent = 512;     // kv_lora_rank (= V width)
 constexpr int kRope = 64;        // qk_rope_head_dim
 constexpr int kDim = kLatent + kRope;
-constexpr int kHalf = kLatent / 2;  // V columns per CTA
-constexpr int kTok = 64;         // tokens per tile (UMMA N of QK, K of PV)
-constexpr int kChunkBytes = kTok * 128;  // one 64-element column chunk of a tile
-constexpr int kSoftWarps = 8;    // two threads per query row, 32 logit columns each
+constexpr int kHalf = kLatent / 2;  // output columns per epilogue thread and per merging CTA
+constexpr int kTok = 64;         // tokens per P / V tile (UMMA K of PV)
+constexpr int kTokQ = 2 * kTok;  // tokens per logit tile (UMMA N of QK)
+constexpr int kChunkBytes = kTok * 128;    // one 64-dim column chunk of a V tile
+constexpr int kChunkBytesQ = kTokQ * 128;  // one 64-dim column chunk of a logit tile
+constexpr int kChunks = kDim / 64;         // chunks of a latent row: 8 latent + 1 rope
+constexpr int kSoftWarps = 8;    // two threads per query row
 constexpr int kSoft = 32 * kSoftWarps;
-constexpr int kSoftWarp0 = 2;    // softmax warps are 2..9: two per TMEM sub-partition
+constexpr int kSoftWarp0 = 2;    // warps 2..9: two per TMEM sub-partition
 constexpr int kThreads = 32 * kSoftWarp0 + kSoft;
 
-// ---- shared memory (offsets from the dynamic base, which is 1024-aligned:
-// checked at run time).  Each CTA keeps two rings: K slots hold a tile's
-// chunks until its QK is done; V slots hold the same latent chunks, fetched
-// again (from L2, right after the QK) until its P.V is done.  Holding a stage
-// only as long as its own use needs lets two slots of each kind cover the
-// tile's whole exchange.  The barrier block sits at the same offset in both
-// CTAs because each CTA signals barriers of its peer.
-constexpr int kXBytes = kRows * kTok * 4;  // one fp32 logit tile
+// ---- messages from the logit CTA to the output CTA
 constexpr int kPBytes = kRows * kTok * 2;  // one bf16 P tile
-constexpr int kFBytes = kRows * 4;         // one rescale factor per row
-constexpr int kPMsg = kPBytes + kFBytes;   // P, then its factors (two copies)
-constexpr int kVBytes = 4 * kChunkBytes;   // the four latent chunks of a tile
-constexpr int kKBytes0 = 4 * kChunkBytes;  // CTA 0 K slot: 4 latent chunks
-constexpr int kKBytes1 = 5 * kChunkBytes;  // CTA 1 K slot: 4 latent chunks + rope
-// CTA 0: K x2 | V x2 | P x2 | factors x2 | logit receive slots x2
-constexpr int kOffV0 = 2 * kKBytes0;
-constexpr int kOffP0 = kOffV0 + 2 * kVBytes;
-constexpr int kOffF0 = kOffP0 + 2 * kPBytes;
-constexpr int kOffRecv = kOffF0 + 2 * kFBytes;
-// CTA 1: K x2 | V x2 | rope query (128 x 64 bf16) | P x2 | factors x2 | send buffer
-constexpr int kOffV1 = 2 * kKBytes1;
-constexpr int kOffQRope = kOffV1 + 2 * kVBytes;
-constexpr int kOffP1 = kOffQRope + kRows * 128;
-constexpr int kOffF1 = kOffP1 + 2 * kPBytes;
-constexpr int kOffSend = kOffF1 + 2 * kFBytes;
-// both: [2][128] floats (CTA 0: row maxima / sums; CTA 1: the final m and l)
-constexpr int kOffRowX = (kOffRecv + 2 * kXBytes) > (kOffSend + kXBytes) ? (kOffRecv + 2 * kXBytes)
-                                                                         : (kOffSend + kXBytes);
-constexpr int kOffBar = kOffRowX + 2 * kRows * 4;
+constexpr int kFBytes = kRows * 4 + 16;    // one rescale factor per row, then a flag word
+constexpr int kPMsg = kPBytes + kFBytes;
+constexpr int kFinBytes = 2 * kRows * 4;   // the final row maxima and sums
+constexpr int kCopyPieces = 4;             // P travels as this many bulk copies
+
+// ---- shared memory (offsets from the dynamic base, which is 1024-aligned:
+// checked at run time).  The barrier block sits at the same offset in both
+// CTAs because each CTA signals barriers of its peer.
+// Output CTA: V x3 | P x2 | factors x2 | final rows
+constexpr int kVBytes = 8 * kChunkBytes;  // the eight latent chunks of a tile
+constexpr int kVSlots = 3;
+constexpr int kOffV = 0;
+constexpr int kOffP = kOffV + kVSlots * kVBytes;
+constexpr int kOffF = kOffP + 2 * kPBytes;
+constexpr int kOffFin = kOffF + 2 * kFBytes;
+// Logit CTA: K chunk ring (128 tokens x 64 dims per slot) | rope query
+// (128 x 64 bf16) | P staging x2 | factor staging x2 | row maxima
+// [2 tiles][2 halves][128] | final rows
+constexpr int kKSlots = 10;
+constexpr int kOffK = 0;
+constexpr int kOffQRope = kOffK + kKSlots * kChunkBytesQ;
+constexpr int kOffPS = kOffQRope + kRows * 128;
+constexpr int kOffFS = kOffPS + 2 * kPBytes;
+constexpr int kOffRowX = kOffFS + 2 * kFBytes;
+constexpr int kOffFinS = kOffRowX + 4 * kRows * 4;
+constexpr int kOffBar =
+    (kOffFin + kFinBytes) > (kOffFinS + kFinBytes) ? (kOffFin + kFinBytes) : (kOffFinS + kFinBytes);
 
 enum BarIdx {
-  kKFull = 0,                   // [2] a K slot's bytes landed
-  kKEmpty = kKFull + 2,         // [2] the QK reading a K slot is done
-  kVFull = kKEmpty + 2,         // [2] a V slot's bytes landed
-  kVEmpty = kVFull + 2,         // [2] the P.V reading a V slot is done
-  kQReady = kVEmpty + 2,        // the query is in tensor / shared memory
-  kSFull = kQReady + 1,         // [2] S tile computed
-  kSFree = kSFull + 2,          // [2] S tile read out of tensor memory
-  kPFull = kSFree + 2,          // P (and any O rescale) ready for the P.V
-  kPvDone = kPFull + 1,         // the last P.V issued is done
-  kDrain = kPvDone + 1,         // every MMA this CTA issued is done
-  kXFull = kDrain + 1,          // CTA 0 [2]: the peer's logit tile landed
-  kXFree = kXFull + 2,          // CTA 1: CTA 0 received the previous logit tile
-  kPIn = kXFree + 1,            // CTA 1 [2]: a P message landed
-  kPSlotFree = kPIn + 2,        // CTA 0 [2]: CTA 1's P.V on that P slot is done
-  kFin = kPSlotFree + 2,        // CTA 1: the final (m, l) rows landed
-  kNumBars = kFin + 1
+  // logit CTA
+  kKFull = 0,                      // [kKSlots] a K chunk landed
+  kKEmpty = kKFull + kKSlots,      // [kKSlots] the QK reading a K chunk is done
+  kSFull = kKEmpty + kKSlots,      // [2] S tile computed
+  kSFree = kSFull + 2,             // [2] S tile read out of tensor memory
+  kQReady = kSFree + 2,            // the query is in tensor / shared memory
+  kPSlotFree = kQReady + 1,        // [2] the output CTA's P.V of that P slot is done
+  // output CTA
+  kVFull = kPSlotFree + 2,         // [kVSlots] a V slot landed
+  kVEmpty = kVFull + kVSlots,      // [kVSlots] the P.V reading a V slot is done
+  kPFull = kVEmpty + kVSlots,      // [2] own expect-tx arrival + the peer's P message
+  kFin = kPFull + 2,               // own expect-tx arrival + the peer's final rows
+  kReq = kFin + 1,                 // the MMA thread posted a request to the warps
+  kOReady = kReq + 1,              // the warps served it
+  kODone = kOReady + 1,            // every P.V issued so far is done
+  // both
+  kDrain = kODone + 1,             // every MMA this CTA issued is done
+  kNumBars = kDrain + 1
 };
 constexpr int kSmem = kOffBar + kNumBars * 8 + 32;
 static_assert(kSmem <= 232448, "shared memory budget");
-static_assert(kOffV0 % 1024 == 0 && kOffP0 % 1024 == 0 && kOffV1 % 1024 == 0 && kOffP1 % 1024 == 0 &&
-                  kOffQRope % 1024 == 0 && kOffRecv % 16 == 0 && kOffSend % 16 == 0 && kOffF0 % 16 == 0 &&
-                  kOffF1 % 16 == 0,
+static_assert(kOffP % 1024 == 0 && kOffQRope % 1024 == 0 && kOffPS % 1024 == 0 && kOffF % 16 == 0 &&
+                  kOffFS % 16 == 0 && kOffFin % 16 == 0 && kOffFinS % 16 == 0 && kFBytes % 16 == 0 &&
+                  kOffBar % 8 == 0,
               "UMMA operands need 1024-byte alignment, bulk copies 16");
-constexpr int kCopyPieces = 4;  // the logit tile and the P tile travel as this many bulk copies
-static_assert(kPBytes % (16 * kCopyPieces) == 0 && kXBytes % (16 * kCopyPieces) == 0, "copy pieces");
+static_assert(kPBytes % (16 * kCopyPieces) == 0, "copy pieces");
 
 // tensor memory columns
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0;     // 256 fp32 columns: O half
-constexpr uint32_t kColQ = 256;   // 128 columns: latent query half, bf16 pairs
-constexpr uint32_t kColS = 384;   // 2 x 64 columns: logits double buffer
+constexpr uint32_t kColO = 0;    // output CTA: 512 fp32 columns of O
+constexpr uint32_t kColQ = 0;    // logit CTA: 256 columns, the latent query as bf16 pairs
+constexpr uint32_t kColS = 256;  // logit CTA: 2 x 128 columns of logits
+
+// requests from the output CTA's MMA thread to its warps
+constexpr int kReqEnd = -1;
+constexpr int kReqRescale = 1 << 30;  // multiply O rows by the tile's factors
+constexpr int kReqTail = 1 << 29;     // zero the V rows past the split's end
+constexpr int kReqTile = (1 << 29) - 1;
 
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by > 2^8
 constexpr int kMaxSplits = 64;       // merge weights [128][splits] fit in shared memory
@@ -169,12 +177,6 @@ __device__ __forceinline__ void bulk_to_peer(uint32_t dst_cluster, uint32_t src_
       "r"(src_cta), "r"(bytes), "r"(bar_cluster)
       : "memory");
 }
-// Tells the peer that this CTA has received what the peer sent.  The arrive
-// carries no data of its own, so relaxed ordering suffices and avoids a
-// cluster-scope release.
-__device__ __forceinline__ void remote_arrive(uint32_t rbar) {
-  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar) : "memory");
-}
 // Arrives once on the barrier at the same offset in every CTA of `mask` when
 // every MMA this thread issued so far is done.
 __device__ __forceinline__ void commit_to(uint64_t* bar, uint16_t mask) {
@@ -187,13 +189,10 @@ __device__ __forceinline__ void commit_to(uint64_t* bar, uint16_t mask) {
 
 __device__ __forceinline__ float ldscale(const float* dev, float host) { return dev ? __ldg(dev) : host; }
 
-// 16-byte unit u (0..15) of row t of a 128 x 64 fp32 buffer, XOR-swizzled by row.
-__device__ __forceinline__ int xunit(int t, int u) { return t * kTok + ((u ^ (t & 15)) & 15) * 4; }
-
-// Multiplies this warp's 32 rows of O columns [128h, 128h + 128) by f.
+// Multiplies this warp's 32 rows of O columns [256h, 256h + 256) by f.
 __device__ __forceinline__ void rescale_o(uint32_t taddr, float f) {
 #pragma unroll 1
-  for (int part = 0; part < kHalf / 64; ++part) {
+  for (int part = 0; part < kHalf / 32; ++part) {
     float o[32];
     umma::tmem_ld32(taddr + 32u * part, o);
     umma::tmem_ld_wait();
@@ -204,14 +203,44 @@ __device__ __forceinline__ void rescale_o(uint32_t taddr, float f) {
   umma::tmem_st_wait();
 }
 
-// Zeroes V rows [r0, kTok) of a stage's four latent chunks: past a split's
+// Zeroes V rows [r0, kTok) of a V slot's eight latent chunks: past a split's
 // last token the rows hold stale or foreign data (possibly NaN), and P = 0
 // there must not meet it in the P.V.
-__device__ __forceinline__ void zero_v_tail(uint8_t* stage, int r0, int st) {
-  for (int idx = st; idx < (kTok - r0) * 4 * 8; idx += kSoft) {
-    const int r = r0 + idx / 32, k = (idx / 8) % 4, u = idx % 8;
-    *reinterpret_cast<uint4*>(stage + k * kChunkBytes + r * 128 + u * 16) = make_uint4(0, 0, 0, 0);
+__device__ __forceinline__ void zero_v_tail(uint8_t* vslot, int r0, int st) {
+  for (int idx = st; idx < (kTok - r0) * 8 * 8; idx += kSoft) {
+    const int r = r0 + idx / 64, k = (idx / 8) % 8, u = idx % 8;
+    *reinterpret_cast<uint4*>(vslot + k * kChunkBytes + r * 128 + u * 16) = make_uint4(0, 0, 0, 0);
   }
+}
+
+// The pieces of a tile of `tok` tokens starting at token tok0: boxes of
+// min(page_size, 64) rows, piece l at tile row 64-aligned l * box rows.  Lane
+// l < n loads piece l; `row` is its first row in the flattened
+// [pages * page_size] row space (a negative row for a page index out of
+// range: the TMA fills zeros there).  Pieces past the split's last page are
+// not loaded.
+struct TilePieces {
+  int n, row;
+  bool bad;
+};
+__device__ __forceinline__ TilePieces tile_pieces(const MlaArgs& a, const int32_t* pt, int tok0, int tok, int pg_hi,
+                                                  int lane) {
+  TilePieces p;
+  const int box = min(a.ps, kTok);
+  const int split_end = pg_hi * a.ps;  // first token past the split's pages
+  p.n = min(tok / box, (split_end - tok0 + box - 1) / box);
+  p.bad = false;
+  p.row = 0;
+  if (lane < p.n) {
+    const int tk = tok0 + lane * box;
+    int page = __ldg(pt + tk / a.ps);
+    if (page < 0 || int64_t(page) >= a.num_pages) {
+      page = -1;
+      p.bad = true;
+    }
+    p.row = page * a.ps + tk % a.ps;
+  }
+  return p;
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -220,13 +249,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
-  int* flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] abort, [1] last CTA
+  int* flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] abort, [1] last CTA, [2] request word
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t c = cluster_rank();
   const uint32_t peer = c ^ 1u;
+  const bool logit_cta = c == 1;
   const int split = blockIdx.x >> 1;
   const int b = blockIdx.z;
+  constexpr unsigned kAll = 0xffffffffu;
 
   // wait for the producer of our inputs, then let the next call start launching
   pdl_wait();
@@ -249,10 +280,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int t_begin = pg_lo * a.ps;
   const int t_end = min(pg_hi * a.ps, L);
   const int ntiles = (nvalid == 0 || t_end <= t_begin) ? 0 : (t_end - t_begin + kTok - 1) / kTok;
-  const int nchunks = c == 0 ? 4 : 5;  // chunks of a K slot
-  const int kbytes = c == 0 ? kKBytes0 : kKBytes1;
-  const int off_v = c == 0 ? kOffV0 : kOffV1;
-  const int off_p = c == 0 ? kOffP0 : kOffP1;
+  const int nqt = (ntiles + 1) / 2;  // logit tiles of 128 tokens
   // the layout assumes a 1024-aligned dynamic base (the 128-byte swizzle
   // atoms of the UMMA operands); both CTAs see the same base and leave together
   if (smem_u32(smem_raw) & 1023u) {
@@ -261,30 +289,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars[kKFull + i], 1);
-      mbar_init(&bars[kKEmpty + i], 1);
-      mbar_init(&bars[kVFull + i], 1);
-      mbar_init(&bars[kVEmpty + i], 1);
+    if (logit_cta) {
+      for (int i = 0; i < kKSlots; ++i) {
+        mbar_init(&bars[kKFull + i], 1);
+        mbar_init(&bars[kKEmpty + i], 1);
+      }
+      for (int k = 0; k < 2; ++k) {
+        mbar_init(&bars[kSFull + k], 1);
+        mbar_init(&bars[kSFree + k], kSoftWarps);
+      }
+      mbar_init(&bars[kQReady], kSoftWarps);
+      for (int k = 0; k < 2; ++k) mbar_init(&bars[kPSlotFree + k], 1);  // the peer's MMA completion
+    } else {
+      for (int k = 0; k < kVSlots; ++k) {
+        mbar_init(&bars[kVFull + k], 1);
+        mbar_init(&bars[kVEmpty + k], 1);
+      }
+      for (int k = 0; k < 2; ++k) mbar_init(&bars[kPFull + k], 1);
+      mbar_init(&bars[kFin], 1);
+      mbar_init(&bars[kReq], 1);
+      mbar_init(&bars[kOReady], kSoftWarps);
+      mbar_init(&bars[kODone], 1);
+      // the first two P messages and the final rows are expected up front
+      for (int k = 0; k < min(2, ntiles); ++k) mbar_arrive_expect_tx(&bars[kPFull + k], kPMsg);
+      mbar_arrive_expect_tx(&bars[kFin], kFinBytes);
     }
-    mbar_init(&bars[kQReady], kSoftWarps);
-    for (int k = 0; k < 2; ++k) {
-      mbar_init(&bars[kSFull + k], 1);
-      mbar_init(&bars[kSFree + k], kSoftWarps);
-      mbar_init(&bars[kXFull + k], 1);      // own expect-tx arrival + the peer's bytes
-      mbar_init(&bars[kPIn + k], 1);        // own expect-tx arrival + the peer's bytes
-      mbar_init(&bars[kPSlotFree + k], 1);  // the peer's MMA completion
-    }
-    mbar_init(&bars[kPFull], kSoftWarps);
-    mbar_init(&bars[kPvDone], 1);
     mbar_init(&bars[kDrain], 1);
-    mbar_init(&bars[kXFree], 1);
-    mbar_init(&bars[kFin], 1);
-    flags[0] = flags[1] = 0;
-    // the first two receive slots and the final rows are expected up front
-    for (int k = 0; k < min(2, ntiles); ++k)
-      mbar_arrive_expect_tx(&bars[c == 0 ? kXFull + k : kPIn + k], c == 0 ? kXBytes : kPMsg);
-    if (c == 1) mbar_arrive_expect_tx(&bars[kFin], 2 * kRows * 4);
+    flags[0] = flags[1] = flags[2] = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -297,194 +328,196 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   umma::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   const uint32_t peer_bars = map_peer(smem_u32(bars), peer);
+  const int32_t* pt = a.page_table + int64_t(b) * a.pps;
+  const uint32_t box_bytes = uint32_t(min(a.ps, kTok)) * 128u;
+  constexpr uint32_t kIdescQK = umma::idesc_f16(kRows, kTokQ, true, false, false);
+  constexpr uint32_t kIdescPV = umma::idesc_f16(kRows, kHalf, true, false, true);
 
   if (warp == 0) {
-    // ================= TMA producer (lane 0 decides, lane j loads page piece j)
-    // K(j) may load once the QK of tile j - 2 is done (its slot is free); V(j)
-    // once the QK of tile j is done and the P.V of tile j - 2 has freed its V
-    // slot.  Tests never block; the loop gives up after kWaitCycles idle.
+    // ================= TMA producer =================
+    // Logit CTA: every chunk of every tile, in order, into the chunk ring; a
+    // chunk slot refills once the QK that read it is done.  Output CTA: the
+    // eight latent chunks of each tile into a V slot once the P.V of the tile
+    // three back is done.  Each wait gives up after kWaitCycles.
     if (ntiles > 0) {
       if (lane == 0) prefetch_tensormap(&tmKV);
-      const int32_t* pt = a.page_table + int64_t(b) * a.pps;
-      const int box_rows = min(a.ps, kTok);
-      const uint32_t box_bytes = uint32_t(box_rows) * 128u;
-      bool bad_page = false;
-      // all tile loads of tile j (nck chunks per page piece) into dst, on bar
-      auto issue = [&](int j, uint8_t* dst, uint64_t* bar, int nck) {
-        const int tok0 = t_begin + j * kTok;
-        const int lp0 = tok0 / a.ps;
-        const int sub = a.ps <= kTok ? 0 : tok0 % a.ps;
-        const int n_piece = a.ps <= kTok ? min(kTok / a.ps, pg_hi - lp0) : 1;
-        if (lane == 0) mbar_arrive_expect_tx(bar, uint32_t(n_piece) * box_bytes * nck);
-        __syncwarp();
-        if (lane < n_piece) {
-          int page = __ldg(pt + lp0 + lane);
-          if (page < 0 || int64_t(page) >= a.num_pages) {
-            page = -1;  // the TMA fills zeros
-            bad_page = true;
+      bool ok = true, bad = false;
+      int issued = 0;
+      if (logit_cta) {
+        TilePieces tp = {0, 0, false};
+        for (int g = 0; ok && g < nqt * kChunks; ++g) {
+          const int slot = g % kKSlots, use = g / kKSlots;
+          const int j = g / kChunks, k = g - j * kChunks;
+          if (k == 0) {
+            tp = tile_pieces(a, pt, t_begin + j * kTokQ, kTokQ, pg_hi, lane);
+            bad |= tp.bad;
+            // the tile two ahead goes into L2 now, so that its chunk loads
+            // (issued only as ring slots free) do not pay HBM latency
+            if (j + 2 < nqt) {
+              const TilePieces pf = tile_pieces(a, pt, t_begin + (j + 2) * kTokQ, kTokQ, pg_hi, lane);
+              if (lane < pf.n && pf.row >= 0)
+                for (int kk = 0; kk < kChunks; ++kk) tma_prefetch_l2_3d(&tmKV, 64 * kk, 0, pf.row);
+            }
           }
-          for (int k = 0; k < nck; ++k) {
-            // chunk k: latent dims 256c + 64k (k < 4) or the rope dims
-            const int x = k < 4 ? int(c) * kHalf + 64 * k : kLatent;
-            tma_load_3d(dst + k * kChunkBytes + lane * box_rows * 128, &tmKV, bar, x, 0, page * a.ps + sub);
-          }
+          if (use > 0) ok = __all_sync(kAll, mbar_wait(&bars[kKEmpty + slot], (use - 1) & 1));
+          if (!ok) break;
+          if (lane == 0) mbar_arrive_expect_tx(&bars[kKFull + slot], uint32_t(tp.n) * box_bytes);
+          __syncwarp();
+          if (lane < tp.n)
+            tma_load_3d(smem + kOffK + slot * kChunkBytesQ + lane * box_bytes, &tmKV, &bars[kKFull + slot],
+                        64 * k, 0, tp.row);
+          __syncwarp();
+          ++issued;
         }
-        __syncwarp();
-      };
-      // the tile two K loads ahead goes into L2 early, so that its own load
-      // (issued only when a K slot frees) does not pay HBM latency
-      auto prefetch = [&](int j) {
-        if (j >= ntiles) return;
-        const int tok0 = t_begin + j * kTok;
-        const int lp0 = tok0 / a.ps;
-        const int sub = a.ps <= kTok ? 0 : tok0 % a.ps;
-        const int n_piece = a.ps <= kTok ? min(kTok / a.ps, pg_hi - lp0) : 1;
-        if (lane < n_piece) {
-          const int pg = __ldg(pt + lp0 + lane);
-          if (pg >= 0 && int64_t(pg) < a.num_pages)
-            for (int k = 0; k < nchunks; ++k)
-              tma_prefetch_l2_3d(&tmKV, k < 4 ? int(c) * kHalf + 64 * k : kLatent, 0, pg * a.ps + sub);
-        }
-      };
-      int nk = 0, nv = 0, seen = 0;  // K loads, V loads issued; QKs seen done (lane 0)
-      long long t_idle = clock64();
-      while (true) {
-        int dec = 0;  // 1: load K(nk), 2: load V(nv), 3: finished, 4: gave up
-        if (lane == 0) {
-          if (seen < nk && mbar_test(&bars[kKEmpty + (seen & 1)], (seen >> 1) & 1)) {
-            ++seen;
-            t_idle = clock64();
-          }
-          if (nv >= ntiles)
-            dec = 3;
-          else if (nk < ntiles && nk < seen + 2)
-            dec = 1;
-          else if (nv < seen && (nv < 2 || mbar_test(&bars[kVEmpty + (nv & 1)], ((nv >> 1) - 1) & 1)))
-            dec = 2;
-          else if (clock64() - t_idle > kWaitCycles)
-            dec = 4;
-        }
-        dec = __shfl_sync(0xffffffffu, dec, 0);
-        if (dec == 3) break;
-        if (dec == 4) {
-          if (lane == 0) flags[0] = 1;
-          break;
-        }
-        if (dec == 1) {
-          issue(nk, smem + (nk & 1) * kbytes, &bars[kKFull + (nk & 1)], nchunks);
-          prefetch(nk + 2);
-          ++nk;
-        } else if (dec == 2) {
-          issue(nv, smem + off_v + (nv & 1) * kVBytes, &bars[kVFull + (nv & 1)], 4);
-          ++nv;
-        }
-        if (dec && lane == 0) t_idle = clock64();
-      }
-      bad_page = __any_sync(0xffffffffu, bad_page);
-      if (lane == 0) {
-        if (bad_page && a.err) atomicOr(a.err, kErrClamped);
         // no load of this CTA may land after it exits
-        for (int t = max(0, nk - 2); t < nk; ++t)
-          if (!mbar_wait(&bars[kKFull + (t & 1)], (t >> 1) & 1)) flags[0] = 1;
-        for (int t = max(0, nv - 2); t < nv; ++t)
-          if (!mbar_wait(&bars[kVFull + (t & 1)], (t >> 1) & 1)) flags[0] = 1;
+        if (lane == 0)
+          for (int g = max(0, issued - kKSlots); g < issued; ++g)
+            if (!mbar_wait(&bars[kKFull + g % kKSlots], (g / kKSlots) & 1)) ok = false;
+      } else {
+        for (int j = 0; ok && j < ntiles; ++j) {
+          const int slot = j % kVSlots, use = j / kVSlots;
+          if (use > 0) ok = __all_sync(kAll, mbar_wait(&bars[kVEmpty + slot], (use - 1) & 1));
+          if (!ok) break;
+          const TilePieces tp = tile_pieces(a, pt, t_begin + j * kTok, kTok, pg_hi, lane);
+          bad |= tp.bad;
+          if (lane == 0) mbar_arrive_expect_tx(&bars[kVFull + slot], uint32_t(tp.n) * box_bytes * 8u);
+          __syncwarp();
+          if (lane < tp.n)
+            for (int k = 0; k < 8; ++k)
+              tma_load_3d(smem + kOffV + slot * kVBytes + k * kChunkBytes + lane * box_bytes, &tmKV,
+                          &bars[kVFull + slot], 64 * k, 0, tp.row);
+          __syncwarp();
+          ++issued;
+        }
+        if (lane == 0)
+          for (int j = max(0, issued - kVSlots); j < issued; ++j)
+            if (!mbar_wait(&bars[kVFull + j % kVSlots], (j / kVSlots) & 1)) ok = false;
+      }
+      bad = __any_sync(kAll, bad);
+      if (lane == 0) {
+        if (bad && a.err) atomicOr(a.err, kErrClamped);
+        if (!ok) flags[0] = 1;
       }
     }
+    __syncwarp();
   } else if (warp == 1) {
-    // ================= MMA issuer =================
+    // ================= MMA issuer (one thread) =================
     if (lane == 0 && ntiles > 0) {
-      constexpr uint32_t kIdescQK = umma::idesc_f16(kRows, kTok, true, false, false);
-      constexpr uint32_t kIdescPV = umma::idesc_f16(kRows, kHalf, true, false, true);
-      const uint32_t kbase = smem_u32(smem);
-      const uint32_t vbase = smem_u32(smem + off_v);
-      const uint32_t pslot = smem_u32(smem + off_p);
-      const uint32_t qrope = smem_u32(smem + kOffQRope);
-      bool ok = mbar_wait(&bars[kQReady], 0);
-      umma::fence_after_sync();
-      auto issue_qk = [&](int j) {
-        const uint32_t st = kbase + (j & 1) * kbytes;
-        const uint32_t sd = tmem + kColS + 64u * uint32_t(j & 1);
-        for (int k = 0; k < 4; ++k)
-          for (int kk = 0; kk < 4; ++kk)
-            umma::mma_ts(sd, tmem + kColQ + 32u * k + 8u * kk,
-                         umma::smem_desc(st + k * kChunkBytes + 32 * kk, 16, 1024, umma::kSw128),
-                         kIdescQK, (k | kk) != 0);
-        if (c == 1)
-          for (int kk = 0; kk < 4; ++kk)
-            umma::mma_ss(sd, umma::smem_desc(qrope + 32 * kk, 16, 1024, umma::kSw128),
-                         umma::smem_desc(st + 4 * kChunkBytes + 32 * kk, 16, 1024, umma::kSw128),
-                         kIdescQK, 1u);
-        umma::commit(&bars[kSFull + (j & 1)]);
-        umma::commit(&bars[kKEmpty + (j & 1)]);  // the K slot may refill
-      };
-      auto issue_pv = [&](int j) {
-        const uint32_t st = vbase + (j & 1) * kVBytes;
-        const uint32_t pa = pslot + (j & 1) * kPBytes;
-        for (int kk = 0; kk < 4; ++kk)
-          umma::mma_ss(tmem + kColO, umma::smem_desc(pa + 32 * kk, 16, 1024, umma::kSw128),
-                       umma::smem_desc(st + 2048 * kk, kChunkBytes, 1024, umma::kSw128), kIdescPV,
-                       (j | kk) != 0);
-        umma::commit(&bars[kVEmpty + (j & 1)]);
-        umma::commit(&bars[kPvDone]);
-        // the P slot may take CTA 0's next message once this P.V has read it
-        if (c == 1) commit_to(&bars[kPSlotFree + (j & 1)], uint16_t(1u));
-      };
-      // Issue whichever is ready: the P.V of the oldest tile (it frees a V
-      // slot) or the logits of the next one, so QK runs ahead of the round
-      // trip that P takes.  Tests never block; the loop gives up after
-      // kWaitCycles without progress.
-      int nq = 0, np = 0;
-      long long t_idle = clock64();
-      while (ok && np < ntiles) {
-        bool moved = false;
-        // CTA 1's P arrives from the peer; CTA 0 wrote its own
-        if (np < nq && mbar_test(&bars[kPFull], np & 1) &&
-            mbar_test(&bars[kVFull + (np & 1)], (np >> 1) & 1) &&
-            (c == 0 || mbar_test(&bars[kPIn + (np & 1)], (np >> 1) & 1))) {
+      bool ok = true;
+      if (logit_cta) {
+        // S(j) = Q K(j)^T over a 128-token tile: 32 N = 128 MMAs with the
+        // latent query from tensor memory, 4 with the rope query from shared
+        // memory, into S buffer j % 2.  All nine chunk waits come before the
+        // tile's MMAs: a barrier wait issued right behind MMAs costs the
+        // issuing thread a few hundred cycles, a run of waits only once.
+        const uint32_t kb = smem_u32(smem + kOffK), qrope = smem_u32(smem + kOffQRope);
+        ok = mbar_wait(&bars[kQReady], 0);
+        for (int j = 0; ok && j < nqt; ++j) {
+          const int sb = j & 1;
+          if (j >= 2) ok = mbar_wait(&bars[kSFree + sb], ((j >> 1) - 1) & 1);
+          for (int k = 0; ok && k < kChunks; ++k) {
+            const int g = j * kChunks + k;
+            ok = mbar_wait(&bars[kKFull + g % kKSlots], (g / kKSlots) & 1);
+          }
+          if (!ok) break;
           umma::fence_after_sync();
-          issue_pv(np++);
-          moved = true;
+          const uint32_t sd = tmem + kColS + 128u * uint32_t(sb);
+#pragma unroll
+          for (int k = 0; k < kChunks; ++k) {
+            const int slot = (j * kChunks + k) % kKSlots;
+            const uint32_t st = kb + slot * kChunkBytesQ;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t bdesc = umma::smem_desc(st + 32 * kk, 16, 1024, umma::kSw128);
+              if (k < 8)
+                umma::mma_ts(sd, tmem + kColQ + 32u * k + 8u * kk, bdesc, kIdescQK, (k | kk) != 0);
+              else
+                umma::mma_ss(sd, umma::smem_desc(qrope + 32 * kk, 16, 1024, umma::kSw128), bdesc, kIdescQK, 1u);
+            }
+            umma::commit(&bars[kKEmpty + slot]);  // the chunk slot may refill
+          }
+          umma::commit(&bars[kSFull + sb]);
         }
-        if (nq < ntiles && mbar_test(&bars[kKFull + (nq & 1)], (nq >> 1) & 1) &&
-            (nq < 2 || mbar_test(&bars[kSFree + (nq & 1)], ((nq >> 1) - 1) & 1))) {
+      } else {
+        // O += P(j) V(j): per 16 tokens, two N = 256 MMAs (O columns 0-255 and
+        // 256-511).  A tile whose factors are not all 1, or whose V rows run
+        // past the split's end, first goes to the warps (a request).
+        const uint32_t vb = smem_u32(smem + kOffV), pb = smem_u32(smem + kOffP);
+        const volatile uint32_t* fmsg = reinterpret_cast<const volatile uint32_t*>(smem + kOffF);
+        volatile int* req = flags + 2;
+        int nreq = 0, nod = 0;
+        for (int j = 0; ok && j < ntiles; ++j) {
+          const int p2 = j & 1, vs = j % kVSlots;
+          ok = mbar_wait(&bars[kPFull + p2], (j >> 1) & 1);
+          if (!ok) break;
+          // the slot's next message (tile j + 2) is sent only after this P.V
+          if (j + 2 < ntiles) mbar_arrive_expect_tx(&bars[kPFull + p2], kPMsg);
+          const bool resc = j > 0 && fmsg[p2 * (kFBytes / 4) + kRows] != 0u;
+          ok = mbar_wait(&bars[kVFull + vs], (j / kVSlots) & 1);
+          if (!ok) break;
+          const bool tail = t_begin + (j + 1) * kTok > t_end;
+          if (resc || tail) {
+            if (resc) {  // O may change only once every earlier P.V is done
+              umma::commit(&bars[kODone]);
+              ok = mbar_wait(&bars[kODone], nod & 1);
+              ++nod;
+              if (!ok) break;
+            }
+            *req = j | (resc ? kReqRescale : 0) | (tail ? kReqTail : 0);
+            mbar_arrive(&bars[kReq]);
+            ok = mbar_wait(&bars[kOReady], nreq & 1);
+            ++nreq;
+            if (!ok) break;
+          }
           umma::fence_after_sync();
-          issue_qk(nq++);
-          moved = true;
+          const uint32_t pa = pb + p2 * kPBytes, va = vb + vs * kVBytes;
+          for (int kk = 0; kk < 4; ++kk)
+            for (int n = 0; n < 2; ++n)
+              umma::mma_ss(tmem + kColO + uint32_t(kHalf * n),
+                           umma::smem_desc(pa + 32 * kk, 16, 1024, umma::kSw128),
+                           umma::smem_desc(va + 4 * n * kChunkBytes + 2048 * kk, kChunkBytes, 1024, umma::kSw128),
+                           kIdescPV, (j | kk) != 0);
+          umma::commit(&bars[kVEmpty + vs]);
+          // the logit CTA may stage and send the P of tile j + 2
+          commit_to(&bars[kPSlotFree + p2], uint16_t(2u));
         }
-        if (moved)
-          t_idle = clock64();
-        else if (clock64() - t_idle > kWaitCycles)
-          ok = false;
       }
       if (!ok) flags[0] = 1;
-      // nothing this thread issued may still run when tensor memory is freed
+      // nothing this thread issued may still run when tensor memory is read or freed
       umma::commit(&bars[kDrain]);
       if (!mbar_wait(&bars[kDrain], 0)) flags[0] = 1;
     }
-  } else {
-    // ================= softmax / logit shipping / epilogue =================
+    if (!logit_cta && lane == 0) {
+      // the warps leave their request loop for the epilogue
+      flags[2] = kReqEnd;
+      mbar_arrive(&bars[kReq]);
+    }
+    // the other lanes wait here, not at the CTA barrier below: lanes parked at
+    // a CTA barrier slow the MMA issue of their warp's active lane
+    __syncwarp();
+  } else if (logit_cta) {
+    // ================= logit CTA: query load, online softmax, P shipping =====
     // Warp w (2..9) reaches TMEM lanes 32 (w % 4) .. +31 (query rows); h = (w - 2) / 4
-    // picks logit columns [32h, 32h + 32) of every tile and O columns [128h, 128h+128).
+    // picks logit columns [32h, 32h + 32) of every tile.
     const int q4 = warp & 3, h = (warp - kSoftWarp0) >> 2;
-    const int t = 32 * q4 + lane;            // query row = TMEM lane
-    const int st = tid - 32 * kSoftWarp0;    // 0 .. kSoft - 1
+    const int t = 32 * q4 + lane;          // query row = TMEM lane
+    const int st = tid - 32 * kSoftWarp0;  // 0 .. kSoft - 1
     const uint32_t lane_base = uint32_t(32 * q4) << 16;
-    const uint32_t o_cols = tmem + lane_base + kColO + 128u * h;
-    const int i = t / a.Hq, hd = t % a.Hq;  // row t = (spec token i, head hd)
+    const int i = t / a.Hq;  // row t = (spec token i, head t % Hq)
     const float q_scale = ldscale(a.q_scale_dev, a.q_scale);
     const float kv_scale = ldscale(a.kv_scale_dev, a.kv_scale);
     const float lscale = a.softmax_scale * q_scale * kv_scale * kLog2e;
-    float* rowx = reinterpret_cast<float*>(smem + kOffRowX);  // [2][128]
-    constexpr unsigned kAll = 0xffffffffu;
+    float* rowx = reinterpret_cast<float*>(smem + kOffRowX);  // [2][2][128]
     constexpr int kC = kTok / 2;  // logit columns per thread
 
-    // ---- query: this thread's half of the row's latent half into tensor
-    // memory; the rope part into shared memory (CTA 1)
+    // ---- query: this thread's half of the latent row into tensor memory
+    // (dims [256h, 256h + 256) -> columns [128h, 128h + 128)), a quarter of
+    // the rope row into shared memory
     {
       const uint16_t* qrow = a.q + (int64_t(b) * a.qs * a.Hq + t) * kDim;
-      const uint4* src = reinterpret_cast<const uint4*>(qrow + c * kHalf + 128 * h);
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {  // 2 x 32 columns = 128 bf16
+      const uint4* src = reinterpret_cast<const uint4*>(qrow + kHalf * h);
+#pragma unroll 1
+      for (int part = 0; part < 4; ++part) {  // 4 x 32 columns = 256 bf16
         uint32_t w[32];
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
@@ -494,13 +527,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           w[4 * v + 2] = x.z;
           w[4 * v + 3] = x.w;
         }
-        umma::tmem_st32(tmem + lane_base + kColQ + 64u * h + 32u * part, w);
+        umma::tmem_st32(tmem + lane_base + kColQ + 128u * h + 32u * part, w);
       }
-      if (c == 1) {
-        const uint4* rsrc = reinterpret_cast<const uint4*>(qrow + kLatent);
-        for (int u = 4 * h; u < 4 * h + 4; ++u)
-          *reinterpret_cast<uint4*>(smem + kOffQRope + umma::sw128(t, u)) = __ldg(rsrc + u);
-      }
+      const uint4* rsrc = reinterpret_cast<const uint4*>(qrow + kLatent);
+      for (int u = 4 * h; u < 4 * h + 4; ++u)
+        *reinterpret_cast<uint4*>(smem + kOffQRope + umma::sw128(t, u)) = __ldg(rsrc + u);
       umma::tmem_st_wait();
       umma::fence_proxy_async_smem();
       umma::fence_before_sync();
@@ -508,250 +539,196 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars[kQReady]);
     }
 
+    const uint32_t p_peer = map_peer(smem_u32(smem + kOffP), peer);
+    const uint32_t f_peer = map_peer(smem_u32(smem + kOffF), peer);
+    const int row_lb = a.win > 0 ? spec0 + i - a.win + 1 : INT_MIN;
+    uint32_t row_mw = 0xffffffffu;
+    if (a.mask) {
+      const uint16_t* mrow = a.mask + (int64_t(b) * a.qs + i) * a.mask_words;
+      row_mw = uint32_t(__ldg(mrow)) | (uint32_t(__ldg(mrow + 1)) << 16);
+    }
     float m_ref = -INFINITY, l_half = 0.f;
     bool ok = true;
-    // Control flow stays uniform across each warp (tcgen05.ld / st are
+    // Control flow stays uniform across each warp (tcgen05.ld is
     // warp-collective) and across the eight softmax warps (named barrier 1):
-    // waits are voted and loops are left collectively.
-    if (c == 0) {
-      // ---------------- CTA 0: full logits, online softmax, P for both CTAs
-      const float* recv = reinterpret_cast<const float*>(smem + kOffRecv);
-      const uint32_t pslot_peer = map_peer(smem_u32(smem + kOffP1), peer);
-      const uint32_t fslot_peer = map_peer(smem_u32(smem + kOffF1), peer);
-      const int row_lb = a.win > 0 ? spec0 + i - a.win + 1 : INT_MIN;
-      uint32_t row_mw = 0xffffffffu;
-      if (a.mask) {
-        const uint16_t* mrow = a.mask + (int64_t(b) * a.qs + i) * a.mask_words;
-        row_mw = uint32_t(__ldg(mrow)) | (uint32_t(__ldg(mrow + 1)) << 16);
+    // waits are voted and the loop is left collectively.
+    // A 128-token logit tile holds two 64-token P tiles: both halves of this
+    // thread's logits come out of tensor memory at once (the S buffer frees
+    // early), then each half goes through the softmax and ships as its own
+    // P message.
+    for (int jq = 0; ok && jq < nqt; ++jq) {
+      const int sb = jq & 1;
+      const int nsub = min(2, ntiles - 2 * jq);
+      float sv[2][kC];
+      ok = __all_sync(kAll, mbar_wait(&bars[kSFull + sb], (jq >> 1) & 1));
+      if (ok) {
+        umma::fence_after_sync();
+        umma::tmem_ld32(tmem + lane_base + kColS + 128u * uint32_t(sb) + 32u * h, sv[0]);
+        if (nsub > 1) umma::tmem_ld32(tmem + lane_base + kColS + 128u * uint32_t(sb) + 64u + 32u * h, sv[1]);
+        umma::tmem_ld_wait();
+        umma::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kSFree + sb]);
       }
-      for (int j = 0; j < ntiles; ++j) {
-        const int sb = j & 1;
-        const uint32_t par = (j >> 1) & 1;
-        float s[kC];
-        ok = __all_sync(kAll, mbar_wait(&bars[kSFull + sb], par));
-        if (ok) {
-          umma::fence_after_sync();
-          umma::tmem_ld32(tmem + lane_base + kColS + 64u * sb + 32u * h, s);
-          umma::tmem_ld_wait();
-          umma::fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[kSFree + sb]);
-          // the peer's partial logits of this tile
-          ok = __all_sync(kAll, mbar_wait(&bars[kXFull + sb], par));
-        }
-        // received: the peer may refill its send buffer (and so this CTA's other
-        // slot); after the last tile nobody waits for the signal, so none is sent
-        if (ok && st == 0 && j + 1 < ntiles) remote_arrive(peer_bars + 8u * kXFree);
-        const int tile0 = t_begin + j * kTok;
-        float mx = -INFINITY;
-        if (ok) {
-          const float* rx = recv + sb * (kXBytes / 4);
 #pragma unroll
-          for (int v = 0; v < kC / 4; ++v) {
-            const float4 p4 = *reinterpret_cast<const float4*>(rx + xunit(t, 8 * h + v));
-            s[4 * v] += p4.x;
-            s[4 * v + 1] += p4.y;
-            s[4 * v + 2] += p4.z;
-            s[4 * v + 3] += p4.w;
-          }
-          // visibility of this thread's 32 columns as one bit each (all set
-          // away from the split's end, the window start and the spec tokens)
-          const bool edge = tile0 + kTok > t_end || tile0 <= row_lb || (a.mask && tile0 + kTok > spec0);
-          uint32_t vis = 0xffffffffu;
-          if (edge) {
-            vis = 0u;
+    for (int u = 0; u < 2; ++u) {
+      if (u >= nsub) break;
+      const int j = 2 * jq + u, p2 = j & 1;
+      float* s = sv[u];
+      // staging slot p2 is free once the output CTA's P.V of tile j - 2 is
+      // done (which also means its message landed)
+      if (ok && j >= 2) ok = __all_sync(kAll, mbar_wait(&bars[kPSlotFree + p2], ((j >> 1) - 1) & 1));
+      const int tile0 = t_begin + j * kTok;
+      float mx = -INFINITY;
+      if (ok) {
+        // visibility of this thread's 32 columns as one bit each (all set
+        // away from the split's end, the window start and the spec tokens)
+        const bool edge = tile0 + kTok > t_end || tile0 <= row_lb || (a.mask && tile0 + kTok > spec0);
+        uint32_t vis = 0xffffffffu;
+        if (edge) {
+          vis = 0u;
 #pragma unroll 1
-            for (int k = 0; k < kC; ++k) {
-              const int tt = tile0 + 32 * h + k;
-              bool v = tt < t_end && tt >= row_lb;
-              if (a.mask && tt >= spec0) v = v && ((row_mw >> (tt - spec0)) & 1u);
-              vis |= uint32_t(v) << k;
-            }
-          }
-#pragma unroll
           for (int k = 0; k < kC; ++k) {
-            const float x = (vis >> k) & 1u ? s[k] * lscale : -INFINITY;
-            s[k] = x;
-            mx = fmaxf(mx, x);
+            const int tt = tile0 + 32 * h + k;
+            bool v = tt < t_end && tt >= row_lb;
+            if (a.mask && tt >= spec0) v = v && ((row_mw >> (tt - spec0)) & 1u);
+            vis |= uint32_t(v) << k;
           }
-          rowx[h * kRows + t] = mx;
         }
-        // both halves of every row published their maxima; the slot is consumed
-        if (named_bar_or(1, kSoft, !ok)) {
-          ok = false;
-          break;
-        }
-        if (st == 0 && j + 2 < ntiles) mbar_arrive_expect_tx(&bars[kXFull + sb], kXBytes);
-        mx = fmaxf(mx, rowx[(1 - h) * kRows + t]);
-        // O may be rescaled once the previous P.V is done; P slot sb is free
-        // once both CTAs' P.V of tile j - 2 are done (which also means its
-        // copy to the peer has landed)
-        if (j > 0) ok = __all_sync(kAll, mbar_wait(&bars[kPvDone], (j - 1) & 1));
-        if (ok && j >= 2) ok = __all_sync(kAll, mbar_wait(&bars[kPSlotFree + sb], ((j >> 1) - 1) & 1));
-        uint8_t* pbuf = smem + kOffP0 + sb * kPBytes;
-        float* fbuf = reinterpret_cast<float*>(smem + kOffF0 + sb * kFBytes);
-        if (ok) {
-          umma::fence_after_sync();
-          const float m_new = fmaxf(m_ref, mx);
-          const bool need = m_new > m_ref + kRescaleLog2 || (m_ref == -INFINITY && m_new != -INFINITY);
-          const float f = (need && m_ref != -INFINITY) ? exp2f(m_ref - m_new) : 1.f;
-          if (need) {
-            l_half *= f;
-            m_ref = m_new;
-          }
-          // P (bf16) for this thread's 32 columns: units 4h..4h+3 of row t; the
-          // row sum takes the rounded weights so O / l stays a convex combination
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            uint32_t w4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float p0 = m_ref == -INFINITY ? 0.f : ex2(s[8 * u + 2 * e] - m_ref);
-              const float p1 = m_ref == -INFINITY ? 0.f : ex2(s[8 * u + 2 * e + 1] - m_ref);
-              w4[e] = pack_f32x2(p0, p1, true);
-              const float2 r = unpack_16x2(w4[e], true);
-              l_half += r.x + r.y;
-            }
-            *reinterpret_cast<uint4*>(pbuf + umma::sw128(t, 4 * h + u)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-          }
-          if (h == 0) fbuf[t] = f;
-          // the split's last tile: its V slot must have landed before the tail is cleared
-          if (tile0 + kTok > t_end) {
-            ok = __all_sync(kAll, mbar_wait(&bars[kVFull + sb], (j >> 1) & 1));
-            if (ok) zero_v_tail(smem + kOffV0 + sb * kVBytes, max(0, t_end - tile0), st);
-          }
-          // whole warp rescales its rows' O half-columns (factor 1 where unchanged)
-          if (__any_sync(kAll, f != 1.f)) rescale_o(o_cols, f);
-          umma::fence_proxy_async_smem();
-          umma::fence_before_sync();
+        for (int k = 0; k < kC; ++k) {
+          const float x = (vis >> k) & 1u ? s[k] * lscale : -INFINITY;
+          s[k] = x;
+          mx = fmaxf(mx, x);
         }
-        // every thread finished P, the factors and the V tail, or someone gave up
-        if (named_bar_or(1, kSoft, !ok)) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) mbar_arrive(&bars[kPFull]);
-        // P in four copies from four warps, the factors in a fifth
-        if ((st & 31) == 0 && st < 32 * kCopyPieces) {
-          const uint32_t off = uint32_t(st >> 5) * (kPBytes / kCopyPieces);
-          bulk_to_peer(pslot_peer + sb * kPBytes + off, smem_u32(pbuf) + off, kPBytes / kCopyPieces,
-                       peer_bars + 8u * (kPIn + sb));
-        } else if (st == 32 * kCopyPieces) {
-          bulk_to_peer(fslot_peer + sb * kFBytes, smem_u32(fbuf), kFBytes, peer_bars + 8u * (kPIn + sb));
-        }
+        rowx[(2 * p2 + h) * kRows + t] = mx;
       }
-    } else {
-      // ---------------- CTA 1: ship partial logits a tile ahead, apply P
-      float* send = reinterpret_cast<float*>(smem + kOffSend);
-      const uint32_t recv_peer = map_peer(smem_u32(smem + kOffRecv), peer);
-      for (int j = 0; j <= ntiles; ++j) {
-        if (j < ntiles) {
-          const int sb = j & 1;
-          float s[kC];
-          ok = __all_sync(kAll, mbar_wait(&bars[kSFull + sb], (j >> 1) & 1));
-          if (ok) {
-            umma::fence_after_sync();
-            umma::tmem_ld32(tmem + lane_base + kColS + 64u * sb + 32u * h, s);
-            umma::tmem_ld_wait();
-            umma::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[kSFree + sb]);
-            // the send buffer and the peer's slot sb are free once the peer
-            // has received the previous tile
-            if (j > 0 && st == 0) ok = mbar_wait(&bars[kXFree], (j - 1) & 1);
-          }
-          if (named_bar_or(1, kSoft, !ok)) {
-            ok = false;
-            break;
-          }
-#pragma unroll
-          for (int v = 0; v < kC / 4; ++v)
-            *reinterpret_cast<float4*>(send + xunit(t, 8 * h + v)) =
-                make_float4(s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3]);
-          umma::fence_proxy_async_smem();
-          named_bar(1, kSoft);
-          if ((st & 31) == 0 && st < 32 * kCopyPieces) {
-            const uint32_t off = uint32_t(st >> 5) * (kXBytes / kCopyPieces);
-            bulk_to_peer(recv_peer + sb * kXBytes + off, smem_u32(send) + off, kXBytes / kCopyPieces,
-                         peer_bars + 8u * (kXFull + sb));
-          }
-        }
-        if (j > 0) {
-          // P of the previous tile: rescale O as the master did, then release the P.V
-          const int jp = j - 1, kp = jp & 1;
-          ok = __all_sync(kAll, mbar_wait(&bars[kPIn + kp], (jp >> 1) & 1));
-          if (ok && jp > 0) ok = __all_sync(kAll, mbar_wait(&bars[kPvDone], (jp - 1) & 1));
-          if (ok) {
-            umma::fence_after_sync();
-            const float f = reinterpret_cast<const float*>(smem + kOffF1 + kp * kFBytes)[t];
-            if (__any_sync(kAll, f != 1.f)) rescale_o(o_cols, f);
-            const int tile0 = t_begin + jp * kTok;
-            if (tile0 + kTok > t_end) {
-              ok = __all_sync(kAll, mbar_wait(&bars[kVFull + kp], (jp >> 1) & 1));
-              if (ok) zero_v_tail(smem + kOffV1 + kp * kVBytes, max(0, t_end - tile0), st);
-            }
-            umma::fence_proxy_async_smem();
-            umma::fence_before_sync();
-          }
-          // the slot's next message (tile jp + 2) is expected before its P.V frees it
-          if (st == 0 && jp + 2 < ntiles) mbar_arrive_expect_tx(&bars[kPIn + kp], kPMsg);
-          if (named_bar_or(1, kSoft, !ok)) {
-            ok = false;
-            break;
-          }
-          if (lane == 0) mbar_arrive(&bars[kPFull]);
-        }
+      // both halves of every row published their maxima
+      if (named_bar_or(1, kSoft, !ok)) {
+        ok = false;
+        break;
       }
+      mx = fmaxf(mx, rowx[(2 * p2 + 1 - h) * kRows + t]);
+      const float m_new = fmaxf(m_ref, mx);
+      const bool need = m_new > m_ref + kRescaleLog2 || (m_ref == -INFINITY && m_new != -INFINITY);
+      const float f = (need && m_ref != -INFINITY) ? exp2f(m_ref - m_new) : 1.f;
+      if (need) {
+        l_half *= f;
+        m_ref = m_new;
+      }
+      // P (bf16) for this thread's 32 columns: units 4h..4h+3 of row t; the
+      // row sum takes the rounded weights so O / l stays a convex combination
+      uint8_t* pstage = smem + kOffPS + p2 * kPBytes;
+      float* fstage = reinterpret_cast<float*>(smem + kOffFS + p2 * kFBytes);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        uint32_t w4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float p0 = m_ref == -INFINITY ? 0.f : ex2(s[8 * u + 2 * e] - m_ref);
+          const float p1 = m_ref == -INFINITY ? 0.f : ex2(s[8 * u + 2 * e + 1] - m_ref);
+          w4[e] = pack_f32x2(p0, p1, true);
+          const float2 r = unpack_16x2(w4[e], true);
+          l_half += r.x + r.y;
+        }
+        *reinterpret_cast<uint4*>(pstage + umma::sw128(t, 4 * h + u)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      }
+      if (h == 0) fstage[t] = f;
+      umma::fence_proxy_async_smem();
+      // every thread wrote its P and factor; does any row need O rescaled?
+      const bool resc = named_bar_or(1, kSoft, f != 1.f);
+      // P in four copies from four warps, the factors and the flag from a fifth
+      if ((st & 31) == 0 && st < 32 * kCopyPieces) {
+        const uint32_t off = uint32_t(st >> 5) * (kPBytes / kCopyPieces);
+        bulk_to_peer(p_peer + p2 * kPBytes + off, smem_u32(pstage) + off, kPBytes / kCopyPieces,
+                     peer_bars + 8u * (kPFull + p2));
+      } else if (st == 32 * kCopyPieces) {
+        reinterpret_cast<uint32_t*>(fstage)[kRows] = resc ? 1u : 0u;
+        umma::fence_proxy_async_smem();
+        bulk_to_peer(f_peer + p2 * kFBytes, smem_u32(fstage), kFBytes, peer_bars + 8u * (kPFull + p2));
+      }
+    }
+    }
+    if (!ok) flags[0] = 1;
+    // ---- the final row maxima and sums go to the output CTA (also when this
+    // split saw no key: m = -inf, l = 0)
+    float* fin = reinterpret_cast<float*>(smem + kOffFinS);
+    named_bar(1, kSoft);
+    rowx[h * kRows + t] = l_half;
+    named_bar(1, kSoft);
+    if (h == 0) {
+      fin[t] = m_ref;
+      fin[kRows + t] = l_half + rowx[kRows + t];
+    }
+    umma::fence_proxy_async_smem();
+    named_bar(1, kSoft);
+    if (st == 0) {
+      bulk_to_peer(map_peer(smem_u32(smem + kOffFin), peer), smem_u32(fin), kFinBytes, peer_bars + 8u * kFin);
+      // the peer's completion signals for the last two P slots must land
+      // before this CTA may exit
+      for (int j = max(0, ntiles - 2); ok && j < ntiles; ++j)
+        if (!mbar_wait(&bars[kPSlotFree + (j & 1)], (j >> 1) & 1)) {
+          flags[0] = 1;
+          ok = false;
+        }
+    }
+  } else {
+    // ================= output CTA: requests, then the epilogue =================
+    // Warp w (2..9) reaches TMEM lanes 32 (w % 4) .. +31; h = (w - 2) / 4 picks
+    // O columns [256h, 256h + 256).
+    const int q4 = warp & 3, h = (warp - kSoftWarp0) >> 2;
+    const int t = 32 * q4 + lane;
+    const int st = tid - 32 * kSoftWarp0;
+    const uint32_t lane_base = uint32_t(32 * q4) << 16;
+    const uint32_t o_cols = tmem + lane_base + kColO + uint32_t(kHalf * h);
+    const int i = t / a.Hq, hd = t % a.Hq;
+    const float kv_scale = ldscale(a.kv_scale_dev, a.kv_scale);
+    bool ok = true;
+    // Requests: rescale O by a tile's factors (every earlier P.V is done) and
+    // / or zero the V rows past the split's end (the V slot has landed).  The
+    // MMA thread waits for each request to be served before the next, so the
+    // request word and the factor slot are stable while the warps read them.
+    for (int k = 0;; ++k) {
+      ok = __all_sync(kAll, mbar_wait(&bars[kReq], k & 1));
+      if (!ok) break;
+      const int r = *reinterpret_cast<volatile int*>(flags + 2);
+      if (r == kReqEnd) break;
+      const int j = r & kReqTile;
+      umma::fence_after_sync();
+      if (r & kReqRescale) {
+        const float f = reinterpret_cast<const float*>(smem + kOffF + (j & 1) * kFBytes)[t];
+        if (__any_sync(kAll, f != 1.f)) rescale_o(o_cols, f);
+      }
+      if (r & kReqTail) zero_v_tail(smem + kOffV + (j % kVSlots) * kVBytes, max(0, t_end - (t_begin + j * kTok)), st);
+      umma::fence_proxy_async_smem();
+      umma::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kOReady]);
     }
     if (!ok) flags[0] = 1;
 
-    // ---- epilogue: wait for the last P.V, agree on (m, l), then finalise or
-    // write the partial
-    const bool have_o = ntiles > 0;
-    if (have_o && ok && !__all_sync(kAll, mbar_wait(&bars[kPvDone], (ntiles - 1) & 1))) {
+    // ---- epilogue: the final (m, l) rows from the logit CTA, then finalise or
+    // write the partial.  Every P.V is done (the end request follows the drain).
+    if (!__all_sync(kAll, mbar_wait(&bars[kFin], 0))) {
       flags[0] = 1;
       ok = false;
     }
     umma::fence_after_sync();
-    float l_run;
-    if (c == 0) {
-      // the peer's completion signals for the last two P slots must land
-      // before this CTA may exit
-      for (int j = max(0, ntiles - 2); ok && j < ntiles; ++j)
-        ok = __all_sync(kAll, mbar_wait(&bars[kPSlotFree + (j & 1)], (j >> 1) & 1));
-      if (!ok) flags[0] = 1;
-      rowx[h * kRows + t] = l_half;
-      named_bar(1, kSoft);
-      l_run = rowx[t] + rowx[kRows + t];
-      named_bar(1, kSoft);
-      if (h == 0) {
-        rowx[t] = m_ref;
-        rowx[kRows + t] = l_run;
-      }
-      umma::fence_proxy_async_smem();
-      named_bar(1, kSoft);
-      if (st == 0)
-        bulk_to_peer(map_peer(smem_u32(rowx), peer), smem_u32(rowx), 2 * kRows * 4, peer_bars + 8u * kFin);
-    } else {
-      if (!__all_sync(kAll, mbar_wait(&bars[kFin], 0))) {
-        flags[0] = 1;
-        ok = false;
-      }
-      m_ref = rowx[t];
-      l_run = rowx[kRows + t];
-    }
+    const float* fin = reinterpret_cast<const float*>(smem + kOffFin);
+    const float m_fin = fin[t], l_fin = fin[kRows + t];
     if (ok) {
+      const bool have_o = ntiles > 0;
       const bool single = nvalid <= 1;
       float mul = 0.f;
       const int64_t row_g = (int64_t(b) * a.qs + i) * a.Hq + hd;
       if (single) {
         const float sig = a.sinks ? __ldg(a.sinks + hd) * kLog2e : -INFINITY;
-        mul = finalize_row(m_ref, l_run, sig, kv_scale * a.rcp_out_scale,
-                           (a.lse && c == 0 && h == 0) ? a.lse + row_g : nullptr);
+        mul = finalize_row(m_fin, l_fin, sig, kv_scale * a.rcp_out_scale,
+                           (a.lse && h == 0) ? a.lse + row_g : nullptr);
       }
       float* wrow = a.ws + ((int64_t(b) * a.nsplit + split) * kRows + t) * (kLatent + 4);
-#pragma unroll
-      for (int part = 0; part < kHalf / 64; ++part) {
+#pragma unroll 1
+      for (int part = 0; part < kHalf / 32; ++part) {
         float o[32];
         if (have_o) {
           umma::tmem_ld32(o_cols + 32u * part, o);
@@ -760,7 +737,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 32; ++k) o[k] = 0.f;
         }
-        const int col = int(c) * kHalf + 128 * h + 32 * part;
+        const int col = kHalf * h + 32 * part;
         if (single) {
           uint4* dst = reinterpret_cast<uint4*>(a.out + row_g * kLatent + col);
 #pragma unroll
@@ -776,10 +753,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       if (!single && h == 0) {
-        wrow[kLatent + 2 * c] = m_ref;
-        wrow[kLatent + 2 * c + 1] = l_run;
+        wrow[kLatent] = m_fin;
+        wrow[kLatent + 1] = l_fin;
       }
     }
+    // the partial is visible device-wide before either CTA of the cluster
+    // takes a merge ticket
+    __threadfence();
   }
 
   // ---- teardown: no tensor-memory or peer traffic may outlive this point
@@ -796,7 +776,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   if (nvalid <= 1) return;
 
-  // ---- split-KV: the last CTA of this column half merges every split
+  // ---- split-KV: the last CTA of this column half merges every split (the
+  // output CTA wrote the whole partial; each CTA of the cluster takes its
+  // ticket after the cluster barrier that follows those writes)
   __threadfence();
   __syncthreads();
   const int unit = b * 2 + int(c);
@@ -816,11 +798,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (tid < kRows) {
     const int row = tid;
     float M = -INFINITY;
-    for (int sp = 0; sp < nvalid; ++sp)
-      M = fmaxf(M, __ldcg(ws_b + (int64_t(sp) * kRows + row) * kStride + kLatent + 2 * c));
+    for (int sp = 0; sp < nvalid; ++sp) M = fmaxf(M, __ldcg(ws_b + (int64_t(sp) * kRows + row) * kStride + kLatent));
     float l = 0.f;
     for (int sp = 0; sp < nvalid; ++sp) {
-      const float* src = ws_b + (int64_t(sp) * kRows + row) * kStride + kLatent + 2 * c;
+      const float* src = ws_b + (int64_t(sp) * kRows + row) * kStride + kLatent;
       const float ms = __ldcg(src);
       const float f = ms == -INFINITY ? 0.f : exp2f(ms - M);
       wts[row * nvalid + sp] = f;
