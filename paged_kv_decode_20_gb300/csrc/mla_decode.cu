@@ -78,12 +78,14 @@ constexpr int kOffV = 0;
 constexpr int kOffP = kOffV + kVSlots * kVBytes;
 constexpr int kOffF = kOffP + 2 * kPBytes;
 constexpr int kOffFin = kOffF + 2 * kFBytes;
-// Logit CTA: K chunk ring (128 tokens x 64 dims per slot) | rope query
-// (128 x 64 bf16) | P staging x2 | factor staging x2 | row maxima
-// [2 tiles][2 halves][128] | final rows
-constexpr int kKSlots = 10;
+// Logit CTA: K ring of three slots, each one group of three chunks (128
+// tokens x 192 dims) | rope query (128 x 64 bf16) | P staging x2 | factor
+// staging x2 | row maxima [2 tiles][2 halves][128] | final rows
+constexpr int kGroup = 3;                     // chunks per ring slot
+constexpr int kKSlots = kChunks / kGroup;     // one slot per group of a logit tile
+constexpr int kGroupBytes = kGroup * kChunkBytesQ;
 constexpr int kOffK = 0;
-constexpr int kOffQRope = kOffK + kKSlots * kChunkBytesQ;
+constexpr int kOffQRope = kOffK + kKSlots * kGroupBytes;
 constexpr int kOffPS = kOffQRope + kRows * 128;
 constexpr int kOffFS = kOffPS + 2 * kPBytes;
 constexpr int kOffRowX = kOffFS + 2 * kFBytes;
@@ -93,8 +95,8 @@ constexpr int kOffBar =
 
 enum BarIdx {
   // logit CTA
-  kKFull = 0,                      // [kKSlots] a K chunk landed
-  kKEmpty = kKFull + kKSlots,      // [kKSlots] the QK reading a K chunk is done
+  kKFull = 0,                      // [kKSlots] a group of K chunks landed
+  kKEmpty = kKFull + kKSlots,      // [kKSlots] the QK reading a group is done
   kSFull = kKEmpty + kKSlots,      // [2] S tile computed
   kSFree = kSFull + 2,             // [2] S tile read out of tensor memory
   kQReady = kSFree + 2,            // the query is in tensor / shared memory
@@ -344,28 +346,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true, bad = false;
       int issued = 0;
       if (logit_cta) {
+        // group gr of logit tile j goes to slot gr (its `j`-th use): one
+        // wait, one expect-tx and three chunk loads per group
         TilePieces tp = {0, 0, false};
-        for (int g = 0; ok && g < nqt * kChunks; ++g) {
-          const int slot = g % kKSlots, use = g / kKSlots;
-          const int j = g / kChunks, k = g - j * kChunks;
-          if (k == 0) {
+        for (int g = 0; ok && g < nqt * kKSlots; ++g) {
+          const int j = g / kKSlots, slot = g - j * kKSlots;
+          if (slot == 0) {
             tp = tile_pieces(a, pt, t_begin + j * kTokQ, kTokQ, pg_hi, lane);
             bad |= tp.bad;
-            // the tile two ahead goes into L2 now, so that its chunk loads
-            // (issued only as ring slots free) do not pay HBM latency
+            // the tile two ahead goes into L2 now, so that its loads (issued
+            // only as ring slots free) do not pay HBM latency
             if (j + 2 < nqt) {
               const TilePieces pf = tile_pieces(a, pt, t_begin + (j + 2) * kTokQ, kTokQ, pg_hi, lane);
               if (lane < pf.n && pf.row >= 0)
                 for (int kk = 0; kk < kChunks; ++kk) tma_prefetch_l2_3d(&tmKV, 64 * kk, 0, pf.row);
             }
           }
-          if (use > 0) ok = __all_sync(kAll, mbar_wait(&bars[kKEmpty + slot], (use - 1) & 1));
+          if (j > 0) ok = __all_sync(kAll, mbar_wait(&bars[kKEmpty + slot], (j - 1) & 1));
           if (!ok) break;
-          if (lane == 0) mbar_arrive_expect_tx(&bars[kKFull + slot], uint32_t(tp.n) * box_bytes);
+          if (lane == 0) mbar_arrive_expect_tx(&bars[kKFull + slot], uint32_t(tp.n) * box_bytes * kGroup);
           __syncwarp();
           if (lane < tp.n)
-            tma_load_3d(smem + kOffK + slot * kChunkBytesQ + lane * box_bytes, &tmKV, &bars[kKFull + slot],
-                        64 * k, 0, tp.row);
+            for (int dk = 0; dk < kGroup; ++dk)
+              tma_load_3d(smem + kOffK + slot * kGroupBytes + dk * kChunkBytesQ + lane * box_bytes, &tmKV,
+                          &bars[kKFull + slot], 64 * (kGroup * slot + dk), 0, tp.row);
           __syncwarp();
           ++issued;
         }
@@ -407,35 +411,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (logit_cta) {
         // S(j) = Q K(j)^T over a 128-token tile: 32 N = 128 MMAs with the
         // latent query from tensor memory, 4 with the rope query from shared
-        // memory, into S buffer j % 2.  All nine chunk waits come before the
-        // tile's MMAs: a barrier wait issued right behind MMAs costs the
-        // issuing thread a few hundred cycles, a run of waits only once.
+        // memory, into S buffer j % 2, one group of three chunks at a time.
+        // Any shared-memory read (a barrier test included) issued between
+        // MMAs costs the issuing thread ~100 cycles, so the waits come once
+        // per group, not per chunk.
         const uint32_t kb = smem_u32(smem + kOffK), qrope = smem_u32(smem + kOffQRope);
         ok = mbar_wait(&bars[kQReady], 0);
         for (int j = 0; ok && j < nqt; ++j) {
           const int sb = j & 1;
           if (j >= 2) ok = mbar_wait(&bars[kSFree + sb], ((j >> 1) - 1) & 1);
-          for (int k = 0; ok && k < kChunks; ++k) {
-            const int g = j * kChunks + k;
-            ok = mbar_wait(&bars[kKFull + g % kKSlots], (g / kKSlots) & 1);
-          }
-          if (!ok) break;
-          umma::fence_after_sync();
           const uint32_t sd = tmem + kColS + 128u * uint32_t(sb);
 #pragma unroll
-          for (int k = 0; k < kChunks; ++k) {
-            const int slot = (j * kChunks + k) % kKSlots;
-            const uint32_t st = kb + slot * kChunkBytesQ;
+          for (int gr = 0; gr < kKSlots; ++gr) {
+            if (ok) ok = mbar_wait(&bars[kKFull + gr], j & 1);
+            if (!ok) break;
+            umma::fence_after_sync();
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t bdesc = umma::smem_desc(st + 32 * kk, 16, 1024, umma::kSw128);
-              if (k < 8)
-                umma::mma_ts(sd, tmem + kColQ + 32u * k + 8u * kk, bdesc, kIdescQK, (k | kk) != 0);
-              else
-                umma::mma_ss(sd, umma::smem_desc(qrope + 32 * kk, 16, 1024, umma::kSw128), bdesc, kIdescQK, 1u);
+            for (int dk = 0; dk < kGroup; ++dk) {
+              const int k = kGroup * gr + dk;
+              const uint32_t st = kb + gr * kGroupBytes + dk * kChunkBytesQ;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t bdesc = umma::smem_desc(st + 32 * kk, 16, 1024, umma::kSw128);
+                if (k < 8)
+                  umma::mma_ts(sd, tmem + kColQ + 32u * k + 8u * kk, bdesc, kIdescQK, (k | kk) != 0);
+                else
+                  umma::mma_ss(sd, umma::smem_desc(qrope + 32 * kk, 16, 1024, umma::kSw128), bdesc, kIdescQK,
+                               1u);
+              }
             }
-            umma::commit(&bars[kKEmpty + slot]);  // the chunk slot may refill
+            umma::commit(&bars[kKEmpty + gr]);  // the group's slot may refill
           }
+          if (!ok) break;
           umma::commit(&bars[kSFull + sb]);
         }
       } else {
