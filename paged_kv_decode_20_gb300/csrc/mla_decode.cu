@@ -135,6 +135,10 @@ constexpr int kReqTile = (1 << 29) - 1;
 
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by > 2^8
 constexpr int kMaxSplits = 64;       // merge weights [128][splits] fit in shared memory
+#ifndef XQA_MLA_WAVES
+#define XQA_MLA_WAVES 4
+#endif
+constexpr int kWaves = XQA_MLA_WAVES;  // cluster waves the split plan aims for
 
 struct MlaArgs {
   const uint16_t* q;  // [B, qs, Hq, 576]
@@ -354,23 +358,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (slot == 0) {
             tp = tile_pieces(a, pt, t_begin + j * kTokQ, kTokQ, pg_hi, lane);
             bad |= tp.bad;
-            // the tile two ahead goes into L2 now, so that its loads (issued
-            // only as ring slots free) do not pay HBM latency
-            if (j + 2 < nqt) {
-              const TilePieces pf = tile_pieces(a, pt, t_begin + (j + 2) * kTokQ, kTokQ, pg_hi, lane);
-              if (lane < pf.n && pf.row >= 0)
-                for (int kk = 0; kk < kChunks; ++kk) tma_prefetch_l2_3d(&tmKV, 64 * kk, 0, pf.row);
-            }
           }
           if (j > 0) ok = __all_sync(kAll, mbar_wait(&bars[kKEmpty + slot], (j - 1) & 1));
           if (!ok) break;
           if (lane == 0) mbar_arrive_expect_tx(&bars[kKFull + slot], uint32_t(tp.n) * box_bytes * kGroup);
           __syncwarp();
-          if (lane < tp.n)
-            for (int dk = 0; dk < kGroup; ++dk)
-              tma_load_3d(smem + kOffK + slot * kGroupBytes + dk * kChunkBytesQ + lane * box_bytes, &tmKV,
-                          &bars[kKFull + slot], 64 * (kGroup * slot + dk), 0, tp.row);
+          {
+            // one box per lane (lane = piece * kGroup + chunk of the group):
+            // issuing a TMA instruction holds its thread for hundreds of
+            // cycles, so the boxes go out from several lanes at once
+            const int row = __shfl_sync(kAll, tp.row, min(lane / kGroup, 31));
+            if (lane < tp.n * kGroup) {
+              const int pc = lane / kGroup, dk = lane - pc * kGroup;
+              tma_load_3d(smem + kOffK + slot * kGroupBytes + dk * kChunkBytesQ + pc * box_bytes, &tmKV,
+                          &bars[kKFull + slot], 64 * (kGroup * slot + dk), 0, row);
+            }
+          }
           __syncwarp();
+          // after the tile's first loads are out, the tile two ahead goes into
+          // L2, so that its loads (issued only as ring slots free) do not pay
+          // HBM latency
+          if (slot == 0 && j + 2 < nqt) {
+            const TilePieces pf = tile_pieces(a, pt, t_begin + (j + 2) * kTokQ, kTokQ, pg_hi, lane);
+            for (int b0 = 0; b0 < pf.n * kChunks; b0 += 32) {
+              const int bx = b0 + lane;
+              const int row = __shfl_sync(kAll, pf.row, min(bx / kChunks, 31));
+              if (bx < pf.n * kChunks && row >= 0) tma_prefetch_l2_3d(&tmKV, 64 * (bx % kChunks), 0, row);
+            }
+          }
           ++issued;
         }
         // no load of this CTA may land after it exits
@@ -386,10 +401,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           bad |= tp.bad;
           if (lane == 0) mbar_arrive_expect_tx(&bars[kVFull + slot], uint32_t(tp.n) * box_bytes * 8u);
           __syncwarp();
-          if (lane < tp.n)
-            for (int k = 0; k < 8; ++k)
-              tma_load_3d(smem + kOffV + slot * kVBytes + k * kChunkBytes + lane * box_bytes, &tmKV,
-                          &bars[kVFull + slot], 64 * k, 0, tp.row);
+          {
+            // one box per lane: lane = piece * 8 + latent chunk (at most 4 pieces)
+            const int row = __shfl_sync(kAll, tp.row, lane >> 3);
+            if (lane < tp.n * 8) {
+              const int pc = lane >> 3, k = lane & 7;
+              tma_load_3d(smem + kOffV + slot * kVBytes + k * kChunkBytes + pc * box_bytes, &tmKV,
+                          &bars[kVFull + slot], 64 * k, 0, row);
+            }
+          }
           __syncwarp();
           ++issued;
         }
@@ -523,22 +543,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     {
       const uint16_t* qrow = a.q + (int64_t(b) * a.qs * a.Hq + t) * kDim;
       const uint4* src = reinterpret_cast<const uint4*>(qrow + kHalf * h);
-#pragma unroll 1
-      for (int part = 0; part < 4; ++part) {  // 4 x 32 columns = 256 bf16
-        uint32_t w[32];
+      // the rope quarter first, then the latent half in two rounds of 16
+      // loads in flight per thread
+      const uint4* rsrc = reinterpret_cast<const uint4*>(qrow + kLatent);
+      uint4 rq[4];
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const uint4 x = __ldg(src + part * 8 + v);
+      for (int u = 0; u < 4; ++u) rq[u] = __ldg(rsrc + 4 * h + u);
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        uint32_t w[64];
+#pragma unroll
+        for (int v = 0; v < 16; ++v) {
+          const uint4 x = __ldg(src + half * 16 + v);
           w[4 * v + 0] = x.x;
           w[4 * v + 1] = x.y;
           w[4 * v + 2] = x.z;
           w[4 * v + 3] = x.w;
         }
-        umma::tmem_st32(tmem + lane_base + kColQ + 128u * h + 32u * part, w);
+        umma::tmem_st32(tmem + lane_base + kColQ + 128u * h + 64u * half, w);
+        umma::tmem_st32(tmem + lane_base + kColQ + 128u * h + 64u * half + 32u, w + 32);
       }
-      const uint4* rsrc = reinterpret_cast<const uint4*>(qrow + kLatent);
-      for (int u = 4 * h; u < 4 * h + 4; ++u)
-        *reinterpret_cast<uint4*>(smem + kOffQRope + umma::sw128(t, u)) = __ldg(rsrc + u);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        *reinterpret_cast<uint4*>(smem + kOffQRope + umma::sw128(t, 4 * h + u)) = rq[u];
       umma::tmem_st_wait();
       umma::fence_proxy_async_smem();
       umma::fence_before_sync();
@@ -914,8 +941,8 @@ bool plan(const xqa_params* p, int sm_count, Plan* pl) {
   const int sm = sm_count_of(p, sm_count);
   if (sm <= 0) return false;
   const int stage_pages = p->page_size <= kTok ? kTok / p->page_size : 1;
-  // one cluster (2 CTAs, one per SM) per (sequence, split); aim for ~8 waves
-  const int64_t pairs = int64_t(sm / 2) * 8;
+  // one cluster (2 CTAs, one per SM) per (sequence, split); aim for ~kWaves waves
+  const int64_t pairs = int64_t(sm / 2) * kWaves;
   int64_t ns = (pairs + p->batch_size - 1) / p->batch_size;
   const int64_t by_tiles = (max_pages + stage_pages - 1) / stage_pages;
   const int64_t by_tokens = std::max<int64_t>(1, int64_t(max_pages) * p->page_size / 1024);
