@@ -134,6 +134,7 @@ constexpr int kReqTail = 1 << 29;     // zero the V rows past the split's end
 constexpr int kReqTile = (1 << 29) - 1;
 
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by > 2^8
+constexpr int kOrderMaxB = 256;      // batches up to this size run their splits longest first
 constexpr int kMaxSplits = 64;       // merge weights [128][splits] fit in shared memory
 #ifndef XQA_MLA_WAVES
 #define XQA_MLA_WAVES 4
@@ -219,6 +220,22 @@ __device__ __forceinline__ void zero_v_tail(uint8_t* vslot, int r0, int st) {
   }
 }
 
+// The pages sequence b's splits cover: a sliding window drops the pages
+// before it; L is the length clamped to the page table's capacity.
+struct SeqGeom {
+  int L, pg_first, pg_last;
+};
+__device__ __forceinline__ SeqGeom seq_geom(const MlaArgs& a, int b) {
+  const int64_t max_len = int64_t(a.pps) * a.ps;
+  const int64_t len_raw = a.seq_lens[b];
+  SeqGeom g;
+  g.L = int(len_raw < max_len ? len_raw : max_len);
+  const int t_lo_all = a.win > 0 ? max(0, g.L - a.qs - a.win + 1) : 0;
+  g.pg_first = t_lo_all / a.ps;
+  g.pg_last = (g.L + a.ps - 1) / a.ps;
+  return g;
+}
+
 // The pieces of a tile of `tok` tokens starting at token tok0: boxes of
 // min(page_size, 64) rows, piece l at tile row 64-aligned l * box rows.  Lane
 // l < n loads piece l; `row` is its first row in the flattened
@@ -261,23 +278,80 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t c = cluster_rank();
   const uint32_t peer = c ^ 1u;
   const bool logit_cta = c == 1;
-  const int split = blockIdx.x >> 1;
-  const int b = blockIdx.z;
+  int split = blockIdx.x >> 1;
+  int b = blockIdx.z;
   constexpr unsigned kAll = 0xffffffffu;
 
   // wait for the producer of our inputs, then let the next call start launching
   pdl_wait();
   pdl_launch_dependents();
 
+  if (a.B <= kOrderMaxB) {
+    // ---- work item.  Clusters take the (sequence, split) items in an order
+    // that runs every full split first (in sequence order), then each
+    // sequence's shorter last split, longest first: clusters start in rank
+    // order, so the short items fill the last wave.  Both CTAs of a cluster
+    // compute the same item.  Shared memory is scratch until the pipeline
+    // starts.
+    int* sc = reinterpret_cast<int*>(smem);  // [3][kOrderMaxB] + the chosen item
+    const int rank = int(blockIdx.z) * int(gridDim.x >> 1) + int(blockIdx.x >> 1);
+    for (int bb = tid; bb < a.B; bb += kThreads) {
+      const SeqGeom g = seq_geom(a, bb);
+      const int np = max(0, g.pg_last - g.pg_first);
+      const int nv = (np + a.split_pages - 1) / a.split_pages;
+      const int last = np - (nv - 1) * a.split_pages;  // pages of the last split (nv > 0)
+      sc[bb] = nv == 0 ? 0 : (last == a.split_pages ? nv : nv - 1);                // full splits
+      sc[kOrderMaxB + bb] = nv == 0 ? 0 : (last == a.split_pages ? -1 : last);    // the short split
+    }
+    __syncthreads();
+    for (int bb = tid; bb < a.B; bb += kThreads) {
+      const int r = sc[kOrderMaxB + bb];
+      int k = -1;  // rank among the short splits: longer first, then lower sequence
+      if (r >= 0) {
+        k = 0;
+        for (int o = 0; o < a.B; ++o) {
+          const int ro = sc[kOrderMaxB + o];
+          k += (ro > r || (ro == r && o < bb)) ? 1 : 0;
+        }
+      }
+      sc[2 * kOrderMaxB + bb] = k;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int acc = 0, nb = -1, ns = 0;
+      for (int bb = 0; bb < a.B; ++bb) {
+        if (rank < acc + sc[bb]) {
+          nb = bb;
+          ns = rank - acc;
+          break;
+        }
+        acc += sc[bb];
+      }
+      if (nb < 0)
+        for (int bb = 0; bb < a.B; ++bb)
+          if (sc[2 * kOrderMaxB + bb] == rank - acc) {
+            nb = bb;
+            ns = sc[bb];  // the short split follows the sequence's full ones
+            break;
+          }
+      sc[3 * kOrderMaxB] = nb;
+      sc[3 * kOrderMaxB + 1] = ns;
+    }
+    __syncthreads();
+    b = sc[3 * kOrderMaxB];
+    split = sc[3 * kOrderMaxB + 1];
+    __syncthreads();
+    if (b < 0) return;  // no item left for this cluster
+  }
+
   // ---- sequence geometry (identical in both CTAs and every split)
-  const int64_t max_len = int64_t(a.pps) * a.ps;
-  const int64_t len_raw = a.seq_lens[b];
-  const int L = int(len_raw < max_len ? len_raw : max_len);
-  if (len_raw > max_len && a.err && tid == 0 && blockIdx.x == 0) atomicOr(a.err, kErrClamped);
+  const SeqGeom geo = seq_geom(a, b);
+  const int L = geo.L;
+  if (int64_t(a.seq_lens[b]) > int64_t(a.pps) * a.ps && a.err && tid == 0 && split == 0 && c == 0)
+    atomicOr(a.err, kErrClamped);
   const int spec0 = L - a.qs;
-  const int t_lo_all = a.win > 0 ? max(0, spec0 - a.win + 1) : 0;
-  const int pg_first = t_lo_all / a.ps;
-  const int pg_last = (L + a.ps - 1) / a.ps;
+  const int pg_first = geo.pg_first;
+  const int pg_last = geo.pg_last;
   const int npages = max(0, pg_last - pg_first);
   const int nvalid = (npages + a.split_pages - 1) / a.split_pages;
   if (split >= max(nvalid, 1)) return;  // both CTAs of the cluster leave together
