@@ -267,7 +267,8 @@ __device__ __forceinline__ TilePieces tile_pieces(const MlaArgs& a, const int32_
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    mla_decode_kernel(const __grid_constant__ CUtensorMap tmKV, const MlaArgs a) {
+    mla_decode_kernel(const __grid_constant__ CUtensorMap tmKV, const __grid_constant__ CUtensorMap tmPF,
+                      const MlaArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
@@ -420,7 +421,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // eight latent chunks of each tile into a V slot once the P.V of the tile
     // three back is done.  Each wait gives up after kWaitCycles.
     if (ntiles > 0) {
-      if (lane == 0) prefetch_tensormap(&tmKV);
+      if (lane == 0) {
+        prefetch_tensormap(&tmKV);
+        if (logit_cta) prefetch_tensormap(&tmPF);
+      }
       bool ok = true, bad = false;
       int issued = 0;
       if (logit_cta) {
@@ -453,12 +457,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // L2, so that its loads (issued only as ring slots free) do not pay
           // HBM latency
           if (slot == 0 && j + 2 < nqt) {
+            // one box per page piece covers all 576 dims of its rows
             const TilePieces pf = tile_pieces(a, pt, t_begin + (j + 2) * kTokQ, kTokQ, pg_hi, lane);
-            for (int b0 = 0; b0 < pf.n * kChunks; b0 += 32) {
-              const int bx = b0 + lane;
-              const int row = __shfl_sync(kAll, pf.row, min(bx / kChunks, 31));
-              if (bx < pf.n * kChunks && row >= 0) tma_prefetch_l2_3d(&tmKV, 64 * (bx % kChunks), 0, row);
-            }
+            if (lane < pf.n && pf.row >= 0) tma_prefetch_l2_3d(&tmPF, 0, 0, pf.row);
           }
           ++issued;
         }
@@ -1097,6 +1098,19 @@ xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_b
     snprintf(err, err_len, "cuTensorMapEncodeTiled failed (%d)", int(r));
     return XQA_ERR_CUDA;
   }
+  // L2 prefetch view of the same rows: (64 elements, 9 chunks, rows), so that
+  // one box covers a page piece's rows across all 576 dims
+  CUtensorMap tpf;
+  cuuint64_t pdims[3] = {64, cuuint64_t(kChunks), cuuint64_t(p->page_size) * cuuint64_t(p->num_pages)};
+  cuuint64_t pstrides[2] = {128, cuuint64_t(kDim) * 2};
+  cuuint32_t pbox[3] = {64, cuuint32_t(kChunks), cuuint32_t(std::min(p->page_size, kTok))};
+  r = enc(&tpf, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p->k_cache), pdims, pstrides, pbox, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(err, err_len, "cuTensorMapEncodeTiled (prefetch view) failed (%d)", int(r));
+    return XQA_ERR_CUDA;
+  }
   MlaArgs a;
   memset(&a, 0, sizeof a);
   a.q = static_cast<const uint16_t*>(p->q);
@@ -1141,7 +1155,7 @@ xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_b
   attr[0].val.programmaticStreamSerializationAllowed = p->enable_pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, mla_decode_kernel, tm, a);
+  e = cudaLaunchKernelEx(&cfg, mla_decode_kernel, tm, tpf, a);
   if (e != cudaSuccess) {
     snprintf(err, err_len, "MLA kernel launch: %s", cudaGetErrorString(e));
     return XQA_ERR_CUDA;
