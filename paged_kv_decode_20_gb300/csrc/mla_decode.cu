@@ -71,6 +71,10 @@ constexpr int kCopyPieces = 4;             // P travels as this many bulk copies
 // ---- shared memory (offsets from the dynamic base, which is 1024-aligned:
 // checked at run time).  The barrier block sits at the same offset in both
 // CTAs because each CTA signals barriers of its peer.
+// Tiles in shared memory are stored row group by row group: [8-row group]
+// [64-dim chunk][8 rows][128 bytes], so that one TMA box (a page piece's rows
+// across several chunks) fills a contiguous run and every 8-row UMMA atom
+// stays 1024-byte aligned.
 // Output CTA: V x3 | P x2 | factors x2 | final rows
 constexpr int kVBytes = 8 * kChunkBytes;  // the eight latent chunks of a tile
 constexpr int kVSlots = 3;
@@ -210,14 +214,24 @@ __device__ __forceinline__ void rescale_o(uint32_t taddr, float f) {
   umma::tmem_st_wait();
 }
 
-// Zeroes V rows [r0, kTok) of a V slot's eight latent chunks: past a split's
-// last token the rows hold stale or foreign data (possibly NaN), and P = 0
-// there must not meet it in the P.V.
+// Zeroes V rows [r0, kTok) of a V slot's eight latent chunks ([row group]
+// [chunk][8 rows][128 B]): past a split's last token the rows hold stale or
+// foreign data (possibly NaN), and P = 0 there must not meet it in the P.V.
 __device__ __forceinline__ void zero_v_tail(uint8_t* vslot, int r0, int st) {
   for (int idx = st; idx < (kTok - r0) * 8 * 8; idx += kSoft) {
     const int r = r0 + idx / 64, k = (idx / 8) % 8, u = idx % 8;
-    *reinterpret_cast<uint4*>(vslot + k * kChunkBytes + r * 128 + u * 16) = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(vslot + ((r >> 3) * 8 + k) * 1024 + (r & 7) * 128 + u * 16) = make_uint4(0, 0, 0, 0);
   }
+}
+
+// One 4-D TMA box (row-group view of the latent rows) into shared memory.
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
+                                            int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
 }
 
 // The pages sequence b's splits cover: a sliding window drops the pages
@@ -267,8 +281,8 @@ __device__ __forceinline__ TilePieces tile_pieces(const MlaArgs& a, const int32_
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    mla_decode_kernel(const __grid_constant__ CUtensorMap tmKV, const __grid_constant__ CUtensorMap tmPF,
-                      const MlaArgs a) {
+    mla_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                      const __grid_constant__ CUtensorMap tmPF, const MlaArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
@@ -422,7 +436,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // three back is done.  Each wait gives up after kWaitCycles.
     if (ntiles > 0) {
       if (lane == 0) {
-        prefetch_tensormap(&tmKV);
+        prefetch_tensormap(logit_cta ? &tmK : &tmV);
         if (logit_cta) prefetch_tensormap(&tmPF);
       }
       bool ok = true, bad = false;
@@ -441,17 +455,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!ok) break;
           if (lane == 0) mbar_arrive_expect_tx(&bars[kKFull + slot], uint32_t(tp.n) * box_bytes * kGroup);
           __syncwarp();
-          {
-            // one box per lane (lane = piece * kGroup + chunk of the group):
-            // issuing a TMA instruction holds its thread for hundreds of
-            // cycles, so the boxes go out from several lanes at once
-            const int row = __shfl_sync(kAll, tp.row, min(lane / kGroup, 31));
-            if (lane < tp.n * kGroup) {
-              const int pc = lane / kGroup, dk = lane - pc * kGroup;
-              tma_load_3d(smem + kOffK + slot * kGroupBytes + dk * kChunkBytesQ + pc * box_bytes, &tmKV,
-                          &bars[kKFull + slot], 64 * (kGroup * slot + dk), 0, row);
-            }
-          }
+          // one box per page piece (its rows across the group's three chunks),
+          // one piece per lane: issuing a TMA instruction holds its thread for
+          // hundreds of cycles
+          if (lane < tp.n)
+            tma_load_4d(smem + kOffK + slot * kGroupBytes + lane * kGroup * int(box_bytes), &tmK,
+                        &bars[kKFull + slot], 0, 0, kGroup * slot, tp.row >> 3);
           __syncwarp();
           // after the tile's first loads are out, the tile two ahead goes into
           // L2, so that its loads (issued only as ring slots free) do not pay
@@ -476,15 +485,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           bad |= tp.bad;
           if (lane == 0) mbar_arrive_expect_tx(&bars[kVFull + slot], uint32_t(tp.n) * box_bytes * 8u);
           __syncwarp();
-          {
-            // one box per lane: lane = piece * 8 + latent chunk (at most 4 pieces)
-            const int row = __shfl_sync(kAll, tp.row, lane >> 3);
-            if (lane < tp.n * 8) {
-              const int pc = lane >> 3, k = lane & 7;
-              tma_load_3d(smem + kOffV + slot * kVBytes + k * kChunkBytes + pc * box_bytes, &tmKV,
-                          &bars[kVFull + slot], 64 * k, 0, row);
-            }
-          }
+          // one box per page piece: its rows across the eight latent chunks
+          if (lane < tp.n)
+            tma_load_4d(smem + kOffV + slot * kVBytes + lane * 8 * int(box_bytes), &tmV, &bars[kVFull + slot], 0, 0,
+                        0, tp.row >> 3);
           __syncwarp();
           ++issued;
         }
@@ -524,10 +528,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int dk = 0; dk < kGroup; ++dk) {
               const int k = kGroup * gr + dk;
-              const uint32_t st = kb + gr * kGroupBytes + dk * kChunkBytesQ;
+              // chunk dk of the group: 8-row atoms every kGroup KB
+              const uint32_t st = kb + gr * kGroupBytes + dk * 1024;
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t bdesc = umma::smem_desc(st + 32 * kk, 16, 1024, umma::kSw128);
+                const uint64_t bdesc = umma::smem_desc(st + 32 * kk, 16, kGroup * 1024, umma::kSw128);
                 if (k < 8)
                   umma::mma_ts(sd, tmem + kColQ + 32u * k + 8u * kk, bdesc, kIdescQK, (k | kk) != 0);
                 else
@@ -577,7 +582,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int n = 0; n < 2; ++n)
               umma::mma_ss(tmem + kColO + uint32_t(kHalf * n),
                            umma::smem_desc(pa + 32 * kk, 16, 1024, umma::kSw128),
-                           umma::smem_desc(va + 4 * n * kChunkBytes + 2048 * kk, kChunkBytes, 1024, umma::kSw128),
+                           // V, MN-major: 64-dim atoms 1 KB apart, 8-row groups 8 KB apart
+                           umma::smem_desc(va + 4 * n * 1024 + 2 * 8192 * kk, 1024, 8192, umma::kSw128),
                            kIdescPV, (j | kk) != 0);
           umma::commit(&bars[kVEmpty + vs]);
           // the logit CTA may stage and send the P of tile j + 2
@@ -1086,14 +1092,24 @@ xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_b
     return XQA_ERR_CUDA;
   }
   // NHD and HND coincide for one kv head: rows of 576 elements, token-major.
-  CUtensorMap tm;
-  cuuint64_t dims[3] = {cuuint64_t(kDim), 1, cuuint64_t(p->page_size) * cuuint64_t(p->num_pages)};
-  cuuint64_t strides[2] = {cuuint64_t(kDim) * 2, cuuint64_t(kDim) * 2};
-  cuuint32_t box[3] = {64, 1, cuuint32_t(std::min(p->page_size, kTok))};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p->k_cache), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  // Row-group view (64 elements, 8 rows, 9 chunks, row groups): a box of one
+  // page piece's rows across several chunks lands as [row group][chunk][8
+  // rows][128 B].  Logit tiles take three chunks per box, V tiles eight.
+  const cuuint32_t box_rows = cuuint32_t(std::min(p->page_size, kTok));
+  const cuuint64_t nrows = cuuint64_t(p->page_size) * cuuint64_t(p->num_pages);
+  cuuint64_t dims[4] = {64, 8, cuuint64_t(kChunks), nrows / 8};
+  cuuint64_t strides[3] = {cuuint64_t(kDim) * 2, 128, cuuint64_t(kDim) * 2 * 8};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUtensorMap tk, tv;
+  cuuint32_t kbox[4] = {64, 8, cuuint32_t(kGroup), box_rows / 8};
+  cuuint32_t vbox[4] = {64, 8, 8, box_rows / 8};
+  CUresult r = enc(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(p->k_cache), dims, strides, kbox,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r == CUDA_SUCCESS)
+    r = enc(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(p->k_cache), dims, strides, vbox, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     snprintf(err, err_len, "cuTensorMapEncodeTiled failed (%d)", int(r));
     return XQA_ERR_CUDA;
@@ -1103,7 +1119,7 @@ xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_b
   CUtensorMap tpf;
   cuuint64_t pdims[3] = {64, cuuint64_t(kChunks), cuuint64_t(p->page_size) * cuuint64_t(p->num_pages)};
   cuuint64_t pstrides[2] = {128, cuuint64_t(kDim) * 2};
-  cuuint32_t pbox[3] = {64, cuuint32_t(kChunks), cuuint32_t(std::min(p->page_size, kTok))};
+  cuuint32_t pbox[3] = {64, cuuint32_t(kChunks), box_rows};
   r = enc(&tpf, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p->k_cache), pdims, pstrides, pbox, estr,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -1155,7 +1171,7 @@ xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_b
   attr[0].val.programmaticStreamSerializationAllowed = p->enable_pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, mla_decode_kernel, tm, tpf, a);
+  e = cudaLaunchKernelEx(&cfg, mla_decode_kernel, tk, tv, tpf, a);
   if (e != cudaSuccess) {
     snprintf(err, err_len, "MLA kernel launch: %s", cudaGetErrorString(e));
     return XQA_ERR_CUDA;
