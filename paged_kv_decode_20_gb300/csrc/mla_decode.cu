@@ -141,7 +141,7 @@ constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by > 2
 constexpr int kOrderMaxB = 256;      // batches up to this size run their splits longest first
 constexpr int kMaxSplits = 64;       // merge weights [128][splits] fit in shared memory
 #ifndef XQA_MLA_WAVES
-#define XQA_MLA_WAVES 4
+#define XQA_MLA_WAVES 3
 #endif
 constexpr int kWaves = XQA_MLA_WAVES;  // cluster waves the split plan aims for
 
