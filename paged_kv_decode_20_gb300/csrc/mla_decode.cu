@@ -929,40 +929,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int sp = 0; sp < nvalid; ++sp) wts[row * nvalid + sp] *= mul;
   }
   __syncthreads();
-  // phase 2: every (row, 4-column group) sums the weighted partials
-  for (int item = tid; item < kRows * (kHalf / 4); item += kThreads) {
-    const int row = item / (kHalf / 4);
-    const int col = int(c) * kHalf + 4 * (item % (kHalf / 4));
-    const float* w = wts + row * nvalid;
-    const float* src = ws_b + int64_t(row) * kStride + col;
-    const int64_t sstride = int64_t(kRows) * kStride;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    int sp = 0;
-    for (; sp + 4 <= nvalid; sp += 4) {
-      float4 v[4];
+  // phase 2: every (row, 4-column group) sums the weighted partials; each
+  // thread keeps four items and four splits of loads in flight (the merge
+  // ends the call for the last sequence, so its latency counts)
+  constexpr int kIt = 4;
+  constexpr int kItems = kRows * (kHalf / 4);
+  const int64_t sstride = int64_t(kRows) * kStride;
+  for (int base = tid; base < kItems; base += kThreads * kIt) {
+    float4 acc[kIt];
+    int rows[kIt], cols[kIt];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) v[u] = __ldcg(reinterpret_cast<const float4*>(src + (sp + u) * sstride));
+    for (int u = 0; u < kIt; ++u) {
+      const int item = min(base + u * kThreads, kItems - 1);
+      rows[u] = item / (kHalf / 4);
+      cols[u] = int(c) * kHalf + 4 * (item % (kHalf / 4));
+      acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int sp0 = 0; sp0 < nvalid; sp0 += 4) {
+      float4 v[kIt][4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float f = w[sp + u];
-        acc.x += f * v[u].x;
-        acc.y += f * v[u].y;
-        acc.z += f * v[u].z;
-        acc.w += f * v[u].w;
-      }
+      for (int u = 0; u < kIt; ++u)
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          v[u][q] = sp0 + q < nvalid ? __ldcg(reinterpret_cast<const float4*>(ws_b + int64_t(rows[u]) * kStride +
+                                                                              cols[u] + (sp0 + q) * sstride))
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < kIt; ++u)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float f = sp0 + q < nvalid ? wts[rows[u] * nvalid + sp0 + q] : 0.f;
+          acc[u].x += f * v[u][q].x;
+          acc[u].y += f * v[u][q].y;
+          acc[u].z += f * v[u][q].z;
+          acc[u].w += f * v[u][q].w;
+        }
     }
-    for (; sp < nvalid; ++sp) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(src + sp * sstride));
-      const float f = w[sp];
-      acc.x += f * v.x;
-      acc.y += f * v.y;
-      acc.z += f * v.z;
-      acc.w += f * v.w;
+#pragma unroll
+    for (int u = 0; u < kIt; ++u) {
+      if (base + u * kThreads >= kItems) continue;
+      const int ii = rows[u] / a.Hq, hh = rows[u] % a.Hq;
+      const int64_t oi = ((int64_t(b) * a.qs + ii) * a.Hq + hh) * kLatent + cols[u];
+      *reinterpret_cast<uint2*>(a.out + oi) =
+          make_uint2(pack_f32x2(acc[u].x, acc[u].y, true), pack_f32x2(acc[u].z, acc[u].w, true));
     }
-    const int ii = row / a.Hq, hh = row % a.Hq;
-    const int64_t oi = ((int64_t(b) * a.qs + ii) * a.Hq + hh) * kLatent + col;
-    *reinterpret_cast<uint2*>(a.out + oi) =
-        make_uint2(pack_f32x2(acc.x, acc.y, true), pack_f32x2(acc.z, acc.w, true));
   }
   if (tid == 0) a.sems[unit] = 0u;
 }
