@@ -138,7 +138,8 @@ constexpr int kReqTail = 1 << 29;     // zero the V rows past the split's end
 constexpr int kReqTile = (1 << 29) - 1;
 
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by > 2^8
-constexpr int kOrderMaxB = 256;      // batches up to this size run their splits longest first
+constexpr int kOrderMaxB = 256;      // batches up to this size run on persistent clusters
+constexpr int kMaxPieces = 128;      // persistent clusters (a sequence's pieces) at most
 constexpr int kMaxSplits = 64;       // merge weights [128][splits] fit in shared memory
 #ifndef XQA_MLA_WAVES
 #define XQA_MLA_WAVES 3
@@ -160,6 +161,7 @@ struct MlaArgs {
   float* lse;  // optional [B, qs, Hq] natural-log log-sum-exp per row
   int64_t num_pages;
   int B, Hq, qs, ps, pps, win, nsplit, split_pages, mask_words;
+  int ncl;  // persistent clusters
   float q_scale, kv_scale, softmax_scale, rcp_out_scale;
   int q_bf16;
 };
@@ -234,6 +236,15 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// The cluster whose slice of the persistent schedule holds scheduled page P
+// (slice k = [tot * k / ncl, tot * (k + 1) / ncl)).
+__device__ __forceinline__ int cluster_of(int64_t P, int64_t tot, int ncl) {
+  int64_t k = P * ncl / tot;
+  while (k + 1 < ncl && tot * (k + 1) / ncl <= P) ++k;
+  while (k > 0 && tot * k / ncl > P) --k;
+  return int(k);
+}
+
 // The pages sequence b's splits cover: a sliding window drops the pages
 // before it; L is the length clamped to the page table's capacity.
 struct SeqGeom {
@@ -287,7 +298,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
-  int* flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] abort, [1] last CTA, [2] request word
+  int* flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] abort, [1] last CTA, [2] request word, [3] cluster abort
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t c = cluster_rank();
@@ -301,64 +312,70 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   pdl_wait();
   pdl_launch_dependents();
 
-  if (a.B <= kOrderMaxB) {
-    // ---- work item.  Clusters take the (sequence, split) items in an order
-    // that runs every full split first (in sequence order), then each
-    // sequence's shorter last split, longest first: clusters start in rank
-    // order, so the short items fill the last wave.  Both CTAs of a cluster
-    // compute the same item.  Shared memory is scratch until the pipeline
-    // starts.
-    int* sc = reinterpret_cast<int*>(smem);  // [3][kOrderMaxB] + the chosen item
-    const int rank = int(blockIdx.z) * int(gridDim.x >> 1) + int(blockIdx.x >> 1);
-    for (int bb = tid; bb < a.B; bb += kThreads) {
-      const SeqGeom g = seq_geom(a, bb);
-      const int np = max(0, g.pg_last - g.pg_first);
-      const int nv = (np + a.split_pages - 1) / a.split_pages;
-      const int last = np - (nv - 1) * a.split_pages;  // pages of the last split (nv > 0)
-      sc[bb] = nv == 0 ? 0 : (last == a.split_pages ? nv : nv - 1);                // full splits
-      sc[kOrderMaxB + bb] = nv == 0 ? 0 : (last == a.split_pages ? -1 : last);    // the short split
-    }
-    __syncthreads();
-    for (int bb = tid; bb < a.B; bb += kThreads) {
-      const int r = sc[kOrderMaxB + bb];
-      int k = -1;  // rank among the short splits: longer first, then lower sequence
-      if (r >= 0) {
-        k = 0;
-        for (int o = 0; o < a.B; ++o) {
-          const int ro = sc[kOrderMaxB + o];
-          k += (ro > r || (ro == r && o < bb)) ? 1 : 0;
-        }
-      }
-      sc[2 * kOrderMaxB + bb] = k;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      int acc = 0, nb = -1, ns = 0;
-      for (int bb = 0; bb < a.B; ++bb) {
-        if (rank < acc + sc[bb]) {
-          nb = bb;
-          ns = rank - acc;
-          break;
-        }
-        acc += sc[bb];
-      }
-      if (nb < 0)
-        for (int bb = 0; bb < a.B; ++bb)
-          if (sc[2 * kOrderMaxB + bb] == rank - acc) {
-            nb = bb;
-            ns = sc[bb];  // the short split follows the sequence's full ones
-            break;
-          }
-      sc[3 * kOrderMaxB] = nb;
-      sc[3 * kOrderMaxB + 1] = ns;
-    }
-    __syncthreads();
-    b = sc[3 * kOrderMaxB];
-    split = sc[3 * kOrderMaxB + 1];
-    __syncthreads();
-    if (b < 0) return;  // no item left for this cluster
+  // the layout assumes a 1024-aligned dynamic base (the 128-byte swizzle
+  // atoms of the UMMA operands); both CTAs see the same base and leave together
+  if (smem_u32(smem_raw) & 1023u) {
+    if (tid == 0 && a.err) atomicOr(a.err, kErrTimeout);
+    return;
   }
 
+  // ---- schedule.  Up to kOrderMaxB sequences the clusters are persistent:
+  // cluster k takes the k-th of ncl equal slices of the batch's pages laid end
+  // to end (an empty sequence counts as one page, so that one cluster writes
+  // its output) and runs the pieces of the sequences that meet its slice one
+  // after another.  A sequence cut across clusters leaves one fp32 partial per
+  // piece in workspace slot (cluster, 0) for a cluster's first piece or
+  // (cluster, 1) for its last; the last CTA of each column half to finish the
+  // sequence merges them.  Larger batches take one fixed split per cluster.
+  const bool persistent = a.B <= kOrderMaxB;
+  const int k_cl = int(blockIdx.x >> 1);
+  int64_t tot = 1, s_lo = 0, s_hi = 0;  // all scheduled pages; this cluster's slice
+  int ncl = a.ncl;                      // clusters with a non-empty slice
+  int cur_b = b;                        // next sequence to look at
+  int64_t cur_S = 0;                    // its first scheduled page
+  if (persistent) {
+    int* sc = reinterpret_cast<int*>(smem);  // scratch: scheduled pages per sequence
+    for (int bb = tid; bb < a.B; bb += kThreads) {
+      const SeqGeom g = seq_geom(a, bb);
+      sc[bb] = max(1, g.pg_last - g.pg_first);
+    }
+    __syncthreads();
+    tot = 0;
+    for (int bb = 0; bb < a.B; ++bb) tot += sc[bb];
+    // fewer pages than clusters: the last clusters get no slice, every other
+    // slice holds at least one page (so a sequence's pieces are exactly the
+    // clusters from its first page's to its last page's)
+    ncl = int(min(int64_t(a.ncl), tot));
+    s_lo = k_cl < ncl ? tot * k_cl / ncl : tot;
+    s_hi = k_cl < ncl ? tot * (k_cl + 1) / ncl : tot;
+    cur_b = 0;
+    while (cur_b < a.B && cur_S + sc[cur_b] <= s_lo) cur_S += sc[cur_b++];
+    __syncthreads();  // the scratch is reused below
+  }
+  if (tid == 0) flags[0] = flags[1] = flags[2] = flags[3] = 0;  // also for a cluster with no piece
+  if (warp == 0) {
+    umma::tmem_alloc(tmem_slot, kTmemCols);
+    umma::tmem_relinquish();
+  }
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t peer_bars = map_peer(smem_u32(bars), peer);
+  const uint32_t box_bytes = uint32_t(min(a.ps, kTok)) * 128u;
+  constexpr uint32_t kIdescQK = umma::idesc_f16(kRows, kTokQ, true, false, false);
+  constexpr uint32_t kIdescPV = umma::idesc_f16(kRows, kHalf, true, false, true);
+  bool first_piece = true;
+
+  for (;;) {
+  // ---- the piece: sequence b, pages [pg_lo, pg_hi), its index among the
+  // sequence's nvalid pieces, and where its partial goes
+  int nvalid, pg_lo, pg_hi, kf = 0;
+  bool cl_first = true;  // the piece is its cluster's first (persistent)
+  if (persistent) {
+    if (cur_b >= a.B || cur_S >= s_hi) break;
+    b = cur_b;
+  }
   // ---- sequence geometry (identical in both CTAs and every split)
   const SeqGeom geo = seq_geom(a, b);
   const int L = geo.L;
@@ -368,22 +385,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int pg_first = geo.pg_first;
   const int pg_last = geo.pg_last;
   const int npages = max(0, pg_last - pg_first);
-  const int nvalid = (npages + a.split_pages - 1) / a.split_pages;
-  if (split >= max(nvalid, 1)) return;  // both CTAs of the cluster leave together
-  const int pg_lo = pg_first + split * a.split_pages;
-  const int pg_hi = min(pg_lo + a.split_pages, pg_last);
+  const int nsched = max(1, npages);  // scheduled pages (persistent)
+  if (persistent) {
+    const int64_t v_lo = max(s_lo, cur_S) - cur_S, v_hi = min(s_hi, cur_S + nsched) - cur_S;
+    pg_lo = pg_first + int(min(v_lo, int64_t(npages)));
+    pg_hi = pg_first + int(min(v_hi, int64_t(npages)));
+    kf = cluster_of(cur_S, tot, ncl);
+    const int kl = cluster_of(cur_S + nsched - 1, tot, ncl);
+    nvalid = npages == 0 ? 0 : kl - kf + 1;
+    split = k_cl - kf;
+    cl_first = cur_S <= s_lo;
+  } else {
+    nvalid = (npages + a.split_pages - 1) / a.split_pages;
+    if (split >= max(nvalid, 1)) break;  // both CTAs of the cluster leave together
+    pg_lo = pg_first + split * a.split_pages;
+    pg_hi = min(pg_lo + a.split_pages, pg_last);
+  }
   const int t_begin = pg_lo * a.ps;
   const int t_end = min(pg_hi * a.ps, L);
   const int ntiles = (nvalid == 0 || t_end <= t_begin) ? 0 : (t_end - t_begin + kTok - 1) / kTok;
   const int nqt = (ntiles + 1) / 2;  // logit tiles of 128 tokens
-  // the layout assumes a 1024-aligned dynamic base (the 128-byte swizzle
-  // atoms of the UMMA operands); both CTAs see the same base and leave together
-  if (smem_u32(smem_raw) & 1023u) {
-    if (tid == 0 && a.err) atomicOr(a.err, kErrTimeout);
-    return;
-  }
-
+  // barriers are set up afresh for every piece (after the previous piece's
+  // last wait, both CTAs having passed the cluster barrier that ends it)
   if (tid == 0) {
+    if (!first_piece) {
+      if (logit_cta) {
+        for (int i = kKFull; i <= kPSlotFree + 1; ++i) mbar_inval(&bars[i]);
+      } else {
+        for (int i = kVFull; i <= kODone; ++i) mbar_inval(&bars[i]);
+      }
+      mbar_inval(&bars[kDrain]);
+    }
     if (logit_cta) {
       for (int i = 0; i < kKSlots; ++i) {
         mbar_init(&bars[kKFull + i], 1);
@@ -413,20 +445,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     flags[0] = flags[1] = flags[2] = 0;
     fence_mbar_init();
   }
-  if (warp == 0) {
-    umma::tmem_alloc(tmem_slot, kTmemCols);
-    umma::tmem_relinquish();
-  }
   umma::fence_before_sync();
   __syncthreads();
   cluster_sync();  // the peer's barriers exist before any remote access
   umma::fence_after_sync();
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t peer_bars = map_peer(smem_u32(bars), peer);
   const int32_t* pt = a.page_table + int64_t(b) * a.pps;
-  const uint32_t box_bytes = uint32_t(min(a.ps, kTok)) * 128u;
-  constexpr uint32_t kIdescQK = umma::idesc_f16(kRows, kTokQ, true, false, false);
-  constexpr uint32_t kIdescPV = umma::idesc_f16(kRows, kHalf, true, false, true);
 
   if (warp == 0) {
     // ================= TMA producer =================
@@ -841,7 +864,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mul = finalize_row(m_fin, l_fin, sig, kv_scale * a.rcp_out_scale,
                            (a.lse && h == 0) ? a.lse + row_g : nullptr);
       }
-      float* wrow = a.ws + ((int64_t(b) * a.nsplit + split) * kRows + t) * (kLatent + 4);
+      const int64_t slot = persistent ? 2 * int64_t(k_cl) + (cl_first ? 0 : 1) : int64_t(b) * a.nsplit + split;
+      float* wrow = a.ws + (slot * kRows + t) * (kLatent + 4);
 #pragma unroll 1
       for (int part = 0; part < kHalf / 32; ++part) {
         float o[32];
@@ -877,21 +901,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __threadfence();
   }
 
-  // ---- teardown: no tensor-memory or peer traffic may outlive this point
+  // ---- end of the piece: no tensor-memory or peer traffic may outlive this
+  // point.  A wait that gave up in either CTA ends the loop for both (each
+  // reads the other's flag between two cluster barriers), so the CTAs of a
+  // cluster always pass the same cluster barriers.
   umma::fence_before_sync();
   __syncthreads();
   cluster_sync();
-  if (warp == 0) {
-    umma::fence_after_sync();
-    umma::tmem_dealloc(tmem, kTmemCols);
+  if (tid == 0) {
+    uint32_t peer_abort;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(peer_abort) : "r"(map_peer(smem_u32(flags), peer)) : "memory");
+    flags[3] = flags[0] | int(peer_abort);
   }
-  if (flags[0]) {
-    if (tid == 0 && a.err) atomicOr(a.err, kErrTimeout);
-    return;
-  }
-  if (nvalid <= 1) return;
-
-  // ---- split-KV: the last CTA of this column half merges every split (the
+  cluster_sync();
+  if (flags[3]) break;
+  if (nvalid > 1) {
+  // ---- split-KV: the last CTA of this column half merges every piece (the
   // output CTA wrote the whole partial; each CTA of the cluster takes its
   // ticket after the cluster barrier that follows those writes)
   __threadfence();
@@ -902,21 +927,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     flags[1] = prev == uint32_t(nvalid - 1) ? 1 : 0;
   }
   __syncthreads();
-  if (!flags[1]) return;
+  if (flags[1]) {
   __threadfence();
   const float kv_scale = ldscale(a.kv_scale_dev, a.kv_scale);
   constexpr int kStride = kLatent + 4;
-  const float* ws_b = a.ws + int64_t(b) * a.nsplit * kRows * kStride;
+  // the partial of piece sp of this sequence: a persistent piece sits in its
+  // cluster's slot 0 unless it is the sequence's first piece starting inside
+  // the cluster's slice (slot 1)
+  const bool first_in_slot1 = persistent && cur_S > tot * kf / ncl;
+  const int64_t base_slot = persistent ? 2 * int64_t(kf) : int64_t(b) * a.nsplit;
+  const int64_t slot_step = persistent ? 2 : 1;
+#define PART(sp) (a.ws + (base_slot + slot_step * (sp) + ((sp) == 0 && first_in_slot1 ? 1 : 0)) * kRows * kStride)
   // phase 1: one thread per row folds the split maxima, the sink and the
   // output scales into one weight per (row, split), staged in shared memory
   float* wts = reinterpret_cast<float*>(smem);  // [kRows][nvalid]
   if (tid < kRows) {
     const int row = tid;
     float M = -INFINITY;
-    for (int sp = 0; sp < nvalid; ++sp) M = fmaxf(M, __ldcg(ws_b + (int64_t(sp) * kRows + row) * kStride + kLatent));
+    for (int sp = 0; sp < nvalid; ++sp) M = fmaxf(M, __ldcg(PART(sp) + int64_t(row) * kStride + kLatent));
     float l = 0.f;
     for (int sp = 0; sp < nvalid; ++sp) {
-      const float* src = ws_b + (int64_t(sp) * kRows + row) * kStride + kLatent;
+      const float* src = PART(sp) + int64_t(row) * kStride + kLatent;
       const float ms = __ldcg(src);
       const float f = ms == -INFINITY ? 0.f : exp2f(ms - M);
       wts[row * nvalid + sp] = f;
@@ -934,7 +965,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // ends the call for the last sequence, so its latency counts)
   constexpr int kIt = 4;
   constexpr int kItems = kRows * (kHalf / 4);
-  const int64_t sstride = int64_t(kRows) * kStride;
   for (int base = tid; base < kItems; base += kThreads * kIt) {
     float4 acc[kIt];
     int rows[kIt], cols[kIt];
@@ -951,8 +981,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int u = 0; u < kIt; ++u)
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          v[u][q] = sp0 + q < nvalid ? __ldcg(reinterpret_cast<const float4*>(ws_b + int64_t(rows[u]) * kStride +
-                                                                              cols[u] + (sp0 + q) * sstride))
+          v[u][q] = sp0 + q < nvalid ? __ldcg(reinterpret_cast<const float4*>(PART(sp0 + q) +
+                                                                              int64_t(rows[u]) * kStride + cols[u]))
                                      : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int u = 0; u < kIt; ++u)
@@ -974,7 +1004,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           make_uint2(pack_f32x2(acc[u].x, acc[u].y, true), pack_f32x2(acc[u].z, acc[u].w, true));
     }
   }
+#undef PART
   if (tid == 0) a.sems[unit] = 0u;
+  }  // last CTA
+  __syncthreads();  // shared memory (the merge weights) is free again
+  }  // nvalid > 1
+  first_piece = false;
+  if (!persistent) break;
+  cur_S += nsched;
+  ++cur_b;
+  }  // pieces
+
+  // ---- teardown
+  umma::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    umma::fence_after_sync();
+    umma::tmem_dealloc(tmem, kTmemCols);
+  }
+  if (flags[0] && tid == 0 && a.err) atomicOr(a.err, kErrTimeout);
 }
 
 // ---------------------------------------------------------------- host side
@@ -998,7 +1046,8 @@ EncodeTiledFn encode_fn() {
 }
 
 struct Plan {
-  int nsplit = 1, split_pages = 1;
+  int nsplit = 1, split_pages = 1, ncl = 1;
+  bool persistent = false;
   size_t ws_bytes = 0, nsems = 0;
 };
 
@@ -1045,6 +1094,14 @@ bool plan(const xqa_params* p, int sm_count, Plan* pl) {
   pl->nsplit = (max_pages + sp - 1) / sp;
   pl->nsems = size_t(p->batch_size) * 2;
   pl->ws_bytes = pl->nsplit > 1 ? size_t(p->batch_size) * pl->nsplit * kRows * (kLatent + 4) * sizeof(float) : 0;
+  // up to kOrderMaxB sequences: persistent clusters, one per SM pair (at most
+  // kMaxPieces, so that a sequence's merge weights fit in shared memory), two
+  // partial slots each
+  pl->persistent = p->batch_size <= kOrderMaxB;
+  if (pl->persistent) {
+    pl->ncl = std::max(1, std::min(sm / 2, kMaxPieces));
+    pl->ws_bytes = pl->ncl > 1 ? size_t(pl->ncl) * 2 * kRows * (kLatent + 4) * sizeof(float) : 0;
+  }
   return true;
 }
 
@@ -1160,6 +1217,7 @@ xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_b
   a.win = p->sliding_win_size;
   a.nsplit = pl.nsplit;
   a.split_pages = pl.split_pages;
+  a.ncl = pl.ncl;
   a.mask_words = ((p->q_seq_len + 31) / 32) * 2;
   a.q_scale = p->q_scale;
   a.kv_scale = p->kv_scale;
@@ -1172,7 +1230,7 @@ xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_b
     return XQA_ERR_CUDA;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * pl.nsplit, 1, p->batch_size);
+  cfg.gridDim = pl.persistent ? dim3(2 * pl.ncl, 1, 1) : dim3(2 * pl.nsplit, 1, p->batch_size);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = stream;
