@@ -29,7 +29,7 @@ def mla_case(lens, ps=64, seed=0, heads=128, qs=1, **kw):
                        q_seq_len=qs, softmax_scale=SCALE, seed=seed, **kw)
 
 
-def run_and_compare(c, tol=TOL, runs=2, **kw):
+def run_and_compare(c, tol=TOL, runs=2, out_round=False, **kw):
     from paged_kv_decode_20_gb300.runner import Decoder
     dec = Decoder(c.to("cuda"), **kw)
     outs = []
@@ -44,7 +44,12 @@ def run_and_compare(c, tol=TOL, runs=2, **kw):
     got = outs[0].cpu().to(torch.float64)
     ref = oracle.xqa_attention(c.q, c.k_cache, c.v_cache, c.page_table, c.seq_lens, **c.kwargs())
     assert not torch.isnan(got).any()
-    err = (got - ref).abs().max().item()
+    d = (got - ref).abs()
+    if out_round:
+        # the output's own rounding to bf16 (half an ulp, 2^-9 relative) on top of
+        # the decode bound: peaked rows of short sequences reach |out| ~ 3.5
+        d = d - 2.0 ** -9 * ref.abs()
+    err = d.max().item()
     l2 = ((got - ref).norm() / ref.norm().clamp_min(1e-30)).item()
     assert err <= tol, f"max abs {err:.3e}"
     assert l2 <= 1e-2, f"rel L2 {l2:.3e}"
@@ -78,3 +83,22 @@ def test_mla_sinks_window_and_spec_tokens():
 def test_mla_empty_and_nan_poison():
     c = mla_case([0, 1, 129], seed=6, pool_pages=12, poison=True)
     run_and_compare(c)
+
+
+def test_mla_persistent_clusters_loop_over_many_sequences():
+    """Few persistent clusters (sm_count 8 -> 4 clusters) each run dozens of
+    sequences one after another, re-arming their barriers per piece; the
+    lengths mix empty, one-token, page-boundary and multi-page sequences so that
+    slices start and end inside sequences."""
+    g = torch.Generator().manual_seed(11)
+    lens = torch.randint(0, 400, (60,), generator=g).tolist()
+    lens[:6] = [0, 1, 63, 64, 65, 0]
+    run_and_compare(mla_case(lens, ps=32, seed=12), sm_count=8)
+
+
+def test_mla_large_batch_takes_fixed_splits():
+    """Batches above 256 sequences launch one cluster per (sequence, split)
+    instead of persistent clusters."""
+    g = torch.Generator().manual_seed(13)
+    lens = torch.randint(1, 160, (260,), generator=g).tolist()
+    run_and_compare(mla_case(lens, ps=64, seed=14), runs=1, out_round=True)
