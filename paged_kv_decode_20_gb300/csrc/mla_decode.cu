@@ -7,28 +7,34 @@
 //
 // The 128 query rows (heads x speculative tokens) form one M = 128 UMMA tile.
 // Their fp32 output (128 x 512) alone fills a CTA's 512 tensor-memory
-// columns, so a cluster of two CTAs shares each (sequence, KV split) and the
+// columns, so a cluster of two CTAs shares each piece of a sequence and the
 // two split the work by stage:
 //
 //   CTA 1 (the logit CTA) holds the whole query: the latent part in tensor
 //   memory, the rope part in shared memory.  It streams each 576-wide latent
-//   row of the split through a ring of 64-token x 64-dim chunks (TMA, 128-byte
-//   swizzle).  It computes the logits S = Q K^T with tcgen05.mma and runs the
-//   online softmax.  P (bf16, already in UMMA operand layout) and one rescale
-//   factor per row travel into CTA 0's shared memory by bulk copy.
+//   row of the piece through a ring of three-chunk groups (128 tokens x 192
+//   dims, TMA, 128-byte swizzle) and computes the logits S = Q K^T over
+//   128-token tiles with tcgen05.mma, then runs the online softmax.  P (bf16,
+//   already in UMMA operand layout) and one rescale factor per row travel into
+//   CTA 0's shared memory by bulk copy, 64 tokens at a time.
 //   CTA 0 (the output CTA) holds the whole fp32 output in tensor memory.  It
-//   fetches the first 512 dims of each tile (V) again, from L2, and
+//   fetches the first 512 dims of each 64-token tile (V) again, from L2, and
 //   accumulates O += P V with two N = 256 MMAs per 16 tokens.  Its eight spare
 //   warps rescale O when the softmax raised a row maximum by more than 2^8,
-//   clear V rows past the split's end, and run the epilogue.
+//   clear V rows past the piece's end, and run the epilogue.
 //
 // Only P crosses the cluster (16.5 KB per 64 tokens, one way), and every
 // latent byte is read from HBM once.  Warp roles in both CTAs: 0 = TMA
 // producer and tensor-memory allocator, 1 = MMA issuer, 2..9 = softmax
 // (logit CTA) or rescale / epilogue (output CTA); warp w reaches TMEM lanes
-// 32 (w % 4).., so two threads share each query row.  Split-KV partials merge
-// as in the grouped-query kernel: the last CTA of each column half to take a
-// ticket merges every split.
+// 32 (w % 4).., so two threads share each query row.
+//
+// Up to 256 sequences the clusters are persistent: cluster k runs, one after
+// another, the pieces of the sequences that meet the k-th equal slice of the
+// batch's pages.  A sequence cut across clusters leaves one partial per piece;
+// the last CTA of each column half to take the sequence's ticket merges them.
+// Larger batches take one cluster per (sequence, fixed-size split).
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdio.h>
