@@ -22,6 +22,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -100,14 +101,22 @@ KERNEL_FILES = {
 }
 
 
+def _code_only(text):
+    """Source text without comments and with whitespace collapsed, so that an
+    edit to comments alone keeps a kernel's hash."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(kernel):
-    """Hash of the source files that make up one kernel."""
+    """Hash of the code (comments aside) of the source files that make up one kernel."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_decode_20_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.startswith(KERNEL_FILES[kernel]):
             h.update(f.encode())
-            h.update(open(os.path.join(csrc, f), "rb").read())
+            h.update(_code_only(open(os.path.join(csrc, f), encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 
