@@ -241,3 +241,32 @@ PREP_BAD = [
 def test_prep_validation_rejects_before_launch(lib, over, text):
     assert lib.xqa_mla_decode_prep(ctypes.byref(fake_prep(**over)), None) == X.XQA_ERR_INVALID_ARG
     assert text in lib.xqa_last_error().decode()
+
+
+# ---------------------------------------------------------------- MLA sizing
+MLA_PARTIAL = 128 * (512 + 4) * 4  # one fp32 partial: 128 rows of 512 + (m, l) + padding
+
+
+def mla_params(**over):
+    base = dict(num_kv_heads=1, num_q_heads=128, head_dim=576, pages_per_seq=512, num_pages=4096)
+    base.update(over)
+    return fake_params(**base)
+
+
+@pytest.mark.parametrize("sm,clusters", [(152, 76), (2, 1), (1000, 128)])
+def test_mla_workspace_persistent_clusters(lib, sm, clusters):
+    """Up to 256 sequences: one persistent cluster per SM pair (at most 128), two
+    partial slots each; a single cluster needs no partials."""
+    p = mla_params(batch_size=64)
+    expect = clusters * 2 * MLA_PARTIAL if clusters > 1 else 0
+    assert lib.xqa_mla_workspace_size(ctypes.byref(p), 512, sm) == expect
+    assert lib.xqa_mla_semaphore_count(ctypes.byref(p), 512) == 64 * 2
+
+
+def test_mla_workspace_fixed_splits_above_256_sequences(lib):
+    """Above 256 sequences: a partial per (sequence, split) of a fixed page count
+    aimed at 3 waves of SM pairs (at least 1024 tokens per split)."""
+    p = mla_params(batch_size=300)
+    assert lib.xqa_mla_workspace_size(ctypes.byref(p), 512, 152) == 0  # one split each
+    # 500 pairs x 3 waves / 300 sequences -> 5 splits of 103 pages
+    assert lib.xqa_mla_workspace_size(ctypes.byref(p), 512, 1000) == 300 * 5 * MLA_PARTIAL
