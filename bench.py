@@ -57,6 +57,9 @@ def parse():
     ap.add_argument("--op", default="decode", choices=["decode", "merge", "prep"])
     ap.add_argument("--out-dtype", default=None, choices=["e4m3"],
                     help="fp8 output (workloads with an fp8 cache)")
+    ap.add_argument("--workloads", default="1,2,3,4,5",
+                    help="named workloads also timed into the line's `workloads` object "
+                         "(comma list, or 'none')")
     return ap.parse_args()
 
 
@@ -96,7 +99,7 @@ def peaks():
 
 
 KERNEL_FILES = {
-    "gqa_decode_kernel": ("gqa_", "ptx.cuh", "kernel_args.h", "finalize.cuh"),
+    "gqa_decode_kernel": ("gqa_", "ptx.cuh", "kernel_args.h", "finalize.cuh", "xqa_api.cu"),
     "mla_decode_kernel": ("mla_", "umma.cuh", "ptx.cuh", "kernel_args.h", "finalize.cuh"),
 }
 
@@ -190,6 +193,75 @@ def build_case(idx, device, batch=None):
     return W.workload(idx, device=device, poison=False, batch=batch)
 
 
+L2_FLUSH_BYTES = 256 * 1024 * 1024  # twice the GB300's L2
+
+
+def time_workload(idx, dev, launches, flush):
+    """Times one named workload's decode call on `dev` and returns its summary
+    for the bench line's `workloads` object.
+
+    Workloads whose KV exceeds L2 are timed with events around every launch
+    (launches back to back otherwise).  The small ones (KV inside L2) are
+    timed twice: with L2 flushed before every launch (a 256 MB write outside
+    the event pair), which is the number reported, and back to back (one
+    event pair around all launches; consecutive calls may overlap their
+    launch latency through programmatic dependent launch)."""
+    from paged_kv_decode_20_gb300.runner import Decoder
+
+    case = build_case(idx, dev)
+    dec = Decoder(case, error_word=False)
+    stream = torch.cuda.current_stream(dev)
+    kv, qb = case.kv_bytes(), case.q_bytes()
+    small = kv <= 129e6
+    for _ in range(5):
+        dec.run(stream)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(launches)]
+    with Clocks(dev.index) as clk:
+        for k in range(launches):
+            if small:
+                flush.fill_(float(k))
+            ev[k][0].record(stream)
+            dec.run(stream)
+            ev[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+        b2b = None
+        if small:
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            for _ in range(launches):
+                dec.run(stream)
+            t1.record(stream)
+            torch.cuda.synchronize(dev)
+            b2b = t0.elapsed_time(t1) / launches
+    ms = sum(a.elapsed_time(b) for a, b in ev) / launches
+    peak, kind = peaks()
+    achieved = (kv + qb) / (ms * 1e-3) / 1e9
+    out = {"workload": W.WORKLOADS[idx], "kernel": KERNEL_NAMES[idx],
+           "ms_per_launch": round(ms, 5),
+           "timing": "L2 flushed before every launch" if small else "inputs larger than L2 (no flush)",
+           "kv_bytes": kv, "q_bytes": qb,
+           "kv_gbs": round(kv / (ms * 1e-3) / 1e9, 2),
+           "decode_tokens_per_s": round(case.batch * case.q_seq_len / (ms * 1e-3), 1),
+           "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                        "frac": round(achieved / peak, 4), "peak_source": kind}}
+    if b2b is not None:
+        out["back_to_back_ms_per_launch"] = round(b2b, 5)
+    traffic = recorded_traffic(idx)
+    if traffic is not None:
+        out["traffic_over_algorithmic"] = round(traffic / (kv + qb), 4)
+    if case.mla:
+        flops = case.visible_tokens() * case.q_seq_len * case.q.shape[2] * 2 * (case.q.shape[3] + case.dv)
+        tf = flops / (ms * 1e-3) / 1e12
+        tpeak, tkind = tensor_peak()
+        out["roofline_tensor"] = {"bound": "tensor", "achieved": round(tf, 2), "peak": tpeak,
+                                  "unit": "TFLOP/s", "frac": round(tf / tpeak, 4), "peak_source": tkind}
+    out["clocks"] = clk.summary()
+    del dec, case
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_gb300(args):
     from paged_kv_decode_20_gb300 import build as B
     from paged_kv_decode_20_gb300 import xqa as X
@@ -215,6 +287,12 @@ def run_gb300(args):
     kv_bytes = case.kv_bytes()
     q_bytes = case.q_bytes()
     tokens = case.batch * case.q_seq_len
+    batch = case.batch
+    mla = case.mla
+    flops = (case.visible_tokens() * case.q_seq_len * case.q.shape[2] * 2 * (case.q.shape[3] + case.dv)
+             if mla else 0)
+    dtype_name = {torch.bfloat16: "bf16", torch.float16: "f16",
+                  torch.float8_e4m3fn: "e4m3 kv, bf16 q"}[case.k_cache.dtype]
 
     # ---- device-resident timing: K steps, events around each launch
     for _ in range(args.warmup):
@@ -278,10 +356,25 @@ def run_gb300(args):
                "ms_per_step": round(e_ms, 4), "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h}
 
-    # ---- CPU baseline: the oracle, all rows of this workload once (rank 0)
+    # ---- CPU baseline: the oracle on this workload, on all host threads and
+    # on one (rank 0)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(case.to("cpu"), args.workload)
+        cpu_case = case.to("cpu")
+        cpu = cpu_baseline(cpu_case, args.workload, min_seconds=6.0)
+        one = cpu_baseline(cpu_case, args.workload, max_rows=64, min_seconds=3.0, threads=1)
+        cpu["single_thread"] = {k: one[k] for k in ("value", "unit", "cores", "sample", "seconds")}
+
+    # ---- every named workload, one after another (rank 0 reports them)
+    per_workload = None
+    if rank == 0 and args.workloads != "none" and args.batch is None:
+        del dec, case
+        torch.cuda.empty_cache()
+        flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        per_workload = {}
+        for idx in [int(x) for x in args.workloads.split(",")]:
+            per_workload[str(idx)] = time_workload(idx, dev, max(args.steps, 20), flush)
+        del flush
 
     if world > 1:
         dist.barrier()
@@ -303,11 +396,10 @@ def run_gb300(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": {torch.bfloat16: "bf16", torch.float16: "f16",
-                  torch.float8_e4m3fn: "e4m3 kv, bf16 q"}[case.k_cache.dtype],
+        "dtype": dtype_name,
         "data": "synthetic (seeded N(0,1) q/K/V, shuffled page pool)",
         "config": {"workload": W.WORKLOADS[args.workload] + (", fp8 output" if args.out_dtype else ""),
-                   "global_batch": case.batch * world,
+                   "global_batch": batch * world,
                    "kv_bytes_per_step": kv_bytes * world, "q_bytes_per_step": q_bytes * world,
                    "l2": "inputs larger than L2 (no flush)" if kv_bytes > 129e6
                    else "KV fits in L2: numbers are L2-assisted",
@@ -326,11 +418,12 @@ def run_gb300(args):
         "cpu_baseline": cpu,
         "clocks": clk.summary(),
     }
-    if case.mla:
+    if per_workload is not None:
+        line["workloads"] = per_workload
+    if mla:
         # the latent workload sits near the ridge: report the tensor pipe too
         # (QK over 576 dims and P.V over 512, 2 flops per multiply-add, per
         # visible token and query row)
-        flops = case.visible_tokens() * case.q_seq_len * case.q.shape[2] * 2 * (case.q.shape[3] + case.dv)
         tf = flops / (avg_launch_ms * 1e-3) / 1e12
         tpeak, tkind = tensor_peak()
         line["roofline_tensor"] = {"bound": "tensor", "achieved": round(tf, 2), "peak": tpeak,
@@ -341,13 +434,13 @@ def run_gb300(args):
         dist.destroy_process_group()
 
 
-def cpu_baseline(case, idx, max_rows=None, min_seconds=10.0):
+def cpu_baseline(case, idx, max_rows=None, min_seconds=10.0, threads=None):
     """Time the float64 oracle on all rows of the workload (or a bounded
-    sample of whole (b, kv head) units) with every host thread."""
+    sample of whole (b, kv head) units) with every host thread (or `threads`)."""
     import oracle
     B, qs, Hq, _ = case.q.shape
     G = Hq // case.num_kv_heads
-    threads = os.cpu_count() or 1
+    threads = threads or os.cpu_count() or 1
     units = None
     frac = 1.0
     rows = B * qs * Hq

@@ -28,11 +28,15 @@
  *    allocates, frees or synchronises.  Calls are asynchronous on `stream`.
  *  - `output` is written in place (the API page: "modified in place").
  *  - Host-side validation returns a status before anything is launched; a
- *    launch failure returns XQA_ERR_CUDA.
+ *    launch failure returns XQA_ERR_CUDA.  Alignment: caches 16 bytes; q 4
+ *    bytes; output 8 bytes (16-bit) or 4 bytes (e4m3); page_table, seq_lens,
+ *    sinks, lse, error_word and the device scales 4 bytes; mask 2 bytes.
  *  - Device code never traps.  A page_table entry outside [0, num_pages)
  *    reads as zeros (TMA bounds fill) and a seq_len above
  *    pages_per_seq * page_size is clamped to it; both set bit 0 of
- *    `error_word` when the caller provides one.
+ *    `error_word` when the caller provides one.  Every pipeline wait is
+ *    bounded (about a second); one that gives up sets bit 1 and the call's
+ *    output is then undefined.
  */
 #ifndef XQA_GB300_H
 #define XQA_GB300_H
@@ -120,7 +124,8 @@ size_t xqa_workspace_size(const xqa_params* params, int sm_count);
 
 /* Number of uint32 semaphores xqa_decode needs.  They must be zero on the
    first call; every call leaves them zero again (the last CTA to finish a
-   split-KV reduction resets its counter). */
+   split-KV reduction resets its counter), also a call whose pipeline wait
+   gave up (bit 1 of error_word): its CTAs still take their tickets. */
 size_t xqa_semaphore_count(const xqa_params* params);
 
 /* Paged decode attention (the XQA-style call).  workspace: caller-owned device
@@ -136,7 +141,11 @@ size_t xqa_mla_semaphore_count(const xqa_params* params, int v_head_dim);
 
 /* MLA latent decode: params->num_kv_heads must be 1, head_dim the latent width
    (kv_lora_rank + rope) and v_head_dim the kv_lora_rank prefix used as V.
-   k_cache and v_cache may be the same pointer (the latent cache). */
+   k_cache and v_cache may be the same pointer (the latent cache).  q and
+   output must be 16-byte aligned.  The semaphores (xqa_mla_semaphore_count,
+   zero on the first call) are left zero by every call that completes; after
+   a call that reported a pipeline timeout (bit 1 of error_word) their
+   contents are undefined: zero them again before the next call. */
 xqa_status xqa_mla_decode(const xqa_params* params, int v_head_dim, void* workspace,
                           size_t workspace_bytes, uint32_t* semaphores, xqa_stream_t stream);
 
@@ -150,6 +159,8 @@ xqa_status xqa_mla_decode(const xqa_params* params, int v_head_dim, void* worksp
    the process exits.  It never calls cudaMalloc or cudaFree.
    - The first call on a device looks up that device's scratch address
      (cudaGetSymbolAddress); make that first call before any stream capture.
+     A lookup that fails returns XQA_ERR_CUDA and is tried again by the next
+     call; a successful one is kept for the life of the process.
    - Problems whose workspace or ticket count exceed the built-in sizes are
      rejected with XQA_ERR_WORKSPACE_TOO_SMALL (see xqa_last_error) before
      anything is launched; use xqa_decode with your own buffers for them.

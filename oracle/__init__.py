@@ -16,8 +16,10 @@ vLLM Kimi-K3 MultiHeadLatentAttention page (``head_size``, ``scale`` and the
 from __future__ import annotations
 
 import ctypes
+import hashlib
 import math
 import os
+import platform
 import subprocess
 import threading
 
@@ -35,15 +37,32 @@ _F16, _BF16, _E4M3 = 0, 1, 2
 _DTYPE_CODE = {torch.float16: _F16, torch.bfloat16: _BF16, torch.float8_e4m3fn: _E4M3}
 
 
+_GCC = ["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c11"]
+
+
+def _digest() -> str:
+    """SHA-256 of the source, the compiler flags and the host machine."""
+    h = hashlib.sha256()
+    with open(_SRC, "rb") as fh:
+        h.update(fh.read())
+    h.update(" ".join(_GCC).encode())
+    h.update(platform.machine().encode())
+    return h.hexdigest()
+
+
 def build(force: bool = False) -> str:
-    """Compile xqa_oracle.c into a shared library (gcc, -O2, OpenMP)."""
+    """Compile xqa_oracle.c into a shared library (gcc, -O2, OpenMP); rebuilt
+    whenever the source's content (not its modification time) changes."""
     os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
-    stale = not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)
-    if force or stale:
+    digest, stamp = _digest(), _LIB_PATH + ".sha256"
+    current = os.path.exists(_LIB_PATH) and os.path.exists(stamp) and open(stamp).read().strip() == digest
+    if force or not current:
         tmp = _LIB_PATH + f".{os.getpid()}.tmp"
-        cmd = ["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c11", "-o", tmp, _SRC, "-lm"]
-        subprocess.run(cmd, check=True)
+        subprocess.run(_GCC + ["-o", tmp, _SRC, "-lm"], check=True)
         os.replace(tmp, _LIB_PATH)
+        with open(stamp + f".{os.getpid()}.tmp", "w") as fh:
+            fh.write(digest + "\n")
+        os.replace(stamp + f".{os.getpid()}.tmp", stamp)
     return _LIB_PATH
 
 

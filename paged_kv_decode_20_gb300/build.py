@@ -8,7 +8,9 @@ ABI of include/xqa.h.
 from __future__ import annotations
 
 import concurrent.futures as cf
+import hashlib
 import os
+import platform
 import shutil
 import subprocess
 
@@ -32,10 +34,37 @@ def sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def _deps():
-    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+STAMP = LIB + ".sha256"
+
+
+def source_files():
+    """Every file the library is built from: csrc/ and the public header."""
+    files = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh", ".h")))
     files.append(os.path.join(INCLUDE, "xqa.h"))
-    return max(os.path.getmtime(f) for f in files)
+    return files
+
+
+def source_digest(files=None):
+    """SHA-256 over the sources' names and contents, the compiler flags and the
+    host machine: the library is rebuilt whenever any of them changes, whatever
+    the files' modification times say."""
+    h = hashlib.sha256()
+    for f in files if files is not None else source_files():
+        h.update(os.path.basename(f).encode() + b"\0")
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+        h.update(b"\0")
+    h.update(" ".join(ARCH + FLAGS).encode())
+    h.update(platform.machine().encode())
+    return h.hexdigest()
+
+
+def is_current(lib, stamp, digest):
+    """True when `lib` exists and `stamp` records that it was built from `digest`."""
+    if not (os.path.exists(lib) and os.path.exists(stamp)):
+        return False
+    with open(stamp) as fh:
+        return fh.read().strip() == digest
 
 
 def _compile(src, verbose):
@@ -52,7 +81,8 @@ def _compile(src, verbose):
 def build(force=False, verbose=False):
     """Compile every .cu under csrc/ and link libxqa_gb300.so; returns its path."""
     os.makedirs(BUILD, exist_ok=True)
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps():
+    digest = source_digest()
+    if not force and is_current(LIB, STAMP, digest):
         return LIB
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
@@ -66,6 +96,9 @@ def build(force=False, verbose=False):
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(STAMP + f".{os.getpid()}.tmp", "w") as fh:
+        fh.write(digest + "\n")
+    os.replace(STAMP + f".{os.getpid()}.tmp", STAMP)
     return LIB
 
 

@@ -279,8 +279,11 @@ __global__ void __launch_bounds__(160, 2)
       }
       float qmul = 1.f;
       if (kF8 && qbf) {
-        // bf16 q feeds an f16 MMA: rescale by a power of two into f16 range
-        // (exact) and fold the inverse into the logit scale.
+        // bf16 q feeds an f16 MMA: rescale by a power of two (the largest |q|
+        // of the CTA's rows lands in [2^14, 2^15)) and fold the inverse into
+        // the logit scale.  Elements down to 2^-31 of that maximum convert
+        // exactly (8 significant bits stay on the f16 grid); smaller ones round
+        // to the f16 subnormal grid, an error below 2^-40 of the maximum.
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         int e = 0;
@@ -575,7 +578,11 @@ __global__ void __launch_bounds__(160, 2)
     }
   }
   __syncthreads();
-  if (flags[0]) return;  // a wait gave up: the error word says so, write nothing
+  // A wait gave up: the error word says so and nothing is written, but with
+  // several splits the CTA still takes its ticket below, so that the last CTA
+  // of the unit resets the semaphore and the next call starts from zero.
+  const bool aborted = flags[0] != 0;
+  if (aborted && nvalid <= 1) return;
 
   // ================= epilogue (all 160 threads) =================
   const float kv_scale = load_scale(a.kv_scale_dev, a.kv_scale);
@@ -587,7 +594,7 @@ __global__ void __launch_bounds__(160, 2)
 
   // phase 1: one thread per row folds the four warps' maxima (and, with one
   // split, the sink and the output scales) into one weight per warp
-  if (tid < rows_here) {
+  if (!aborted && tid < rows_here) {
     const int row = tid;
     float mw[4], M = -INFINITY;
 #pragma unroll
@@ -615,7 +622,7 @@ __global__ void __launch_bounds__(160, 2)
   }
   __syncthreads();
   // phase 2: every (row, 4 columns) combines the warps' partial O
-  for (int item = tid; item < rows_here * (D / 4); item += C::kThreads) {
+  for (int item = aborted ? rows_here * (D / 4) : tid; item < rows_here * (D / 4); item += C::kThreads) {
     const int row = item / (D / 4);
     const int dv = 4 * (item % (D / 4));
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -653,6 +660,10 @@ __global__ void __launch_bounds__(160, 2)
   }
   __syncthreads();
   if (!flags[1]) return;
+  if (aborted) {  // the last ticket: reset the semaphore, merge nothing
+    if (tid == 0) a.sems[unit] = 0u;
+    return;
+  }
   __threadfence();
   // phase 1: one thread per row folds the split maxima, the sink and the
   // output scales into one weight per (row, split), staged in shared memory

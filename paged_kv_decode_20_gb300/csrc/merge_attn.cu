@@ -111,6 +111,9 @@ extern "C" xqa_status xqa_merge_attn_states(const xqa_merge_params* p, xqa_strea
     return merge_fail(XQA_ERR_INVALID_ARG, "a required pointer is NULL");
   if (misaligned(p->output) || misaligned(p->suffix_output) || (pre && misaligned(p->prefix_output)))
     return merge_fail(XQA_ERR_INVALID_ARG, "outputs must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(p->output_lse) | reinterpret_cast<uintptr_t>(p->suffix_lse) |
+       reinterpret_cast<uintptr_t>(pre ? p->prefix_lse : nullptr)) & 3)
+    return merge_fail(XQA_ERR_INVALID_ARG, "lse arrays must be 4-byte aligned");
   const int64_t st[6] = {p->out_stride_token,    p->out_stride_head,    p->suffix_stride_token,
                          p->suffix_stride_head,  p->prefix_stride_token, p->prefix_stride_head};
   for (int k = 0; k < (pre ? 6 : 4); ++k)

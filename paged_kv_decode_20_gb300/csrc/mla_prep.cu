@@ -132,6 +132,10 @@ extern "C" xqa_status xqa_mla_decode_prep(const xqa_mla_prep_params* p, xqa_stre
     return prep_fail(XQA_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
   if (p->cos_sin_cache && (reinterpret_cast<uintptr_t>(p->cos_sin_cache) & 3))
     return prep_fail(XQA_ERR_INVALID_ARG, "cos_sin_cache must be 4-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(p->positions) | reinterpret_cast<uintptr_t>(p->slot_mapping)) & 7)
+    return prep_fail(XQA_ERR_INVALID_ARG, "positions and slot_mapping must be 8-byte aligned");
+  if (reinterpret_cast<uintptr_t>(p->error_word) & 3)
+    return prep_fail(XQA_ERR_INVALID_ARG, "error_word must be 4-byte aligned");
   const int64_t st[6] = {p->ql_stride_token, p->ql_stride_head, p->qpe_stride_token, p->qpe_stride_head,
                          p->kvc_stride_token, p->kpe_stride_token};
   for (int k = 0; k < 6; ++k)

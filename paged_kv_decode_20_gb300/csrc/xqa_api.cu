@@ -117,8 +117,17 @@ xqa_status validate_common(const xqa_params* p) {
     return fail(XQA_ERR_UNSUPPORTED, "cache too large for 32-bit TMA coordinates");
   if ((reinterpret_cast<uintptr_t>(p->k_cache) | reinterpret_cast<uintptr_t>(p->v_cache)) & 15)
     return fail(XQA_ERR_INVALID_ARG, "k_cache and v_cache must be 16-byte aligned");
-  if ((reinterpret_cast<uintptr_t>(p->q) | reinterpret_cast<uintptr_t>(p->output)) & 3)
-    return fail(XQA_ERR_INVALID_ARG, "q and output must be 4-byte aligned");
+  // the kernels read q as 32-bit element pairs and store four output elements
+  // at once: one 8-byte store for a 16-bit output, one 4-byte store for e4m3
+  if (reinterpret_cast<uintptr_t>(p->q) & 3) return fail(XQA_ERR_INVALID_ARG, "q must be 4-byte aligned");
+  if (reinterpret_cast<uintptr_t>(p->output) & (p->out_dtype == XQA_E4M3 ? 3 : 7))
+    return fail(XQA_ERR_INVALID_ARG, "output must be %d-byte aligned for its dtype",
+                p->out_dtype == XQA_E4M3 ? 4 : 8);
+  if ((reinterpret_cast<uintptr_t>(p->page_table) | reinterpret_cast<uintptr_t>(p->seq_lens) |
+       reinterpret_cast<uintptr_t>(p->sinks) | reinterpret_cast<uintptr_t>(p->error_word) |
+       reinterpret_cast<uintptr_t>(p->q_scale_dev) | reinterpret_cast<uintptr_t>(p->kv_scale_dev)) & 3)
+    return fail(XQA_ERR_INVALID_ARG,
+                "page_table, seq_lens, sinks, error_word and the device scales must be 4-byte aligned");
   if (p->mask && (reinterpret_cast<uintptr_t>(p->mask) & 1))
     return fail(XQA_ERR_INVALID_ARG, "mask must be 2-byte aligned");
   return XQA_OK;

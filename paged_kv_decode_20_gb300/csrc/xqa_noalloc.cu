@@ -32,22 +32,28 @@ constexpr int kMaxDevices = 64;
 struct DeviceScratch {
   void* workspace = nullptr;
   uint32_t* semaphores = nullptr;
-  cudaError_t status = cudaSuccess;
 };
 
-// Device addresses of the two arrays on device `dev`, looked up once per
-// device (with that device current).  The host-side symbols are stand-ins and
-// must never be passed to a kernel.
-const DeviceScratch& scratch_for(int dev) {
+// Device addresses of the two arrays on device `dev` (the current device),
+// looked up on the first call that succeeds and kept from then on; a failed
+// lookup (for example one attempted during a stream capture) is not kept, so
+// a later call tries again.  The host-side symbols are stand-ins and must
+// never be passed to a kernel.
+cudaError_t scratch_for(int dev, DeviceScratch* out) {
   static DeviceScratch table[kMaxDevices];
-  static std::once_flag once[kMaxDevices];
-  std::call_once(once[dev], [dev] {
-    DeviceScratch& d = table[dev];
-    d.status = cudaGetSymbolAddress(&d.workspace, g_scratch_workspace);
-    if (d.status == cudaSuccess)
-      d.status = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.semaphores), g_scratch_semaphores);
-  });
-  return table[dev];
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  DeviceScratch& d = table[dev];
+  if (!d.workspace || !d.semaphores) {
+    DeviceScratch fresh;
+    cudaError_t e = cudaGetSymbolAddress(&fresh.workspace, g_scratch_workspace);
+    if (e == cudaSuccess)
+      e = cudaGetSymbolAddress(reinterpret_cast<void**>(&fresh.semaphores), g_scratch_semaphores);
+    if (e != cudaSuccess) return e;
+    d = fresh;
+  }
+  *out = d;
+  return cudaSuccess;
 }
 
 xqa_status fail(xqa_status st, const char* msg) {
@@ -73,8 +79,13 @@ extern "C" xqa_status xqa_decode_noalloc(const xqa_params* params, xqa_stream_t 
              need_ws, need_sems, kScratchWorkspaceBytes, kScratchSemaphores);
     return fail(XQA_ERR_WORKSPACE_TOO_SMALL, msg);
   }
-  const DeviceScratch& s = scratch_for(dev);
-  if (s.status != cudaSuccess) return fail(XQA_ERR_CUDA, "xqa_decode_noalloc: cudaGetSymbolAddress failed");
+  DeviceScratch s;
+  e = scratch_for(dev, &s);
+  if (e != cudaSuccess) {
+    char msg[256];
+    snprintf(msg, sizeof msg, "xqa_decode_noalloc: cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
+    return fail(XQA_ERR_CUDA, msg);
+  }
   // Tickets must start at zero; a call that was cut short could have left some set.
   e = cudaMemsetAsync(s.semaphores, 0, need_sems * sizeof(uint32_t), reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(XQA_ERR_CUDA, "xqa_decode_noalloc: clearing the tickets failed");

@@ -270,3 +270,58 @@ def test_mla_workspace_fixed_splits_above_256_sequences(lib):
     assert lib.xqa_mla_workspace_size(ctypes.byref(p), 512, 152) == 0  # one split each
     # 500 pairs x 3 waves / 300 sequences -> 5 splits of 103 pages
     assert lib.xqa_mla_workspace_size(ctypes.byref(p), 512, 1000) == 300 * 5 * MLA_PARTIAL
+
+
+def test_rebuild_is_keyed_on_content_not_mtime(tmp_path):
+    """A library built from other sources is stale even when it is newer than
+    them: the stamp beside it records the sources' digest, not a time."""
+    src = tmp_path / "kernel.cu"
+    src.write_text("int a = 1;\n")
+    lib, stamp = tmp_path / "lib.so", tmp_path / "lib.so.sha256"
+    lib.write_bytes(b"built")
+    digest = B.source_digest([str(src)])
+    stamp.write_text(digest + "\n")
+    assert B.is_current(str(lib), str(stamp), B.source_digest([str(src)]))
+    # same length, older modification time than the library: only the content moved
+    st = os.stat(src)
+    src.write_text("int a = 2;\n")
+    os.utime(src, (st.st_atime - 100, st.st_mtime - 100))
+    assert os.path.getmtime(lib) > os.path.getmtime(src)
+    assert not B.is_current(str(lib), str(stamp), B.source_digest([str(src)]))
+    assert not B.is_current(str(tmp_path / "missing.so"), str(stamp), digest)
+
+
+def test_output_alignment_checked_before_launch(lib):
+    """Four 16-bit outputs go out as one 8-byte store: an output 4 bytes off an
+    8-byte boundary is rejected on the host (nothing is launched)."""
+    p = fake_params(output=0x10004)
+    assert lib.xqa_decode(ctypes.byref(p), None, 0, None, None) == X.XQA_ERR_INVALID_ARG
+    assert "output must be 8-byte aligned" in lib.xqa_last_error().decode()
+    # an e4m3 output needs 4 bytes
+    # (head_dim 64 is unsupported with fp8 KV: the call fails on that later
+    # check, after alignment passed, and launches nothing on any machine)
+    p = fake_params(output=0x10004, kv_dtype=X.XQA_E4M3, out_dtype=X.XQA_E4M3, head_dim=64)
+    assert lib.xqa_decode(ctypes.byref(p), None, 0, None, None) == X.XQA_ERR_UNSUPPORTED
+    assert "head_dim" in lib.xqa_last_error().decode()
+    p = fake_params(output=0x10002, kv_dtype=X.XQA_E4M3, out_dtype=X.XQA_E4M3)
+    assert lib.xqa_decode(ctypes.byref(p), None, 0, None, None) == X.XQA_ERR_INVALID_ARG
+    assert "4-byte aligned" in lib.xqa_last_error().decode()
+
+
+@pytest.mark.parametrize("field", ["page_table", "seq_lens", "sinks", "error_word", "q_scale_dev",
+                                   "kv_scale_dev"])
+def test_int_and_float_pointers_need_4_byte_alignment(lib, field):
+    p = fake_params(**{field: 0x10002})
+    assert lib.xqa_decode(ctypes.byref(p), None, 0, None, None) == X.XQA_ERR_INVALID_ARG
+    assert "4-byte aligned" in lib.xqa_last_error().decode()
+
+
+def test_merge_lse_alignment_checked(lib):
+    st = lib.xqa_merge_attn_states(ctypes.byref(fake_merge(suffix_lse=0x20002)), None)
+    assert st == X.XQA_ERR_INVALID_ARG
+    assert "lse arrays must be 4-byte aligned" in lib.xqa_last_error().decode()
+
+
+def test_prep_index_alignment_checked(lib):
+    assert lib.xqa_mla_decode_prep(ctypes.byref(fake_prep(slot_mapping=0x20004)), None) == X.XQA_ERR_INVALID_ARG
+    assert "8-byte aligned" in lib.xqa_last_error().decode()

@@ -1,4 +1,4 @@
-"""xqa_decode_noalloc against xqa_decode.
+"""xqa_decode_noalloc against xqa_decode and against the float64 oracle.
 
 xqa_decode_noalloc serves callers that may not allocate device memory where
 they run decode attention (a runtime that has reserved the GPU's memory for its
@@ -6,8 +6,9 @@ own KV-cache pool, or code whose allocator is owned elsewhere): it takes its
 split workspace and tickets from a scratch array built into the library.  The
 test calls it through the C ABI twice in a row -- the second call finds the
 first call's leftovers in the shared array -- and checks both outputs against
-the ordinary entry point with caller-provided buffers, within the tolerance
-the parity tests use.  This file is collected last on purpose.
+the ordinary entry point with caller-provided buffers and against the oracle,
+within the tolerance the parity tests use.  This file is collected last on
+purpose.
 """
 
 import ctypes
@@ -47,7 +48,11 @@ CASES = [
 def test_noalloc_matches_caller_buffers_twice(lib, name, make, tol):
     from paged_kv_decode_20_gb300 import xqa as X
     from paged_kv_decode_20_gb300.runner import Decoder
-    case = make().to("cuda")
+    import oracle
+    cpu_case = make()
+    exact = oracle.xqa_attention(cpu_case.q, cpu_case.k_cache, cpu_case.v_cache, cpu_case.page_table,
+                                 cpu_case.seq_lens, **cpu_case.kwargs())
+    case = cpu_case.to("cuda")
     ref_dec = Decoder(case)
     ref = ref_dec.run().clone()
     out = torch.empty_like(ref)
@@ -64,6 +69,8 @@ def test_noalloc_matches_caller_buffers_twice(lib, name, make, tol):
         assert not torch.isnan(out).any()
         err = (out.float() - ref.float()).abs().max().item()
         assert err <= tol, f"{name}: max abs difference {err:.3e}"
+        err_o = (out.cpu().to(torch.float64) - exact).abs().max().item()
+        assert err_o <= tol, f"{name}: max abs error against the oracle {err_o:.3e}"
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(lib):
