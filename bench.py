@@ -57,7 +57,9 @@ def parse():
     ap.add_argument("--op", default="decode", choices=["decode", "merge", "prep"])
     ap.add_argument("--out-dtype", default=None, choices=["e4m3"],
                     help="fp8 output (workloads with an fp8 cache)")
-    ap.add_argument("--workloads", default="1,2,3,4,5",
+    ap.add_argument("--kv-dtype", default=None, choices=["e4m3"],
+                    help="workload 5 with an e4m3 latent cache and query")
+    ap.add_argument("--workloads", default="1,2,3,4,5,5e4m3",
                     help="named workloads also timed into the line's `workloads` object "
                          "(comma list, or 'none')")
     return ap.parse_args()
@@ -125,13 +127,13 @@ def kernel_source_hash(kernel):
 
 def recorded_traffic(workload):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel sources; else None."""
+    the current kernel sources; else None.  workload: 1..5 or '5e4m3'."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         d = json.load(open(path))[str(workload)]
     except Exception:
         return None
-    same = d.get("kernel_hash") == kernel_source_hash(KERNEL_NAMES[workload])
+    same = d.get("kernel_hash") == kernel_source_hash(KERNEL_NAMES[workload_key(workload)[0]])
     return d["dram_bytes_per_launch"] if same else None
 
 
@@ -189,14 +191,44 @@ class Clocks:
                 "samples": len(sm)}
 
 
-def build_case(idx, device, batch=None):
-    return W.workload(idx, device=device, poison=False, batch=batch)
+def workload_key(key):
+    """'5' -> (5, None); '5e4m3' -> (5, torch.float8_e4m3fn)."""
+    key = str(key)
+    if key.endswith("e4m3"):
+        return int(key[:-4]), torch.float8_e4m3fn
+    return int(key), None
+
+
+def workload_name(idx, kv_dtype=None):
+    return W.WORKLOAD_5_E4M3 if kv_dtype is not None else W.WORKLOADS[idx]
+
+
+def build_case(idx, device, batch=None, kv_dtype=None):
+    return W.workload(idx, device=device, poison=False, batch=batch, kv_dtype=kv_dtype)
 
 
 L2_FLUSH_BYTES = 256 * 1024 * 1024  # twice the GB300's L2
 
 
-def time_workload(idx, dev, launches, flush):
+def tensor_roofline(case, ms):
+    """Tensor-pipe roofline of the MLA latent decode: Q K^T over 576 dims and
+    P V over 512, 2 flops per multiply-add, per visible token and query row.
+    Each contraction is priced at the peak of its own type: bf16 at the
+    measured bf16 peak; an e4m3 Q K^T at twice it (the nominal fp8 : bf16
+    ratio), its P V (f16 against the widened V) at the bf16 peak.  frac = the
+    time both would take at those peaks / the measured time."""
+    rows = case.visible_tokens() * case.q_seq_len * case.q.shape[2]
+    qk, pv = rows * 2 * case.q.shape[3], rows * 2 * case.dv
+    tpeak, tkind = tensor_peak()
+    qk_peak = tpeak * (2.0 if case.k_cache.dtype == torch.float8_e4m3fn else 1.0)
+    t_ideal = qk / (qk_peak * 1e12) + pv / (tpeak * 1e12)
+    return {"bound": "tensor", "achieved": round((qk + pv) / (ms * 1e-3) / 1e12, 2),
+            "peak": round((qk + pv) / t_ideal / 1e12, 1), "unit": "TFLOP/s",
+            "frac": round(t_ideal / (ms * 1e-3), 4), "peak_source": tkind + " (bf16; fp8 at 2x)",
+            "flops_per_launch": qk + pv}
+
+
+def time_workload(key, dev, launches, flush):
     """Times one named workload's decode call on `dev` and returns its summary
     for the bench line's `workloads` object.
 
@@ -208,7 +240,8 @@ def time_workload(idx, dev, launches, flush):
     launch latency through programmatic dependent launch)."""
     from paged_kv_decode_20_gb300.runner import Decoder
 
-    case = build_case(idx, dev)
+    idx, kv_dtype = workload_key(key)
+    case = build_case(idx, dev, kv_dtype=kv_dtype)
     dec = Decoder(case, error_word=False)
     stream = torch.cuda.current_stream(dev)
     kv, qb = case.kv_bytes(), case.q_bytes()
@@ -237,7 +270,7 @@ def time_workload(idx, dev, launches, flush):
     ms = sum(a.elapsed_time(b) for a, b in ev) / launches
     peak, kind = peaks()
     achieved = (kv + qb) / (ms * 1e-3) / 1e9
-    out = {"workload": W.WORKLOADS[idx], "kernel": KERNEL_NAMES[idx],
+    out = {"workload": workload_name(idx, kv_dtype), "kernel": KERNEL_NAMES[idx],
            "ms_per_launch": round(ms, 5),
            "timing": "L2 flushed before every launch" if small else "inputs larger than L2 (no flush)",
            "kv_bytes": kv, "q_bytes": qb,
@@ -247,15 +280,11 @@ def time_workload(idx, dev, launches, flush):
                         "frac": round(achieved / peak, 4), "peak_source": kind}}
     if b2b is not None:
         out["back_to_back_ms_per_launch"] = round(b2b, 5)
-    traffic = recorded_traffic(idx)
+    traffic = recorded_traffic(key)
     if traffic is not None:
         out["traffic_over_algorithmic"] = round(traffic / (kv + qb), 4)
     if case.mla:
-        flops = case.visible_tokens() * case.q_seq_len * case.q.shape[2] * 2 * (case.q.shape[3] + case.dv)
-        tf = flops / (ms * 1e-3) / 1e12
-        tpeak, tkind = tensor_peak()
-        out["roofline_tensor"] = {"bound": "tensor", "achieved": round(tf, 2), "peak": tpeak,
-                                  "unit": "TFLOP/s", "frac": round(tf / tpeak, 4), "peak_source": tkind}
+        out["roofline_tensor"] = tensor_roofline(case, ms)
     out["clocks"] = clk.summary()
     del dec, case
     torch.cuda.empty_cache()
@@ -280,7 +309,8 @@ def run_gb300(args):
         dist.barrier()
     X.load()
 
-    case = build_case(args.workload, dev, args.batch)
+    kv_dtype = torch.float8_e4m3fn if args.kv_dtype == "e4m3" else None
+    case = build_case(args.workload, dev, args.batch, kv_dtype)
     dec = Decoder(case, error_word=False,
                   out_dtype=torch.float8_e4m3fn if args.out_dtype == "e4m3" else None)
     stream = torch.cuda.current_stream(dev)
@@ -289,10 +319,10 @@ def run_gb300(args):
     tokens = case.batch * case.q_seq_len
     batch = case.batch
     mla = case.mla
-    flops = (case.visible_tokens() * case.q_seq_len * case.q.shape[2] * 2 * (case.q.shape[3] + case.dv)
-             if mla else 0)
     dtype_name = {torch.bfloat16: "bf16", torch.float16: "f16",
                   torch.float8_e4m3fn: "e4m3 kv, bf16 q"}[case.k_cache.dtype]
+    if case.q.dtype == torch.float8_e4m3fn:
+        dtype_name = "e4m3 kv and q, bf16 out"
 
     # ---- device-resident timing: K steps, events around each launch
     for _ in range(args.warmup):
@@ -320,6 +350,7 @@ def run_gb300(args):
     launch_ms = [a.elapsed_time(b) for a, b in ev]
     ms_per_step = total_ms / args.steps
     avg_launch_ms = sum(launch_ms) / len(launch_ms)
+    tensor_rl = tensor_roofline(case, avg_launch_ms) if mla else None
 
     # ---- end to end through the C ABI with host buffers
     e2e = None
@@ -372,8 +403,8 @@ def run_gb300(args):
         torch.cuda.empty_cache()
         flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
         per_workload = {}
-        for idx in [int(x) for x in args.workloads.split(",")]:
-            per_workload[str(idx)] = time_workload(idx, dev, max(args.steps, 20), flush)
+        for key in args.workloads.split(","):
+            per_workload[key] = time_workload(key, dev, max(args.steps, 20), flush)
         del flush
 
     if world > 1:
@@ -398,7 +429,7 @@ def run_gb300(args):
         "vs_baseline": None,
         "dtype": dtype_name,
         "data": "synthetic (seeded N(0,1) q/K/V, shuffled page pool)",
-        "config": {"workload": W.WORKLOADS[args.workload] + (", fp8 output" if args.out_dtype else ""),
+        "config": {"workload": workload_name(args.workload, kv_dtype) + (", fp8 output" if args.out_dtype else ""),
                    "global_batch": batch * world,
                    "kv_bytes_per_step": kv_bytes * world, "q_bytes_per_step": q_bytes * world,
                    "l2": "inputs larger than L2 (no flush)" if kv_bytes > 129e6
@@ -409,7 +440,8 @@ def run_gb300(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": peak_kind,
-                     "traffic": recorded_traffic(args.workload),
+                     "traffic": recorded_traffic(f"{args.workload}e4m3" if kv_dtype is not None
+                                                 else args.workload),
                      "kernel": KERNEL_NAMES[args.workload],
                      "algorithmic_bytes_per_launch": kv_bytes + q_bytes,
                      "avg_launch_ms": round(avg_launch_ms, 5)},
@@ -422,13 +454,7 @@ def run_gb300(args):
         line["workloads"] = per_workload
     if mla:
         # the latent workload sits near the ridge: report the tensor pipe too
-        # (QK over 576 dims and P.V over 512, 2 flops per multiply-add, per
-        # visible token and query row)
-        tf = flops / (avg_launch_ms * 1e-3) / 1e12
-        tpeak, tkind = tensor_peak()
-        line["roofline_tensor"] = {"bound": "tensor", "achieved": round(tf, 2), "peak": tpeak,
-                                   "unit": "TFLOP/s", "frac": round(tf / tpeak, 4), "peak_source": tkind,
-                                   "flops_per_launch": flops}
+        line["roofline_tensor"] = tensor_rl
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

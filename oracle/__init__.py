@@ -117,7 +117,8 @@ def xqa_attention(q, k_cache, v_cache, page_table, seq_lens, *, num_kv_heads, pa
                   mask=None, units=None, threads=0, return_lse=False):
     """Exact float64 paged decode attention.
 
-    q: [B, q_seq_len, Hq, D] (or [B, Hq, D]) fp16/bf16.  k_cache, v_cache:
+    q: [B, q_seq_len, Hq, D] (or [B, Hq, D]) fp16/bf16, or float8_e4m3fn (the
+    fp8 query an fp8 latent cache takes; decoded like the cache).  k_cache, v_cache:
     [num_pages, page_size, Hkv, D] (NHD) or [num_pages, Hkv, page_size, D]
     (HND), fp16/bf16/float8_e4m3fn; for the MLA variant pass the same latent
     cache twice and v_head_dim < D.  page_table: int32 [B, pages_per_seq].
@@ -153,7 +154,7 @@ def xqa_attention(q, k_cache, v_cache, page_table, seq_lens, *, num_kv_heads, pa
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
     layout_hnd = {"NHD": 0, "HND": 1}[kv_layout.upper()]
-    q_bits = q.view(torch.int16)
+    q_bits = q.view(torch.uint8) if q.dtype == torch.float8_e4m3fn else q.view(torch.int16)
     kv_code = _DTYPE_CODE[k_cache.dtype]
     k_bits = k_cache.view(torch.uint8) if kv_code == _E4M3 else k_cache.view(torch.int16)
     v_bits = v_cache.view(torch.uint8) if kv_code == _E4M3 else v_cache.view(torch.int16)

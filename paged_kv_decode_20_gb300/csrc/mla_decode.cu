@@ -52,89 +52,129 @@
 namespace xqa {
 namespace mla {
 
-constexpr int kRows = 128;       // UMMA M: query rows (heads x spec tokens)
+constexpr int kRows = 128;       // UMMA M: query rows (heads x spec tokens), padded to 128
 constexpr int kLatent = 512;     // kv_lora_rank (= V width)
 constexpr int kRope = 64;        // qk_rope_head_dim
 constexpr int kDim = kLatent + kRope;
 constexpr int kHalf = kLatent / 2;  // output columns per epilogue thread and per merging CTA
 constexpr int kTok = 64;         // tokens per P / V tile (UMMA K of PV)
 constexpr int kTokQ = 2 * kTok;  // tokens per logit tile (UMMA N of QK)
-constexpr int kChunkBytes = kTok * 128;    // one 64-dim column chunk of a V tile
-constexpr int kChunkBytesQ = kTokQ * 128;  // one 64-dim column chunk of a logit tile
-constexpr int kChunks = kDim / 64;         // chunks of a latent row: 8 latent + 1 rope
+constexpr int kChunkBytes = kTok * 128;    // one 128-byte column chunk of a V tile
+constexpr int kChunkBytesQ = kTokQ * 128;  // one 128-byte column chunk of a logit tile
+constexpr int kGroups = 3;       // K groups (ring slots) per logit tile
 constexpr int kSoftWarps = 8;    // two threads per query row
 constexpr int kSoft = 32 * kSoftWarps;
 constexpr int kSoftWarp0 = 2;    // warps 2..9: two per TMEM sub-partition
 constexpr int kThreads = 32 * kSoftWarp0 + kSoft;
 
 // ---- messages from the logit CTA to the output CTA
-constexpr int kPBytes = kRows * kTok * 2;  // one bf16 P tile
+constexpr int kPBytes = kRows * kTok * 2;  // one 16-bit P tile
 constexpr int kFBytes = kRows * 4 + 16;    // one rescale factor per row, then a flag word
 constexpr int kPMsg = kPBytes + kFBytes;
 constexpr int kFinBytes = 2 * kRows * 4;   // the final row maxima and sums
 constexpr int kCopyPieces = 4;             // P travels as this many bulk copies
 
 // ---- shared memory (offsets from the dynamic base, which is 1024-aligned:
-// checked at run time).  The barrier block sits at the same offset in both
-// CTAs because each CTA signals barriers of its peer.
+// checked at run time), per element type of the latent cache.  The barrier
+// block sits at the same offset in both CTAs because each CTA signals
+// barriers of its peer.
 // Tiles in shared memory are stored row group by row group: [8-row group]
-// [64-dim chunk][8 rows][128 bytes], so that one TMA box (a page piece's rows
-// across several chunks) fills a contiguous run and every 8-row UMMA atom
-// stays 1024-byte aligned.
-// Output CTA: V x3 | P x2 | factors x2 | final rows
-constexpr int kVBytes = 8 * kChunkBytes;  // the eight latent chunks of a tile
-constexpr int kVSlots = 3;
-constexpr int kOffV = 0;
-constexpr int kOffP = kOffV + kVSlots * kVBytes;
-constexpr int kOffF = kOffP + 2 * kPBytes;
-constexpr int kOffFin = kOffF + 2 * kFBytes;
-// Logit CTA: K ring of three slots, each one group of three chunks (128
-// tokens x 192 dims) | rope query (128 x 64 bf16) | P staging x2 | factor
-// staging x2 | row maxima [2 tiles][2 halves][128] | final rows
-constexpr int kGroup = 3;                     // chunks per ring slot
-constexpr int kKSlots = kChunks / kGroup;     // one slot per group of a logit tile
-constexpr int kGroupBytes = kGroup * kChunkBytesQ;
-constexpr int kOffK = 0;
-constexpr int kOffQRope = kOffK + kKSlots * kGroupBytes;
-constexpr int kOffPS = kOffQRope + kRows * 128;
-constexpr int kOffFS = kOffPS + 2 * kPBytes;
-constexpr int kOffRowX = kOffFS + 2 * kFBytes;
-constexpr int kOffFinS = kOffRowX + 4 * kRows * 4;
-constexpr int kOffBar =
-    (kOffFin + kFinBytes) > (kOffFinS + kFinBytes) ? (kOffFin + kFinBytes) : (kOffFinS + kFinBytes);
+// [128-byte column chunk][8 rows][128 bytes], so that one TMA box (a page
+// piece's rows across several chunks) fills a contiguous run and every 8-row
+// UMMA atom stays 1024-byte aligned.
+//
+// bf16 cache (a latent row is nine 64-dim chunks):
+//   logit CTA: K ring of one logit tile, three slots of one 3-chunk group
+//     (128 tokens x 192 dims, 48 KB) | rope query (128 x 64 bf16) | P staging x2
+//     | factor staging x2 | row maxima [2 tiles][2 halves][128] | final rows
+//   output CTA: V x3 (the 8 latent chunks of a 64-token tile, 64 KB) | P x2 |
+//     factors x2 | final rows
+// e4m3 cache (a latent row is four 128-dim chunks and a 64-byte rope part):
+//   logit CTA: K ring of two logit tiles, each three slots: latent chunks 0-1,
+//     latent chunks 2-3 (32 KB each) and the rope part (128 rows of 64 bytes,
+//     64-byte swizzle, 8 KB) | rope query (128 x 64 e4m3, 64-byte swizzle) | the rest as bf16
+//   output CTA: V x2 (e4m3, the 4 latent chunks of a 64-token tile, 32 KB) |
+//     widened V x2 (f16, laid out as the bf16 V tile, 64 KB) | P x2 | factors x2 | final rows
+template <bool F8>
+struct Lay {
+  static constexpr int kRingTiles = F8 ? 2 : 1;
+  static constexpr int kKSlots = kGroups * kRingTiles;
+  static constexpr int kGroupChunks = F8 ? 2 : 3;       // 128-byte chunks per latent group
+  static constexpr int kLatGroupBytes = kGroupChunks * kChunkBytesQ;
+  static constexpr int kTileBytes = F8 ? 2 * kLatGroupBytes + kTokQ * 64 : 3 * kLatGroupBytes;
+  // slot s of the ring (group s % 3 of a tile)
+  __host__ __device__ static constexpr int slot_off(int s) {
+    return (s / kGroups) * kTileBytes + (s % kGroups) * kLatGroupBytes;
+  }
+  __host__ __device__ static constexpr uint32_t slot_tx(int s, uint32_t rows) {  // bytes a slot receives
+    return F8 && s % kGroups == 2 ? rows * 64u : rows * 128u * uint32_t(kGroupChunks);
+  }
+  static constexpr int kOffK = 0;
+  static constexpr int kOffQRope = kOffK + kRingTiles * kTileBytes;
+  static constexpr int kOffPS = kOffQRope + kRows * (F8 ? 64 : 128);
+  static constexpr int kOffFS = kOffPS + 2 * kPBytes;
+  static constexpr int kOffRowX = kOffFS + 2 * kFBytes;
+  static constexpr int kOffFinS = kOffRowX + 4 * kRows * 4;
+  static constexpr int kLogitEnd = kOffFinS + kFinBytes;
+  static constexpr int kVSlots = F8 ? 2 : 3;
+  static constexpr int kVChunks = F8 ? 4 : 8;  // 128-byte chunks of a V tile row
+  static constexpr int kVBytes = kVChunks * kChunkBytes;
+  static constexpr int kHSlots = F8 ? 2 : 0;
+  static constexpr int kHBytes = 8 * kChunkBytes;  // 512 f16 dims x 64 tokens
+  static constexpr int kOffV = 0;
+  static constexpr int kOffH = kOffV + kVSlots * kVBytes;
+  static constexpr int kOffP = kOffH + kHSlots * kHBytes;
+  static constexpr int kOffF = kOffP + 2 * kPBytes;
+  static constexpr int kOffFin = kOffF + 2 * kFBytes;
+  static constexpr int kOutEnd = kOffFin + kFinBytes;
+  static constexpr int kOffBar = kLogitEnd > kOutEnd ? kLogitEnd : kOutEnd;
+};
 
+constexpr int kMaxKSlots = 6;
+constexpr int kMaxVSlots = 3;
 enum BarIdx {
   // logit CTA
   kKFull = 0,                      // [kKSlots] a group of K chunks landed
-  kKEmpty = kKFull + kKSlots,      // [kKSlots] the QK reading a group is done
-  kSFull = kKEmpty + kKSlots,      // [2] S tile computed
+  kKEmpty = kKFull + kMaxKSlots,   // [kKSlots] the QK reading a group is done
+  kSFull = kKEmpty + kMaxKSlots,   // [2] S tile computed
   kSFree = kSFull + 2,             // [2] S tile read out of tensor memory
   kQReady = kSFree + 2,            // the query is in tensor / shared memory
   kPSlotFree = kQReady + 1,        // [2] the output CTA's P.V of that P slot is done
   // output CTA
   kVFull = kPSlotFree + 2,         // [kVSlots] a V slot landed
-  kVEmpty = kVFull + kVSlots,      // [kVSlots] the P.V reading a V slot is done
-  kPFull = kVEmpty + kVSlots,      // [2] own expect-tx arrival + the peer's P message
+  kVEmpty = kVFull + kMaxVSlots,   // [kVSlots] the P.V (bf16) or the widening (e4m3) read a V slot
+  kPFull = kVEmpty + kMaxVSlots,   // [2] own expect-tx arrival + the peer's P message
   kFin = kPFull + 2,               // own expect-tx arrival + the peer's final rows
-  kReq = kFin + 1,                 // the MMA thread posted a request to the warps
+  kReq = kFin + 1,                 // the MMA thread posted a request (bf16) / drained (e4m3)
   kOReady = kReq + 1,              // the warps served it
   kODone = kOReady + 1,            // every P.V issued so far is done
+  kHFull = kODone + 1,             // [2] e4m3: the warps widened a V tile into an f16 slot
+  kHEmpty = kHFull + 2,            // [2] e4m3: the P.V reading an f16 slot is done
+  kDec = kHEmpty + 2,              // [2] e4m3: the MMA thread's rescale decision for a tile
   // both
-  kDrain = kODone + 1,             // every MMA this CTA issued is done
+  kDrain = kDec + 2,               // every MMA this CTA issued is done
   kNumBars = kDrain + 1
 };
-constexpr int kSmem = kOffBar + kNumBars * 8 + 32;
-static_assert(kSmem <= 232448, "shared memory budget");
-static_assert(kOffP % 1024 == 0 && kOffQRope % 1024 == 0 && kOffPS % 1024 == 0 && kOffF % 16 == 0 &&
-                  kOffFS % 16 == 0 && kOffFin % 16 == 0 && kOffFinS % 16 == 0 && kFBytes % 16 == 0 &&
-                  kOffBar % 8 == 0,
-              "UMMA operands need 1024-byte alignment, bulk copies 16");
-static_assert(kPBytes % (16 * kCopyPieces) == 0, "copy pieces");
+template <bool F8>
+constexpr int smem_bytes() {
+  return Lay<F8>::kOffBar + kNumBars * 8 + 32;
+}
+template <bool F8>
+constexpr bool layout_ok() {
+  using SL = Lay<F8>;
+  return smem_bytes<F8>() <= 232448 && SL::kOffP % 1024 == 0 && SL::kOffH % 1024 == 0 && SL::kOffQRope % 1024 == 0 &&
+         SL::kOffPS % 1024 == 0 && SL::kTileBytes % 1024 == 0 && SL::kLatGroupBytes % 1024 == 0 &&
+         SL::kOffF % 16 == 0 && SL::kOffFS % 16 == 0 && SL::kOffFin % 16 == 0 && SL::kOffFinS % 16 == 0 &&
+         SL::kOffBar % 8 == 0 && SL::kKSlots <= kMaxKSlots && SL::kVSlots <= kMaxVSlots;
+}
+static_assert(layout_ok<false>() && layout_ok<true>(),
+              "shared memory budget; UMMA operands need 1024-byte alignment, bulk copies 16");
+static_assert(kFBytes % 16 == 0 && kPBytes % (16 * kCopyPieces) == 0, "copy pieces");
 
 // tensor memory columns
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;    // output CTA: 512 fp32 columns of O
-constexpr uint32_t kColQ = 0;    // logit CTA: 256 columns, the latent query as bf16 pairs
+constexpr uint32_t kColQ = 0;    // logit CTA: the latent query, 256 columns of bf16 pairs or 128 of e4m3 quads
 constexpr uint32_t kColS = 256;  // logit CTA: 2 x 128 columns of logits
 
 // requests from the output CTA's MMA thread to its warps
@@ -153,8 +193,8 @@ constexpr int kMaxSplits = 64;       // merge weights [128][splits] fit in share
 constexpr int kWaves = XQA_MLA_WAVES;  // cluster waves the split plan aims for
 
 struct MlaArgs {
-  const uint16_t* q;  // [B, qs, Hq, 576]
-  uint16_t* out;      // [B, qs, Hq, 512]
+  const uint8_t* q;   // [B, qs, Hq, 576] bf16 or e4m3
+  uint16_t* out;      // [B, qs, Hq, 512] bf16
   const int32_t* page_table;
   const uint32_t* seq_lens;
   const float* sinks;
@@ -167,9 +207,9 @@ struct MlaArgs {
   float* lse;  // optional [B, qs, Hq] natural-log log-sum-exp per row
   int64_t num_pages;
   int B, Hq, qs, ps, pps, win, nsplit, split_pages, mask_words;
+  int R;    // real query rows Hq * qs (<= 128); rows R..127 of the tile are padding
   int ncl;  // persistent clusters
   float q_scale, kv_scale, softmax_scale, rcp_out_scale;
-  int q_bf16;
 };
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -229,6 +269,31 @@ __device__ __forceinline__ void zero_v_tail(uint8_t* vslot, int r0, int st) {
   for (int idx = st; idx < (kTok - r0) * 8 * 8; idx += kSoft) {
     const int r = r0 + idx / 64, k = (idx / 8) % 8, u = idx % 8;
     *reinterpret_cast<uint4*>(vslot + ((r >> 3) * 8 + k) * 1024 + (r & 7) * 128 + u * 16) = make_uint4(0, 0, 0, 0);
+  }
+}
+
+// Widens one e4m3 V tile (64 tokens x 512 dims, [row group][128-dim chunk][8
+// rows][128 B], 128-byte swizzle) into the f16 V tile the P.V reads ([row
+// group][64-dim chunk][8 rows][128 B], 128-byte swizzle); the cvt from e4m3 to
+// f16 is exact.  Rows at or past `rows_valid` (past the split's end: stale,
+// possibly NaN) are written as zeros.  Threads st = 0..kSoft-1.
+__device__ __forceinline__ void widen_v(const uint8_t* v8, uint8_t* h16, int rows_valid, int st) {
+#pragma unroll 4
+  for (int idx = st; idx < kTok * 4 * 8; idx += kSoft) {
+    const int u = idx & 7, r = (idx >> 3) & 7, c = (idx >> 6) & 3, rg = idx >> 8;
+    uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+    if (rg * 8 + r < rows_valid) {
+      const uint4 x = *reinterpret_cast<const uint4*>(v8 + rg * 4096 + c * 1024 + r * 128 + ((u ^ r) << 4));
+      e4m3x4_to_f16x2x2(x.x, lo.x, lo.y);
+      e4m3x4_to_f16x2x2(x.y, lo.z, lo.w);
+      e4m3x4_to_f16x2x2(x.z, hi.x, hi.y);
+      e4m3x4_to_f16x2x2(x.w, hi.z, hi.w);
+    }
+    // dims 128c + 16u .. +15: units 2(u % 4) and 2(u % 4) + 1 of 64-dim chunk 2c + u / 4
+    uint8_t* dst = h16 + rg * 8192 + (2 * c + (u >> 2)) * 1024 + r * 128;
+    const int u2 = 2 * (u & 3);
+    *reinterpret_cast<uint4*>(dst + ((u2 ^ r) << 4)) = lo;
+    *reinterpret_cast<uint4*>(dst + (((u2 + 1) ^ r) << 4)) = hi;
   }
 }
 
@@ -297,14 +362,22 @@ __device__ __forceinline__ TilePieces tile_pieces(const MlaArgs& a, const int32_
   return p;
 }
 
+// F8: e4m3 latent cache and e4m3 query (Q K^T on kind::f8f6f4, P in f16, V
+// widened to f16 in shared memory); else bf16 throughout.  tmK: the latent
+// chunks of a logit tile's groups; tmKR: the rope part of an e4m3 row (unused
+// for bf16, whose third group carries it); tmV: a V tile; tmPF: L2 prefetch.
+template <bool F8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    mla_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                      const __grid_constant__ CUtensorMap tmPF, const MlaArgs a) {
+    mla_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmKR,
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmPF,
+                      const MlaArgs a) {
+  using SL = Lay<F8>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SL::kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
-  int* flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] abort, [1] last CTA, [2] request word, [3] cluster abort
+  // [0] abort, [1] last CTA, [2] request word, [3] cluster abort, [4..5] rescale decisions (e4m3)
+  int* flags = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t c = cluster_rank();
@@ -368,9 +441,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   umma::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   const uint32_t peer_bars = map_peer(smem_u32(bars), peer);
-  const uint32_t box_bytes = uint32_t(min(a.ps, kTok)) * 128u;
-  constexpr uint32_t kIdescQK = umma::idesc_f16(kRows, kTokQ, true, false, false);
-  constexpr uint32_t kIdescPV = umma::idesc_f16(kRows, kHalf, true, false, true);
+  const uint32_t box_rows = uint32_t(min(a.ps, kTok));
+  // Q K^T: bf16 (kind::f16) or e4m3 (kind::f8f6f4); P V: bf16, or f16 when V is widened from e4m3
+  constexpr uint32_t kIdescQK =
+      F8 ? umma::idesc_e4m3(kRows, kTokQ, false, false) : umma::idesc_f16(kRows, kTokQ, true, false, false);
+  constexpr uint32_t kIdescPV = umma::idesc_f16(kRows, kHalf, !F8, false, true);
   bool first_piece = true;
 
   for (;;) {
@@ -414,40 +489,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // barriers are set up afresh for every piece (after the previous piece's
   // last wait, both CTAs having passed the cluster barrier that ends it)
   if (tid == 0) {
-    if (!first_piece) {
+    // the barriers this CTA uses, with their arrival counts
+    auto each_bar = [&](auto&& fn) {
       if (logit_cta) {
-        for (int i = kKFull; i <= kPSlotFree + 1; ++i) mbar_inval(&bars[i]);
+        for (int i = 0; i < SL::kKSlots; ++i) {
+          fn(kKFull + i, 1);
+          fn(kKEmpty + i, 1);
+        }
+        for (int k = 0; k < 2; ++k) {
+          fn(kSFull + k, 1);
+          fn(kSFree + k, kSoftWarps);
+          fn(kPSlotFree + k, 1);  // the peer's MMA completion
+        }
+        fn(kQReady, kSoftWarps);
       } else {
-        for (int i = kVFull; i <= kODone; ++i) mbar_inval(&bars[i]);
+        // an e4m3 V slot is freed by the eight warps that widen it, a bf16 one by the P.V
+        for (int k = 0; k < SL::kVSlots; ++k) {
+          fn(kVFull + k, 1);
+          fn(kVEmpty + k, F8 ? kSoftWarps : 1);
+        }
+        for (int k = 0; k < 2; ++k) fn(kPFull + k, 1);
+        fn(kFin, 1);
+        fn(kReq, 1);
+        fn(kOReady, kSoftWarps);
+        fn(kODone, 1);
+        if (F8)
+          for (int k = 0; k < 2; ++k) {
+            fn(kHFull + k, kSoftWarps);
+            fn(kHEmpty + k, 1);
+            fn(kDec + k, 1);
+          }
       }
-      mbar_inval(&bars[kDrain]);
-    }
-    if (logit_cta) {
-      for (int i = 0; i < kKSlots; ++i) {
-        mbar_init(&bars[kKFull + i], 1);
-        mbar_init(&bars[kKEmpty + i], 1);
-      }
-      for (int k = 0; k < 2; ++k) {
-        mbar_init(&bars[kSFull + k], 1);
-        mbar_init(&bars[kSFree + k], kSoftWarps);
-      }
-      mbar_init(&bars[kQReady], kSoftWarps);
-      for (int k = 0; k < 2; ++k) mbar_init(&bars[kPSlotFree + k], 1);  // the peer's MMA completion
-    } else {
-      for (int k = 0; k < kVSlots; ++k) {
-        mbar_init(&bars[kVFull + k], 1);
-        mbar_init(&bars[kVEmpty + k], 1);
-      }
-      for (int k = 0; k < 2; ++k) mbar_init(&bars[kPFull + k], 1);
-      mbar_init(&bars[kFin], 1);
-      mbar_init(&bars[kReq], 1);
-      mbar_init(&bars[kOReady], kSoftWarps);
-      mbar_init(&bars[kODone], 1);
+      fn(kDrain, 1);
+    };
+    if (!first_piece) each_bar([&](int i, int) { mbar_inval(&bars[i]); });
+    each_bar([&](int i, int n) { mbar_init(&bars[i], uint32_t(n)); });
+    if (!logit_cta) {
       // the first two P messages and the final rows are expected up front
       for (int k = 0; k < min(2, ntiles); ++k) mbar_arrive_expect_tx(&bars[kPFull + k], kPMsg);
       mbar_arrive_expect_tx(&bars[kFin], kFinBytes);
     }
-    mbar_init(&bars[kDrain], 1);
     flags[0] = flags[1] = flags[2] = 0;
     fence_mbar_init();
   }
@@ -459,42 +540,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ================= TMA producer =================
-    // Logit CTA: every chunk of every tile, in order, into the chunk ring; a
-    // chunk slot refills once the QK that read it is done.  Output CTA: the
-    // eight latent chunks of each tile into a V slot once the P.V of the tile
-    // three back is done.  Each wait gives up after kWaitCycles.
+    // Logit CTA: every group of every logit tile, in order, into the K ring;
+    // a slot refills once the QK that read it is done.  Output CTA: the latent
+    // chunks of each 64-token tile into a V slot once the P.V (bf16) or the
+    // widening (e4m3) of the tile kVSlots back is done.  Each wait gives up
+    // after kWaitCycles.
     if (ntiles > 0) {
       if (lane == 0) {
         prefetch_tensormap(logit_cta ? &tmK : &tmV);
         if (logit_cta) prefetch_tensormap(&tmPF);
+        if (logit_cta && F8) prefetch_tensormap(&tmKR);
       }
       bool ok = true, bad = false;
       int issued = 0;
       if (logit_cta) {
-        // group gr of logit tile j goes to slot gr (its `j`-th use): one
-        // wait, one expect-tx and three chunk loads per group
+        // group gr of logit tile j (global group g = 3 j + gr) goes to ring
+        // slot g % kKSlots: one wait, one expect-tx and one box per page piece
         TilePieces tp = {0, 0, false};
-        for (int g = 0; ok && g < nqt * kKSlots; ++g) {
-          const int j = g / kKSlots, slot = g - j * kKSlots;
-          if (slot == 0) {
+        for (int g = 0; ok && g < nqt * kGroups; ++g) {
+          const int j = g / kGroups, gr = g - j * kGroups;
+          const int slot = g % SL::kKSlots, use = g / SL::kKSlots;
+          if (gr == 0) {
             tp = tile_pieces(a, pt, t_begin + j * kTokQ, kTokQ, pg_hi, lane);
             bad |= tp.bad;
           }
-          if (j > 0) ok = __all_sync(kAll, mbar_wait(&bars[kKEmpty + slot], (j - 1) & 1));
+          if (use > 0) ok = __all_sync(kAll, mbar_wait(&bars[kKEmpty + slot], (use - 1) & 1));
           if (!ok) break;
-          if (lane == 0) mbar_arrive_expect_tx(&bars[kKFull + slot], uint32_t(tp.n) * box_bytes * kGroup);
+          const uint32_t piece_bytes = SL::slot_tx(slot, box_rows);
+          if (lane == 0) mbar_arrive_expect_tx(&bars[kKFull + slot], uint32_t(tp.n) * piece_bytes);
           __syncwarp();
-          // one box per page piece (its rows across the group's three chunks),
-          // one piece per lane: issuing a TMA instruction holds its thread for
-          // hundreds of cycles
-          if (lane < tp.n)
-            tma_load_4d(smem + kOffK + slot * kGroupBytes + lane * kGroup * int(box_bytes), &tmK,
-                        &bars[kKFull + slot], 0, 0, kGroup * slot, tp.row >> 3);
+          // one box per page piece (its rows across the group's chunks, or the
+          // e4m3 rope part), one piece per lane: issuing a TMA instruction
+          // holds its thread for hundreds of cycles
+          if (lane < tp.n) {
+            uint8_t* dst = smem + SL::kOffK + SL::slot_off(slot) + lane * int(piece_bytes);
+            if (F8 && gr == 2)
+              tma_load_3d(dst, &tmKR, &bars[kKFull + slot], 0, 0, tp.row >> 3);
+            else
+              tma_load_4d(dst, &tmK, &bars[kKFull + slot], 0, 0, SL::kGroupChunks * gr, tp.row >> 3);
+          }
           __syncwarp();
           // after the tile's first loads are out, the tile two ahead goes into
           // L2, so that its loads (issued only as ring slots free) do not pay
           // HBM latency
-          if (slot == 0 && j + 2 < nqt) {
+          if (gr == 0 && j + 2 < nqt) {
             // one box per page piece covers all 576 dims of its rows
             const TilePieces pf = tile_pieces(a, pt, t_begin + (j + 2) * kTokQ, kTokQ, pg_hi, lane);
             if (lane < pf.n && pf.row >= 0) tma_prefetch_l2_3d(&tmPF, 0, 0, pf.row);
@@ -503,27 +592,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         // no load of this CTA may land after it exits
         if (lane == 0)
-          for (int g = max(0, issued - kKSlots); g < issued; ++g)
-            if (!mbar_wait(&bars[kKFull + g % kKSlots], (g / kKSlots) & 1)) ok = false;
+          for (int g = max(0, issued - SL::kKSlots); g < issued; ++g)
+            if (!mbar_wait(&bars[kKFull + g % SL::kKSlots], (g / SL::kKSlots) & 1)) ok = false;
       } else {
+        const uint32_t piece_bytes = uint32_t(box_rows) * 128u * SL::kVChunks;
         for (int j = 0; ok && j < ntiles; ++j) {
-          const int slot = j % kVSlots, use = j / kVSlots;
+          const int slot = j % SL::kVSlots, use = j / SL::kVSlots;
           if (use > 0) ok = __all_sync(kAll, mbar_wait(&bars[kVEmpty + slot], (use - 1) & 1));
           if (!ok) break;
           const TilePieces tp = tile_pieces(a, pt, t_begin + j * kTok, kTok, pg_hi, lane);
           bad |= tp.bad;
-          if (lane == 0) mbar_arrive_expect_tx(&bars[kVFull + slot], uint32_t(tp.n) * box_bytes * 8u);
+          if (lane == 0) mbar_arrive_expect_tx(&bars[kVFull + slot], uint32_t(tp.n) * piece_bytes);
           __syncwarp();
-          // one box per page piece: its rows across the eight latent chunks
+          // one box per page piece: its rows across the latent chunks
           if (lane < tp.n)
-            tma_load_4d(smem + kOffV + slot * kVBytes + lane * 8 * int(box_bytes), &tmV, &bars[kVFull + slot], 0, 0,
-                        0, tp.row >> 3);
+            tma_load_4d(smem + SL::kOffV + slot * SL::kVBytes + lane * int(piece_bytes), &tmV, &bars[kVFull + slot],
+                        0, 0, 0, tp.row >> 3);
           __syncwarp();
           ++issued;
         }
         if (lane == 0)
-          for (int j = max(0, issued - kVSlots); j < issued; ++j)
-            if (!mbar_wait(&bars[kVFull + j % kVSlots], (j / kVSlots) & 1)) ok = false;
+          for (int j = max(0, issued - SL::kVSlots); j < issued; ++j)
+            if (!mbar_wait(&bars[kVFull + j % SL::kVSlots], (j / SL::kVSlots) & 1)) ok = false;
       }
       bad = __any_sync(kAll, bad);
       if (lane == 0) {
@@ -537,59 +627,126 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0 && ntiles > 0) {
       bool ok = true;
       if (logit_cta) {
-        // S(j) = Q K(j)^T over a 128-token tile: 32 N = 128 MMAs with the
-        // latent query from tensor memory, 4 with the rope query from shared
-        // memory, into S buffer j % 2, one group of three chunks at a time.
-        // Any shared-memory read (a barrier test included) issued between
-        // MMAs costs the issuing thread ~100 cycles, so the waits come once
-        // per group, not per chunk.
-        const uint32_t kb = smem_u32(smem + kOffK), qrope = smem_u32(smem + kOffQRope);
+        // S(j) = Q K(j)^T over a 128-token tile into S buffer j % 2, one ring
+        // slot (group) at a time.  bf16: 32 N = 128 MMAs (K = 16) with the
+        // latent query from tensor memory and 4 with the rope query from
+        // shared memory; e4m3: 16 (K = 32, kind::f8f6f4) and 2 over the
+        // 64-byte rope rows.  Any shared-memory read (a barrier test included)
+        // issued between MMAs costs the issuing thread ~100 cycles, so the
+        // waits come once per group, not per chunk.
+        const uint32_t kb = smem_u32(smem + SL::kOffK), qrope = smem_u32(smem + SL::kOffQRope);
         ok = mbar_wait(&bars[kQReady], 0);
         for (int j = 0; ok && j < nqt; ++j) {
           const int sb = j & 1;
           if (j >= 2) ok = mbar_wait(&bars[kSFree + sb], ((j >> 1) - 1) & 1);
           const uint32_t sd = tmem + kColS + 128u * uint32_t(sb);
 #pragma unroll
-          for (int gr = 0; gr < kKSlots; ++gr) {
-            if (ok) ok = mbar_wait(&bars[kKFull + gr], j & 1);
+          for (int gr = 0; gr < kGroups; ++gr) {
+            const int g = kGroups * j + gr, slot = g % SL::kKSlots;
+            if (ok) ok = mbar_wait(&bars[kKFull + slot], (g / SL::kKSlots) & 1);
             if (!ok) break;
             umma::fence_after_sync();
+            const uint32_t sbase = kb + SL::slot_off(slot);
+            if constexpr (F8) {
+              if (gr < 2) {
 #pragma unroll
-            for (int dk = 0; dk < kGroup; ++dk) {
-              const int k = kGroup * gr + dk;
-              // chunk dk of the group: 8-row atoms every kGroup KB
-              const uint32_t st = kb + gr * kGroupBytes + dk * 1024;
+                for (int dk = 0; dk < 2; ++dk) {
+                  const int k = 2 * gr + dk;  // 128-dim chunk of the latent
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t bdesc = umma::smem_desc(st + 32 * kk, 16, kGroup * 1024, umma::kSw128);
-                if (k < 8)
-                  umma::mma_ts(sd, tmem + kColQ + 32u * k + 8u * kk, bdesc, kIdescQK, (k | kk) != 0);
-                else
-                  umma::mma_ss(sd, umma::smem_desc(qrope + 32 * kk, 16, 1024, umma::kSw128), bdesc, kIdescQK,
-                               1u);
+                  for (int kk = 0; kk < 4; ++kk)
+                    umma::mma_ts_f8(sd, tmem + kColQ + 32u * k + 8u * kk,
+                                    umma::smem_desc(sbase + dk * 1024 + 32 * kk, 16, 2 * 1024, umma::kSw128),
+                                    kIdescQK, (k | kk) != 0);
+                }
+              } else {
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk)
+                  umma::mma_ss_f8(sd, umma::smem_desc(qrope + 32 * kk, 16, 512, umma::kSw64),
+                                  umma::smem_desc(sbase + 32 * kk, 16, 512, umma::kSw64), kIdescQK, 1u);
+              }
+            } else {
+#pragma unroll
+              for (int dk = 0; dk < 3; ++dk) {
+                const int k = 3 * gr + dk;
+                // chunk dk of the group: 8-row atoms every 3 KB
+                const uint32_t st = sbase + dk * 1024;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                  const uint64_t bdesc = umma::smem_desc(st + 32 * kk, 16, 3 * 1024, umma::kSw128);
+                  if (k < 8)
+                    umma::mma_ts(sd, tmem + kColQ + 32u * k + 8u * kk, bdesc, kIdescQK, (k | kk) != 0);
+                  else
+                    umma::mma_ss(sd, umma::smem_desc(qrope + 32 * kk, 16, 1024, umma::kSw128), bdesc, kIdescQK,
+                                 1u);
+                }
               }
             }
-            umma::commit(&bars[kKEmpty + gr]);  // the group's slot may refill
+            umma::commit(&bars[kKEmpty + slot]);  // the group's slot may refill
           }
           if (!ok) break;
           umma::commit(&bars[kSFull + sb]);
         }
-      } else {
-        // O += P(j) V(j): per 16 tokens, two N = 256 MMAs (O columns 0-255 and
-        // 256-511).  A tile whose factors are not all 1, or whose V rows run
-        // past the split's end, first goes to the warps (a request).
-        const uint32_t vb = smem_u32(smem + kOffV), pb = smem_u32(smem + kOffP);
-        const volatile uint32_t* fmsg = reinterpret_cast<const volatile uint32_t*>(smem + kOffF);
-        volatile int* req = flags + 2;
+      } else if constexpr (F8) {
+        // O += P(j) V(j) with the V tile the warps widened to f16: per 16
+        // tokens, two N = 256 MMAs.  Each tile's rescale decision goes to the
+        // warps through a two-slot ring (they read it before widening the tile
+        // after next); a rescale waits for every earlier P.V and then for the
+        // warps.
+        const uint32_t hb = smem_u32(smem + SL::kOffH), pb = smem_u32(smem + SL::kOffP);
+        const volatile uint32_t* fmsg = reinterpret_cast<const volatile uint32_t*>(smem + SL::kOffF);
+        volatile int* dec = flags + 4;
         int nreq = 0, nod = 0;
         for (int j = 0; ok && j < ntiles; ++j) {
-          const int p2 = j & 1, vs = j % kVSlots;
+          const int p2 = j & 1;
           ok = mbar_wait(&bars[kPFull + p2], (j >> 1) & 1);
           if (!ok) break;
           // the slot's next message (tile j + 2) is sent only after this P.V
           if (j + 2 < ntiles) mbar_arrive_expect_tx(&bars[kPFull + p2], kPMsg);
           const bool resc = j > 0 && fmsg[p2 * (kFBytes / 4) + kRows] != 0u;
-          ok = mbar_wait(&bars[kVFull + vs], (j / kVSlots) & 1);
+          if (resc) {  // O may change only once every earlier P.V is done
+            umma::commit(&bars[kODone]);
+            ok = mbar_wait(&bars[kODone], nod & 1);
+            ++nod;
+            if (!ok) break;
+          }
+          dec[p2] = resc ? 1 : 0;
+          mbar_arrive(&bars[kDec + p2]);
+          if (resc) {
+            ok = mbar_wait(&bars[kOReady], nreq & 1);
+            ++nreq;
+            if (!ok) break;
+          }
+          ok = mbar_wait(&bars[kHFull + p2], (j >> 1) & 1);
+          if (!ok) break;
+          umma::fence_after_sync();
+          const uint32_t pa = pb + p2 * kPBytes, va = hb + p2 * SL::kHBytes;
+          for (int kk = 0; kk < 4; ++kk)
+            for (int n = 0; n < 2; ++n)
+              umma::mma_ss(tmem + kColO + uint32_t(kHalf * n),
+                           umma::smem_desc(pa + 32 * kk, 16, 1024, umma::kSw128),
+                           // V, MN-major: 64-dim atoms 1 KB apart, 8-row groups 8 KB apart
+                           umma::smem_desc(va + 4 * n * 1024 + 2 * 8192 * kk, 1024, 8192, umma::kSw128),
+                           kIdescPV, (j | kk) != 0);
+          umma::commit(&bars[kHEmpty + p2]);
+          // the logit CTA may stage and send the P of tile j + 2
+          commit_to(&bars[kPSlotFree + p2], uint16_t(2u));
+        }
+      } else {
+        // O += P(j) V(j): per 16 tokens, two N = 256 MMAs (O columns 0-255 and
+        // 256-511).  A tile whose factors are not all 1, or whose V rows run
+        // past the split's end, first goes to the warps (a request).
+        const uint32_t vb = smem_u32(smem + SL::kOffV), pb = smem_u32(smem + SL::kOffP);
+        const volatile uint32_t* fmsg = reinterpret_cast<const volatile uint32_t*>(smem + SL::kOffF);
+        volatile int* req = flags + 2;
+        int nreq = 0, nod = 0;
+        for (int j = 0; ok && j < ntiles; ++j) {
+          const int p2 = j & 1, vs = j % SL::kVSlots;
+          ok = mbar_wait(&bars[kPFull + p2], (j >> 1) & 1);
+          if (!ok) break;
+          // the slot's next message (tile j + 2) is sent only after this P.V
+          if (j + 2 < ntiles) mbar_arrive_expect_tx(&bars[kPFull + p2], kPMsg);
+          const bool resc = j > 0 && fmsg[p2 * (kFBytes / 4) + kRows] != 0u;
+          ok = mbar_wait(&bars[kVFull + vs], (j / SL::kVSlots) & 1);
           if (!ok) break;
           const bool tail = t_begin + (j + 1) * kTok > t_end;
           if (resc || tail) {
@@ -606,7 +763,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!ok) break;
           }
           umma::fence_after_sync();
-          const uint32_t pa = pb + p2 * kPBytes, va = vb + vs * kVBytes;
+          const uint32_t pa = pb + p2 * kPBytes, va = vb + vs * SL::kVBytes;
           for (int kk = 0; kk < 4; ++kk)
             for (int n = 0; n < 2; ++n)
               umma::mma_ss(tmem + kColO + uint32_t(kHalf * n),
@@ -640,42 +797,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int t = 32 * q4 + lane;          // query row = TMEM lane
     const int st = tid - 32 * kSoftWarp0;  // 0 .. kSoft - 1
     const uint32_t lane_base = uint32_t(32 * q4) << 16;
-    const int i = t / a.Hq;  // row t = (spec token i, head t % Hq)
+    // row t = (spec token i, head t % Hq); rows at or past R are padding
+    // (zero query, never stored): they take the last token's window and mask
+    const bool real = t < a.R;
+    const int i = min(t / a.Hq, a.qs - 1);
     const float q_scale = ldscale(a.q_scale_dev, a.q_scale);
     const float kv_scale = ldscale(a.kv_scale_dev, a.kv_scale);
     const float lscale = a.softmax_scale * q_scale * kv_scale * kLog2e;
-    float* rowx = reinterpret_cast<float*>(smem + kOffRowX);  // [2][2][128]
+    float* rowx = reinterpret_cast<float*>(smem + SL::kOffRowX);  // [2][2][128]
     constexpr int kC = kTok / 2;  // logit columns per thread
 
     // ---- query: this thread's half of the latent row into tensor memory
-    // (dims [256h, 256h + 256) -> columns [128h, 128h + 128)), a quarter of
-    // the rope row into shared memory
+    // (bf16: dims [256h, 256h + 256) -> columns [128h, 128h + 128); e4m3: four
+    // codes per column, columns [64h, 64h + 64)), half of its rope part into
+    // shared memory (128- or 64-byte swizzled rows)
     {
-      const uint16_t* qrow = a.q + (int64_t(b) * a.qs * a.Hq + t) * kDim;
-      const uint4* src = reinterpret_cast<const uint4*>(qrow + kHalf * h);
-      // the rope quarter first, then the latent half in two rounds of 16
-      // loads in flight per thread
-      const uint4* rsrc = reinterpret_cast<const uint4*>(qrow + kLatent);
-      uint4 rq[4];
+      constexpr int kLB = F8 ? kLatent : 2 * kLatent;  // latent bytes of a query row
+      constexpr int kRB = F8 ? kRope : 2 * kRope;      // rope bytes
+      constexpr int kRU = kRB / 32;                    // rope 16-byte units per thread
+      const uint8_t* qrow = a.q + (int64_t(b) * a.qs * a.Hq + min(t, a.R - 1)) * (kLB + kRB);
+      const uint4* src = reinterpret_cast<const uint4*>(qrow + (kLB / 2) * h);
+      const uint4* rsrc = reinterpret_cast<const uint4*>(qrow + kLB) + kRU * h;
+      const uint4 zero = make_uint4(0, 0, 0, 0);
+      // the rope part first, then the latent half in rounds of 16 loads in
+      // flight per thread
+      uint4 rq[kRU];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) rq[u] = __ldg(rsrc + 4 * h + u);
+      for (int u = 0; u < kRU; ++u) rq[u] = real ? __ldg(rsrc + u) : zero;
 #pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
+      for (int half = 0; half < kLB / 512; ++half) {
         uint32_t w[64];
 #pragma unroll
         for (int v = 0; v < 16; ++v) {
-          const uint4 x = __ldg(src + half * 16 + v);
+          const uint4 x = real ? __ldg(src + half * 16 + v) : zero;
           w[4 * v + 0] = x.x;
           w[4 * v + 1] = x.y;
           w[4 * v + 2] = x.z;
           w[4 * v + 3] = x.w;
         }
-        umma::tmem_st32(tmem + lane_base + kColQ + 128u * h + 64u * half, w);
-        umma::tmem_st32(tmem + lane_base + kColQ + 128u * h + 64u * half + 32u, w + 32);
+        const uint32_t col = kColQ + uint32_t(kLB / 8) * uint32_t(h) + 64u * uint32_t(half);
+        umma::tmem_st32(tmem + lane_base + col, w);
+        umma::tmem_st32(tmem + lane_base + col + 32u, w + 32);
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        *reinterpret_cast<uint4*>(smem + kOffQRope + umma::sw128(t, 4 * h + u)) = rq[u];
+      for (int u = 0; u < kRU; ++u)
+        *reinterpret_cast<uint4*>(smem + SL::kOffQRope +
+                                  (F8 ? umma::sw64(t, kRU * h + u) : umma::sw128(t, kRU * h + u))) = rq[u];
       umma::tmem_st_wait();
       umma::fence_proxy_async_smem();
       umma::fence_before_sync();
@@ -683,8 +850,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars[kQReady]);
     }
 
-    const uint32_t p_peer = map_peer(smem_u32(smem + kOffP), peer);
-    const uint32_t f_peer = map_peer(smem_u32(smem + kOffF), peer);
+    const uint32_t p_peer = map_peer(smem_u32(smem + SL::kOffP), peer);
+    const uint32_t f_peer = map_peer(smem_u32(smem + SL::kOffF), peer);
     const int row_lb = a.win > 0 ? spec0 + i - a.win + 1 : INT_MIN;
     uint32_t row_mw = 0xffffffffu;
     if (a.mask) {
@@ -760,10 +927,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         l_half *= f;
         m_ref = m_new;
       }
-      // P (bf16) for this thread's 32 columns: units 4h..4h+3 of row t; the
-      // row sum takes the rounded weights so O / l stays a convex combination
-      uint8_t* pstage = smem + kOffPS + p2 * kPBytes;
-      float* fstage = reinterpret_cast<float*>(smem + kOffFS + p2 * kFBytes);
+      // P (bf16, or f16 against a widened e4m3 V) for this thread's 32
+      // columns: units 4h..4h+3 of row t; the row sum takes the rounded
+      // weights so O / l stays a convex combination
+      uint8_t* pstage = smem + SL::kOffPS + p2 * kPBytes;
+      float* fstage = reinterpret_cast<float*>(smem + SL::kOffFS + p2 * kFBytes);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         uint32_t w4[4];
@@ -771,8 +939,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 4; ++e) {
           const float p0 = m_ref == -INFINITY ? 0.f : ex2(s[8 * u + 2 * e] - m_ref);
           const float p1 = m_ref == -INFINITY ? 0.f : ex2(s[8 * u + 2 * e + 1] - m_ref);
-          w4[e] = pack_f32x2(p0, p1, true);
-          const float2 r = unpack_16x2(w4[e], true);
+          w4[e] = pack_f32x2(p0, p1, !F8);
+          const float2 r = unpack_16x2(w4[e], !F8);
           l_half += r.x + r.y;
         }
         *reinterpret_cast<uint4*>(pstage + umma::sw128(t, 4 * h + u)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
@@ -796,7 +964,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (!ok) flags[0] = 1;
     // ---- the final row maxima and sums go to the output CTA (also when this
     // split saw no key: m = -inf, l = 0)
-    float* fin = reinterpret_cast<float*>(smem + kOffFinS);
+    float* fin = reinterpret_cast<float*>(smem + SL::kOffFinS);
     named_bar(1, kSoft);
     rowx[h * kRows + t] = l_half;
     named_bar(1, kSoft);
@@ -807,7 +975,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     umma::fence_proxy_async_smem();
     named_bar(1, kSoft);
     if (st == 0) {
-      bulk_to_peer(map_peer(smem_u32(smem + kOffFin), peer), smem_u32(fin), kFinBytes, peer_bars + 8u * kFin);
+      bulk_to_peer(map_peer(smem_u32(smem + SL::kOffFin), peer), smem_u32(fin), kFinBytes, peer_bars + 8u * kFin);
       // the peer's completion signals for the last two P slots must land
       // before this CTA may exit
       for (int j = max(0, ntiles - 2); ok && j < ntiles; ++j)
@@ -825,29 +993,68 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int st = tid - 32 * kSoftWarp0;
     const uint32_t lane_base = uint32_t(32 * q4) << 16;
     const uint32_t o_cols = tmem + lane_base + kColO + uint32_t(kHalf * h);
-    const int i = t / a.Hq, hd = t % a.Hq;
+    const bool real = t < a.R;  // rows at or past R are padding: computed, never stored
+    const int i = min(t / a.Hq, a.qs - 1), hd = t % a.Hq;
     const float kv_scale = ldscale(a.kv_scale_dev, a.kv_scale);
     bool ok = true;
-    // Requests: rescale O by a tile's factors (every earlier P.V is done) and
-    // / or zero the V rows past the split's end (the V slot has landed).  The
-    // MMA thread waits for each request to be served before the next, so the
-    // request word and the factor slot are stable while the warps read them.
-    for (int k = 0;; ++k) {
-      ok = __all_sync(kAll, mbar_wait(&bars[kReq], k & 1));
-      if (!ok) break;
-      const int r = *reinterpret_cast<volatile int*>(flags + 2);
-      if (r == kReqEnd) break;
-      const int j = r & kReqTile;
-      umma::fence_after_sync();
-      if (r & kReqRescale) {
-        const float f = reinterpret_cast<const float*>(smem + kOffF + (j & 1) * kFBytes)[t];
-        if (__any_sync(kAll, f != 1.f)) rescale_o(o_cols, f);
+    if constexpr (F8) {
+      // Tile by tile: first the rescale decision for the previous tile (O is
+      // multiplied by that tile's factors once every earlier P.V is done; the
+      // MMA thread waits for it), then the e4m3 V tile widened to f16 (rows
+      // past the split's end zeroed) into the f16 slot freed by the P.V of
+      // the tile two back.  Then the end signal, which follows the drain.
+      volatile int* dec = flags + 4;
+      for (int j = 0; j <= ntiles; ++j) {
+        if (j > 0) {
+          const int jp = j - 1;
+          ok = __all_sync(kAll, mbar_wait(&bars[kDec + (jp & 1)], (jp >> 1) & 1));
+          if (!ok) break;
+          if (dec[jp & 1]) {
+            umma::fence_after_sync();
+            const float f = reinterpret_cast<const float*>(smem + SL::kOffF + (jp & 1) * kFBytes)[t];
+            if (__any_sync(kAll, f != 1.f)) rescale_o(o_cols, f);
+            umma::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kOReady]);
+          }
+        }
+        if (j == ntiles) break;
+        ok = __all_sync(kAll, mbar_wait(&bars[kVFull + j % SL::kVSlots], (j / SL::kVSlots) & 1));
+        if (ok && j >= 2) ok = __all_sync(kAll, mbar_wait(&bars[kHEmpty + (j & 1)], ((j >> 1) - 1) & 1));
+        if (!ok) break;
+        widen_v(smem + SL::kOffV + (j % SL::kVSlots) * SL::kVBytes, smem + SL::kOffH + (j & 1) * SL::kHBytes,
+                t_end - (t_begin + j * kTok), st);
+        umma::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bars[kVEmpty + j % SL::kVSlots]);
+          mbar_arrive(&bars[kHFull + (j & 1)]);
+        }
       }
-      if (r & kReqTail) zero_v_tail(smem + kOffV + (j % kVSlots) * kVBytes, max(0, t_end - (t_begin + j * kTok)), st);
-      umma::fence_proxy_async_smem();
-      umma::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kOReady]);
+      if (ok) ok = __all_sync(kAll, mbar_wait(&bars[kReq], 0));
+    } else {
+      // Requests: rescale O by a tile's factors (every earlier P.V is done) and
+      // / or zero the V rows past the split's end (the V slot has landed).  The
+      // MMA thread waits for each request to be served before the next, so the
+      // request word and the factor slot are stable while the warps read them.
+      for (int k = 0;; ++k) {
+        ok = __all_sync(kAll, mbar_wait(&bars[kReq], k & 1));
+        if (!ok) break;
+        const int r = *reinterpret_cast<volatile int*>(flags + 2);
+        if (r == kReqEnd) break;
+        const int j = r & kReqTile;
+        umma::fence_after_sync();
+        if (r & kReqRescale) {
+          const float f = reinterpret_cast<const float*>(smem + SL::kOffF + (j & 1) * kFBytes)[t];
+          if (__any_sync(kAll, f != 1.f)) rescale_o(o_cols, f);
+        }
+        if (r & kReqTail)
+          zero_v_tail(smem + SL::kOffV + (j % SL::kVSlots) * SL::kVBytes, max(0, t_end - (t_begin + j * kTok)), st);
+        umma::fence_proxy_async_smem();
+        umma::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kOReady]);
+      }
     }
     if (!ok) flags[0] = 1;
 
@@ -858,7 +1065,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ok = false;
     }
     umma::fence_after_sync();
-    const float* fin = reinterpret_cast<const float*>(smem + kOffFin);
+    const float* fin = reinterpret_cast<const float*>(smem + SL::kOffFin);
     const float m_fin = fin[t], l_fin = fin[kRows + t];
     if (ok) {
       const bool have_o = ntiles > 0;
@@ -868,7 +1075,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (single) {
         const float sig = a.sinks ? __ldg(a.sinks + hd) * kLog2e : -INFINITY;
         mul = finalize_row(m_fin, l_fin, sig, kv_scale * a.rcp_out_scale,
-                           (a.lse && h == 0) ? a.lse + row_g : nullptr);
+                           (a.lse && h == 0 && real) ? a.lse + row_g : nullptr);
       }
       const int64_t slot = persistent ? 2 * int64_t(k_cl) + (cl_first ? 0 : 1) : int64_t(b) * a.nsplit + split;
       float* wrow = a.ws + (slot * kRows + t) * (kLatent + 4);
@@ -884,6 +1091,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         const int col = kHalf * h + 32 * part;
         if (single) {
+          if (!real) continue;
           uint4* dst = reinterpret_cast<uint4*>(a.out + row_g * kLatent + col);
 #pragma unroll
           for (int v = 0; v < 4; ++v)
@@ -962,7 +1170,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const float sig = a.sinks ? __ldg(a.sinks + row % a.Hq) * kLog2e : -INFINITY;
     const int64_t row_g = (int64_t(b) * a.qs + row / a.Hq) * a.Hq + row % a.Hq;
     const float mul = finalize_row(M, l, sig, kv_scale * a.rcp_out_scale,
-                                   (a.lse && c == 0) ? a.lse + row_g : nullptr);
+                                   (a.lse && c == 0 && row < a.R) ? a.lse + row_g : nullptr);
     for (int sp = 0; sp < nvalid; ++sp) wts[row * nvalid + sp] *= mul;
   }
   __syncthreads();
@@ -1003,7 +1211,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 #pragma unroll
     for (int u = 0; u < kIt; ++u) {
-      if (base + u * kThreads >= kItems) continue;
+      if (base + u * kThreads >= kItems || rows[u] >= a.R) continue;
       const int ii = rows[u] / a.Hq, hh = rows[u] % a.Hq;
       const int64_t oi = ((int64_t(b) * a.qs + ii) * a.Hq + hh) * kLatent + cols[u];
       *reinterpret_cast<uint2*>(a.out + oi) =
@@ -1061,10 +1269,13 @@ const char* check_shape(const xqa_params* p, int v_head_dim) {
   if (p->num_kv_heads != 1) return "the MLA variant has one latent kv head (num_kv_heads must be 1)";
   if (p->head_dim != kDim || v_head_dim != kLatent)
     return "the MLA kernel is built for a 576-wide latent row (512 latent + 64 rope) with v_head_dim 512";
-  if (p->num_q_heads * p->q_seq_len != kRows)
-    return "the MLA kernel needs num_q_heads * q_seq_len == 128 (one UMMA tile of query rows)";
-  if (p->q_dtype != XQA_BF16 || p->kv_dtype != XQA_BF16)
-    return "the MLA kernel is built for bf16 query and latent cache";
+  if (int64_t(p->num_q_heads) * p->q_seq_len > kRows)
+    return "the MLA kernel needs num_q_heads * q_seq_len <= 128 (one UMMA tile of query rows)";
+  const bool bf16 = p->q_dtype == XQA_BF16 && p->kv_dtype == XQA_BF16;
+  const bool e4m3 = p->q_dtype == XQA_E4M3 && p->kv_dtype == XQA_E4M3;
+  if (!bf16 && !e4m3)
+    return "the MLA kernel takes a bf16 query with a bf16 latent cache, or an e4m3 query with an e4m3 cache";
+  if (p->out_dtype != XQA_BF16) return "the MLA kernel writes a bf16 output";
   if (p->kv_layout != XQA_NHD && p->kv_layout != XQA_HND) return "bad kv_layout";
   return nullptr;
 }
@@ -1165,44 +1376,61 @@ xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_b
     return XQA_ERR_CUDA;
   }
   // NHD and HND coincide for one kv head: rows of 576 elements, token-major.
-  // Row-group view (64 elements, 8 rows, 9 chunks, row groups): a box of one
-  // page piece's rows across several chunks lands as [row group][chunk][8
-  // rows][128 B].  Logit tiles take three chunks per box, V tiles eight.
+  // Row-group view (128 bytes, 8 rows, 128-byte chunks, row groups): a box of
+  // one page piece's rows across several chunks lands as [row group][chunk]
+  // [8 rows][128 B].  bf16: nine chunks of 64 dims; logit tiles take three
+  // chunks per box, V tiles eight.  e4m3: four chunks of 128 latent dims
+  // (logit tiles take two per box, V tiles four) and a separate 3-D view of
+  // the 64-byte rope part (64-byte swizzle).
+  const bool f8 = p->kv_dtype == XQA_E4M3;
+  const cuuint64_t elt = f8 ? 1 : 2, row_bytes = cuuint64_t(kDim) * elt;
   const cuuint32_t box_rows = cuuint32_t(std::min(p->page_size, kTok));
   const cuuint64_t nrows = cuuint64_t(p->page_size) * cuuint64_t(p->num_pages);
-  cuuint64_t dims[4] = {64, 8, cuuint64_t(kChunks), nrows / 8};
-  cuuint64_t strides[3] = {cuuint64_t(kDim) * 2, 128, cuuint64_t(kDim) * 2 * 8};
+  const CUtensorMapDataType dt = f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const cuuint32_t chunk_elems = cuuint32_t(128 / elt);
+  const cuuint64_t nchunks = f8 ? kLatent / 128 : kDim / 64;
+  cuuint64_t dims[4] = {chunk_elems, 8, nchunks, nrows / 8};
+  cuuint64_t strides[3] = {row_bytes, 128, row_bytes * 8};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUtensorMap tk, tv;
-  cuuint32_t kbox[4] = {64, 8, cuuint32_t(kGroup), box_rows / 8};
-  cuuint32_t vbox[4] = {64, 8, 8, box_rows / 8};
-  CUresult r = enc(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(p->k_cache), dims, strides, kbox,
-                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUtensorMap tk, tkr, tv;
+  cuuint32_t kbox[4] = {chunk_elems, 8, cuuint32_t(f8 ? Lay<true>::kGroupChunks : Lay<false>::kGroupChunks),
+                        box_rows / 8};
+  cuuint32_t vbox[4] = {chunk_elems, 8, cuuint32_t(f8 ? Lay<true>::kVChunks : Lay<false>::kVChunks), box_rows / 8};
+  CUresult r = enc(&tk, dt, 4, const_cast<void*>(p->k_cache), dims, strides, kbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r == CUDA_SUCCESS)
-    r = enc(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(p->k_cache), dims, strides, vbox, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    r = enc(&tv, dt, 4, const_cast<void*>(p->k_cache), dims, strides, vbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r == CUDA_SUCCESS && f8) {
+    // the rope part of each e4m3 row: (64 bytes, 8 rows, row groups) from byte 512 of the row
+    cuuint64_t rdims[3] = {kRope, 8, nrows / 8};
+    cuuint64_t rstrides[2] = {row_bytes, row_bytes * 8};
+    cuuint32_t rbox[3] = {kRope, 8, box_rows / 8};
+    r = enc(&tkr, dt, 3, static_cast<uint8_t*>(const_cast<void*>(p->k_cache)) + kLatent, rdims, rstrides, rbox, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    tkr = tk;  // unused by the bf16 kernel
+  }
   if (r != CUDA_SUCCESS) {
     snprintf(err, err_len, "cuTensorMapEncodeTiled failed (%d)", int(r));
     return XQA_ERR_CUDA;
   }
-  // L2 prefetch view of the same rows: (64 elements, 9 chunks, rows), so that
-  // one box covers a page piece's rows across all 576 dims
+  // L2 prefetch view of the same rows: (64 elements, 9 pieces, rows), so
+  // that one box covers a page piece's rows across all 576 dims
   CUtensorMap tpf;
-  cuuint64_t pdims[3] = {64, cuuint64_t(kChunks), cuuint64_t(p->page_size) * cuuint64_t(p->num_pages)};
-  cuuint64_t pstrides[2] = {128, cuuint64_t(kDim) * 2};
-  cuuint32_t pbox[3] = {64, cuuint32_t(kChunks), box_rows};
-  r = enc(&tpf, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p->k_cache), pdims, pstrides, pbox, estr,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  cuuint64_t pdims[3] = {64, kDim / 64, nrows};
+  cuuint64_t pstrides[2] = {64 * elt, row_bytes};
+  cuuint32_t pbox[3] = {64, kDim / 64, box_rows};
+  r = enc(&tpf, dt, 3, const_cast<void*>(p->k_cache), pdims, pstrides, pbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     snprintf(err, err_len, "cuTensorMapEncodeTiled (prefetch view) failed (%d)", int(r));
     return XQA_ERR_CUDA;
   }
   MlaArgs a;
   memset(&a, 0, sizeof a);
-  a.q = static_cast<const uint16_t*>(p->q);
+  a.q = static_cast<const uint8_t*>(p->q);
   a.out = static_cast<uint16_t*>(p->output);
   a.page_table = p->page_table;
   a.seq_lens = p->seq_lens;
@@ -1229,8 +1457,10 @@ xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_b
   a.kv_scale = p->kv_scale;
   a.softmax_scale = p->softmax_scale != 0.f ? p->softmax_scale : 1.0f / sqrtf(float(kDim));
   a.rcp_out_scale = p->rcp_out_scale;
-  a.q_bf16 = 1;
-  cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  a.R = p->num_q_heads * p->q_seq_len;
+  const int smem = f8 ? smem_bytes<true>() : smem_bytes<false>();
+  cudaError_t e = f8 ? cudaFuncSetAttribute(mla_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+                     : cudaFuncSetAttribute(mla_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) {
     snprintf(err, err_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     return XQA_ERR_CUDA;
@@ -1238,14 +1468,15 @@ xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_b
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = pl.persistent ? dim3(2 * pl.ncl, 1, 1) : dim3(2 * pl.nsplit, 1, p->batch_size);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmem;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = p->enable_pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, mla_decode_kernel, tk, tv, tpf, a);
+  e = f8 ? cudaLaunchKernelEx(&cfg, mla_decode_kernel<true>, tk, tkr, tv, tpf, a)
+         : cudaLaunchKernelEx(&cfg, mla_decode_kernel<false>, tk, tkr, tv, tpf, a);
   if (e != cudaSuccess) {
     snprintf(err, err_len, "MLA kernel launch: %s", cudaGetErrorString(e));
     return XQA_ERR_CUDA;

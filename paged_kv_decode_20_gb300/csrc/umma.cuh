@@ -1,6 +1,7 @@
 // tcgen05 (5th-generation tensor core) building blocks for sm_103a: tensor
-// memory allocation, shared-memory matrix descriptors, the kind::f16
-// instruction descriptor, MMA issue/commit and tensor-memory loads/stores.
+// memory allocation, shared-memory matrix descriptors, the kind::f16 and
+// kind::f8f6f4 (E4M3) instruction descriptors, MMA issue/commit and
+// tensor-memory loads/stores.
 #pragma once
 #include <stdint.h>
 
@@ -61,8 +62,15 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16, bool a
          (uint32_t(M >> 4) << 24);
 }
 
+// kind::f8f6f4 instruction descriptor with A and B both E4M3 (format code 0
+// at bits 7 and 10), fp32 accumulate; majors, N and M as in idesc_f16.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | (uint32_t(a_mn) << 15) | (uint32_t(b_mn) << 16) | (uint32_t(N >> 3) << 17) |
+         (uint32_t(M >> 4) << 24);
+}
+
 // ---------------------------------------------------------------- MMA
-// D[tmem] (+)= A[smem] * B[smem]
+// D[tmem] (+)= A[smem] * B[smem]; kind::f16 (16-bit A and B, one type)
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -72,13 +80,33 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// D[tmem] (+)= A[tmem] * B[smem]
+// D[tmem] (+)= A[tmem] * B[smem]; kind::f16
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]; kind::f8f6f4 (8-bit A and B, K = 32 per instruction)
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem]; kind::f8f6f4 (four 8-bit A elements per column)
+__device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -127,6 +155,12 @@ __device__ __forceinline__ void tmem_st_wait() {
 // rows are 128 bytes (the TMA SWIZZLE_128B pattern on a 1024-aligned base).
 __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t u) {
   return r * 128u + (((u ^ r) & 7u) << 4);
+}
+// Byte offset of 16-byte unit `u` (0..3) of row `r` in a 64-byte-swizzled tile
+// whose rows are 64 bytes (the TMA SWIZZLE_64B pattern on a 512-aligned base:
+// address bits 4-5 take an XOR with bits 7-8).
+__device__ __forceinline__ uint32_t sw64(uint32_t r, uint32_t u) {
+  return r * 64u + (((u ^ (r >> 1)) & 3u) << 4);
 }
 
 }  // namespace umma

@@ -85,7 +85,10 @@ struct Plan {
   size_t nsems = 0;
 };
 
-xqa_status validate_common(const xqa_params* p) {
+// mla: the latent variant, which also takes an e4m3 query with an e4m3 cache
+// (vLLM Kimi-K3 MultiHeadLatentAttention page, `_decode_concat_cache`: an fp8
+// cache takes an fp8 query) and then writes a bf16 output.
+xqa_status validate_common(const xqa_params* p, bool mla = false) {
   if (!p) return fail(XQA_ERR_INVALID_ARG, "params is NULL");
   if (!p->q || !p->k_cache || !p->v_cache || !p->page_table || !p->seq_lens || !p->output)
     return fail(XQA_ERR_INVALID_ARG, "q, k_cache, v_cache, page_table, seq_lens and output are required");
@@ -104,12 +107,21 @@ xqa_status validate_common(const xqa_params* p) {
   if (p->q_seq_len > 32)
     return fail(XQA_ERR_UNSUPPORTED, "q_seq_len > 32 is not supported (got %d)", p->q_seq_len);
   if (p->sliding_win_size < 0) return fail(XQA_ERR_INVALID_ARG, "sliding_win_size must be >= 0");
-  if (!is_16bit(p->q_dtype)) return fail(XQA_ERR_INVALID_ARG, "q dtype must be float16 or bfloat16");
-  if (!(p->kv_dtype == p->q_dtype || p->kv_dtype == XQA_E4M3))
-    return fail(XQA_ERR_INVALID_ARG, "kv dtype must match q's dtype or be float8_e4m3fn");
-  // the output dtype matches the query, or the fp8 cache (API page, `output`)
-  if (!(p->out_dtype == p->q_dtype || (p->out_dtype == XQA_E4M3 && p->kv_dtype == XQA_E4M3)))
-    return fail(XQA_ERR_UNSUPPORTED, "output dtype must equal the query dtype, or be float8_e4m3fn with an fp8 cache");
+  if (mla && p->q_dtype == XQA_E4M3) {
+    if (p->kv_dtype != XQA_E4M3) return fail(XQA_ERR_INVALID_ARG, "an e4m3 query needs an e4m3 latent cache");
+    if (p->out_dtype != XQA_BF16)
+      return fail(XQA_ERR_UNSUPPORTED, "the MLA decode of an e4m3 query writes a bf16 output");
+  } else {
+    if (!is_16bit(p->q_dtype))
+      return fail(XQA_ERR_INVALID_ARG, mla ? "q dtype must be float16, bfloat16 or (with an e4m3 cache) e4m3"
+                                           : "q dtype must be float16 or bfloat16");
+    if (!(p->kv_dtype == p->q_dtype || p->kv_dtype == XQA_E4M3))
+      return fail(XQA_ERR_INVALID_ARG, "kv dtype must match q's dtype or be float8_e4m3fn");
+    // the output dtype matches the query, or the fp8 cache (API page, `output`)
+    if (!(p->out_dtype == p->q_dtype || (p->out_dtype == XQA_E4M3 && p->kv_dtype == XQA_E4M3)))
+      return fail(XQA_ERR_UNSUPPORTED,
+                  "output dtype must equal the query dtype, or be float8_e4m3fn with an fp8 cache");
+  }
   if (p->head_dim < 1) return fail(XQA_ERR_INVALID_ARG, "head_dim must be >= 1");
   const int64_t big = int64_t(1) << 31;
   if (p->num_pages * std::max(p->page_size, p->num_kv_heads) >= big ||
@@ -377,7 +389,7 @@ size_t xqa_mla_semaphore_count(const xqa_params* p, int v_head_dim) {
 xqa_status xqa_mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_bytes,
                           uint32_t* sems, xqa_stream_t stream) {
   g_last_error[0] = 0;
-  xqa_status st = validate_common(p);
+  xqa_status st = validate_common(p, true);
   if (st != XQA_OK) return st;
   return xqa::mla_decode(p, v_head_dim, ws, ws_bytes, sems, reinterpret_cast<cudaStream_t>(stream),
                          g_last_error, sizeof g_last_error);

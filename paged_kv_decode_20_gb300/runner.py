@@ -19,7 +19,10 @@ class Decoder:
         self.case = case
         dev = case.q.device
         B, qs, Hq, _ = case.q.shape
-        self.output = torch.empty((B, qs, Hq, case.dv), dtype=out_dtype or case.q.dtype, device=dev)
+        # the output takes the query's dtype; an e4m3 query (MLA with an e4m3
+        # latent cache) writes bf16
+        default_out = torch.bfloat16 if case.q.dtype == torch.float8_e4m3fn else case.q.dtype
+        self.output = torch.empty((B, qs, Hq, case.dv), dtype=out_dtype or default_out, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev) if error_word else None
         self.lse = torch.empty((B, qs, Hq), dtype=torch.float32, device=dev) if lse else None
         kw = case.kwargs()

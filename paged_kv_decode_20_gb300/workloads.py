@@ -153,13 +153,14 @@ def full_spec_mask(batch, q_seq_len, device="cpu"):
 
 def make_case(*, batch, num_q_heads, num_kv_heads, head_dim, page_size, seq_lens,
               kv_layout="NHD", q_dtype=torch.bfloat16, kv_dtype=None, q_seq_len=1,
-              v_head_dim=None, mla=False, q_scale=1.0, kv_scale=1.0, kv_divisor=1.0,
+              v_head_dim=None, mla=False, q_scale=1.0, kv_scale=1.0, kv_divisor=1.0, q_divisor=1.0,
               softmax_scale=None, sinks=False, sliding_win_size=0, mask=None,
               rcp_out_scale=1.0, pool_pages=None, pages_per_seq=None, seed=0,
               device="cpu", poison=True, q_mult=1.0, name="case"):
     """Build one seeded problem.  seq_lens: list of ints.  mask: None,
     "causal" or "full".  kv_divisor: K/V drawn as N(0,1)/kv_divisor before the
-    cast to kv_dtype (the fp8 recipe uses 1/kv_scale)."""
+    cast to kv_dtype (the fp8 recipe uses 1/kv_scale); q_divisor likewise for
+    q (an e4m3 query is drawn as N(0,1)/q_scale)."""
     kv_dtype = q_dtype if kv_dtype is None else kv_dtype
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
@@ -182,7 +183,7 @@ def make_case(*, batch, num_q_heads, num_kv_heads, head_dim, page_size, seq_lens
         table[b, :n] = perm[off:off + n].to(torch.int32)
         off += n
 
-    q = _randn_as((batch, q_seq_len, num_q_heads, head_dim), q_dtype, gen, device)
+    q = _randn_as((batch, q_seq_len, num_q_heads, head_dim), q_dtype, gen, device, divisor=q_divisor)
     if q_mult != 1.0:
         q = (q.float() * q_mult).to(q_dtype)
     if kv_layout.upper() == "NHD":
@@ -253,11 +254,20 @@ WORKLOADS = {
        "L~U[2048,16384] W128 q_seq_len4 causal mask NHD bf16)",
     5: "MLA latent decode (B64 Hq128 latent 576/512 ps64 L~U[4096,32768] bf16)",
 }
+# The e4m3 variant of workload 5: the same shapes and lengths with an e4m3
+# latent cache and an e4m3 query (vLLM Kimi-K3 MultiHeadLatentAttention page:
+# an fp8 cache takes an fp8 query), both drawn as N(0,1)/scale with
+# q_scale = kv_scale = 0.05 (the fp8 recipe of workload 3).
+WORKLOAD_5_E4M3 = ("MLA latent decode, e4m3 latent cache and query (B64 Hq128 latent 576/512 ps64 "
+                   "L~U[4096,32768] q_scale=kv_scale=0.05)")
 
 
-def workload(idx, device="cpu", poison=True, batch=None):
+def workload(idx, device="cpu", poison=True, batch=None, kv_dtype=None):
     """The named workload idx (1..5); `batch` truncates B for smaller runs
-    while keeping every other size."""
+    while keeping every other size.  kv_dtype=torch.float8_e4m3fn with idx 5
+    gives its e4m3 variant (e4m3 latent cache and query)."""
+    if kv_dtype is not None and not (idx == 5 and kv_dtype == torch.float8_e4m3fn):
+        raise ValueError("only workload 5 has a kv_dtype variant (torch.float8_e4m3fn)")
     seed = idx
     if idx == 1:
         # 16-page pool, seq0 takes 3 pages and seq1 takes 7.
@@ -289,9 +299,13 @@ def workload(idx, device="cpu", poison=True, batch=None):
     if idx == 5:
         B = 64
         lens = _uniform_lens(4096, 32768, B, seed)[: batch or B]
+        f8 = kv_dtype == torch.float8_e4m3fn
+        dt = torch.float8_e4m3fn if f8 else torch.bfloat16
+        scale = 0.05 if f8 else 1.0
         return make_case(batch=len(lens), num_q_heads=128, num_kv_heads=1, head_dim=576,
                          v_head_dim=512, mla=True, page_size=64, seq_lens=lens,
-                         kv_layout="NHD", softmax_scale=(128 + 64) ** -0.5,
-                         pages_per_seq=32768 // 64, seed=seed, device=device, poison=poison,
-                         name="mla_latent_decode")
+                         kv_layout="NHD", softmax_scale=(128 + 64) ** -0.5, q_dtype=dt,
+                         kv_dtype=dt, q_scale=scale, kv_scale=scale, q_divisor=scale,
+                         kv_divisor=scale, pages_per_seq=32768 // 64, seed=seed, device=device,
+                         poison=poison, name="mla_latent_decode_e4m3" if f8 else "mla_latent_decode")
     raise ValueError(f"unknown workload {idx}")

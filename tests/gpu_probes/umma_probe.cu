@@ -27,9 +27,23 @@ __device__ void fill_rows(uint8_t* dst, const __nv_bfloat16* src, int rows, int 
   }
 }
 
+// rows of 64 bytes with the 64-byte swizzle (row r of the tile = src row r)
+__device__ void fill_rows64(uint8_t* dst, const uint8_t* src, int rows) {
+  for (int idx = threadIdx.x; idx < rows * 4; idx += blockDim.x) {
+    const int r = idx >> 2, u = idx & 3;
+    const uint4 v = *reinterpret_cast<const uint4*>(src + size_t(r) * 64 + 16 * u);
+    *reinterpret_cast<uint4*>(dst + umma::sw64(r, u)) = v;
+  }
+}
+
 // mode 0: D[128x64] = A . B^T, A and B K-major in shared memory
 // mode 1: D[128x256] = A . V, V [64 x 256] MN-major (4 chunks of 64 columns)
 // mode 2: D[128x64] = A . B^T with A in tensor memory
+// mode 3: as mode 0 with E4M3 A [128 x 128] and B [64 x 128] (kind::f8f6f4,
+//         K = 32 per instruction, 128-byte swizzle)
+// mode 4: as mode 3 with A in tensor memory (four codes per column)
+// mode 5: E4M3 A [128 x 64] and B [64 x 64], rows of 64 bytes with the 64-byte swizzle
+// mode 6: as mode 1 with f16 A and V
 __global__ void probe_kernel(int mode, const __nv_bfloat16* A, const __nv_bfloat16* B, float* D,
                              int lbo, int sbo, int* status) {
   extern __shared__ uint8_t smraw[];
@@ -45,19 +59,25 @@ __global__ void probe_kernel(int mode, const __nv_bfloat16* A, const __nv_bfloat
     mbar_init(bar, 1);
     fence_mbar_init();
   }
-  fill_rows(sm + kA, A, 128, 64, 0);
-  if (mode == 1) {
-    for (int c = 0; c < 4; ++c) fill_rows(sm + kB + c * 8192, B, 64, 256, 64 * c);
+  if (mode == 5) {
+    fill_rows64(sm + kA, reinterpret_cast<const uint8_t*>(A), 128);
+    fill_rows64(sm + kB, reinterpret_cast<const uint8_t*>(B), 64);
   } else {
-    fill_rows(sm + kB, B, 64, 64, 0);
+    // (an E4M3 row of 128 codes is 128 bytes, filled like 64 16-bit elements)
+    fill_rows(sm + kA, A, 128, 64, 0);
+    if (mode == 1 || mode == 6) {
+      for (int c = 0; c < 4; ++c) fill_rows(sm + kB + c * 8192, B, 64, 256, 64 * c);
+    } else {
+      fill_rows(sm + kB, B, 64, 64, 0);
+    }
   }
   umma::fence_proxy_async_smem();
   umma::fence_before_sync();
   __syncthreads();
   umma::fence_after_sync();
   const uint32_t tmem = *tslot;
-  const int N = mode == 1 ? 256 : 64;
-  if (mode == 2) {
+  const int N = (mode == 1 || mode == 6) ? 256 : 64;
+  if (mode == 2 || mode == 4) {
     // row t of A into lane t, columns 256.. (two bf16 per 32-bit column)
     uint32_t w[32];
     const uint32_t* src = reinterpret_cast<const uint32_t*>(A + size_t(threadIdx.x) * 64);
@@ -79,9 +99,25 @@ __global__ void probe_kernel(int mode, const __nv_bfloat16* A, const __nv_bfloat
         umma::mma_ss(tmem, umma::smem_desc(a0 + 32 * k, 16, 1024, umma::kSw128),
                      umma::smem_desc(b0 + 2048 * k, lbo, sbo, umma::kSw128),
                      umma::idesc_f16(128, 256, true, false, true), k > 0);
-      } else {
+      } else if (mode == 2) {
         umma::mma_ts(tmem, tmem + 256 + 8 * k, umma::smem_desc(b0 + 32 * k, 16, 1024, umma::kSw128),
                      umma::idesc_f16(128, 64, true, false, false), k > 0);
+      } else if (mode == 3) {
+        umma::mma_ss_f8(tmem, umma::smem_desc(a0 + 32 * k, 16, 1024, umma::kSw128),
+                        umma::smem_desc(b0 + 32 * k, 16, 1024, umma::kSw128),
+                        umma::idesc_e4m3(128, 64, false, false), k > 0);
+      } else if (mode == 4) {
+        umma::mma_ts_f8(tmem, tmem + 256 + 8 * k, umma::smem_desc(b0 + 32 * k, 16, 1024, umma::kSw128),
+                        umma::idesc_e4m3(128, 64, false, false), k > 0);
+      } else if (mode == 5) {
+        if (k < 2)
+          umma::mma_ss_f8(tmem, umma::smem_desc(a0 + 32 * k, 16, 512, umma::kSw64),
+                          umma::smem_desc(b0 + 32 * k, 16, 512, umma::kSw64),
+                          umma::idesc_e4m3(128, 64, false, false), k > 0);
+      } else {
+        umma::mma_ss(tmem, umma::smem_desc(a0 + 32 * k, 16, 1024, umma::kSw128),
+                     umma::smem_desc(b0 + 2048 * k, lbo, sbo, umma::kSw128),
+                     umma::idesc_f16(128, 256, false, false, true), k > 0);
       }
     }
     umma::commit(bar);

@@ -1,7 +1,8 @@
 """GPU parity of the MLA latent decode kernel (one 576-wide latent kv head, V =
 its first 512 elements; vLLM Kimi-K3 MultiHeadLatentAttention page) against
-the float64 oracle on identical seeded inputs.  Tolerance: max-abs 1e-2 and
-relative L2 1e-2 (bf16 output; P rounded to bf16 before P.V)."""
+the float64 oracle on identical seeded inputs.  Tolerance: max-abs 1e-2 (bf16
+cache) or 3e-2 (e4m3 cache and query, the fp8 bound) and relative L2 1e-2
+(bf16 output; P rounded to bf16, or to f16 against the widened e4m3 V)."""
 
 import pytest
 import torch
@@ -23,7 +24,15 @@ def _built():
     B.build()
 
 
-def mla_case(lens, ps=64, seed=0, heads=128, qs=1, **kw):
+F8 = torch.float8_e4m3fn
+TOL_F8 = 3e-2
+
+
+def mla_case(lens, ps=64, seed=0, heads=128, qs=1, dtype=torch.bfloat16, **kw):
+    if dtype == F8:
+        # e4m3 latent cache and query drawn as N(0,1)/scale (the fp8 recipe)
+        kw = dict(dict(q_dtype=F8, kv_dtype=F8, q_scale=0.05, kv_scale=0.05, q_divisor=0.05,
+                       kv_divisor=0.05), **kw)
     return W.make_case(batch=len(lens), num_q_heads=heads, num_kv_heads=1, head_dim=576,
                        v_head_dim=512, mla=True, page_size=ps, seq_lens=lens, kv_layout="NHD",
                        q_seq_len=qs, softmax_scale=SCALE, seed=seed, **kw)
@@ -102,3 +111,83 @@ def test_mla_large_batch_takes_fixed_splits():
     g = torch.Generator().manual_seed(13)
     lens = torch.randint(1, 160, (260,), generator=g).tolist()
     run_and_compare(mla_case(lens, ps=64, seed=14), runs=1, out_round=True)
+
+
+# ---------------------------------------------------------------- padded query rows
+@pytest.mark.parametrize("heads,qs", [(16, 1), (32, 1), (64, 1), (32, 2), (24, 3)])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, F8], ids=["bf16", "e4m3"])
+def test_mla_fewer_than_128_query_rows(heads, qs, dtype):
+    """Tensor-parallel shards of the heads (num_local_heads = num_heads / tp)
+    run as a 128-row tile whose rows past heads x q_seq_len are padding: never
+    stored, no lse written (checked by NaN-filled outputs and lse)."""
+    from paged_kv_decode_20_gb300.runner import Decoder
+    c = mla_case([700, 65, 2000], seed=20 + heads + qs, heads=heads, qs=qs, dtype=dtype, sinks=True,
+                 mask="causal" if qs > 1 else None)
+    run_and_compare(c, tol=TOL_F8 if dtype == F8 else TOL)
+    dec = Decoder(c.to("cuda"), lse=True)
+    dec.lse.fill_(float("nan"))
+    dec.run()
+    _, ref_lse = oracle.xqa_attention(c.q, c.k_cache, c.v_cache, c.page_table, c.seq_lens,
+                                      return_lse=True, **c.kwargs())
+    torch.cuda.synchronize()
+    assert (dec.lse.cpu().double() - ref_lse).abs().max().item() <= 3e-3
+
+
+# ---------------------------------------------------------------- e4m3 latent cache and query
+def test_mla_e4m3_workload_first_sequences():
+    run_and_compare(W.workload(5, batch=2, kv_dtype=F8), tol=TOL_F8)
+
+
+@pytest.mark.parametrize("ps", [16, 32, 64, 128])
+def test_mla_e4m3_page_sizes(ps):
+    run_and_compare(mla_case([1, 63, 64, 65, 700], ps=ps, seed=40 + ps, dtype=F8), tol=TOL_F8)
+
+
+@pytest.mark.parametrize("sm_count", [2, 40, 1000])
+def test_mla_e4m3_split_counts(sm_count):
+    run_and_compare(mla_case([5000, 130], seed=43, dtype=F8), tol=TOL_F8, sm_count=sm_count)
+
+
+def test_mla_e4m3_peaked_rows_force_rescales():
+    # (q x 2.5 keeps the e4m3 query inside its finite range: |q| <= ~250)
+    run_and_compare(mla_case([3000, 77], seed=44, dtype=F8, q_mult=2.5), tol=TOL_F8, out_round=True)
+
+
+def test_mla_e4m3_sinks_window_and_spec_tokens():
+    c = mla_case([900, 300], seed=45, heads=64, qs=2, dtype=F8, sinks=True, sliding_win_size=200,
+                 mask="causal")
+    run_and_compare(c, tol=TOL_F8)
+
+
+def test_mla_e4m3_empty_and_nan_poison():
+    c = mla_case([0, 1, 129], seed=46, pool_pages=12, poison=True, dtype=F8)
+    run_and_compare(c, tol=TOL_F8)
+
+
+def test_mla_e4m3_scales_from_device_and_output_scale():
+    """q_scale and kv_scale as device scalars, rcp_out_scale != 1."""
+    from paged_kv_decode_20_gb300 import xqa as X
+    c = mla_case([1500, 40], seed=47, dtype=F8, rcp_out_scale=0.5).to("cuda")
+    out = torch.empty((2, 1, 128, 512), dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(1 << 26, dtype=torch.uint8, device="cuda")
+    sems = torch.zeros(4, dtype=torch.int32, device="cuda")
+    X.xqa_mla(c.q, c.k_cache, c.page_table, c.seq_lens, out, ws, sems, page_size=64, v_head_dim=512,
+              softmax_scale=SCALE, q_scale=torch.tensor([0.05], device="cuda"),
+              kv_scale=torch.tensor([0.05], device="cuda"), rcp_out_scale=0.5)
+    torch.cuda.synchronize()
+    cc = c.to("cpu")
+    ref = oracle.xqa_attention(cc.q, cc.k_cache, cc.v_cache, cc.page_table, cc.seq_lens, **cc.kwargs())
+    assert (out.cpu().double() - ref).abs().max().item() <= TOL_F8
+
+
+def test_mla_e4m3_persistent_clusters_loop_over_many_sequences():
+    g = torch.Generator().manual_seed(48)
+    lens = torch.randint(0, 400, (60,), generator=g).tolist()
+    lens[:6] = [0, 1, 63, 64, 65, 0]
+    run_and_compare(mla_case(lens, ps=32, seed=49, dtype=F8), tol=TOL_F8, sm_count=8)
+
+
+def test_mla_e4m3_large_batch_takes_fixed_splits():
+    g = torch.Generator().manual_seed(50)
+    lens = torch.randint(1, 160, (260,), generator=g).tolist()
+    run_and_compare(mla_case(lens, ps=64, seed=51, dtype=F8), tol=TOL_F8, runs=1, out_round=True)

@@ -60,3 +60,36 @@ def test_a_from_tensor_memory(probe):
     A, B = _rand(128, 64, seed=5), _rand(64, 64, seed=6)
     D = _run(probe, 2, A, B, 64)
     torch.testing.assert_close(D, A.float() @ B.float().T, rtol=1e-4, atol=1e-3)
+
+
+def _rand_e4m3(*shape, seed):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    return (torch.randn(*shape, generator=g, device="cuda") * 4).to(torch.float8_e4m3fn)
+
+
+def test_e4m3_kmajor_ss(probe):
+    """kind::f8f6f4 with E4M3 A and B, K-major, 128-byte swizzle: four K = 32 steps."""
+    A, B = _rand_e4m3(128, 128, seed=7), _rand_e4m3(64, 128, seed=8)
+    D = _run(probe, 3, A, B, 64)
+    torch.testing.assert_close(D, A.float() @ B.float().T, rtol=1e-4, atol=1e-3)
+
+
+def test_e4m3_a_from_tensor_memory(probe):
+    A, B = _rand_e4m3(128, 128, seed=9), _rand_e4m3(64, 128, seed=10)
+    D = _run(probe, 4, A, B, 64)
+    torch.testing.assert_close(D, A.float() @ B.float().T, rtol=1e-4, atol=1e-3)
+
+
+def test_e4m3_kmajor_64_byte_swizzle(probe):
+    """64-byte rows (the rope part of an E4M3 latent row) with the 64-byte swizzle."""
+    A, B = _rand_e4m3(128, 64, seed=11), _rand_e4m3(64, 64, seed=12)
+    D = _run(probe, 5, A, B, 64)
+    torch.testing.assert_close(D, A.float() @ B.float().T, rtol=1e-4, atol=1e-3)
+
+
+def test_f16_b_mn_major(probe):
+    g = torch.Generator(device="cuda").manual_seed(13)
+    A = torch.rand(128, 64, generator=g, device="cuda").to(torch.float16)
+    V = torch.randn(64, 256, generator=g, device="cuda").to(torch.float16)
+    D = _run(probe, 6, A, V, 256, lbo=8192, sbo=1024)
+    torch.testing.assert_close(D, A.float() @ V.float(), rtol=1e-4, atol=1e-3)
