@@ -223,7 +223,14 @@ xqa_status xqa_merge_attn_states(const xqa_merge_params* params, xqa_stream_t st
    [num_slots, Lr + R] (num_pages * page_size rows of the latent cache, NHD);
    q_out [T, H, Lr + R] contiguous.  Lr and R multiples of 8, strides multiples
    of 8 elements, tensors 16-byte aligned.  Asynchronous on `stream`; returns
-   XQA_ERR_INVALID_ARG before any launch for malformed arguments. */
+   XQA_ERR_INVALID_ARG before any launch for malformed arguments.
+   fp8 != 0 is the plain per-tensor fp8 cache of the same page's
+   `_decode_concat_cache` (an fp8 cache takes an fp8 query): q_out and kv_cache
+   are then float8_e4m3fn, and every element written is x * q_scale_inv (query)
+   or x * cache_scale_inv (cache row), x the fp32 value above, rounded to
+   nearest even and saturated at +-448.  q_scale_inv and cache_scale_inv are
+   device fp32 scalars (the reciprocals of q_scale and kv_scale), required
+   then; the inputs stay bf16. */
 typedef struct xqa_mla_prep_params {
   const void* ql_nope;
   int64_t ql_stride_token, ql_stride_head;
@@ -245,6 +252,9 @@ typedef struct xqa_mla_prep_params {
   int32_t kv_lora_rank;        /* Lr */
   int32_t rope_dim;            /* R */
   uint32_t* error_word;        /* optional */
+  int32_t fp8;                 /* 0: bf16 q_out and cache; else e4m3 (see above) */
+  const float* q_scale_inv;    /* device scalar, fp8 only */
+  const float* cache_scale_inv; /* device scalar, fp8 only */
 } xqa_mla_prep_params;
 
 xqa_status xqa_mla_decode_prep(const xqa_mla_prep_params* params, xqa_stream_t stream);

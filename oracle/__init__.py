@@ -257,3 +257,27 @@ def mla_decode_prep(ql_nope, q_pe, kv_c, k_pe, positions, cos_sin_cache, slot_ma
             cache[slot, :Lr] = kc[t]
             cache[slot, Lr:] = rope_pairs(kp[t], c, s)
     return q, cache
+
+
+def mla_decode_prep_e4m3(ql_nope, q_pe, kv_c, k_pe, positions, cos_sin_cache, slot_mapping, kv_cache,
+                         q_scale_inv, cache_scale_inv):
+    """The fused decode prep for a plain per-tensor fp8 latent cache (Kimi-K3
+    MultiHeadLatentAttention page, `_decode_concat_cache`: an fp8 cache takes
+    an fp8 query, quantised with q_scale_inv, the inserted latent row with
+    cache_scale_inv).  The float64 values of ``mla_decode_prep`` times the
+    inverse scale, encoded as E4M3 (``encode_e4m3``: nearest even, saturated
+    at +-448).  kv_cache: uint8 codes [num_slots, Lr + R] (not modified).
+
+    Returns (q codes uint8 [T, H, Lr + R], cache codes uint8 with the rows
+    written at their slots)."""
+    codes = _cpu_contig(kv_cache).view(torch.uint8).reshape(-1, kv_cache.shape[-1])
+    q64, cache64 = mla_decode_prep(ql_nope, q_pe, kv_c, k_pe, positions, cos_sin_cache, slot_mapping,
+                                   torch.zeros(codes.shape, dtype=torch.float64))
+    T, H, W = q64.shape
+    q_codes = encode_e4m3(q64 * float(q_scale_inv)).reshape(T, H, W)
+    out = codes.clone()
+    for t in range(T):
+        slot = int(slot_mapping[t])
+        if slot >= 0:
+            out[slot] = encode_e4m3(cache64[slot] * float(cache_scale_inv))
+    return q_codes, out

@@ -5,11 +5,15 @@
 // the GPT-J (non-neox) pairing of get_rope(..., is_neox_style=False), computed
 // in fp32 from the fp32 cos/sin table (the page's fused epilogues read that
 // table directly in fp32).  A streaming op: one thread per 8-element output
-// chunk, 16-byte loads and stores.
+// chunk, 16-byte loads and stores.  The fp8 variant (a plain per-tensor fp8
+// cache takes an fp8 query, same page) multiplies each fp32 value by the
+// query's or the cache's inverse scale and rounds it to e4m3 (8-byte stores).
 #include <cuda_runtime.h>
 #include <stdarg.h>
 #include <stdint.h>
 #include <stdio.h>
+
+#include <cuda_fp8.h>
 
 #include "ptx.cuh"
 #include "xqa.h"
@@ -28,9 +32,11 @@ struct PrepArgs {
   const int64_t* pos;
   const float* cs;
   const int64_t* slots;
-  uint16_t* cache;
-  uint16_t* qout;
+  void* cache;   // bf16 or (fp8) e4m3 rows of W elements
+  void* qout;
   uint32_t* err;
+  const float* q_inv;      // fp8: device scalars multiplying the query and the cache row
+  const float* cache_inv;
   int64_t ql_st, ql_sh, qpe_st, qpe_sh, kvc_st, kpe_st, max_pos, num_slots, T;
   int H, Lr, R, W;          // W = Lr + R
   int64_t q_chunks, chunks;  // query chunks, then cache chunks
@@ -50,6 +56,40 @@ __device__ __forceinline__ uint4 rope8(uint4 x, const float* cs, int R, int p0, 
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// The same rotation in fp32, all eight values returned (the e4m3 variant
+// scales them before it rounds).
+__device__ __forceinline__ void rope8f(uint4 x, const float* cs, int R, int p0, bool rotate, float* out) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 v = unpack_16x2(w[k], true);
+    if (rotate) {
+      const float c = __ldg(cs + p0 + k), s = __ldg(cs + R / 2 + p0 + k);
+      out[2 * k] = v.x * c - v.y * s;
+      out[2 * k + 1] = v.y * c + v.x * s;
+    } else {
+      out[2 * k] = v.x;
+      out[2 * k + 1] = v.y;
+    }
+  }
+}
+
+// Eight fp32 values times `mul`, rounded to nearest even into e4m3 and
+// saturated at +-448, as one 8-byte word (element k in byte k).
+__device__ __forceinline__ uint2 to_e4m3x8(const float* v, float mul) {
+  uint32_t w[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const uint32_t lo =
+        __nv_cvt_float2_to_fp8x2(make_float2(v[4 * k] * mul, v[4 * k + 1] * mul), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi =
+        __nv_cvt_float2_to_fp8x2(make_float2(v[4 * k + 2] * mul, v[4 * k + 3] * mul), __NV_SATFINITE, __NV_E4M3);
+    w[k] = (lo & 0xffffu) | (hi << 16);
+  }
+  return make_uint2(w[0], w[1]);
+}
+
+template <bool F8>
 __global__ void __launch_bounds__(kThreads) prep_kernel(const PrepArgs a) {
   const int64_t idx = int64_t(blockIdx.x) * kThreads + threadIdx.x;
   if (idx >= a.chunks) return;
@@ -72,6 +112,29 @@ __global__ void __launch_bounds__(kThreads) prep_kernel(const PrepArgs a) {
       atomicOr(a.err, 1u);
     }
   }
+  if constexpr (F8) {
+    int64_t dst_row = row;
+    uint8_t* dst_base = static_cast<uint8_t*>(a.qout);
+    if (!is_q) {
+      const int64_t slot = a.slots[t];
+      if (slot < 0) return;  // padding token: nothing to insert
+      if (slot >= a.num_slots) {
+        if (a.err && e == 0) atomicOr(a.err, 1u);
+        return;
+      }
+      dst_row = slot;
+      dst_base = static_cast<uint8_t*>(a.cache);
+    }
+    const uint4 x = e < a.Lr ? __ldg(reinterpret_cast<const uint4*>(is_q ? a.ql + t * a.ql_st + h * a.ql_sh + e
+                                                                         : a.kvc + t * a.kvc_st + e))
+                             : __ldg(reinterpret_cast<const uint4*>(
+                                   is_q ? a.qpe + t * a.qpe_st + h * a.qpe_sh + (e - a.Lr)
+                                        : a.kpe + t * a.kpe_st + (e - a.Lr)));
+    float v[8];
+    rope8f(x, cs, a.R, (e - a.Lr) >> 1, e >= a.Lr && rotate, v);
+    *reinterpret_cast<uint2*>(dst_base + dst_row * a.W + e) = to_e4m3x8(v, __ldg(is_q ? a.q_inv : a.cache_inv));
+    return;
+  }
   if (is_q) {
     uint4 v;
     if (e < a.Lr)
@@ -79,7 +142,7 @@ __global__ void __launch_bounds__(kThreads) prep_kernel(const PrepArgs a) {
     else
       v = rope8(__ldg(reinterpret_cast<const uint4*>(a.qpe + t * a.qpe_st + h * a.qpe_sh + (e - a.Lr))), cs,
                 a.R, (e - a.Lr) >> 1, rotate);
-    *reinterpret_cast<uint4*>(a.qout + row * a.W + e) = v;
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.qout) + row * a.W + e) = v;
   } else {
     const int64_t slot = a.slots[t];
     if (slot < 0) return;  // padding token: nothing to insert
@@ -93,7 +156,7 @@ __global__ void __launch_bounds__(kThreads) prep_kernel(const PrepArgs a) {
     else
       v = rope8(__ldg(reinterpret_cast<const uint4*>(a.kpe + t * a.kpe_st + (e - a.Lr))), cs, a.R,
                 (e - a.Lr) >> 1, rotate);
-    *reinterpret_cast<uint4*>(a.cache + slot * a.W + e) = v;
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.cache) + slot * a.W + e) = v;
   }
 }
 
@@ -136,6 +199,10 @@ extern "C" xqa_status xqa_mla_decode_prep(const xqa_mla_prep_params* p, xqa_stre
     return prep_fail(XQA_ERR_INVALID_ARG, "positions and slot_mapping must be 8-byte aligned");
   if (reinterpret_cast<uintptr_t>(p->error_word) & 3)
     return prep_fail(XQA_ERR_INVALID_ARG, "error_word must be 4-byte aligned");
+  if (p->fp8 && (!p->q_scale_inv || !p->cache_scale_inv))
+    return prep_fail(XQA_ERR_INVALID_ARG, "the fp8 prep needs q_scale_inv and cache_scale_inv (device scalars)");
+  if ((reinterpret_cast<uintptr_t>(p->q_scale_inv) | reinterpret_cast<uintptr_t>(p->cache_scale_inv)) & 3)
+    return prep_fail(XQA_ERR_INVALID_ARG, "q_scale_inv and cache_scale_inv must be 4-byte aligned");
   const int64_t st[6] = {p->ql_stride_token, p->ql_stride_head, p->qpe_stride_token, p->qpe_stride_head,
                          p->kvc_stride_token, p->kpe_stride_token};
   for (int k = 0; k < 6; ++k)
@@ -149,9 +216,11 @@ extern "C" xqa_status xqa_mla_decode_prep(const xqa_mla_prep_params* p, xqa_stre
   a.pos = p->positions;
   a.cs = p->cos_sin_cache;
   a.slots = p->slot_mapping;
-  a.cache = static_cast<uint16_t*>(p->kv_cache);
-  a.qout = static_cast<uint16_t*>(p->q_out);
+  a.cache = p->kv_cache;
+  a.qout = p->q_out;
   a.err = p->error_word;
+  a.q_inv = p->q_scale_inv;
+  a.cache_inv = p->cache_scale_inv;
   a.ql_st = p->ql_stride_token;
   a.ql_sh = p->ql_stride_head;
   a.qpe_st = p->qpe_stride_token;
@@ -169,7 +238,10 @@ extern "C" xqa_status xqa_mla_decode_prep(const xqa_mla_prep_params* p, xqa_stre
   a.chunks = a.q_chunks + a.T * (a.W / 8);
   const int64_t blocks = (a.chunks + kThreads - 1) / kThreads;
   if (blocks > 0x7fffffffLL) return prep_fail(XQA_ERR_UNSUPPORTED, "too many tokens for one launch");
-  prep_kernel<<<unsigned(blocks), kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+  if (p->fp8)
+    prep_kernel<true><<<unsigned(blocks), kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+  else
+    prep_kernel<false><<<unsigned(blocks), kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return prep_fail(XQA_ERR_CUDA, "prep kernel launch: %s", cudaGetErrorString(e));
   return XQA_OK;

@@ -118,6 +118,9 @@ class XqaMlaPrepParams(ctypes.Structure):
         ("kv_lora_rank", ctypes.c_int32),
         ("rope_dim", ctypes.c_int32),
         ("error_word", ctypes.c_void_p),
+        ("fp8", ctypes.c_int32),
+        ("q_scale_inv", ctypes.c_void_p),
+        ("cache_scale_inv", ctypes.c_void_p),
     ]
 
 
@@ -400,12 +403,15 @@ def merge_attn_states(output, prefix_output, prefix_lse, suffix_output, suffix_l
 
 
 def mla_decode_prep(ql_nope, q_pe, kv_c, k_pe, positions, cos_sin_cache, slot_mapping, kv_cache,
-                    q_out=None, error_word=None, stream=None):
+                    q_out=None, error_word=None, q_scale_inv=None, cache_scale_inv=None, stream=None):
     """Fused MLA decode prep through the C ABI (Kimi-K3 MultiHeadLatentAttention
     page, `_decode_concat_cache`): returns q_out [T, H, Lr + R] = [ql_nope |
     rope(q_pe)] and writes [kv_c | rope(k_pe)] into kv_cache at slot_mapping.
-    bf16 tensors with a contiguous last dim; kv_cache [num_pages, page_size,
-    (1,) Lr + R] contiguous; positions and slot_mapping int64 [T]."""
+    bf16 inputs with a contiguous last dim; kv_cache [num_pages, page_size,
+    (1,) Lr + R] contiguous; positions and slot_mapping int64 [T].  An e4m3
+    kv_cache (the page's plain fp8 cache) takes the fp8 path: q_out and the
+    inserted rows are e4m3 of the values times q_scale_inv / cache_scale_inv
+    (fp32 device scalars, required then)."""
     T, H, Lr = ql_nope.shape
     R = q_pe.shape[-1]
     kc = kv_c.reshape(T, Lr)
@@ -413,8 +419,16 @@ def mla_decode_prep(ql_nope, q_pe, kv_c, k_pe, positions, cos_sin_cache, slot_ma
     for name, t in (("ql_nope", ql_nope), ("q_pe", q_pe), ("kv_c", kc), ("k_pe", kp)):
         if t.dtype != torch.bfloat16 or t.stride(-1) != 1:
             raise ValueError(f"{name} must be bf16 with a contiguous last dim")
-    if kv_cache.dtype != torch.bfloat16 or not kv_cache.is_contiguous() or kv_cache.shape[-1] != Lr + R:
-        raise ValueError(f"kv_cache must be contiguous bf16 with rows of {Lr + R}")
+    fp8 = kv_cache.dtype == torch.float8_e4m3fn
+    if kv_cache.dtype not in (torch.bfloat16, torch.float8_e4m3fn) or not kv_cache.is_contiguous() \
+            or kv_cache.shape[-1] != Lr + R:
+        raise ValueError(f"kv_cache must be contiguous bf16 or e4m3 with rows of {Lr + R}")
+    scales = []
+    if fp8:
+        for name, t in (("q_scale_inv", q_scale_inv), ("cache_scale_inv", cache_scale_inv)):
+            if t is None or t.dtype != torch.float32 or t.numel() != 1:
+                raise ValueError(f"the e4m3 prep needs {name} as a one-element float32 device tensor")
+            scales.append(t.contiguous())
     for name, t in (("slot_mapping", slot_mapping), ("positions", positions)):
         if t is not None and (t.dtype != torch.int64 or not t.is_contiguous() or t.numel() != T):
             raise ValueError(f"{name} must be contiguous int64 [{T}]")
@@ -422,7 +436,9 @@ def mla_decode_prep(ql_nope, q_pe, kv_c, k_pe, positions, cos_sin_cache, slot_ma
                                       or cos_sin_cache.shape[-1] != R):
         raise ValueError(f"cos_sin_cache must be contiguous fp32 [max_position, {R}]")
     if q_out is None:
-        q_out = torch.empty((T, H, Lr + R), dtype=torch.bfloat16, device=ql_nope.device)
+        q_out = torch.empty((T, H, Lr + R), dtype=kv_cache.dtype, device=ql_nope.device)
+    if q_out.dtype != kv_cache.dtype:
+        raise ValueError("q_out takes the cache's dtype")
     p = XqaMlaPrepParams()
     p.ql_nope, p.ql_stride_token, p.ql_stride_head = _ptr(ql_nope), ql_nope.stride(0), ql_nope.stride(1)
     p.q_pe, p.qpe_stride_token, p.qpe_stride_head = _ptr(q_pe), q_pe.stride(0), q_pe.stride(1)
@@ -437,5 +453,8 @@ def mla_decode_prep(ql_nope, q_pe, kv_c, k_pe, positions, cos_sin_cache, slot_ma
     p.q_out = _ptr(q_out)
     p.num_tokens, p.num_heads, p.kv_lora_rank, p.rope_dim = T, H, Lr, R
     p.error_word = _ptr(error_word)
+    p.fp8 = 1 if fp8 else 0
+    if fp8:
+        p.q_scale_inv, p.cache_scale_inv = _ptr(scales[0]), _ptr(scales[1])
     _check(load().xqa_mla_decode_prep(ctypes.byref(p), _stream(stream)))
     return q_out

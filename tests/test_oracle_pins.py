@@ -164,6 +164,11 @@ SMALL = [
          mla=True, page_size=16, seq_lens=[18, 40], kv_layout="NHD", softmax_scale=0.2),
     dict(name="peaked", batch=2, num_q_heads=4, num_kv_heads=2, head_dim=16, page_size=16,
          seq_lens=[9, 23], kv_layout="NHD", q_mult=8.0, sinks=True),
+    # an e4m3 query against an e4m3 latent cache (the fp8 MLA decode), both scaled
+    dict(name="mla_e4m3_query", batch=2, num_q_heads=4, num_kv_heads=1, head_dim=24, v_head_dim=16,
+         mla=True, page_size=16, seq_lens=[18, 40], kv_layout="NHD", softmax_scale=0.2,
+         q_dtype=torch.float8_e4m3fn, kv_dtype=torch.float8_e4m3fn, q_scale=0.25, kv_scale=0.125,
+         q_divisor=0.25, kv_divisor=0.125, sinks=True),
 ]
 
 

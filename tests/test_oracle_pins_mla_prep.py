@@ -81,3 +81,50 @@ def test_prep_concat_and_insert_by_hand():
             kw[0::2] = k[0::2] * c - k[1::2] * s
             kw[1::2] = k[1::2] * c + k[0::2] * s
             torch.testing.assert_close(c2[slot[t], Lr:], kw)
+
+
+def _prep_inputs(seed, T=5, H=3, Lr=16, R=8, slots_n=40):
+    g = torch.Generator().manual_seed(seed)
+    ql = torch.randn(T, H, Lr, generator=g).to(torch.bfloat16)
+    qp = torch.randn(T, H, R, generator=g).to(torch.bfloat16)
+    kc = torch.randn(T, Lr, generator=g).to(torch.bfloat16)
+    kp = torch.randn(T, R, generator=g).to(torch.bfloat16)
+    table, _ = cos_sin_table(64, R)
+    pos = torch.randint(0, 64, (T,), generator=g)
+    slots = torch.randperm(slots_n, generator=g)[:T]
+    slots[1] = -1
+    return ql, qp, kc, kp, pos, table, slots
+
+
+def test_e4m3_prep_is_torch_cast_of_the_scaled_values():
+    """The fp8 prep's codes equal torch's float8_e4m3fn cast (nearest even) of
+    the float64 prep values times the inverse scales (all inside +-448 here);
+    untouched slots and the padding token's keep their codes."""
+    ql, qp, kc, kp, pos, table, slots = _prep_inputs(3)
+    g = torch.Generator().manual_seed(4)
+    cache = torch.randint(0, 256, (40, 24), generator=g).to(torch.uint8)
+    cache[cache == 0x7F] = 0  # no NaN codes in the untouched rows (compared with equal)
+    q_inv, c_inv = 20.0, 12.5
+    q_codes, c_codes = oracle.mla_decode_prep_e4m3(ql, qp, kc, kp, pos, table, slots, cache, q_inv, c_inv)
+    q64, c64 = oracle.mla_decode_prep(ql, qp, kc, kp, pos, table, slots, torch.zeros(40, 24))
+    assert (q64 * q_inv).abs().max() < 448 and (c64 * c_inv).abs().max() < 448
+    want_q = (q64 * q_inv).to(torch.float8_e4m3fn).view(torch.uint8)
+    assert torch.equal(q_codes, want_q)
+    hit = slots[slots >= 0]
+    want_c = cache.clone()
+    want_c[hit] = (c64[hit] * c_inv).to(torch.float8_e4m3fn).view(torch.uint8)
+    assert torch.equal(c_codes, want_c)
+
+
+def test_e4m3_prep_saturates_beyond_448():
+    """Out of range the prep saturates to +-448 (the reading for the fp8
+    output and the fp8 prep; torch's cast gives NaN there instead)."""
+    ql, qp, kc, kp, pos, table, slots = _prep_inputs(5)
+    cache = torch.zeros(40, 24, dtype=torch.uint8)
+    q_codes, c_codes = oracle.mla_decode_prep_e4m3(ql, qp, kc, kp, pos, table, slots, cache, 1e4, 1e4)
+    q64, _ = oracle.mla_decode_prep(ql, qp, kc, kp, pos, table, slots, torch.zeros(40, 24))
+    big = (q64 * 1e4).abs() > 464
+    assert big.any()
+    dec = q_codes.view(torch.float8_e4m3fn).to(torch.float64)
+    assert torch.equal(dec[big].abs(), torch.full_like(dec[big], 448.0))
+    assert torch.equal(torch.sign(dec[big]), torch.sign(q64[big]))
