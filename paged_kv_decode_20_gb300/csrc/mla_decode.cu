@@ -98,6 +98,12 @@ constexpr int kCopyPieces = 4;             // P travels as this many bulk copies
 template <bool F8>
 struct Lay {
   static constexpr int kRingTiles = F8 ? 2 : 1;
+  // The L2 prefetch of the latent rows is issued by the output CTA's
+  // producer, this many 128-token tiles ahead of the V tile it loads (it
+  // trails the logit CTA's loads by about a tile): a TMA instruction holds
+  // its issuing thread for as long as the unit takes to generate the box's
+  // requests, so the logit CTA's producer issues only its K loads.
+  static constexpr int kPrefetchTilesOut = 2 * kRingTiles;
   static constexpr int kKSlots = kGroups * kRingTiles;
   static constexpr int kGroupChunks = F8 ? 2 : 3;       // 128-byte chunks per latent group
   static constexpr int kLatGroupBytes = kGroupChunks * kChunkBytesQ;
@@ -113,8 +119,8 @@ struct Lay {
   static constexpr int kOffQRope = kOffK + kRingTiles * kTileBytes;
   static constexpr int kOffPS = kOffQRope + kRows * (F8 ? 64 : 128);
   static constexpr int kOffFS = kOffPS + 2 * kPBytes;
-  static constexpr int kOffRowX = kOffFS + 2 * kFBytes;
-  static constexpr int kOffFinS = kOffRowX + 4 * kRows * 4;
+  static constexpr int kOffRowX = kOffFS + 2 * kFBytes;  // row maxima of the two threads of a row [2][128]
+  static constexpr int kOffFinS = kOffRowX + 2 * kRows * 4;
   static constexpr int kLogitEnd = kOffFinS + kFinBytes;
   static constexpr int kVSlots = F8 ? 2 : 3;
   static constexpr int kVChunks = F8 ? 4 : 8;  // 128-byte chunks of a V tile row
@@ -332,40 +338,54 @@ __device__ __forceinline__ SeqGeom seq_geom(const MlaArgs& a, int b) {
   return g;
 }
 
+// Page indices of the piece a producer warp streams, 32 pages at a time in
+// its registers: lane i holds the index of page base + i (-1 for an index
+// outside the pool).  A tile's pieces then come from shuffles, and the page
+// table is read once per 32 pages instead of on every tile, off the path
+// from a freed ring slot to its next load.
+struct PageWindow {
+  int base = -(1 << 30), mine = 0;
+  // Makes pages [first, last] (last < first + 32) available; whole warp.
+  __device__ __forceinline__ void cover(const MlaArgs& a, const int32_t* pt, int first, int last, int pg_hi,
+                                        int lane) {
+    if (first >= base && last < base + 32) return;
+    base = first;
+    mine = 0;
+    if (base + lane < pg_hi) {
+      const int p = __ldg(pt + base + lane);
+      mine = (p < 0 || int64_t(p) >= a.num_pages) ? -1 : p;
+    }
+  }
+};
+
 // The pieces of a tile of `tok` tokens starting at token tok0: boxes of
-// min(page_size, 64) rows, piece l at tile row 64-aligned l * box rows.  Lane
-// l < n loads piece l; `row` is its first row in the flattened
-// [pages * page_size] row space (a negative row for a page index out of
-// range: the TMA fills zeros there).  Pieces past the split's last page are
-// not loaded.
+// min(page_size, 64) rows, piece l at tile row l * box.  Lane l < n loads
+// piece l; `row` is its first row in the flattened [pages * page_size] row
+// space (a negative row for a page index out of range: the TMA fills zeros
+// there).  Pieces past the split's last page are not loaded.  Whole warp.
 struct TilePieces {
   int n, row;
   bool bad;
 };
-__device__ __forceinline__ TilePieces tile_pieces(const MlaArgs& a, const int32_t* pt, int tok0, int tok, int pg_hi,
-                                                  int lane) {
+__device__ __forceinline__ TilePieces tile_pieces(const MlaArgs& a, PageWindow& w, const int32_t* pt, int tok0,
+                                                  int tok, int pg_hi, int lane) {
   TilePieces p;
   const int box = min(a.ps, kTok);
   const int split_end = pg_hi * a.ps;  // first token past the split's pages
   p.n = min(tok / box, (split_end - tok0 + box - 1) / box);
   p.bad = false;
   p.row = 0;
+  if (p.n <= 0) return p;
+  w.cover(a, pt, tok0 / a.ps, (tok0 + p.n * box - 1) / a.ps, pg_hi, lane);
+  const int tk = tok0 + min(lane, p.n - 1) * box;
+  const int page = __shfl_sync(0xffffffffu, w.mine, (tk / a.ps - w.base) & 31);
   if (lane < p.n) {
-    const int tk = tok0 + lane * box;
-    int page = __ldg(pt + tk / a.ps);
-    if (page < 0 || int64_t(page) >= a.num_pages) {
-      page = -1;
-      p.bad = true;
-    }
+    p.bad = page < 0;
     p.row = page * a.ps + tk % a.ps;
   }
   return p;
 }
 
-// F8: e4m3 latent cache and e4m3 query (Q K^T on kind::f8f6f4, P in f16, V
-// widened to f16 in shared memory); else bf16 throughout.  tmK: the latent
-// chunks of a logit tile's groups; tmKR: the rope part of an e4m3 row (unused
-// for bf16, whose third group carries it); tmV: a V tile; tmPF: L2 prefetch.
 template <bool F8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmKR,
@@ -446,6 +466,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   constexpr uint32_t kIdescQK =
       F8 ? umma::idesc_e4m3(kRows, kTokQ, false, false) : umma::idesc_f16(kRows, kTokQ, true, false, false);
   constexpr uint32_t kIdescPV = umma::idesc_f16(kRows, kHalf, !F8, false, true);
+
   bool first_piece = true;
 
   for (;;) {
@@ -548,11 +569,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (ntiles > 0) {
       if (lane == 0) {
         prefetch_tensormap(logit_cta ? &tmK : &tmV);
-        if (logit_cta) prefetch_tensormap(&tmPF);
+        prefetch_tensormap(&tmPF);
         if (logit_cta && F8) prefetch_tensormap(&tmKR);
       }
       bool ok = true, bad = false;
       int issued = 0;
+      PageWindow win, win_pf;  // the tiles' pages; the L2-prefetched tiles' pages
       if (logit_cta) {
         // group gr of logit tile j (global group g = 3 j + gr) goes to ring
         // slot g % kKSlots: one wait, one expect-tx and one box per page piece
@@ -561,7 +583,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int j = g / kGroups, gr = g - j * kGroups;
           const int slot = g % SL::kKSlots, use = g / SL::kKSlots;
           if (gr == 0) {
-            tp = tile_pieces(a, pt, t_begin + j * kTokQ, kTokQ, pg_hi, lane);
+            tp = tile_pieces(a, win, pt, t_begin + j * kTokQ, kTokQ, pg_hi, lane);
             bad |= tp.bad;
           }
           if (use > 0) ok = __all_sync(kAll, mbar_wait(&bars[kKEmpty + slot], (use - 1) & 1));
@@ -580,14 +602,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               tma_load_4d(dst, &tmK, &bars[kKFull + slot], 0, 0, SL::kGroupChunks * gr, tp.row >> 3);
           }
           __syncwarp();
-          // after the tile's first loads are out, the tile two ahead goes into
-          // L2, so that its loads (issued only as ring slots free) do not pay
-          // HBM latency
-          if (gr == 0 && j + 2 < nqt) {
-            // one box per page piece covers all 576 dims of its rows
-            const TilePieces pf = tile_pieces(a, pt, t_begin + (j + 2) * kTokQ, kTokQ, pg_hi, lane);
-            if (lane < pf.n && pf.row >= 0) tma_prefetch_l2_3d(&tmPF, 0, 0, pf.row);
-          }
           ++issued;
         }
         // no load of this CTA may land after it exits
@@ -600,7 +614,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int slot = j % SL::kVSlots, use = j / SL::kVSlots;
           if (use > 0) ok = __all_sync(kAll, mbar_wait(&bars[kVEmpty + slot], (use - 1) & 1));
           if (!ok) break;
-          const TilePieces tp = tile_pieces(a, pt, t_begin + j * kTok, kTok, pg_hi, lane);
+          const TilePieces tp = tile_pieces(a, win, pt, t_begin + j * kTok, kTok, pg_hi, lane);
           bad |= tp.bad;
           if (lane == 0) mbar_arrive_expect_tx(&bars[kVFull + slot], uint32_t(tp.n) * piece_bytes);
           __syncwarp();
@@ -609,6 +623,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma_load_4d(smem + SL::kOffV + slot * SL::kVBytes + lane * int(piece_bytes), &tmV, &bars[kVFull + slot],
                         0, 0, 0, tp.row >> 3);
           __syncwarp();
+          // at the start of each 128-token logit tile, the latent rows of the
+          // logit tile kPrefetchTilesOut ahead go into L2, so that the logit
+          // CTA's loads (issued only as its ring slots free) do not pay HBM
+          // latency; one box per page piece covers all 576 dims of its rows
+          if ((j & 1) == 0 && j / 2 + SL::kPrefetchTilesOut < nqt) {
+            const TilePieces pf =
+                tile_pieces(a, win_pf, pt, t_begin + (j / 2 + SL::kPrefetchTilesOut) * kTokQ, kTokQ, pg_hi, lane);
+            if (lane < pf.n && pf.row >= 0) tma_prefetch_l2_3d(&tmPF, 0, 0, pf.row);
+          }
           ++issued;
         }
         if (lane == 0)
@@ -804,7 +827,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const float q_scale = ldscale(a.q_scale_dev, a.q_scale);
     const float kv_scale = ldscale(a.kv_scale_dev, a.kv_scale);
     const float lscale = a.softmax_scale * q_scale * kv_scale * kLog2e;
-    float* rowx = reinterpret_cast<float*>(smem + SL::kOffRowX);  // [2][2][128]
+    float* rowx = reinterpret_cast<float*>(smem + SL::kOffRowX);  // [2][128]
     constexpr int kC = kTok / 2;  // logit columns per thread
 
     // ---- query: this thread's half of the latent row into tensor memory
@@ -912,14 +935,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           s[k] = x;
           mx = fmaxf(mx, x);
         }
-        rowx[(2 * p2 + h) * kRows + t] = mx;
+        // (one buffer: the reads of the previous subtile's maxima precede
+        // the barrier that ended it)
+        rowx[h * kRows + t] = mx;
       }
       // both halves of every row published their maxima
       if (named_bar_or(1, kSoft, !ok)) {
         ok = false;
         break;
       }
-      mx = fmaxf(mx, rowx[(2 * p2 + 1 - h) * kRows + t]);
+      mx = fmaxf(mx, rowx[(1 - h) * kRows + t]);
       const float m_new = fmaxf(m_ref, mx);
       const bool need = m_new > m_ref + kRescaleLog2 || (m_ref == -INFINITY && m_new != -INFINITY);
       const float f = (need && m_ref != -INFINITY) ? exp2f(m_ref - m_new) : 1.f;
