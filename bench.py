@@ -40,7 +40,7 @@ from paged_kv_decode_20_gb300 import workloads as W  # noqa: E402
 METRIC = "paged decode attention: KV GB/s & % of GB300 HBM peak; decode tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_NAMES = {1: "gqa_decode_kernel", 2: "gqa_decode_kernel", 3: "gqa_decode_kernel",
-                4: "gqa_decode_kernel", 5: "mla_decode_kernel"}
+                4: "gqa_decode_kernel", 5: "mla_decode_kernel", "large_group": "gqa_decode_kernel"}
 
 
 def parse():
@@ -48,7 +48,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--workload", default="2", help="1..5 or large_group")
     ap.add_argument("--batch", type=int, default=None,
                     help="keep only the first B sequences (profiling a smaller case)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
@@ -59,7 +59,7 @@ def parse():
                     help="fp8 output (workloads with an fp8 cache)")
     ap.add_argument("--kv-dtype", default=None, choices=["e4m3"],
                     help="workload 5 with an e4m3 latent cache and query")
-    ap.add_argument("--workloads", default="1,2,3,4,5,5e4m3",
+    ap.add_argument("--workloads", default="1,2,3,4,5,5e4m3,large_group",
                     help="named workloads also timed into the line's `workloads` object "
                          "(comma list, or 'none')")
     return ap.parse_args()
@@ -192,18 +192,24 @@ class Clocks:
 
 
 def workload_key(key):
-    """'5' -> (5, None); '5e4m3' -> (5, torch.float8_e4m3fn)."""
+    """'5' -> (5, None); '5e4m3' -> (5, torch.float8_e4m3fn); 'large_group' -> ('large_group', None)."""
     key = str(key)
+    if key == "large_group":
+        return key, None
     if key.endswith("e4m3"):
         return int(key[:-4]), torch.float8_e4m3fn
     return int(key), None
 
 
 def workload_name(idx, kv_dtype=None):
+    if idx == "large_group":
+        return W.LARGE_GROUP
     return W.WORKLOAD_5_E4M3 if kv_dtype is not None else W.WORKLOADS[idx]
 
 
 def build_case(idx, device, batch=None, kv_dtype=None):
+    if idx == "large_group":
+        return W.large_group_workload(device=device, poison=False, batch=batch)
     return W.workload(idx, device=device, poison=False, batch=batch, kv_dtype=kv_dtype)
 
 
@@ -470,7 +476,8 @@ def cpu_baseline(case, idx, max_rows=None, min_seconds=10.0, threads=None):
     units = None
     frac = 1.0
     rows = B * qs * Hq
-    budget_rows = max_rows if max_rows is not None else {1: rows, 2: rows, 3: 256, 4: rows, 5: 128}[idx]
+    budget_rows = max_rows if max_rows is not None else {1: rows, 2: rows, 3: 256, 4: rows, 5: 128,
+                                                         "large_group": 512}[idx]
     if budget_rows < rows:
         # whole (b, kvh) units, spread over the batch
         per_unit = qs * G
@@ -514,10 +521,10 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    case = W.workload(args.workload, device="cpu", poison=False, batch=args.batch)
+    case = build_case(args.workload, "cpu", args.batch)
     B = case.batch
     # each step: a few whole (sequence, kv head) units
-    rows_per_step = {1: 16, 2: 32, 3: 8, 4: 64, 5: 128}[args.workload]
+    rows_per_step = {1: 16, 2: 32, 3: 8, 4: 64, 5: 128, "large_group": 64}[args.workload]
     for _ in range(args.warmup):
         cpu_baseline(case, args.workload, max_rows=rows_per_step, min_seconds=0.0)
     times, vals = [], []
@@ -542,7 +549,7 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded N(0,1) q/K/V, shuffled page pool)",
-        "config": {"workload": W.WORKLOADS[args.workload], "global_batch": B,
+        "config": {"workload": workload_name(args.workload), "global_batch": B,
                    "parallelism": "CPU oracle, rank 0 only"},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": os.cpu_count(),
                          "kind": "oracle", "sample": r["sample"] + " per step"},
@@ -777,6 +784,7 @@ def run_prep(args):
 
 def main():
     args = parse()
+    args.workload = int(args.workload) if str(args.workload).isdigit() else args.workload
     if args.op == "merge":
         run_merge(args)
     elif args.op == "prep":

@@ -3,7 +3,9 @@
 //
 // One CTA owns (sequence b, kv head kvh, row group rg, KV split).  Its rows are
 // the q_seq_len x G query rows that share kv head kvh (speculative tokens and
-// the GQA group stacked), padded to 16-row MMA blocks.
+// the GQA group stacked), padded to 16-row MMA blocks: RB blocks per consumer
+// warp, and WR warp row groups (1, 2 or 4) that split the CTA's rows, so that
+// up to 64 rows (D = 128) or 128 rows (D = 64) read each page of KV once.
 //
 //   warp 4 (producer, one lane): walks page_table and issues one TMA tile load
 //     per (page, 128-byte column chunk) for K and for V into a ring of stages
@@ -11,8 +13,10 @@
 //     a full/empty mbarrier pair.  NHD and HND differ only in the tensor map
 //     and the coordinates.  TMA writes the rows with the 128-byte swizzle, so
 //     ldmatrix reads are bank-conflict free.
-//   warps 0-3 (consumers): each takes a quarter of every stage (16 or 32
-//     tokens, i.e. two or four independent 8-token MMA chains).
+//   warps 0-3 (consumers): warp w holds row group w % WR (RB 16-row blocks)
+//     and takes the (w / WR)-th of 4 / WR equal token ranges of every stage
+//     (WR = 1: a quarter of each stage, 16 or 32 tokens, i.e. two or four
+//     independent 8-token MMA chains).
 //     S = Q K^T with mma.sync m16n8k16 (rows on M, tokens on N), fp32 online
 //     softmax in the exp2 domain with window / spec-mask / tail masking by
 //     select, then O += P V (P re-used from the S accumulator registers).
@@ -36,7 +40,7 @@ namespace xqa {
 
 enum KvKind { kKvF16 = 0, kKvBf16 = 1, kKvE4m3 = 2 };
 
-template <int KV, int D, int RB>
+template <int KV, int D, int RB, int WR = 1>
 struct GqaCfg {
   static constexpr bool kF8 = (KV == kKvE4m3);
   static constexpr int kElt = kF8 ? 1 : 2;
@@ -45,15 +49,17 @@ struct GqaCfg {
   static constexpr int kChunks = kRowBytes / 128;
   // tokens per stage: 128 when a row is one 128-byte chunk and one 16-row
   // block suffices (four MMA chains per warp), else 64 (register budget)
-  static constexpr int kTok = (kRowBytes == 128 && RB == 1) ? 128 : 64;
+  static constexpr int kTok = (kRowBytes == 128 && RB == 1 && WR == 1) ? 128 : 64;
+  static constexpr int kTS = 4 / WR;  // warps sharing a row group (token splits)
+  static_assert(WR == 1 || WR == 2 || WR == 4, "warp row groups");
   static constexpr int kTile = kTok * kRowBytes;           // K (or V) bytes per stage
   static constexpr int kStage = 2 * kTile;
   static constexpr int kNumStages = kStage >= 32768 ? 3 : 5;  // 96 KB or 80 KB per CTA
-  static constexpr int kRows = 16 * RB;
+  static constexpr int kRows = 16 * RB * WR;
   static constexpr int kThreads = 160;
-  // epilogue scratch: per-warp O [4][rows][D], m and l [4][rows], then per-row
-  // weights [rows][4] and the row's (max, sum) for a partial
-  static constexpr int kScratch = 4 * kRows * D * 4 + 2 * 4 * kRows * 4 + 6 * kRows * 4;
+  // epilogue scratch: per token split O [kTS][rows][D], m and l [kTS][rows],
+  // then per-row weights [rows][kTS] and the row's (max, sum) for a partial
+  static constexpr int kScratch = kTS * kRows * D * 4 + 2 * kTS * kRows * 4 + (kTS + 2) * kRows * 4;
   static constexpr int kRing = kNumStages * kStage;
   static_assert(kScratch <= kRing, "epilogue scratch reuses the stage ring");
   static constexpr int kBarOff = kRing;
@@ -64,11 +70,12 @@ __device__ __forceinline__ float load_scale(const float* dev, float host) {
   return dev ? __ldg(dev) : host;
 }
 
-template <int KV, int D, int RB>
+template <int KV, int D, int RB, int WR>
 __global__ void __launch_bounds__(160, 2)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const DecodeArgs a) {
-  using C = GqaCfg<KV, D, RB>;
+  using C = GqaCfg<KV, D, RB, WR>;
+  constexpr int TS = C::kTS;
   constexpr bool kF8 = C::kF8;
   constexpr bool kMmaBf16 = (KV == kKvBf16);
   constexpr int kKSteps = D / 16;
@@ -96,7 +103,7 @@ __global__ void __launch_bounds__(160, 2)
   // (Built only where it costs no registers in the main loop: 16-bit K/V
   // with one row block; the fp8 and two-row-block variants would spill.)
   int b = blockIdx.z;
-  if (!kF8 && RB == 1 && a.sort_b) {
+  if (!kF8 && RB == 1 && WR == 1 && a.sort_b) {
     int* eff = reinterpret_cast<int*>(smem);  // the stage ring is unused until the first load
     const int64_t cap = int64_t(a.pps) * a.ps;
     if (tid < a.B) {
@@ -151,11 +158,11 @@ __global__ void __launch_bounds__(160, 2)
   __syncthreads();
 
   const int unit = (b * a.Hkv + kvh) * a.rg_count + rg;
-  float* scratch = reinterpret_cast<float*>(smem);  // epilogue: [4][rows][D] O, then m, l
-  float* sc_m = scratch + 4 * C::kRows * D;
-  float* sc_l = sc_m + 4 * C::kRows;
-  float* sc_w = sc_l + 4 * C::kRows;  // [rows][4] per-warp weights (scales folded in)
-  float* sc_ml = sc_w + 4 * C::kRows;  // [rows][2] merged (max, sum) of a split partial
+  float* scratch = reinterpret_cast<float*>(smem);  // epilogue: [TS][rows][D] O, then m, l
+  float* sc_m = scratch + TS * C::kRows * D;
+  float* sc_l = sc_m + TS * C::kRows;
+  float* sc_w = sc_l + TS * C::kRows;  // [rows][TS] per-split weights (scales folded in)
+  float* sc_ml = sc_w + TS * C::kRows;  // [rows][2] merged (max, sum) of a split partial
 
   if (warp == 4) {
     // ================= producer (whole warp fetches page indices, lane 0 issues TMA)
@@ -234,6 +241,8 @@ __global__ void __launch_bounds__(160, 2)
   } else {
     // ================= consumers =================
     const int g = lane >> 2, qd = lane & 3;
+    const int wr = warp % WR, ts = warp / WR;  // this warp's row group and token split
+    const int row0 = wr * RB * 16;             // its first row in the CTA's rows
     const float q_scale = load_scale(a.q_scale_dev, a.q_scale);
     const float kv_scale = load_scale(a.kv_scale_dev, a.kv_scale);
     float lscale = a.softmax_scale * q_scale * kv_scale * kLog2e;
@@ -249,7 +258,7 @@ __global__ void __launch_bounds__(160, 2)
       for (int rb = 0; rb < RB; ++rb) {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          const int r = rg * C::kRows + rb * 16 + g + 8 * hh;
+          const int r = rg * C::kRows + row0 + rb * 16 + g + 8 * hh;
           const bool ok = r < a.R;
           const int i = ok ? r / a.G : 0, gg = ok ? r % a.G : 0;
           const uint16_t* src =
@@ -312,7 +321,7 @@ __global__ void __launch_bounds__(160, 2)
     for (int rb = 0; rb < RB; ++rb)
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        const int r = rg * C::kRows + rb * 16 + g + 8 * hh;
+        const int r = rg * C::kRows + row0 + rb * 16 + g + 8 * hh;
         const int i = r < a.R ? r / a.G : 0;
         row_lb[rb][hh] = a.win > 0 ? spec0 + i - a.win + 1 : INT_MIN;
         uint32_t mw = 0xffffffffu;
@@ -334,9 +343,9 @@ __global__ void __launch_bounds__(160, 2)
       for (int j = 0; j < kDvTiles; ++j) o[rb][j][0] = o[rb][j][1] = o[rb][j][2] = o[rb][j][3] = 0.f;
     }
 
-    constexpr int KB = C::kTok / 64;  // 16-token blocks per warp and stage
-    constexpr int NT = 2 * KB;        // 8-token MMA n-tiles per warp and stage
-    const int wt0 = 16 * KB * warp;   // this warp's first row of every stage
+    constexpr int KB = C::kTok / (16 * TS);  // 16-token blocks per warp and stage
+    constexpr int NT = 2 * KB;               // 8-token MMA n-tiles per warp and stage
+    const int wt0 = 16 * KB * ts;            // this warp's first row of every stage
     const int mat = lane >> 3;
     for (int s = 0; s < nst; ++s) {
       const int slot = s % C::kNumStages;
@@ -562,17 +571,17 @@ __global__ void __launch_bounds__(160, 2)
       for (int j = 0; j < kDvTiles; ++j)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int row = rb * 16 + g + 8 * (e >> 1);
+          const int row = row0 + rb * 16 + g + 8 * (e >> 1);
           const int n = 2 * qd + (e & 1);
           const int dv = kF8 ? (32 * (j >> 2) + 4 * n + (j & 3)) : (8 * j + n);
-          scratch[(warp * C::kRows + row) * D + dv] = o[rb][j][e];
+          scratch[(ts * C::kRows + row) * D + dv] = o[rb][j][e];
         }
       if (qd == 0) {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          const int row = rb * 16 + g + 8 * hh;
-          sc_m[warp * C::kRows + row] = m_run[rb][hh];
-          sc_l[warp * C::kRows + row] = l_run[rb][hh];
+          const int row = row0 + rb * 16 + g + 8 * hh;
+          sc_m[ts * C::kRows + row] = m_run[rb][hh];
+          sc_l[ts * C::kRows + row] = l_run[rb][hh];
         }
       }
     }
@@ -592,19 +601,18 @@ __global__ void __launch_bounds__(160, 2)
   const int row_stride = D + 4;  // O, then m and l; padded so rows stay 16-byte aligned
   float* ws_unit = a.ws + (int64_t(unit) * a.nsplit) * C::kRows * row_stride;
 
-  // phase 1: one thread per row folds the four warps' maxima (and, with one
-  // split, the sink and the output scales) into one weight per warp
-  if (!aborted && tid < rows_here) {
-    const int row = tid;
-    float mw[4], M = -INFINITY;
+  // phase 1: one thread per row folds the maxima of the warps holding it (and,
+  // with one split, the sink and the output scales) into one weight per warp
+  for (int row = aborted ? rows_here : tid; row < rows_here; row += C::kThreads) {
+    float mw[TS], M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
+    for (int w = 0; w < TS; ++w) {
       mw[w] = sc_m[w * C::kRows + row];
       M = fmaxf(M, mw[w]);
     }
-    float f[4], l = 0.f;
+    float f[TS], l = 0.f;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
+    for (int w = 0; w < TS; ++w) {
       f[w] = (mw[w] == -INFINITY) ? 0.f : exp2f(mw[w] - M);
       l += f[w] * sc_l[w * C::kRows + row];
     }
@@ -618,7 +626,7 @@ __global__ void __launch_bounds__(160, 2)
       sc_ml[2 * row + 1] = l;
     }
 #pragma unroll
-    for (int w = 0; w < 4; ++w) sc_w[4 * row + w] = f[w] * mul;
+    for (int w = 0; w < TS; ++w) sc_w[TS * row + w] = f[w] * mul;
   }
   __syncthreads();
   // phase 2: every (row, 4 columns) combines the warps' partial O
@@ -627,8 +635,8 @@ __global__ void __launch_bounds__(160, 2)
     const int dv = 4 * (item % (D / 4));
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const float f = sc_w[4 * row + w];
+    for (int w = 0; w < TS; ++w) {
+      const float f = sc_w[TS * row + w];
       const float4 v = *reinterpret_cast<const float4*>(scratch + (w * C::kRows + row) * D + dv);
       acc.x += f * v.x;
       acc.y += f * v.y;

@@ -8,16 +8,18 @@
 
 namespace xqa {
 
-// kv: 0 f16, 1 bf16, 2 e4m3.  Returns cudaErrorInvalidValue when no kernel is
-// built for (kv, head_dim, row_blocks).  With launch == false only the
-// occupancy (CTAs per SM) is reported.
-cudaError_t gqa_launch_f16(int head_dim, int row_blocks, bool launch, dim3 grid,
+// kv: 0 f16, 1 bf16, 2 e4m3.  row_blocks: 16-row MMA blocks per consumer
+// warp; warp_rows: warp row groups splitting a CTA's rows (1, 2 or 4).
+// Returns cudaErrorInvalidValue when no kernel is built for (kv, head_dim,
+// row_blocks, warp_rows).  With launch == false only the occupancy (CTAs per
+// SM) is reported.
+cudaError_t gqa_launch_f16(int head_dim, int row_blocks, int warp_rows, bool launch, dim3 grid,
                            const CUtensorMap* tk, const CUtensorMap* tv, const DecodeArgs* args,
                            cudaStream_t stream, int* ctas_per_sm);
-cudaError_t gqa_launch_bf16(int head_dim, int row_blocks, bool launch, dim3 grid,
+cudaError_t gqa_launch_bf16(int head_dim, int row_blocks, int warp_rows, bool launch, dim3 grid,
                             const CUtensorMap* tk, const CUtensorMap* tv, const DecodeArgs* args,
                             cudaStream_t stream, int* ctas_per_sm);
-cudaError_t gqa_launch_e4m3(int head_dim, int row_blocks, bool launch, dim3 grid,
+cudaError_t gqa_launch_e4m3(int head_dim, int row_blocks, int warp_rows, bool launch, dim3 grid,
                             const CUtensorMap* tk, const CUtensorMap* tv, const DecodeArgs* args,
                             cudaStream_t stream, int* ctas_per_sm);
 

@@ -5,12 +5,12 @@
 
 namespace xqa {
 
-template <int KV, int D, int RB>
+template <int KV, int D, int RB, int WR>
 cudaError_t gqa_launch_one(bool launch, dim3 grid, const CUtensorMap* tk, const CUtensorMap* tv,
                            const DecodeArgs* args, cudaStream_t stream, int* ctas_per_sm) {
   const bool pdl = args && args->pdl;
-  using C = GqaCfg<KV, D, RB>;
-  auto kern = gqa_decode_kernel<KV, D, RB>;
+  using C = GqaCfg<KV, D, RB, WR>;
+  auto kern = gqa_decode_kernel<KV, D, RB, WR>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   if (ctas_per_sm) {

@@ -78,7 +78,7 @@ int elt_bytes(xqa_dtype t) { return t == XQA_E4M3 ? 1 : 2; }
 struct Plan {
   bool mla = false;
   int D = 0, Dv = 0, G = 0, R = 0;
-  int row_blocks = 1, rows = 16, rg_count = 1;
+  int row_blocks = 1, warp_rows = 1, rows = 16, rg_count = 1;
   int nsplit = 1, split_pages = 1;
   int max_pages = 1;
   size_t ws_bytes = 0;
@@ -186,8 +186,23 @@ void choose_splits(const xqa_params* p, Plan* pl, int sm_count, int ctas_per_sm,
 // Tokens per pipeline stage of the GQA kernel: 128 when a K row is one
 // 128-byte swizzle chunk (fp8 D=128, 16-bit D=64) and one 16-row block holds
 // the rows, else 64.  Must match GqaCfg::kTok.
-int stage_tokens(const xqa_params* p, int row_blocks) {
-  return (p->head_dim * elt_bytes(p->kv_dtype) == 128 && row_blocks == 1) ? 128 : 64;
+int stage_tokens(const xqa_params* p, int row_blocks, int warp_rows) {
+  return (p->head_dim * elt_bytes(p->kv_dtype) == 128 && row_blocks == 1 && warp_rows == 1) ? 128 : 64;
+}
+
+// Rows of one GQA CTA for R = q_seq_len x G query rows per kv head: 16-row
+// blocks per consumer warp (row_blocks) and warp row groups (warp_rows), so
+// that up to 64 rows share one pass over the KV pages; more rows take
+// several row groups.
+void row_shape(int D, int R, int* row_blocks, int* warp_rows) {
+  *row_blocks = 1;
+  *warp_rows = 1;
+  if (R <= 16) return;
+  if (D == 64 && R <= 32) {
+    *row_blocks = 2;  // two blocks per warp, the stage split four ways
+    return;
+  }
+  *warp_rows = (D == 128 && R <= 32) ? 2 : 4;
 }
 
 xqa_status plan_gqa(const xqa_params* p, int sm_count_in, Plan* pl) {
@@ -199,8 +214,8 @@ xqa_status plan_gqa(const xqa_params* p, int sm_count_in, Plan* pl) {
   pl->D = pl->Dv = D;
   pl->G = p->num_q_heads / p->num_kv_heads;
   pl->R = p->q_seq_len * pl->G;
-  pl->row_blocks = (D == 64 && pl->R > 16) ? 2 : 1;
-  pl->rows = 16 * pl->row_blocks;
+  row_shape(D, pl->R, &pl->row_blocks, &pl->warp_rows);
+  pl->rows = 16 * pl->row_blocks * pl->warp_rows;
   pl->rg_count = (pl->R + pl->rows - 1) / pl->rows;
   pl->max_pages = pages_bound(p);
   const int sm = resolve_sm_count(p, sm_count_in);
@@ -208,13 +223,16 @@ xqa_status plan_gqa(const xqa_params* p, int sm_count_in, Plan* pl) {
   int occ = 0;
   cudaError_t e;
   if (p->kv_dtype == XQA_E4M3)
-    e = xqa::gqa_launch_e4m3(D, pl->row_blocks, false, dim3(), nullptr, nullptr, nullptr, nullptr, &occ);
+    e = xqa::gqa_launch_e4m3(D, pl->row_blocks, pl->warp_rows, false, dim3(), nullptr, nullptr, nullptr, nullptr,
+                             &occ);
   else if (p->kv_dtype == XQA_BF16)
-    e = xqa::gqa_launch_bf16(D, pl->row_blocks, false, dim3(), nullptr, nullptr, nullptr, nullptr, &occ);
+    e = xqa::gqa_launch_bf16(D, pl->row_blocks, pl->warp_rows, false, dim3(), nullptr, nullptr, nullptr, nullptr,
+                             &occ);
   else
-    e = xqa::gqa_launch_f16(D, pl->row_blocks, false, dim3(), nullptr, nullptr, nullptr, nullptr, &occ);
+    e = xqa::gqa_launch_f16(D, pl->row_blocks, pl->warp_rows, false, dim3(), nullptr, nullptr, nullptr, nullptr,
+                            &occ);
   if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
-  const int tok = stage_tokens(p, pl->row_blocks);
+  const int tok = stage_tokens(p, pl->row_blocks, pl->warp_rows);
   const int stage_pages = p->page_size <= tok ? tok / p->page_size : 1;
   choose_splits(p, pl, sm, occ, stage_pages);
   const int64_t units = int64_t(p->batch_size) * p->num_kv_heads * pl->rg_count;
@@ -347,7 +365,9 @@ size_t xqa_semaphore_count(const xqa_params* p) {
   if (st != XQA_OK) return size_t(-1);
   const int G = p->num_q_heads / p->num_kv_heads;
   const int R = p->q_seq_len * G;
-  const int rows = (p->head_dim == 64 && R > 16) ? 32 : 16;
+  int rb = 1, wr = 1;
+  row_shape(p->head_dim, R, &rb, &wr);
+  const int rows = 16 * rb * wr;
   return size_t(p->batch_size) * p->num_kv_heads * ((R + rows - 1) / rows);
 }
 
@@ -360,7 +380,7 @@ xqa_status xqa_decode(const xqa_params* p, void* ws, size_t ws_bytes, uint32_t* 
   st = check_buffers(pl, ws, ws_bytes, sems);
   if (st != XQA_OK) return st;
   CUtensorMap tk, tv;
-  const int box_rows = std::min(p->page_size, stage_tokens(p, pl.row_blocks));
+  const int box_rows = std::min(p->page_size, stage_tokens(p, pl.row_blocks, pl.warp_rows));
   st = make_maps(p, pl.D, box_rows, &tk, &tv);
   if (st != XQA_OK) return st;
   xqa::DecodeArgs a;
@@ -369,11 +389,11 @@ xqa_status xqa_decode(const xqa_params* p, void* ws, size_t ws_bytes, uint32_t* 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (p->kv_dtype == XQA_E4M3)
-    e = xqa::gqa_launch_e4m3(pl.D, pl.row_blocks, true, grid, &tk, &tv, &a, s, nullptr);
+    e = xqa::gqa_launch_e4m3(pl.D, pl.row_blocks, pl.warp_rows, true, grid, &tk, &tv, &a, s, nullptr);
   else if (p->kv_dtype == XQA_BF16)
-    e = xqa::gqa_launch_bf16(pl.D, pl.row_blocks, true, grid, &tk, &tv, &a, s, nullptr);
+    e = xqa::gqa_launch_bf16(pl.D, pl.row_blocks, pl.warp_rows, true, grid, &tk, &tv, &a, s, nullptr);
   else
-    e = xqa::gqa_launch_f16(pl.D, pl.row_blocks, true, grid, &tk, &tv, &a, s, nullptr);
+    e = xqa::gqa_launch_f16(pl.D, pl.row_blocks, pl.warp_rows, true, grid, &tk, &tv, &a, s, nullptr);
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
   return XQA_OK;
 }

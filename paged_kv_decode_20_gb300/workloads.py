@@ -262,6 +262,23 @@ WORKLOAD_5_E4M3 = ("MLA latent decode, e4m3 latent cache and query (B64 Hq128 la
                    "L~U[4096,32768] q_scale=kv_scale=0.05)")
 
 
+LARGE_GROUP = ("speculative decode on a large group (B64 Hq128 Hkv8 D128 ps64 L~U[1024,8192] HND bf16, "
+               "q_seq_len4 causal mask: 64 query rows per kv head)")
+
+
+def large_group_workload(device="cpu", poison=True, batch=None):
+    """The Llama-3-8B-shaped cache (workload 2's lengths and pool) with four
+    speculative tokens and a group of 16 query heads per kv head: 64 rows per
+    kv head, the tile the grouped-query kernel's warp row groups serve in one
+    pass over the pages."""
+    B = 64
+    lens = _uniform_lens(1024, 8192, B, 2)[: batch or B]
+    return make_case(batch=len(lens), num_q_heads=128, num_kv_heads=8, head_dim=128, page_size=64,
+                     seq_lens=lens, kv_layout="HND", q_seq_len=4, mask="causal",
+                     pages_per_seq=8192 // 64, seed=12, device=device, poison=poison,
+                     name="large_group_spec")
+
+
 def workload(idx, device="cpu", poison=True, batch=None, kv_dtype=None):
     """The named workload idx (1..5); `batch` truncates B for smaller runs
     while keeping every other size.  kv_dtype=torch.float8_e4m3fn with idx 5

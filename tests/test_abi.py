@@ -116,12 +116,19 @@ def test_null_params_rejected(lib):
 
 def test_semaphore_count_is_one_per_row_group(lib):
     assert lib.xqa_semaphore_count(ctypes.byref(fake_params())) == 4 * 8
-    # 64 rows of D=128 per kv head -> four 16-row groups
+    # up to 64 rows per kv head (here 8 tokens x G 8) share one CTA row group
     p = fake_params(num_q_heads=64, q_seq_len=8)
-    assert lib.xqa_semaphore_count(ctypes.byref(p)) == 4 * 8 * 4
-    # D=64 uses 32-row groups
+    assert lib.xqa_semaphore_count(ctypes.byref(p)) == 4 * 8 * 1
+    # 128 rows -> two 64-row groups
+    p = fake_params(num_q_heads=64, q_seq_len=16)
+    assert lib.xqa_semaphore_count(ctypes.byref(p)) == 4 * 8 * 2
+    # D=64: 32 rows (two blocks per warp), then 64-row groups
     p = fake_params(head_dim=64, num_q_heads=64, q_seq_len=4)
     assert lib.xqa_semaphore_count(ctypes.byref(p)) == 4 * 8 * 1
+    p = fake_params(head_dim=64, num_q_heads=128, q_seq_len=4)
+    assert lib.xqa_semaphore_count(ctypes.byref(p)) == 4 * 8 * 1
+    p = fake_params(head_dim=64, num_q_heads=256, q_seq_len=4)
+    assert lib.xqa_semaphore_count(ctypes.byref(p)) == 4 * 8 * 2
 
 
 def test_product_path_never_touches_the_oracle():

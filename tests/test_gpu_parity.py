@@ -119,6 +119,42 @@ def test_group_and_spec_rows_d64(G, qs):
     check(c)
 
 
+# Large grouped tiles (speculative tokens x a large GQA group): up to 64 rows per
+# kv head run as one CTA per (sequence, kv head, split) whose four consumer
+# warps split the rows (warp row groups), so each KV page is read once; 128
+# rows take two such row groups.
+LARGE = [(8, 4, torch.bfloat16), (16, 2, torch.bfloat16), (16, 4, torch.bfloat16), (32, 2, torch.float16),
+         (32, 4, torch.bfloat16), (8, 4, torch.float8_e4m3fn), (16, 4, torch.float8_e4m3fn),
+         (24, 1, torch.bfloat16)]
+
+
+@pytest.mark.parametrize("G,qs,kv", LARGE, ids=[f"G{g}-qs{q}-{str(k).split('.')[-1]}" for g, q, k in LARGE])
+def test_large_group_tiles_d128(G, qs, kv):
+    f8 = kv == torch.float8_e4m3fn
+    extra = dict(kv_scale=0.25, kv_divisor=0.25) if f8 else {}
+    c = W.make_case(batch=3, num_q_heads=2 * G, num_kv_heads=2, head_dim=128, page_size=32 if qs % 2 else 64,
+                    seq_lens=[900, 37, 2500], q_seq_len=qs, mask="causal" if qs > 1 else None, sinks=True,
+                    kv_layout="HND" if G % 16 else "NHD", q_dtype=torch.float16 if kv == torch.float16 else
+                    torch.bfloat16, kv_dtype=kv, seed=100 * G + qs, **extra)
+    check(c, tol=TOL_FP8 if f8 else TOL_16)
+
+
+@pytest.mark.parametrize("sm_count", [1, 30, 10000])
+def test_large_group_tiles_split_counts(sm_count):
+    c = W.make_case(batch=2, num_q_heads=64, num_kv_heads=4, head_dim=128, page_size=16,
+                    seq_lens=[3000, 130], q_seq_len=4, mask="causal", sinks=True, sliding_win_size=700,
+                    seed=77)
+    check(c, sm_count=sm_count)
+
+
+@pytest.mark.parametrize("G,qs", [(16, 4), (32, 4), (64, 1)])
+def test_large_group_tiles_d64(G, qs):
+    c = W.make_case(batch=2, num_q_heads=2 * G, num_kv_heads=2, head_dim=64, page_size=16,
+                    seq_lens=[600, 45], q_seq_len=qs, mask="causal" if qs > 1 else None,
+                    sinks=True, seed=7 * G + qs)
+    check(c)
+
+
 def test_f16_query_with_fp8_cache():
     c = W.make_case(batch=2, num_q_heads=8, num_kv_heads=1, head_dim=128, page_size=64,
                     seq_lens=[513, 1000], q_dtype=torch.float16, kv_dtype=torch.float8_e4m3fn,
