@@ -23,4 +23,10 @@ cudaError_t gqa_launch_e4m3(int head_dim, int row_blocks, int warp_rows, bool la
                             const CUtensorMap* tk, const CUtensorMap* tv, const DecodeArgs* args,
                             cudaStream_t stream, int* ctas_per_sm);
 
+// The tensor-core grouped-query kernel (16-bit K/V, head_dim 64 or 128) for
+// more than 16 (head_dim 128) or 32 (head_dim 64) query rows per kv head: 128
+// rows per CTA, one CTA per SM.
+cudaError_t gqa_tc_launch(bool bf16, int head_dim, bool launch, dim3 grid, const CUtensorMap* tk,
+                          const CUtensorMap* tv, const DecodeArgs* args, cudaStream_t stream, int* ctas_per_sm);
+
 }  // namespace xqa

@@ -79,6 +79,7 @@ struct Plan {
   bool mla = false;
   int D = 0, Dv = 0, G = 0, R = 0;
   int row_blocks = 1, warp_rows = 1, rows = 16, rg_count = 1;
+  bool tc = false;  // the tensor-core kernel (large grouped tiles, 16-bit K/V)
   int nsplit = 1, split_pages = 1;
   int max_pages = 1;
   size_t ws_bytes = 0;
@@ -190,10 +191,17 @@ int stage_tokens(const xqa_params* p, int row_blocks, int warp_rows) {
   return (p->head_dim * elt_bytes(p->kv_dtype) == 128 && row_blocks == 1 && warp_rows == 1) ? 128 : 64;
 }
 
-// Rows of one GQA CTA for R = q_seq_len x G query rows per kv head: 16-row
-// blocks per consumer warp (row_blocks) and warp row groups (warp_rows), so
-// that up to 64 rows share one pass over the KV pages; more rows take
-// several row groups.
+// Large grouped tiles with 16-bit K/V run on the tensor-core kernel: more
+// than 16 rows per kv head at head_dim 128, more than 32 at head_dim 64 (the
+// sizes the mma.sync kernel holds in one 16-row block per warp, or two).
+bool use_tc(const xqa_params* p, int R) {
+  return is_16bit(p->kv_dtype) && ((p->head_dim == 128 && R > 16) || (p->head_dim == 64 && R > 32));
+}
+
+// Rows of one CTA of the mma.sync kernel for R = q_seq_len x G query rows per
+// kv head: 16-row blocks per consumer warp (row_blocks) and warp row groups
+// (warp_rows), so that up to 64 rows share one pass over the KV pages (e4m3
+// K/V; 16-bit K/V take the tensor-core kernel beyond one or two blocks).
 void row_shape(int D, int R, int* row_blocks, int* warp_rows) {
   *row_blocks = 1;
   *warp_rows = 1;
@@ -214,15 +222,18 @@ xqa_status plan_gqa(const xqa_params* p, int sm_count_in, Plan* pl) {
   pl->D = pl->Dv = D;
   pl->G = p->num_q_heads / p->num_kv_heads;
   pl->R = p->q_seq_len * pl->G;
+  pl->tc = use_tc(p, pl->R);
   row_shape(D, pl->R, &pl->row_blocks, &pl->warp_rows);
-  pl->rows = 16 * pl->row_blocks * pl->warp_rows;
+  pl->rows = pl->tc ? 128 : 16 * pl->row_blocks * pl->warp_rows;
   pl->rg_count = (pl->R + pl->rows - 1) / pl->rows;
   pl->max_pages = pages_bound(p);
   const int sm = resolve_sm_count(p, sm_count_in);
   if (sm <= 0) return fail(XQA_ERR_CUDA, "cannot query the SM count of the current device");
   int occ = 0;
   cudaError_t e;
-  if (p->kv_dtype == XQA_E4M3)
+  if (pl->tc)
+    e = xqa::gqa_tc_launch(p->kv_dtype == XQA_BF16, D, false, dim3(), nullptr, nullptr, nullptr, nullptr, &occ);
+  else if (p->kv_dtype == XQA_E4M3)
     e = xqa::gqa_launch_e4m3(D, pl->row_blocks, pl->warp_rows, false, dim3(), nullptr, nullptr, nullptr, nullptr,
                              &occ);
   else if (p->kv_dtype == XQA_BF16)
@@ -232,7 +243,7 @@ xqa_status plan_gqa(const xqa_params* p, int sm_count_in, Plan* pl) {
     e = xqa::gqa_launch_f16(D, pl->row_blocks, pl->warp_rows, false, dim3(), nullptr, nullptr, nullptr, nullptr,
                             &occ);
   if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
-  const int tok = stage_tokens(p, pl->row_blocks, pl->warp_rows);
+  const int tok = pl->tc ? 128 : stage_tokens(p, pl->row_blocks, pl->warp_rows);
   const int stage_pages = p->page_size <= tok ? tok / p->page_size : 1;
   choose_splits(p, pl, sm, occ, stage_pages);
   const int64_t units = int64_t(p->batch_size) * p->num_kv_heads * pl->rg_count;
@@ -367,7 +378,7 @@ size_t xqa_semaphore_count(const xqa_params* p) {
   const int R = p->q_seq_len * G;
   int rb = 1, wr = 1;
   row_shape(p->head_dim, R, &rb, &wr);
-  const int rows = 16 * rb * wr;
+  const int rows = use_tc(p, R) ? 128 : 16 * rb * wr;
   return size_t(p->batch_size) * p->num_kv_heads * ((R + rows - 1) / rows);
 }
 
@@ -380,7 +391,7 @@ xqa_status xqa_decode(const xqa_params* p, void* ws, size_t ws_bytes, uint32_t* 
   st = check_buffers(pl, ws, ws_bytes, sems);
   if (st != XQA_OK) return st;
   CUtensorMap tk, tv;
-  const int box_rows = std::min(p->page_size, stage_tokens(p, pl.row_blocks, pl.warp_rows));
+  const int box_rows = std::min(p->page_size, pl.tc ? 64 : stage_tokens(p, pl.row_blocks, pl.warp_rows));
   st = make_maps(p, pl.D, box_rows, &tk, &tv);
   if (st != XQA_OK) return st;
   xqa::DecodeArgs a;
@@ -388,7 +399,9 @@ xqa_status xqa_decode(const xqa_params* p, void* ws, size_t ws_bytes, uint32_t* 
   dim3 grid(pl.nsplit, p->num_kv_heads * pl.rg_count, p->batch_size);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (p->kv_dtype == XQA_E4M3)
+  if (pl.tc)
+    e = xqa::gqa_tc_launch(p->kv_dtype == XQA_BF16, pl.D, true, grid, &tk, &tv, &a, s, nullptr);
+  else if (p->kv_dtype == XQA_E4M3)
     e = xqa::gqa_launch_e4m3(pl.D, pl.row_blocks, pl.warp_rows, true, grid, &tk, &tv, &a, s, nullptr);
   else if (p->kv_dtype == XQA_BF16)
     e = xqa::gqa_launch_bf16(pl.D, pl.row_blocks, pl.warp_rows, true, grid, &tk, &tv, &a, s, nullptr);

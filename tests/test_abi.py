@@ -116,18 +116,24 @@ def test_null_params_rejected(lib):
 
 def test_semaphore_count_is_one_per_row_group(lib):
     assert lib.xqa_semaphore_count(ctypes.byref(fake_params())) == 4 * 8
-    # up to 64 rows per kv head (here 8 tokens x G 8) share one CTA row group
-    p = fake_params(num_q_heads=64, q_seq_len=8)
+    # 16-bit K/V: more than 16 rows per kv head (D=128) run 128-row tensor-core tiles
+    p = fake_params(num_q_heads=64, q_seq_len=8)       # 64 rows
     assert lib.xqa_semaphore_count(ctypes.byref(p)) == 4 * 8 * 1
-    # 128 rows -> two 64-row groups
-    p = fake_params(num_q_heads=64, q_seq_len=16)
+    p = fake_params(num_q_heads=64, q_seq_len=16)      # 128 rows
+    assert lib.xqa_semaphore_count(ctypes.byref(p)) == 4 * 8 * 1
+    p = fake_params(num_q_heads=64, q_seq_len=32)      # 256 rows -> two row groups
     assert lib.xqa_semaphore_count(ctypes.byref(p)) == 4 * 8 * 2
-    # D=64: 32 rows (two blocks per warp), then 64-row groups
+    # e4m3 K/V: warp row groups of up to 64 rows
+    p = fake_params(num_q_heads=64, q_seq_len=8, kv_dtype=X.XQA_E4M3)
+    assert lib.xqa_semaphore_count(ctypes.byref(p)) == 4 * 8 * 1
+    p = fake_params(num_q_heads=64, q_seq_len=16, kv_dtype=X.XQA_E4M3)
+    assert lib.xqa_semaphore_count(ctypes.byref(p)) == 4 * 8 * 2
+    # D=64: 32 rows (two blocks per warp), then 128-row tensor-core tiles
     p = fake_params(head_dim=64, num_q_heads=64, q_seq_len=4)
     assert lib.xqa_semaphore_count(ctypes.byref(p)) == 4 * 8 * 1
-    p = fake_params(head_dim=64, num_q_heads=128, q_seq_len=4)
-    assert lib.xqa_semaphore_count(ctypes.byref(p)) == 4 * 8 * 1
     p = fake_params(head_dim=64, num_q_heads=256, q_seq_len=4)
+    assert lib.xqa_semaphore_count(ctypes.byref(p)) == 4 * 8 * 1
+    p = fake_params(head_dim=64, num_q_heads=256, q_seq_len=8)
     assert lib.xqa_semaphore_count(ctypes.byref(p)) == 4 * 8 * 2
 
 
