@@ -348,8 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[C::kSFree + sb]);
       }
-      // window, spec mask and the split's end by select (never multiply by
-      // 0); the maximum over the raw logits in four independent chains
+      // scale; window, spec mask and the split's end by select (never
+      // multiply by 0); the maximum in four independent chains
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (ok) {
         const bool edge = tile0 + kC > t_end || tile0 <= row_lb || (a.mask && tile0 + kC > spec0);
@@ -359,13 +359,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int tt = tile0 + k;
             bool v = tt < t_end && tt >= row_lb;
             if (a.mask && tt >= spec0) v = v && ((row_mw >> (tt - spec0)) & 1u);
-            x[k] = v ? x[k] : -INFINITY;
+            x[k] = v ? x[k] * lscale : -INFINITY;
           }
+        } else {
+#pragma unroll
+          for (int k = 0; k < kC; ++k) x[k] *= lscale;
         }
 #pragma unroll
         for (int k = 0; k < kC; ++k) mx4[k & 3] = fmaxf(mx4[k & 3], x[k]);
-        // (lscale > 0: the maximum of the scaled logits is the scaled maximum)
-        rowx[h * kRows + t] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * lscale;
+        rowx[h * kRows + t] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       }
       // both halves of every row published their maxima
       if (named_bar_or(1, kSoft, !ok)) {
@@ -391,15 +393,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the [64-token chunk][128 rows][128 B] swizzled P tile
       uint8_t* prow = smem + C::kOffP + sb * C::kPBytes + h * 16384;
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
-      const float mneg = m_ref == -INFINITY ? 0.f : -m_ref;
 #pragma unroll
       for (int u = 0; u < kC / 8; ++u) {
         uint32_t w4[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          // 2^(s * lscale - m): one fma per weight (-inf gives +0)
-          const float p0 = m_ref == -INFINITY ? 0.f : ex2(fmaf(x[8 * u + 2 * e], lscale, mneg));
-          const float p1 = m_ref == -INFINITY ? 0.f : ex2(fmaf(x[8 * u + 2 * e + 1], lscale, mneg));
+          const float p0 = m_ref == -INFINITY ? 0.f : ex2(x[8 * u + 2 * e] - m_ref);
+          const float p1 = m_ref == -INFINITY ? 0.f : ex2(x[8 * u + 2 * e + 1] - m_ref);
           w4[e] = pack_f32x2(p0, p1, kBf16);
           const float2 rr = unpack_16x2(w4[e], kBf16);
           ls[e] += rr.x + rr.y;

@@ -929,12 +929,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             vis |= uint32_t(v) << k;
           }
         }
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // independent chains
 #pragma unroll
         for (int k = 0; k < kC; ++k) {
           const float x = (vis >> k) & 1u ? s[k] * lscale : -INFINITY;
           s[k] = x;
-          mx = fmaxf(mx, x);
+          mx4[k & 3] = fmaxf(mx4[k & 3], x);
         }
+        mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
         // (one buffer: the reads of the previous subtile's maxima precede
         // the barrier that ended it)
         rowx[h * kRows + t] = mx;
@@ -957,6 +959,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // weights so O / l stays a convex combination
       uint8_t* pstage = smem + SL::kOffPS + p2 * kPBytes;
       float* fstage = reinterpret_cast<float*>(smem + SL::kOffFS + p2 * kFBytes);
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};  // independent chains
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         uint32_t w4[4];
@@ -965,11 +968,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const float p0 = m_ref == -INFINITY ? 0.f : ex2(s[8 * u + 2 * e] - m_ref);
           const float p1 = m_ref == -INFINITY ? 0.f : ex2(s[8 * u + 2 * e + 1] - m_ref);
           w4[e] = pack_f32x2(p0, p1, !F8);
-          const float2 r = unpack_16x2(w4[e], !F8);
-          l_half += r.x + r.y;
+          if constexpr (F8) {
+            // f16 keeps 11 significant bits: summing the unrounded weights
+            // differs from the rounded ones by < 2^-12 of the sum
+            ls[e] += p0 + p1;
+          } else {
+            const float2 r = unpack_16x2(w4[e], true);
+            ls[e] += r.x + r.y;
+          }
         }
         *reinterpret_cast<uint4*>(pstage + umma::sw128(t, 4 * h + u)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
       }
+      l_half += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       if (h == 0) fstage[t] = f;
       umma::fence_proxy_async_smem();
       // every thread wrote its P and factor; does any row need O rescaled?
