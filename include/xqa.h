@@ -135,17 +135,21 @@ size_t xqa_semaphore_count(const xqa_params* params);
 xqa_status xqa_decode(const xqa_params* params, void* workspace, size_t workspace_bytes,
                       uint32_t* semaphores, xqa_stream_t stream);
 
-/* Same sizing queries for the MLA latent variant (num_kv_heads = 1). */
+/* Same sizing queries for the MLA latent variant (num_kv_heads = 1).  The
+   workspace holds the split partials (fp32).  xqa_mla_semaphore_count returns
+   0: the MLA call takes no semaphores (its split merge is a second kernel in
+   the same stream). */
 size_t xqa_mla_workspace_size(const xqa_params* params, int v_head_dim, int sm_count);
 size_t xqa_mla_semaphore_count(const xqa_params* params, int v_head_dim);
 
 /* MLA latent decode: params->num_kv_heads must be 1, head_dim the latent width
    (kv_lora_rank + rope) and v_head_dim the kv_lora_rank prefix used as V.
    k_cache and v_cache may be the same pointer (the latent cache).  q and
-   output must be 16-byte aligned.  The semaphores (xqa_mla_semaphore_count,
-   zero on the first call) are left zero by every call that completes; after
-   a call that reported a pipeline timeout (bit 1 of error_word) their
-   contents are undefined: zero them again before the next call. */
+   output must be 16-byte aligned.  One or two kernel launches on `stream`:
+   the decode, then (when the workspace size is not 0) the merge of the
+   sequences cut across clusters or splits, launched with programmatic
+   dependent launch (its CTAs wait for the decode grid).  `semaphores` is
+   unused and may be NULL. */
 xqa_status xqa_mla_decode(const xqa_params* params, int v_head_dim, void* workspace,
                           size_t workspace_bytes, uint32_t* semaphores, xqa_stream_t stream);
 

@@ -10,14 +10,8 @@ cudaError_t gqa_launch_bf16(int head_dim, int row_blocks, int warp_rows, bool la
     return gqa_launch_one<kKvBf16, 64, 1, 1>(launch, grid, tk, tv, args, stream, ctas_per_sm);
   if (head_dim == 64 && row_blocks == 2 && warp_rows == 1)
     return gqa_launch_one<kKvBf16, 64, 2, 1>(launch, grid, tk, tv, args, stream, ctas_per_sm);
-  if (head_dim == 64 && row_blocks == 1 && warp_rows == 4)
-    return gqa_launch_one<kKvBf16, 64, 1, 4>(launch, grid, tk, tv, args, stream, ctas_per_sm);
   if (head_dim == 128 && row_blocks == 1 && warp_rows == 1)
     return gqa_launch_one<kKvBf16, 128, 1, 1>(launch, grid, tk, tv, args, stream, ctas_per_sm);
-  if (head_dim == 128 && row_blocks == 1 && warp_rows == 2)
-    return gqa_launch_one<kKvBf16, 128, 1, 2>(launch, grid, tk, tv, args, stream, ctas_per_sm);
-  if (head_dim == 128 && row_blocks == 1 && warp_rows == 4)
-    return gqa_launch_one<kKvBf16, 128, 1, 4>(launch, grid, tk, tv, args, stream, ctas_per_sm);
   return cudaErrorInvalidValue;
 }
 

@@ -9,7 +9,8 @@
 namespace xqa {
 
 // kv: 0 f16, 1 bf16, 2 e4m3.  row_blocks: 16-row MMA blocks per consumer
-// warp; warp_rows: warp row groups splitting a CTA's rows (1, 2 or 4).
+// warp; warp_rows: warp row groups splitting a CTA's rows (1, 2 or 4; built
+// for e4m3 K/V only, since larger 16-bit tiles take the tensor-core kernel).
 // Returns cudaErrorInvalidValue when no kernel is built for (kv, head_dim,
 // row_blocks, warp_rows).  With launch == false only the occupancy (CTAs per
 // SM) is reported.

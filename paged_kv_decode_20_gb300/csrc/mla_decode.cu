@@ -197,6 +197,14 @@ constexpr int kMaxSplits = 64;       // merge weights [128][splits] fit in share
 #define XQA_MLA_WAVES 3
 #endif
 constexpr int kWaves = XQA_MLA_WAVES;  // cluster waves the split plan aims for
+#ifndef XQA_MLA_PIECE_TOKENS
+#define XQA_MLA_PIECE_TOKENS 768
+#endif
+// a persistent piece's fixed cost in KV tokens of streaming time: the query
+// load, the pipeline fill and drain, and the epilogue's stores, all latency-
+// bound while the other clusters stream the cache (measured on the latent
+// workload: 768 tokens, about 14 us, balances the clusters' end times)
+constexpr int kPieceTokens = XQA_MLA_PIECE_TOKENS;
 
 struct MlaArgs {
   const uint8_t* q;   // [B, qs, Hq, 576] bf16 or e4m3
@@ -207,14 +215,14 @@ struct MlaArgs {
   const uint16_t* mask;
   const float* q_scale_dev;
   const float* kv_scale_dev;
-  float* ws;
-  uint32_t* sems;
+  float* ws;    // split partials: [slot][128 rows][512 + 4] fp32 (O, then m and l)
   uint32_t* err;
   float* lse;  // optional [B, qs, Hq] natural-log log-sum-exp per row
   int64_t num_pages;
   int B, Hq, qs, ps, pps, win, nsplit, split_pages, mask_words;
   int R;    // real query rows Hq * qs (<= 128); rows R..127 of the tile are padding
   int ncl;  // persistent clusters
+  int piece_cost;  // scheduled pages charged to each sequence start (a piece's fixed cost)
   float q_scale, kv_scale, softmax_scale, rcp_out_scale;
 };
 
@@ -311,6 +319,27 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
       " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
+}
+
+// An L2 policy that keeps the lines it tags ahead of streamed data: a split
+// partial is read back by the merge, up to a whole call later, while the
+// other clusters stream the cache through L2.
+__device__ __forceinline__ uint64_t l2_keep_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void st_keep4(float* dst, float x, float y, float z, float w, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst), "f"(x), "f"(y), "f"(z),
+               "f"(w), "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void st_keep2(float* dst, float x, float y, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;" ::"l"(dst), "f"(x), "f"(y), "l"(pol) : "memory");
+}
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // The cluster whose slice of the persistent schedule holds scheduled page P
@@ -419,24 +448,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 
   // ---- schedule.  Up to kOrderMaxB sequences the clusters are persistent:
-  // cluster k takes the k-th of ncl equal slices of the batch's pages laid end
-  // to end (an empty sequence counts as one page, so that one cluster writes
-  // its output) and runs the pieces of the sequences that meet its slice one
-  // after another.  A sequence cut across clusters leaves one fp32 partial per
-  // piece in workspace slot (cluster, 0) for a cluster's first piece or
-  // (cluster, 1) for its last; the last CTA of each column half to finish the
-  // sequence merges them.  Larger batches take one fixed split per cluster.
+  // cluster k takes the k-th of ncl equal slices of the batch's scheduled
+  // pages laid end to end and runs the pieces of the sequences whose pages
+  // meet its slice one after another.  A sequence schedules piece_cost
+  // overhead pages and then its own pages (an empty sequence counts one page,
+  // so that one cluster writes its output): a slice that starts more
+  // sequences gets fewer pages, and a slice that covers only a sequence's
+  // overhead takes no piece of it.  A sequence cut across clusters leaves one
+  // fp32 partial per piece in workspace slot (cluster, 0) for the slice's
+  // first sequence or (cluster, 1) for its last; the last CTA of each column
+  // half to finish the sequence merges them.  A cluster runs its cut pieces
+  // first (the slice's first sequence, then its last when that one runs on
+  // past the slice), then the whole sequences between them: partials and
+  // merges happen early, while the call's end is made of whole sequences.
+  // Larger batches take one fixed split per cluster.
   const bool persistent = a.B <= kOrderMaxB;
   const int k_cl = int(blockIdx.x >> 1);
   int64_t tot = 1, s_lo = 0, s_hi = 0;  // all scheduled pages; this cluster's slice
   int ncl = a.ncl;                      // clusters with a non-empty slice
-  int cur_b = b;                        // next sequence to look at
+  int cur_b = b;                        // next sequence to look at (in order)
   int64_t cur_S = 0;                    // its first scheduled page
+  int z_b = -1;                         // the slice's last sequence when it runs on past the slice
+  int64_t z_S = 0;                      // (taken second), and its first scheduled page
   if (persistent) {
     int* sc = reinterpret_cast<int*>(smem);  // scratch: scheduled pages per sequence
     for (int bb = tid; bb < a.B; bb += kThreads) {
       const SeqGeom g = seq_geom(a, bb);
-      sc[bb] = max(1, g.pg_last - g.pg_first);
+      sc[bb] = a.piece_cost + max(1, g.pg_last - g.pg_first);
     }
     __syncthreads();
     tot = 0;
@@ -449,6 +487,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     s_hi = k_cl < ncl ? tot * (k_cl + 1) / ncl : tot;
     cur_b = 0;
     while (cur_b < a.B && cur_S + sc[cur_b] <= s_lo) cur_S += sc[cur_b++];
+    if (cur_b < a.B) {
+      int bb = cur_b;
+      int64_t S = cur_S;
+      while (bb + 1 < a.B && S + sc[bb] + a.piece_cost < s_hi) S += sc[bb++];
+      if (bb > cur_b && S + sc[bb] > s_hi) {
+        z_b = bb;
+        z_S = S;
+      }
+    }
     __syncthreads();  // the scratch is reused below
   }
   if (tid == 0) flags[0] = flags[1] = flags[2] = flags[3] = 0;  // also for a cluster with no piece
@@ -468,15 +515,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   constexpr uint32_t kIdescPV = umma::idesc_f16(kRows, kHalf, !F8, false, true);
 
   bool first_piece = true;
+  int order = 0;  // pieces taken so far (persistent)
 
   for (;;) {
   // ---- the piece: sequence b, pages [pg_lo, pg_hi), its index among the
   // sequence's nvalid pieces, and where its partial goes
   int nvalid, pg_lo, pg_hi, kf = 0;
-  bool cl_first = true;  // the piece is its cluster's first (persistent)
+  bool cl_first = true;  // the piece is its slice's first sequence (persistent)
+  const bool z_now = persistent && order == 1 && z_b >= 0;  // the slice's last sequence, out of order
+  int64_t S_b = 0;                                          // the sequence's first scheduled page
   if (persistent) {
-    if (cur_b >= a.B || cur_S >= s_hi) break;
-    b = cur_b;
+    if (z_now) {
+      b = z_b;
+      S_b = z_S;
+    } else {
+      if (cur_b >= a.B || cur_S + a.piece_cost >= s_hi || cur_b == z_b) break;
+      b = cur_b;
+      S_b = cur_S;
+    }
   }
   // ---- sequence geometry (identical in both CTAs and every split)
   const SeqGeom geo = seq_geom(a, b);
@@ -489,14 +545,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int npages = max(0, pg_last - pg_first);
   const int nsched = max(1, npages);  // scheduled pages (persistent)
   if (persistent) {
-    const int64_t v_lo = max(s_lo, cur_S) - cur_S, v_hi = min(s_hi, cur_S + nsched) - cur_S;
+    const int64_t S0 = S_b + a.piece_cost;  // the sequence's first own page
+    const int64_t v_lo = max(s_lo, S0) - S0, v_hi = min(s_hi, S0 + nsched) - S0;
     pg_lo = pg_first + int(min(v_lo, int64_t(npages)));
     pg_hi = pg_first + int(min(v_hi, int64_t(npages)));
-    kf = cluster_of(cur_S, tot, ncl);
-    const int kl = cluster_of(cur_S + nsched - 1, tot, ncl);
+    kf = cluster_of(S0, tot, ncl);
+    const int kl = cluster_of(S0 + nsched - 1, tot, ncl);
     nvalid = npages == 0 ? 0 : kl - kf + 1;
     split = k_cl - kf;
-    cl_first = cur_S <= s_lo;
+    cl_first = S0 <= s_lo;
   } else {
     nvalid = (npages + a.split_pages - 1) / a.split_pages;
     if (split >= max(nvalid, 1)) break;  // both CTAs of the cluster leave together
@@ -558,6 +615,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();  // the peer's barriers exist before any remote access
   umma::fence_after_sync();
   const int32_t* pt = a.page_table + int64_t(b) * a.pps;
+  if (persistent && logit_cta && tid == 32 * kSoftWarp0) {
+    // the query of this cluster's next sequence, into L2 ahead of its piece
+    // (a latency-bound load while the other clusters stream the cache)
+    int nb = -1;
+    if (z_b >= 0 && order == 0)
+      nb = z_b;
+    else if (z_now)
+      nb = cur_b < z_b ? cur_b : -1;
+    else if (b + 1 < a.B && b + 1 != z_b && S_b + 2 * a.piece_cost + nsched < s_hi)
+      nb = b + 1;
+    if (nb >= 0) {
+      const int64_t qbytes = int64_t(a.qs) * a.Hq * kDim * (F8 ? 1 : 2);
+      prefetch_l2_bulk(a.q + int64_t(nb) * qbytes, uint32_t(qbytes));
+    }
+  }
 
   if (warp == 0) {
     // ================= TMA producer =================
@@ -1113,6 +1185,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                            (a.lse && h == 0 && real) ? a.lse + row_g : nullptr);
       }
       const int64_t slot = persistent ? 2 * int64_t(k_cl) + (cl_first ? 0 : 1) : int64_t(b) * a.nsplit + split;
+      const uint64_t keep = l2_keep_policy();
       float* wrow = a.ws + (slot * kRows + t) * (kLatent + 4);
 #pragma unroll 1
       for (int part = 0; part < kHalf / 32; ++part) {
@@ -1135,15 +1208,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 pack_f32x2(o[8 * v + 4] * mul, o[8 * v + 5] * mul, true),
                                 pack_f32x2(o[8 * v + 6] * mul, o[8 * v + 7] * mul, true));
         } else {
-          float4* dst = reinterpret_cast<float4*>(wrow + col);
 #pragma unroll
-          for (int v = 0; v < 8; ++v) dst[v] = make_float4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+          for (int v = 0; v < 8; ++v) st_keep4(wrow + col + 4 * v, o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3], keep);
         }
       }
-      if (!single && h == 0) {
-        wrow[kLatent] = m_fin;
-        wrow[kLatent + 1] = l_fin;
-      }
+      if (!single && h == 0) st_keep2(wrow + kLatent, m_fin, l_fin, keep);
     }
     // the partial is visible device-wide before either CTA of the cluster
     // takes a merge ticket
@@ -1164,104 +1233,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   cluster_sync();
   if (flags[3]) break;
-  if (nvalid > 1) {
-  // ---- split-KV: the last CTA of this column half merges every piece (the
-  // output CTA wrote the whole partial; each CTA of the cluster takes its
-  // ticket after the cluster barrier that follows those writes)
-  __threadfence();
-  __syncthreads();
-  const int unit = b * 2 + int(c);
-  if (tid == 0) {
-    const uint32_t prev = atomicAdd(a.sems + unit, 1u);
-    flags[1] = prev == uint32_t(nvalid - 1) ? 1 : 0;
-  }
-  __syncthreads();
-  if (flags[1]) {
-  __threadfence();
-  const float kv_scale = ldscale(a.kv_scale_dev, a.kv_scale);
-  constexpr int kStride = kLatent + 4;
-  // the partial of piece sp of this sequence: a persistent piece sits in its
-  // cluster's slot 0 unless it is the sequence's first piece starting inside
-  // the cluster's slice (slot 1)
-  const bool first_in_slot1 = persistent && cur_S > tot * kf / ncl;
-  const int64_t base_slot = persistent ? 2 * int64_t(kf) : int64_t(b) * a.nsplit;
-  const int64_t slot_step = persistent ? 2 : 1;
-#define PART(sp) (a.ws + (base_slot + slot_step * (sp) + ((sp) == 0 && first_in_slot1 ? 1 : 0)) * kRows * kStride)
-  // phase 1: one thread per row folds the split maxima, the sink and the
-  // output scales into one weight per (row, split), staged in shared memory
-  float* wts = reinterpret_cast<float*>(smem);  // [kRows][nvalid]
-  if (tid < kRows) {
-    const int row = tid;
-    float M = -INFINITY;
-    for (int sp = 0; sp < nvalid; ++sp) M = fmaxf(M, __ldcg(PART(sp) + int64_t(row) * kStride + kLatent));
-    float l = 0.f;
-    for (int sp = 0; sp < nvalid; ++sp) {
-      const float* src = PART(sp) + int64_t(row) * kStride + kLatent;
-      const float ms = __ldcg(src);
-      const float f = ms == -INFINITY ? 0.f : exp2f(ms - M);
-      wts[row * nvalid + sp] = f;
-      l += f * __ldcg(src + 1);
-    }
-    const float sig = a.sinks ? __ldg(a.sinks + row % a.Hq) * kLog2e : -INFINITY;
-    const int64_t row_g = (int64_t(b) * a.qs + row / a.Hq) * a.Hq + row % a.Hq;
-    const float mul = finalize_row(M, l, sig, kv_scale * a.rcp_out_scale,
-                                   (a.lse && c == 0 && row < a.R) ? a.lse + row_g : nullptr);
-    for (int sp = 0; sp < nvalid; ++sp) wts[row * nvalid + sp] *= mul;
-  }
-  __syncthreads();
-  // phase 2: every (row, 4-column group) sums the weighted partials; each
-  // thread keeps four items and four splits of loads in flight (the merge
-  // ends the call for the last sequence, so its latency counts)
-  constexpr int kIt = 4;
-  constexpr int kItems = kRows * (kHalf / 4);
-  for (int base = tid; base < kItems; base += kThreads * kIt) {
-    float4 acc[kIt];
-    int rows[kIt], cols[kIt];
-#pragma unroll
-    for (int u = 0; u < kIt; ++u) {
-      const int item = min(base + u * kThreads, kItems - 1);
-      rows[u] = item / (kHalf / 4);
-      cols[u] = int(c) * kHalf + 4 * (item % (kHalf / 4));
-      acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    for (int sp0 = 0; sp0 < nvalid; sp0 += 4) {
-      float4 v[kIt][4];
-#pragma unroll
-      for (int u = 0; u < kIt; ++u)
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          v[u][q] = sp0 + q < nvalid ? __ldcg(reinterpret_cast<const float4*>(PART(sp0 + q) +
-                                                                              int64_t(rows[u]) * kStride + cols[u]))
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int u = 0; u < kIt; ++u)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float f = sp0 + q < nvalid ? wts[rows[u] * nvalid + sp0 + q] : 0.f;
-          acc[u].x += f * v[u][q].x;
-          acc[u].y += f * v[u][q].y;
-          acc[u].z += f * v[u][q].z;
-          acc[u].w += f * v[u][q].w;
-        }
-    }
-#pragma unroll
-    for (int u = 0; u < kIt; ++u) {
-      if (base + u * kThreads >= kItems || rows[u] >= a.R) continue;
-      const int ii = rows[u] / a.Hq, hh = rows[u] % a.Hq;
-      const int64_t oi = ((int64_t(b) * a.qs + ii) * a.Hq + hh) * kLatent + cols[u];
-      *reinterpret_cast<uint2*>(a.out + oi) =
-          make_uint2(pack_f32x2(acc[u].x, acc[u].y, true), pack_f32x2(acc[u].z, acc[u].w, true));
-    }
-  }
-#undef PART
-  if (tid == 0) a.sems[unit] = 0u;
-  }  // last CTA
-  __syncthreads();  // shared memory (the merge weights) is free again
-  }  // nvalid > 1
   first_piece = false;
   if (!persistent) break;
-  cur_S += nsched;
-  ++cur_b;
+  if (!z_now) {
+    cur_S += a.piece_cost + nsched;
+    ++cur_b;
+  }
+  ++order;
   }  // pieces
 
   // ---- teardown
@@ -1272,6 +1250,172 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     umma::tmem_dealloc(tmem, kTmemCols);
   }
   if (flags[0] && tid == 0 && a.err) atomicOr(a.err, kErrTimeout);
+}
+
+// ---------------------------------------------------------------- split merge
+// A second kernel in the same stream (programmatic dependent launch: its
+// CTAs wait until every decode CTA has finished and its writes are visible)
+// merges the partials of every sequence cut across clusters or splits with
+// the log-sum-exp rule of merge_attn_states, adds the sinks and the output
+// scales, and writes the bf16 rows (and their log-sum-exp).  It runs while
+// the memory system is otherwise idle: merged at the end of the pieces that
+// finish a sequence, the same loads compete with every cluster still
+// streaming the cache, and the last ones end the call.
+// Persistent: kMergeCtasPerSm CTAs per SM take the work items (sequence,
+// column half, block of kMergeRows rows) in turn; each CTA first lays out the
+// schedule of every sequence once (the decode kernel's integer arithmetic on
+// the same lengths: pieces and partial slots).  Per item, the first pieces'
+// partial rows are requested first; meanwhile one thread per row folds the
+// pieces' maxima, the sink and the output scales into one weight per (row,
+// piece) in shared memory (the merge_attn_states rule); then every thread
+// sums its four rows x four columns.
+constexpr int kMergeRows = 16;
+constexpr int kMergeThreads = 256;
+constexpr int kMergeChunk = 2;  // pieces of partial rows in flight per thread
+constexpr int kMergeCtasPerSm = 3;
+static_assert(kOrderMaxB <= kMergeThreads, "one sequence per thread in the schedule scan");
+
+__global__ void __launch_bounds__(kMergeThreads, kMergeCtasPerSm) mla_merge_kernel(const MlaArgs a) {
+  __shared__ int s_nvalid[kOrderMaxB], s_first[kOrderMaxB];  // per sequence (persistent schedule)
+  __shared__ long long s_warp[kMergeThreads / 32];
+  __shared__ float s_w[kMergeRows * kMaxPieces];  // per (row, piece): the maximum, then the weight
+  __shared__ float s_l[kMergeRows * kMaxPieces];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool persistent = a.B <= kOrderMaxB;
+  if (persistent) {
+    // scheduled pages per sequence, their inclusive prefix sum over the batch
+    long long sc = 0;
+    int npages = 0;
+    if (tid < a.B) {
+      const SeqGeom g = seq_geom(a, tid);
+      npages = max(0, g.pg_last - g.pg_first);
+      sc = a.piece_cost + max(1, npages);
+    }
+    long long incl = sc;
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    long long before_warp = 0, tot = 0;
+    for (int w = 0; w < kMergeThreads / 32; ++w) {
+      if (w < warp) before_warp += s_warp[w];
+      tot += s_warp[w];
+    }
+    if (tid < a.B) {
+      const int64_t S0 = before_warp + incl - sc + a.piece_cost;
+      const int ncl = int(min(int64_t(a.ncl), int64_t(tot)));
+      const int kf = cluster_of(S0, tot, ncl);
+      const int kl = cluster_of(S0 + max(1, npages) - 1, tot, ncl);
+      s_nvalid[tid] = npages == 0 ? 0 : kl - kf + 1;
+      // slot 2 kf, or 2 kf + 1 when the first piece starts inside cluster kf's slice
+      s_first[tid] = 2 * kf + (S0 > tot * kf / ncl ? 1 : 0);
+    }
+    __syncthreads();
+  }
+  // the decode grid has finished and its partials are visible
+  pdl_wait();
+  pdl_launch_dependents();
+  constexpr int kStride = kLatent + 4;
+  constexpr int kQuads = kMergeThreads / (kHalf / 4);  // row groups of the CTA's threads
+  constexpr int kRowsPer = kMergeRows / kQuads;
+  constexpr int kBlocks = kRows / kMergeRows;
+  const int c4 = tid % (kHalf / 4), rq = tid / (kHalf / 4);
+  const float out_mul = ldscale(a.kv_scale_dev, a.kv_scale) * a.rcp_out_scale;
+  const int items = a.B * 2 * kBlocks;
+  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    const int b = item / (2 * kBlocks), c = (item / kBlocks) & 1, r0 = (item % kBlocks) * kMergeRows;
+    if (r0 >= a.R) continue;
+    // pieces; piece 0's slot, and piece sp >= 1's at slot1 + step (sp - 1):
+    // slot 2 (kf + sp) of the persistent schedule, or split sp
+    int nvalid, slot0, slot1, step;
+    if (persistent) {
+      nvalid = s_nvalid[b];
+      slot0 = s_first[b];
+      slot1 = (slot0 & ~1) + 2;
+      step = 2;
+    } else {
+      const SeqGeom g = seq_geom(a, b);
+      nvalid = (max(0, g.pg_last - g.pg_first) + a.split_pages - 1) / a.split_pages;
+      slot0 = b * a.nsplit;
+      slot1 = slot0 + 1;
+      step = 1;
+    }
+    if (nvalid <= 1 || nvalid > kMaxPieces) continue;
+    auto part_row = [&](int sp, int rr) {
+      const int64_t slot = sp == 0 ? slot0 : slot1 + int64_t(step) * (sp - 1);
+      return a.ws + (slot * kRows + r0 + rr) * kStride;
+    };
+    const int nrows = min(kMergeRows, a.R - r0);
+    const int col = c * kHalf + 4 * c4;
+    float4 v[kRowsPer][kMergeChunk];
+    auto load_chunk = [&](int sp0) {
+#pragma unroll
+      for (int q = 0; q < kMergeChunk; ++q)
+#pragma unroll
+        for (int u = 0; u < kRowsPer; ++u) {
+          const int rr = rq + kQuads * u;
+          v[u][q] = (sp0 + q < nvalid && rr < nrows)
+                        ? __ldcg(reinterpret_cast<const float4*>(part_row(sp0 + q, rr) + col))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+    load_chunk(0);
+    // (m, l) of every (row, piece), then one weight per (row, piece)
+    for (int it = tid; it < nrows * nvalid; it += kMergeThreads) {
+      const int rr = it / nvalid, sp = it - rr * nvalid;
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(part_row(sp, rr) + kLatent));
+      s_w[it] = ml.x;
+      s_l[it] = ml.y;
+    }
+    __syncthreads();
+    if (tid < nrows) {
+      float* w = s_w + tid * nvalid;
+      const float* lp = s_l + tid * nvalid;
+      float M = -INFINITY;
+      for (int sp = 0; sp < nvalid; ++sp) M = fmaxf(M, w[sp]);
+      float l = 0.f;
+      for (int sp = 0; sp < nvalid; ++sp) {
+        const float f = w[sp] == -INFINITY ? 0.f : exp2f(w[sp] - M);
+        w[sp] = f;
+        l += f * lp[sp];
+      }
+      const int row = r0 + tid;
+      const int64_t row_g = (int64_t(b) * a.qs + row / a.Hq) * a.Hq + row % a.Hq;
+      const float sig = a.sinks ? __ldg(a.sinks + row % a.Hq) * kLog2e : -INFINITY;
+      const float mul = finalize_row(M, l, sig, out_mul, (a.lse && c == 0) ? a.lse + row_g : nullptr);
+      for (int sp = 0; sp < nvalid; ++sp) w[sp] *= mul;
+    }
+    __syncthreads();
+    float4 acc[kRowsPer];
+#pragma unroll
+    for (int u = 0; u < kRowsPer; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sp0 = 0; sp0 < nvalid; sp0 += kMergeChunk) {
+      if (sp0 > 0) load_chunk(sp0);
+#pragma unroll
+      for (int q = 0; q < kMergeChunk; ++q)
+#pragma unroll
+        for (int u = 0; u < kRowsPer; ++u) {
+          const int rr = rq + kQuads * u;
+          const float f = (sp0 + q < nvalid && rr < nrows) ? s_w[rr * nvalid + sp0 + q] : 0.f;
+          acc[u].x += f * v[u][q].x;
+          acc[u].y += f * v[u][q].y;
+          acc[u].z += f * v[u][q].z;
+          acc[u].w += f * v[u][q].w;
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kRowsPer; ++u) {
+      const int rr = rq + kQuads * u;
+      if (rr >= nrows) continue;
+      const int row = r0 + rr;
+      const int64_t row_g = (int64_t(b) * a.qs + row / a.Hq) * a.Hq + row % a.Hq;
+      *reinterpret_cast<uint2*>(a.out + row_g * kLatent + col) =
+          make_uint2(pack_f32x2(acc[u].x, acc[u].y, true), pack_f32x2(acc[u].z, acc[u].w, true));
+    }
+    __syncthreads();  // the weights are rewritten by the next item
+  }
 }
 
 // ---------------------------------------------------------------- host side
@@ -1297,7 +1441,8 @@ EncodeTiledFn encode_fn() {
 struct Plan {
   int nsplit = 1, split_pages = 1, ncl = 1;
   bool persistent = false;
-  size_t ws_bytes = 0, nsems = 0;
+  size_t ws_bytes = 0;   // split partials, then the per-sequence merge records
+  size_t part_bytes = 0;  // the partials alone
 };
 
 const char* check_shape(const xqa_params* p, int v_head_dim) {
@@ -1344,16 +1489,16 @@ bool plan(const xqa_params* p, int sm_count, Plan* pl) {
   sp = ((sp + stage_pages - 1) / stage_pages) * stage_pages;
   pl->split_pages = sp;
   pl->nsplit = (max_pages + sp - 1) / sp;
-  pl->nsems = size_t(p->batch_size) * 2;
-  pl->ws_bytes = pl->nsplit > 1 ? size_t(p->batch_size) * pl->nsplit * kRows * (kLatent + 4) * sizeof(float) : 0;
+  pl->part_bytes = pl->nsplit > 1 ? size_t(p->batch_size) * pl->nsplit * kRows * (kLatent + 4) * sizeof(float) : 0;
   // up to kOrderMaxB sequences: persistent clusters, one per SM pair (at most
   // kMaxPieces, so that a sequence's merge weights fit in shared memory), two
   // partial slots each
   pl->persistent = p->batch_size <= kOrderMaxB;
   if (pl->persistent) {
     pl->ncl = std::max(1, std::min(sm / 2, kMaxPieces));
-    pl->ws_bytes = pl->ncl > 1 ? size_t(pl->ncl) * 2 * kRows * (kLatent + 4) * sizeof(float) : 0;
+    pl->part_bytes = pl->ncl > 1 ? size_t(pl->ncl) * 2 * kRows * (kLatent + 4) * sizeof(float) : 0;
   }
+  pl->ws_bytes = pl->part_bytes;
   return true;
 }
 
@@ -1368,7 +1513,7 @@ size_t mla_workspace_size(const xqa_params* p, int v_head_dim, int sm_count) {
 
 size_t mla_semaphore_count(const xqa_params* p, int v_head_dim) {
   if (!p || mla::check_shape(p, v_head_dim)) return size_t(-1);
-  return size_t(p->batch_size) * 2;
+  return 0;  // the split merge is a second kernel: no tickets
 }
 
 xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_bytes, uint32_t* sems,
@@ -1396,15 +1541,12 @@ xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_b
       snprintf(err, err_len, "workspace needs %zu bytes, got %zu", pl.ws_bytes, ws ? ws_bytes : size_t(0));
       return XQA_ERR_WORKSPACE_TOO_SMALL;
     }
-    if (!sems) {
-      snprintf(err, err_len, "semaphores are required (%zu needed)", pl.nsems);
-      return XQA_ERR_WORKSPACE_TOO_SMALL;
-    }
     if (reinterpret_cast<uintptr_t>(ws) & 15) {
       snprintf(err, err_len, "workspace must be 16-byte aligned");
       return XQA_ERR_INVALID_ARG;
     }
   }
+  (void)sems;
   EncodeTiledFn enc = encode_fn();
   if (!enc) {
     snprintf(err, err_len, "cuTensorMapEncodeTiled is unavailable");
@@ -1474,7 +1616,6 @@ xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_b
   a.q_scale_dev = p->q_scale_dev;
   a.kv_scale_dev = p->kv_scale_dev;
   a.ws = static_cast<float*>(ws);
-  a.sems = sems;
   a.err = p->error_word;
   a.lse = p->lse;
   a.num_pages = p->num_pages;
@@ -1487,6 +1628,7 @@ xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_b
   a.nsplit = pl.nsplit;
   a.split_pages = pl.split_pages;
   a.ncl = pl.ncl;
+  a.piece_cost = (kPieceTokens + p->page_size - 1) / p->page_size;
   a.mask_words = ((p->q_seq_len + 31) / 32) * 2;
   a.q_scale = p->q_scale;
   a.kv_scale = p->kv_scale;
@@ -1515,6 +1657,26 @@ xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_b
   if (e != cudaSuccess) {
     snprintf(err, err_len, "MLA kernel launch: %s", cudaGetErrorString(e));
     return XQA_ERR_CUDA;
+  }
+  if (pl.ws_bytes > 0) {
+    // the split merge, launched behind the decode kernel (its CTAs wait in
+    // griddepcontrol.wait for the decode grid to finish)
+    cudaLaunchConfig_t mcfg = {};
+    const int sm = sm_count_of(p, 0);
+    const int items = p->batch_size * 2 * (kRows / kMergeRows);
+    mcfg.gridDim = dim3(std::max(1, std::min(items, sm * kMergeCtasPerSm)), 1, 1);
+    mcfg.blockDim = dim3(kMergeThreads);
+    mcfg.stream = stream;
+    cudaLaunchAttribute mattr[1];
+    mattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    mattr[0].val.programmaticStreamSerializationAllowed = 1;
+    mcfg.attrs = mattr;
+    mcfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&mcfg, mla_merge_kernel, a);
+    if (e != cudaSuccess) {
+      snprintf(err, err_len, "MLA merge kernel launch: %s", cudaGetErrorString(e));
+      return XQA_ERR_CUDA;
+    }
   }
   return XQA_OK;
 }
