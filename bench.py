@@ -40,7 +40,7 @@ from paged_kv_decode_20_gb300 import workloads as W  # noqa: E402
 METRIC = "paged decode attention: KV GB/s & % of GB300 HBM peak; decode tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_NAMES = {1: "gqa_decode_kernel", 2: "gqa_decode_kernel", 3: "gqa_decode_kernel",
-                4: "gqa_decode_kernel", 5: "mla_decode_kernel", "large_group": "gqa_decode_kernel"}
+                4: "gqa_decode_kernel", 5: "mla_decode_kernel", "large_group": "gqa_tc_kernel"}
 
 
 def parse():
@@ -101,8 +101,10 @@ def peaks():
 
 
 KERNEL_FILES = {
-    "gqa_decode_kernel": ("gqa_", "ptx.cuh", "kernel_args.h", "finalize.cuh", "xqa_api.cu"),
-    "mla_decode_kernel": ("mla_", "umma.cuh", "ptx.cuh", "kernel_args.h", "finalize.cuh"),
+    "gqa_decode_kernel": ("gqa_kernel.cuh", "gqa_launch", "gqa_bf16.cu", "gqa_f16.cu", "gqa_e4m3.cu", "ptx.cuh",
+                          "kernel_args.h", "finalize.cuh", "xqa_api.cu"),
+    "gqa_tc_kernel": ("gqa_tc.cu", "umma.cuh", "ptx.cuh", "kernel_args.h", "finalize.cuh", "xqa_api.cu"),
+    "mla_decode_kernel": ("mla_decode.cu", "umma.cuh", "ptx.cuh", "kernel_args.h", "finalize.cuh"),
 }
 
 
@@ -278,6 +280,7 @@ def time_workload(key, dev, launches, flush):
     achieved = (kv + qb) / (ms * 1e-3) / 1e9
     out = {"workload": workload_name(idx, kv_dtype), "kernel": KERNEL_NAMES[idx],
            "ms_per_launch": round(ms, 5),
+           "kernel_launches_per_call": dec.launches_per_call,
            "timing": "L2 flushed before every launch" if small else "inputs larger than L2 (no flush)",
            "kv_bytes": kv, "q_bytes": qb,
            "kv_gbs": round(kv / (ms * 1e-3) / 1e9, 2),
@@ -320,6 +323,7 @@ def run_gb300(args):
     dec = Decoder(case, error_word=False,
                   out_dtype=torch.float8_e4m3fn if args.out_dtype == "e4m3" else None)
     stream = torch.cuda.current_stream(dev)
+    launches_per_call = dec.launches_per_call
     kv_bytes = case.kv_bytes()
     q_bytes = case.q_bytes()
     tokens = case.batch * case.q_seq_len
@@ -451,7 +455,7 @@ def run_gb300(args):
                      "kernel": KERNEL_NAMES[args.workload],
                      "algorithmic_bytes_per_launch": kv_bytes + q_bytes,
                      "avg_launch_ms": round(avg_launch_ms, 5)},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_call,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "clocks": clk.summary(),

@@ -39,6 +39,9 @@ class Decoder:
             ws = X.xqa_workspace_size(self.params)
             ns = X.xqa_semaphore_count(self.params)
         self.workspace = torch.zeros(max(ws, 16), dtype=torch.uint8, device=dev)
+        # kernel launches per call: the latent decode adds its split merge
+        # kernel whenever it needs a workspace
+        self.launches_per_call = 2 if (self.mla and ws > 0) else 1
         self.semaphores = torch.zeros(max(ns, 1), dtype=torch.int32, device=dev)
 
     def run(self, stream=None):
