@@ -515,7 +515,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   constexpr uint32_t kIdescPV = umma::idesc_f16(kRows, kHalf, !F8, false, true);
 
   bool first_piece = true;
-  int order = 0;  // pieces taken so far (persistent)
+  int order = 0;      // pieces taken so far (persistent)
+  int q_loaded = -1;  // logit CTA's softmax warps: the sequence whose query is in tensor memory
 
   for (;;) {
   // ---- the piece: sequence b, pages [pg_lo, pg_hi), its index among the
@@ -615,20 +616,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();  // the peer's barriers exist before any remote access
   umma::fence_after_sync();
   const int32_t* pt = a.page_table + int64_t(b) * a.pps;
-  if (persistent && logit_cta && tid == 32 * kSoftWarp0) {
-    // the query of this cluster's next sequence, into L2 ahead of its piece
-    // (a latency-bound load while the other clusters stream the cache)
-    int nb = -1;
+  // this cluster's next sequence (persistent), whose query the logit CTA's
+  // producer prefetches into L2 once it has issued this piece's last K load:
+  // the query load at a piece's start is latency-bound while the other
+  // clusters stream the cache
+  int next_b = -1;
+  if (persistent) {
     if (z_b >= 0 && order == 0)
-      nb = z_b;
+      next_b = z_b;
     else if (z_now)
-      nb = cur_b < z_b ? cur_b : -1;
+      next_b = cur_b < z_b ? cur_b : -1;
     else if (b + 1 < a.B && b + 1 != z_b && S_b + 2 * a.piece_cost + nsched < s_hi)
-      nb = b + 1;
-    if (nb >= 0) {
-      const int64_t qbytes = int64_t(a.qs) * a.Hq * kDim * (F8 ? 1 : 2);
-      prefetch_l2_bulk(a.q + int64_t(nb) * qbytes, uint32_t(qbytes));
-    }
+      next_b = b + 1;
   }
 
   if (warp == 0) {
@@ -675,6 +674,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
           ++issued;
+        }
+        if (lane == 0 && next_b >= 0) {
+          const int64_t qbytes = int64_t(a.qs) * a.Hq * kDim * (F8 ? 1 : 2);
+          prefetch_l2_bulk(a.q + int64_t(next_b) * qbytes, uint32_t(qbytes));
         }
         // no load of this CTA may land after it exits
         if (lane == 0)
@@ -905,12 +908,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ---- query: this thread's half of the latent row into tensor memory
     // (bf16: dims [256h, 256h + 256) -> columns [128h, 128h + 128); e4m3: four
     // codes per column, columns [64h, 64h + 64)), half of its rope part into
-    // shared memory (128- or 64-byte swizzled rows)
-    {
+    // shared memory (128- or 64-byte swizzled rows).  Loaded here for the
+    // cluster's first piece; for the next ones at the end of the previous
+    // piece, while the output CTA finishes its epilogue.
+    auto load_q = [&](int bq) {
       constexpr int kLB = F8 ? kLatent : 2 * kLatent;  // latent bytes of a query row
       constexpr int kRB = F8 ? kRope : 2 * kRope;      // rope bytes
       constexpr int kRU = kRB / 32;                    // rope 16-byte units per thread
-      const uint8_t* qrow = a.q + (int64_t(b) * a.qs * a.Hq + min(t, a.R - 1)) * (kLB + kRB);
+      const uint8_t* qrow = a.q + (int64_t(bq) * a.qs * a.Hq + min(t, a.R - 1)) * (kLB + kRB);
       const uint4* src = reinterpret_cast<const uint4*>(qrow + (kLB / 2) * h);
       const uint4* rsrc = reinterpret_cast<const uint4*>(qrow + kLB) + kRU * h;
       const uint4 zero = make_uint4(0, 0, 0, 0);
@@ -940,10 +945,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                   (F8 ? umma::sw64(t, kRU * h + u) : umma::sw128(t, kRU * h + u))) = rq[u];
       umma::tmem_st_wait();
       umma::fence_proxy_async_smem();
-      umma::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kQReady]);
-    }
+    };
+    if (q_loaded != b) load_q(b);
+    umma::fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars[kQReady]);
 
     const uint32_t p_peer = map_peer(smem_u32(smem + SL::kOffP), peer);
     const uint32_t f_peer = map_peer(smem_u32(smem + SL::kOffF), peer);
@@ -1091,6 +1097,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ok = false;
         }
     }
+    // the next piece's query (every Q K^T of this piece is done: the softmax
+    // read the last S tile, whose commit follows every earlier MMA)
+    // (warp-uniform: the tensor-memory stores are warp-collective, and the
+    // waits above ran on one lane)
+    q_loaded = -1;
+    if (__all_sync(kAll, ok) && next_b >= 0) {
+      load_q(next_b);
+      q_loaded = next_b;
+    }
   } else {
     // ================= output CTA: requests, then the epilogue =================
     // Warp w (2..9) reaches TMEM lanes 32 (w % 4) .. +31; h = (w - 2) / 4 picks
@@ -1214,9 +1229,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       if (!single && h == 0) st_keep2(wrow + kLatent, m_fin, l_fin, keep);
     }
-    // the partial is visible device-wide before either CTA of the cluster
-    // takes a merge ticket
-    __threadfence();
+    // (the partials reach the merge kernel through the end of this grid)
   }
 
   // ---- end of the piece: no tensor-memory or peer traffic may outlive this
