@@ -136,9 +136,8 @@ xqa_status xqa_decode(const xqa_params* params, void* workspace, size_t workspac
                       uint32_t* semaphores, xqa_stream_t stream);
 
 /* Same sizing queries for the MLA latent variant (num_kv_heads = 1).  The
-   workspace holds the split partials (fp32).  xqa_mla_semaphore_count returns
-   0: the MLA call takes no semaphores (its split merge is a second kernel in
-   the same stream). */
+   workspace holds the split partials (fp32); the semaphores (two per
+   sequence) count each sequence's finished pieces and finished merge items. */
 size_t xqa_mla_workspace_size(const xqa_params* params, int v_head_dim, int sm_count);
 size_t xqa_mla_semaphore_count(const xqa_params* params, int v_head_dim);
 
@@ -148,8 +147,12 @@ size_t xqa_mla_semaphore_count(const xqa_params* params, int v_head_dim);
    output must be 16-byte aligned.  One or two kernel launches on `stream`:
    the decode, then (when the workspace size is not 0) the merge of the
    sequences cut across clusters or splits, launched with programmatic
-   dependent launch (its CTAs wait for the decode grid).  `semaphores` is
-   unused and may be NULL. */
+   dependent launch: its CTAs take the SMs the decode CTAs leave and merge a
+   sequence once the decode has counted all of its pieces done.  The
+   semaphores (xqa_mla_semaphore_count uint32, 4-byte aligned; may be NULL
+   when the workspace size is 0) must be zero on the first call; every call
+   that runs to its end leaves them zero, also one that reported a timeout
+   (bit 1 of error_word): a merge that gave up waiting still counts itself. */
 xqa_status xqa_mla_decode(const xqa_params* params, int v_head_dim, void* workspace,
                           size_t workspace_bytes, uint32_t* semaphores, xqa_stream_t stream);
 

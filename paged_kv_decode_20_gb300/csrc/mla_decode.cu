@@ -215,7 +215,8 @@ struct MlaArgs {
   const uint16_t* mask;
   const float* q_scale_dev;
   const float* kv_scale_dev;
-  float* ws;    // split partials: [slot][128 rows][512 + 4] fp32 (O, then m and l)
+  float* ws;        // split partials: [slot][128 rows][512 + 4] fp32 (O, then m and l)
+  uint32_t* sems;   // [2][B]: pieces of sequence b finished; its merge items done
   uint32_t* err;
   float* lse;  // optional [B, qs, Hq] natural-log log-sum-exp per row
   int64_t num_pages;
@@ -919,17 +920,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint4* src = reinterpret_cast<const uint4*>(qrow + (kLB / 2) * h);
       const uint4* rsrc = reinterpret_cast<const uint4*>(qrow + kLB) + kRU * h;
       const uint4 zero = make_uint4(0, 0, 0, 0);
-      // the rope part first, then the latent half in rounds of 16 loads in
-      // flight per thread
-      uint4 rq[kRU];
+      // every load of the row's half in flight at once (one memory latency:
+      // the load is latency-bound while the other clusters stream the cache)
+      uint4 rq[kRU], xq[kLB / 32];
 #pragma unroll
       for (int u = 0; u < kRU; ++u) rq[u] = real ? __ldg(rsrc + u) : zero;
-#pragma unroll 1
+#pragma unroll
+      for (int v = 0; v < kLB / 32; ++v) xq[v] = real ? __ldg(src + v) : zero;
+#pragma unroll
       for (int half = 0; half < kLB / 512; ++half) {
         uint32_t w[64];
 #pragma unroll
         for (int v = 0; v < 16; ++v) {
-          const uint4 x = real ? __ldg(src + half * 16 + v) : zero;
+          const uint4 x = xq[half * 16 + v];
           w[4 * v + 0] = x.x;
           w[4 * v + 1] = x.y;
           w[4 * v + 2] = x.z;
@@ -1229,7 +1232,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       if (!single && h == 0) st_keep2(wrow + kLatent, m_fin, l_fin, keep);
     }
-    // (the partials reach the merge kernel through the end of this grid)
+    // the partial is visible device-wide before the piece is counted done
+    if (nvalid > 1) __threadfence();
   }
 
   // ---- end of the piece: no tensor-memory or peer traffic may outlive this
@@ -1238,6 +1242,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // cluster always pass the same cluster barriers.
   umma::fence_before_sync();
   __syncthreads();
+  // one more finished piece of a sequence cut into several (the merge kernel
+  // waits for all of them; counted also after an abort, which the error word
+  // reports, so that the merge does not wait out its time limit)
+  if (!logit_cta && tid == 0 && nvalid > 1) atomicAdd(a.sems + b, 1u);
   cluster_sync();
   if (tid == 0) {
     uint32_t peer_abort;
@@ -1293,6 +1301,7 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeCtasPerSm) mla_merge_kern
   __shared__ long long s_warp[kMergeThreads / 32];
   __shared__ float s_w[kMergeRows * kMaxPieces];  // per (row, piece): the maximum, then the weight
   __shared__ float s_l[kMergeRows * kMaxPieces];
+  __shared__ bool s_ready;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool persistent = a.B <= kOrderMaxB;
   if (persistent) {
@@ -1327,8 +1336,9 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeCtasPerSm) mla_merge_kern
     }
     __syncthreads();
   }
-  // the decode grid has finished and its partials are visible
-  pdl_wait();
+  // (no griddepcontrol.wait: the CTAs are placed as decode CTAs exit and
+  // merge each sequence as soon as its pieces are counted done, while the
+  // last clusters still run; the next call's decode waits for this grid)
   pdl_launch_dependents();
   constexpr int kStride = kLatent + 4;
   constexpr int kQuads = kMergeThreads / (kHalf / 4);  // row groups of the CTA's threads
@@ -1356,6 +1366,18 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeCtasPerSm) mla_merge_kern
       step = 1;
     }
     if (nvalid <= 1 || nvalid > kMaxPieces) continue;
+    // every piece of the sequence is done and its partial visible
+    if (tid == 0) {
+      const long long t0 = clock64();
+      uint32_t n;
+      do {
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(n) : "l"(a.sems + b) : "memory");
+      } while (n < uint32_t(nvalid) && clock64() - t0 < kWaitCycles);
+      s_ready = n >= uint32_t(nvalid);
+      if (!s_ready && a.err) atomicOr(a.err, kErrTimeout);
+    }
+    __syncthreads();
+    const bool ready = s_ready;
     auto part_row = [&](int sp, int rr) {
       const int64_t slot = sp == 0 ? slot0 : slot1 + int64_t(step) * (sp - 1);
       return a.ws + (slot * kRows + r0 + rr) * kStride;
@@ -1421,13 +1443,22 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeCtasPerSm) mla_merge_kern
 #pragma unroll
     for (int u = 0; u < kRowsPer; ++u) {
       const int rr = rq + kQuads * u;
-      if (rr >= nrows) continue;
+      if (rr >= nrows || !ready) continue;
       const int row = r0 + rr;
       const int64_t row_g = (int64_t(b) * a.qs + row / a.Hq) * a.Hq + row % a.Hq;
       *reinterpret_cast<uint2*>(a.out + row_g * kLatent + col) =
           make_uint2(pack_f32x2(acc[u].x, acc[u].y, true), pack_f32x2(acc[u].z, acc[u].w, true));
     }
     __syncthreads();  // the weights are rewritten by the next item
+    // the last of the sequence's merge items zeroes both of its counters for
+    // the next call (every other item has passed its wait)
+    if (tid == 0) {
+      const uint32_t items_b = 2u * uint32_t((a.R + kMergeRows - 1) / kMergeRows);
+      if (atomicAdd(a.sems + a.B + b, 1u) == items_b - 1) {
+        a.sems[b] = 0u;
+        a.sems[a.B + b] = 0u;
+      }
+    }
   }
 }
 
@@ -1526,7 +1557,7 @@ size_t mla_workspace_size(const xqa_params* p, int v_head_dim, int sm_count) {
 
 size_t mla_semaphore_count(const xqa_params* p, int v_head_dim) {
   if (!p || mla::check_shape(p, v_head_dim)) return size_t(-1);
-  return 0;  // the split merge is a second kernel: no tickets
+  return size_t(p->batch_size) * 2;  // per sequence: finished pieces, finished merge items
 }
 
 xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_bytes, uint32_t* sems,
@@ -1558,8 +1589,15 @@ xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_b
       snprintf(err, err_len, "workspace must be 16-byte aligned");
       return XQA_ERR_INVALID_ARG;
     }
+    if (!sems) {
+      snprintf(err, err_len, "semaphores are required (%zu needed)", size_t(p->batch_size) * 2);
+      return XQA_ERR_WORKSPACE_TOO_SMALL;
+    }
+    if (reinterpret_cast<uintptr_t>(sems) & 3) {
+      snprintf(err, err_len, "semaphores must be 4-byte aligned");
+      return XQA_ERR_INVALID_ARG;
+    }
   }
-  (void)sems;
   EncodeTiledFn enc = encode_fn();
   if (!enc) {
     snprintf(err, err_len, "cuTensorMapEncodeTiled is unavailable");
@@ -1629,6 +1667,7 @@ xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_b
   a.q_scale_dev = p->q_scale_dev;
   a.kv_scale_dev = p->kv_scale_dev;
   a.ws = static_cast<float*>(ws);
+  a.sems = sems;
   a.err = p->error_word;
   a.lse = p->lse;
   a.num_pages = p->num_pages;

@@ -269,12 +269,12 @@ def mla_params(**over):
 @pytest.mark.parametrize("sm,clusters", [(152, 76), (2, 1), (1000, 128)])
 def test_mla_workspace_persistent_clusters(lib, sm, clusters):
     """Up to 256 sequences: one persistent cluster per SM pair (at most 128), two
-    partial slots each; a single cluster needs no partials.  The split merge
-    is a second kernel: no semaphores."""
+    partial slots each; a single cluster needs no partials.  Two semaphores
+    per sequence: its finished pieces and its finished merge items."""
     p = mla_params(batch_size=64)
     expect = clusters * 2 * MLA_PARTIAL if clusters > 1 else 0
     assert lib.xqa_mla_workspace_size(ctypes.byref(p), 512, sm) == expect
-    assert lib.xqa_mla_semaphore_count(ctypes.byref(p), 512) == 0
+    assert lib.xqa_mla_semaphore_count(ctypes.byref(p), 512) == 64 * 2
 
 
 def test_mla_workspace_fixed_splits_above_256_sequences(lib):
