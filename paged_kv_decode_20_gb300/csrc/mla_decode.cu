@@ -145,7 +145,8 @@ enum BarIdx {
   kSFull = kKEmpty + kMaxKSlots,   // [2] S tile computed
   kSFree = kSFull + 2,             // [2] S tile read out of tensor memory
   kQReady = kSFree + 2,            // the query is in tensor / shared memory
-  kPSlotFree = kQReady + 1,        // [2] the output CTA's P.V of that P slot is done
+  kQLoad = kQReady + 1,            // bf16: the query's rows landed in the K ring (staging)
+  kPSlotFree = kQLoad + 1,         // [2] the output CTA's P.V of that P slot is done
   // output CTA
   kVFull = kPSlotFree + 2,         // [kVSlots] a V slot landed
   kVEmpty = kVFull + kMaxVSlots,   // [kVSlots] the P.V (bf16) or the widening (e4m3) read a V slot
@@ -198,12 +199,12 @@ constexpr int kMaxSplits = 64;       // merge weights [128][splits] fit in share
 #endif
 constexpr int kWaves = XQA_MLA_WAVES;  // cluster waves the split plan aims for
 #ifndef XQA_MLA_PIECE_TOKENS
-#define XQA_MLA_PIECE_TOKENS 768
+#define XQA_MLA_PIECE_TOKENS 1024
 #endif
-// a persistent piece's fixed cost in KV tokens of streaming time: the query
-// load, the pipeline fill and drain, and the epilogue's stores, all latency-
-// bound while the other clusters stream the cache (measured on the latent
-// workload: 768 tokens, about 14 us, balances the clusters' end times)
+// a persistent piece's fixed cost in KV tokens of streaming time: the
+// pipeline fill and drain, the epilogue's stores and the barriers between
+// pieces, all latency-bound while the other clusters stream the cache
+// (measured on the latent workload: about 19 us, 1024 tokens)
 constexpr int kPieceTokens = XQA_MLA_PIECE_TOKENS;
 
 struct MlaArgs {
@@ -420,7 +421,7 @@ template <bool F8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmKR,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmPF,
-                      const MlaArgs a) {
+                      const __grid_constant__ CUtensorMap tmQ, const MlaArgs a) {
   using SL = Lay<F8>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
@@ -582,6 +583,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           fn(kPSlotFree + k, 1);  // the peer's MMA completion
         }
         fn(kQReady, kSoftWarps);
+        fn(kQLoad, 1);
       } else {
         // an e4m3 V slot is freed by the eight warps that widen it, a bf16 one by the P.V
         for (int k = 0; k < SL::kVSlots; ++k) {
@@ -651,6 +653,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // group gr of logit tile j (global group g = 3 j + gr) goes to ring
         // slot g % kKSlots: one wait, one expect-tx and one box per page piece
         TilePieces tp = {0, 0, false};
+        // the query's loads go first (at the call's start every cluster loads
+        // one at once; a piece after the first finds it loaded already)
+        if (nqt > 0) ok = __all_sync(kAll, mbar_wait(&bars[kQReady], 0));
         for (int g = 0; ok && g < nqt * kGroups; ++g) {
           const int j = g / kGroups, gr = g - j * kGroups;
           const int slot = g % SL::kKSlots, use = g / SL::kKSlots;
@@ -912,27 +917,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // shared memory (128- or 64-byte swizzled rows).  Loaded here for the
     // cluster's first piece; for the next ones at the end of the previous
     // piece, while the output CTA finishes its epilogue.
+    int qload_n = 0;  // uses of the query-load barrier in this piece
     auto load_q = [&](int bq) {
       constexpr int kLB = F8 ? kLatent : 2 * kLatent;  // latent bytes of a query row
       constexpr int kRB = F8 ? kRope : 2 * kRope;      // rope bytes
       constexpr int kRU = kRB / 32;                    // rope 16-byte units per thread
-      const uint8_t* qrow = a.q + (int64_t(bq) * a.qs * a.Hq + min(t, a.R - 1)) * (kLB + kRB);
-      const uint4* src = reinterpret_cast<const uint4*>(qrow + (kLB / 2) * h);
-      const uint4* rsrc = reinterpret_cast<const uint4*>(qrow + kLB) + kRU * h;
+      constexpr int kLU = kLB / 32;                    // latent 16-byte units per thread
       const uint4 zero = make_uint4(0, 0, 0, 0);
-      // every load of the row's half in flight at once (one memory latency:
-      // the load is latency-bound while the other clusters stream the cache)
-      uint4 rq[kRU], xq[kLB / 32];
+      uint4 rq[kRU];
+      // latent units of this thread's half: from the staged rows (bf16) or
+      // from registers loaded all at once (e4m3, half the bytes)
+      uint4 xq[F8 ? kLU : 1];
+      const uint8_t* row = smem + SL::kOffK + t * (kLB + kRB);
+      auto unit = [&](int chunk, int u) {
+        // an address's 16-byte unit is XORed with its bits 7-9 (128-byte swizzle)
+        const uint32_t off = uint32_t(t * (kLB + kRB) + chunk * 128);
+        return *reinterpret_cast<const uint4*>(row + chunk * 128 + ((u ^ int((off >> 7) & 7u)) << 4));
+      };
+      if constexpr (!F8) {
+        // bf16: the sequence's 128 query rows in one TMA box ([row][9 chunks]
+        // [128 B], 128-byte swizzle) into the free K ring; each thread then
+        // reads its row's half (the swizzle spreads a warp's rows over the
+        // banks)
+        if (st == 0) {
+          mbar_arrive_expect_tx(&bars[kQLoad], uint32_t(kRows * (kLB + kRB)));
+          tma_load_3d(smem + SL::kOffK, &tmQ, &bars[kQLoad], 0, 0, bq * a.R);
+        }
+        const bool got = __all_sync(kAll, mbar_wait(&bars[kQLoad], qload_n & 1));
+        ++qload_n;
+        if (!got) flags[0] = 1;
 #pragma unroll
-      for (int u = 0; u < kRU; ++u) rq[u] = real ? __ldg(rsrc + u) : zero;
+        for (int u = 0; u < kRU; ++u) rq[u] = real ? unit(8, kRU * h + u) : zero;
+      } else {
+        const uint8_t* qrow = a.q + (int64_t(bq) * a.qs * a.Hq + min(t, a.R - 1)) * (kLB + kRB);
+        const uint4* src = reinterpret_cast<const uint4*>(qrow + (kLB / 2) * h);
+        const uint4* rsrc = reinterpret_cast<const uint4*>(qrow + kLB) + kRU * h;
 #pragma unroll
-      for (int v = 0; v < kLB / 32; ++v) xq[v] = real ? __ldg(src + v) : zero;
+        for (int u = 0; u < kRU; ++u) rq[u] = real ? __ldg(rsrc + u) : zero;
 #pragma unroll
+        for (int v = 0; v < kLU; ++v) xq[F8 ? v : 0] = real ? __ldg(src + v) : zero;
+      }
+#pragma unroll 1
       for (int half = 0; half < kLB / 512; ++half) {
         uint32_t w[64];
 #pragma unroll
         for (int v = 0; v < 16; ++v) {
-          const uint4 x = xq[half * 16 + v];
+          const int vv = half * 16 + v;
+          const uint4 x = F8 ? xq[F8 ? vv : 0] : (real ? unit(4 * h + vv / 8, vv % 8) : zero);
           w[4 * v + 0] = x.x;
           w[4 * v + 1] = x.y;
           w[4 * v + 2] = x.z;
@@ -1656,6 +1687,21 @@ xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_b
     snprintf(err, err_len, "cuTensorMapEncodeTiled (prefetch view) failed (%d)", int(r));
     return XQA_ERR_CUDA;
   }
+  // bf16 query rows as (64 elements, 9 chunks, rows): one box is a
+  // sequence's 128 query rows (rows past it are padding, never stored)
+  CUtensorMap tq = tpf;  // unused by the e4m3 kernel
+  if (!f8) {
+    cuuint64_t qdims[3] = {64, kDim / 64, cuuint64_t(p->batch_size) * p->q_seq_len * p->num_q_heads};
+    cuuint64_t qstrides[2] = {128, cuuint64_t(kDim) * 2};
+    cuuint32_t qbox[3] = {64, kDim / 64, kRows};
+    r = enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p->q), qdims, qstrides, qbox, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+      snprintf(err, err_len, "cuTensorMapEncodeTiled (query view) failed (%d)", int(r));
+      return XQA_ERR_CUDA;
+    }
+  }
   MlaArgs a;
   memset(&a, 0, sizeof a);
   a.q = static_cast<const uint8_t*>(p->q);
@@ -1704,8 +1750,8 @@ xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_b
   attr[0].val.programmaticStreamSerializationAllowed = p->enable_pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = f8 ? cudaLaunchKernelEx(&cfg, mla_decode_kernel<true>, tk, tkr, tv, tpf, a)
-         : cudaLaunchKernelEx(&cfg, mla_decode_kernel<false>, tk, tkr, tv, tpf, a);
+  e = f8 ? cudaLaunchKernelEx(&cfg, mla_decode_kernel<true>, tk, tkr, tv, tpf, tq, a)
+         : cudaLaunchKernelEx(&cfg, mla_decode_kernel<false>, tk, tkr, tv, tpf, tq, a);
   if (e != cudaSuccess) {
     snprintf(err, err_len, "MLA kernel launch: %s", cudaGetErrorString(e));
     return XQA_ERR_CUDA;
