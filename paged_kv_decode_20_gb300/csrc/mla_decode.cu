@@ -72,6 +72,11 @@ constexpr int kPBytes = kRows * kTok * 2;  // one 16-bit P tile
 constexpr int kFBytes = kRows * 4 + 16;    // one rescale factor per row, then a flag word
 constexpr int kPMsg = kPBytes + kFBytes;
 constexpr int kFinBytes = 2 * kRows * 4;   // the final row maxima and sums
+// epilogue staging (in the output CTA's V ring and P slots, 224 KB), both
+// halves of O: fp32 partial parts of 32 columns (32 KB), bf16 output pairs of
+// parts, 64 columns (32 KB)
+constexpr int kStageF32 = 7;
+constexpr int kStageBf16 = kRows * 128 * 2;
 constexpr int kCopyPieces = 4;             // P travels as this many bulk copies
 
 // ---- shared memory (offsets from the dynamic base, which is 1024-aligned:
@@ -339,6 +344,33 @@ __device__ __forceinline__ void st_keep4(float* dst, float x, float y, float z, 
 __device__ __forceinline__ void st_keep2(float* dst, float x, float y, uint64_t pol) {
   asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;" ::"l"(dst), "f"(x), "f"(y), "l"(pol) : "memory");
 }
+// One 2-D TMA box from shared memory to global memory (a bulk async-group),
+// optionally with an L2 cache policy.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* map, const void* src, int x, int y, uint64_t pol) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y), "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Waits until every bulk group of this thread has completed (its global
+// writes performed), then makes them visible device-wide.
+__device__ __forceinline__ void bulk_wait_all_visible() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  __threadfence();
+}
 // Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.
 __device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
@@ -421,7 +453,8 @@ template <bool F8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmKR,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmPF,
-                      const __grid_constant__ CUtensorMap tmQ, const MlaArgs a) {
+                      const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmWs,
+                      const __grid_constant__ CUtensorMap tmO, const MlaArgs a) {
   using SL = Lay<F8>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
@@ -519,6 +552,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   bool first_piece = true;
   int order = 0;      // pieces taken so far (persistent)
   int q_loaded = -1;  // logit CTA's softmax warps: the sequence whose query is in tensor memory
+  int pend_b = -1;    // output CTA's first epilogue thread: the sequence whose partial is still being stored
 
   for (;;) {
   // ---- the piece: sequence b, pages [pg_lo, pg_hi), its index among the
@@ -1153,6 +1187,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int i = min(t / a.Hq, a.qs - 1), hd = t % a.Hq;
     const float kv_scale = ldscale(a.kv_scale_dev, a.kv_scale);
     bool ok = true;
+    // the previous piece's partial stores have had a piece's start to land:
+    // count that piece done for the merge kernel
+    if (st == 0 && pend_b >= 0) {
+      bulk_wait_all_visible();
+      atomicAdd(a.sems + pend_b, 1u);
+      pend_b = -1;
+    }
     if constexpr (F8) {
       // Tile by tile: first the rescale decision for the previous tile (O is
       // multiplied by that tile's factors once every earlier P.V is done; the
@@ -1223,6 +1264,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     umma::fence_after_sync();
     const float* fin = reinterpret_cast<const float*>(smem + SL::kOffFin);
     const float m_fin = fin[t], l_fin = fin[kRows + t];
+    // (the staged stores below take named barriers: all eight warps decide together)
+    ok = !named_bar_or(2, kSoft, !ok);
     if (ok) {
       const bool have_o = ntiles > 0;
       const bool single = nvalid <= 1;
@@ -1235,7 +1278,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       const int64_t slot = persistent ? 2 * int64_t(k_cl) + (cl_first ? 0 : 1) : int64_t(b) * a.nsplit + split;
       const uint64_t keep = l2_keep_policy();
-      float* wrow = a.ws + (slot * kRows + t) * (kLatent + 4);
+      // O leaves through TMA stores of 32-column parts staged in the free V
+      // ring and P slots (a part's two halves, swizzled rows), so that the
+      // epilogue threads write shared memory only: one thread per row writing
+      // its row straight to global memory touches 32 lines per warp store.
+      // fp32 partial: [half][128 rows][128 B] per part, seven 32 KB buffers;
+      // bf16 output: [half][128 rows][128 B] per pair of parts, four 32 KB
+      // buffers, only the R real rows stored (128-byte swizzle).
+      uint8_t* const stage = smem + SL::kOffV;
 #pragma unroll 1
       for (int part = 0; part < kHalf / 32; ++part) {
         float o[32];
@@ -1246,25 +1296,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 32; ++k) o[k] = 0.f;
         }
-        const int col = kHalf * h + 32 * part;
         if (single) {
-          if (!real) continue;
-          uint4* dst = reinterpret_cast<uint4*>(a.out + row_g * kLatent + col);
+          // two parts (64 bf16 columns, 128 bytes) per staged row
+          uint8_t* buf = stage + (part >> 1) * kStageBf16 + h * (kStageBf16 / 2);
 #pragma unroll
           for (int v = 0; v < 4; ++v)
-            dst[v] = make_uint4(pack_f32x2(o[8 * v] * mul, o[8 * v + 1] * mul, true),
-                                pack_f32x2(o[8 * v + 2] * mul, o[8 * v + 3] * mul, true),
-                                pack_f32x2(o[8 * v + 4] * mul, o[8 * v + 5] * mul, true),
-                                pack_f32x2(o[8 * v + 6] * mul, o[8 * v + 7] * mul, true));
+            *reinterpret_cast<uint4*>(buf + umma::sw128(t, 4 * (part & 1) + v)) =
+                make_uint4(pack_f32x2(o[8 * v] * mul, o[8 * v + 1] * mul, true),
+                           pack_f32x2(o[8 * v + 2] * mul, o[8 * v + 3] * mul, true),
+                           pack_f32x2(o[8 * v + 4] * mul, o[8 * v + 5] * mul, true),
+                           pack_f32x2(o[8 * v + 6] * mul, o[8 * v + 7] * mul, true));
         } else {
+          // the buffer of the part kStageF32 back is free once its stores read it
+          if (part >= kStageF32) {
+            if (st == 0) bulk_wait_read<kStageF32 - 1>();
+            named_bar(2, kSoft);
+          }
+          uint8_t* buf = stage + (part % kStageF32) * (kRows * 256) + h * (kRows * 128);
 #pragma unroll
-          for (int v = 0; v < 8; ++v) st_keep4(wrow + col + 4 * v, o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3], keep);
+          for (int v = 0; v < 8; ++v)
+            *reinterpret_cast<float4*>(buf + umma::sw128(t, v)) =
+                make_float4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+        }
+        if (single && (part & 1) == 0) continue;  // (the pair's second part stores both)
+        umma::fence_proxy_async_smem();
+        named_bar(2, kSoft);
+        if (st == 0) {
+          for (int hh = 0; hh < 2; ++hh) {
+            if (single)
+              tma_store_2d(&tmO, stage + (part >> 1) * kStageBf16 + hh * (kStageBf16 / 2),
+                           kHalf * hh + 32 * (part - 1), b * a.R);
+            else
+              tma_store_2d_hint(&tmWs, stage + (part % kStageF32) * (kRows * 256) + hh * (kRows * 128),
+                                kHalf * hh + 32 * part, int(slot) * kRows, keep);
+          }
+          bulk_commit();
         }
       }
-      if (!single && h == 0) st_keep2(wrow + kLatent, m_fin, l_fin, keep);
+      if (!single && h == 0) {
+        float* wrow = a.ws + (slot * kRows + t) * (kLatent + 4);
+        st_keep2(wrow + kLatent, m_fin, l_fin, keep);
+      }
+      // the staging is free again before the next piece loads V into it
+      if (st == 0) bulk_wait_read<0>();
     }
-    // the partial is visible device-wide before the piece is counted done
-    if (nvalid > 1) __threadfence();
+    // a partial is counted done once its stores have landed (at the next
+    // piece's start, or at the end); also after an abort, which the error
+    // word reports, so that the merge does not wait out its time limit
+    if (st == 0 && nvalid > 1) pend_b = b;
   }
 
   // ---- end of the piece: no tensor-memory or peer traffic may outlive this
@@ -1273,10 +1352,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // cluster always pass the same cluster barriers.
   umma::fence_before_sync();
   __syncthreads();
-  // one more finished piece of a sequence cut into several (the merge kernel
-  // waits for all of them; counted also after an abort, which the error word
-  // reports, so that the merge does not wait out its time limit)
-  if (!logit_cta && tid == 0 && nvalid > 1) atomicAdd(a.sems + b, 1u);
   cluster_sync();
   if (tid == 0) {
     uint32_t peer_abort;
@@ -1295,6 +1370,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }  // pieces
 
   // ---- teardown
+  if (pend_b >= 0) {  // (the output CTA's first epilogue thread)
+    bulk_wait_all_visible();
+    atomicAdd(a.sems + pend_b, 1u);
+  }
   umma::fence_before_sync();
   __syncthreads();
   if (warp == 0) {
@@ -1702,6 +1781,30 @@ xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_b
       return XQA_ERR_CUDA;
     }
   }
+  // epilogue store views: the output (bf16, 512 per row; a box is 64
+  // columns of one sequence's R real rows) and the split partials (fp32,
+  // 512 + 4 per row; a box is 32 columns of a slot's 128 rows)
+  CUtensorMap to, tws = tpf;
+  {
+    const int R = p->num_q_heads * p->q_seq_len;
+    cuuint64_t odims[2] = {kLatent, cuuint64_t(p->batch_size) * R};
+    cuuint64_t ostrides[1] = {kLatent * 2};
+    cuuint32_t obox[2] = {64, cuuint32_t(R)};
+    r = enc(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->output, odims, ostrides, obox, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r == CUDA_SUCCESS && pl.ws_bytes > 0) {
+      cuuint64_t wdims[2] = {kLatent + 4, cuuint64_t(pl.ws_bytes / ((kLatent + 4) * sizeof(float)))};
+      cuuint64_t wstrides[1] = {(kLatent + 4) * sizeof(float)};
+      cuuint32_t wbox[2] = {32, kRows};
+      r = enc(&tws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ws, wdims, wstrides, wbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (r != CUDA_SUCCESS) {
+      snprintf(err, err_len, "cuTensorMapEncodeTiled (epilogue views) failed (%d)", int(r));
+      return XQA_ERR_CUDA;
+    }
+  }
   MlaArgs a;
   memset(&a, 0, sizeof a);
   a.q = static_cast<const uint8_t*>(p->q);
@@ -1750,8 +1853,8 @@ xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_b
   attr[0].val.programmaticStreamSerializationAllowed = p->enable_pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = f8 ? cudaLaunchKernelEx(&cfg, mla_decode_kernel<true>, tk, tkr, tv, tpf, tq, a)
-         : cudaLaunchKernelEx(&cfg, mla_decode_kernel<false>, tk, tkr, tv, tpf, tq, a);
+  e = f8 ? cudaLaunchKernelEx(&cfg, mla_decode_kernel<true>, tk, tkr, tv, tpf, tq, tws, to, a)
+         : cudaLaunchKernelEx(&cfg, mla_decode_kernel<false>, tk, tkr, tv, tpf, tq, tws, to, a);
   if (e != cudaSuccess) {
     snprintf(err, err_len, "MLA kernel launch: %s", cudaGetErrorString(e));
     return XQA_ERR_CUDA;
