@@ -11,7 +11,9 @@
 // two split the work by stage:
 //
 //   CTA 1 (the logit CTA) holds the whole query: the latent part in tensor
-//   memory, the rope part in shared memory.  It streams each 576-wide latent
+//   memory, the rope part in shared memory (bf16: the rows arrive in one TMA
+//   box; the next piece's query loads while the previous piece's epilogue
+//   runs).  It streams each 576-wide latent
 //   row of the piece through a ring of three-chunk groups (128 tokens x 192
 //   dims, TMA, 128-byte swizzle) and computes the logits S = Q K^T over
 //   128-token tiles with tcgen05.mma, then runs the online softmax.  P (bf16,
@@ -21,7 +23,8 @@
 //   fetches the first 512 dims of each 64-token tile (V) again, from L2, and
 //   accumulates O += P V with two N = 256 MMAs per 16 tokens.  Its eight spare
 //   warps rescale O when the softmax raised a row maximum by more than 2^8,
-//   clear V rows past the piece's end, and run the epilogue.
+//   clear V rows past the piece's end, and run the epilogue (O staged in
+//   shared memory and stored by TMA).
 //
 // Only P crosses the cluster (16.5 KB per 64 tokens, one way), and every
 // latent byte is read from HBM once.  Warp roles in both CTAs: 0 = TMA
@@ -31,9 +34,15 @@
 //
 // Up to 256 sequences the clusters are persistent: cluster k runs, one after
 // another, the pieces of the sequences that meet the k-th equal slice of the
-// batch's pages.  A sequence cut across clusters leaves one partial per piece;
-// the last CTA of each column half to take the sequence's ticket merges them.
-// Larger batches take one cluster per (sequence, fixed-size split).
+// batch's pages (each sequence start charged a fixed piece cost), cut pieces
+// first.  A sequence cut across clusters leaves one partial per piece, counted
+// done on a per-sequence semaphore; a second kernel (mla_merge_kernel) merges
+// each such sequence once its pieces are done.  Larger batches take one
+// cluster per (sequence, fixed-size split), merged the same way.
+//
+// The logit CTA is bound by its MMA instruction rate: an M = 128, N = 128,
+// K = 16 tcgen05.mma accumulating into one tile takes ~140 cycles, and a
+// 128-token logit tile is 36 of them.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
