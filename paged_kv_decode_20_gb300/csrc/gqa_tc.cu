@@ -109,9 +109,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int split = blockIdx.x;
   const int kvh = blockIdx.y / a.rg_count, rg = blockIdx.y % a.rg_count;
-  const int b = blockIdx.z;
+  int b = blockIdx.z;
   pdl_wait();
   pdl_launch_dependents();
+
+  // Longest sequences first: CTAs launch in blockIdx order, so grid slot z
+  // takes the sequence with the z-th most visible tokens (ties by index), and
+  // the long CTAs start in the first wave instead of trailing the last one.
+  // Every CTA ranks the (at most 160) sequences itself in shared memory (the
+  // K ring, unused until the first load).
+  if (a.sort_b) {
+    int* eff = reinterpret_cast<int*>(smem + C::kOffK);
+    const int64_t cap = int64_t(a.pps) * a.ps;
+    if (tid < a.B) {
+      int64_t e = a.seq_lens[tid];
+      e = e < cap ? e : cap;
+      if (a.win > 0) e = min(e, int64_t(a.win) + a.qs - 1);
+      eff[tid] = int(e);
+    }
+    __syncthreads();
+    if (tid < a.B) {
+      const int mine = eff[tid];
+      int rank = 0;
+      for (int j = 0; j < a.B; ++j) {
+        const int o = eff[j];
+        rank += (o > mine) || (o == mine && j < tid);
+      }
+      if (rank == b) eff[a.B] = tid;
+    }
+    __syncthreads();
+    b = eff[a.B];
+    __syncthreads();  // (read before anything else uses the ring)
+  }
 
   // ---- sequence geometry (identical in every CTA of this (b, kvh, rg))
   const int64_t max_len = int64_t(a.pps) * a.ps;
