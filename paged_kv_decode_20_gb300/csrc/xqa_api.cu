@@ -169,10 +169,25 @@ int pages_bound(const xqa_params* p) {
 // Splits so that B * Hkv * row_groups * splits covers several waves of the
 // GPU (split count from B, the table bound and the SM count), in whole
 // pipeline stages and never below 256 tokens per split.
+// Splits aim at this many waves of CTAs (the tensor-core kernel: fewer, for
+// its per-CTA costs, the query into tensor memory and the pipeline fill, are
+// larger; measured on the large-group workload: 2 waves 0.232 ms, 4 waves
+// 0.257 ms, 8 waves 0.280 ms)
+#ifndef XQA_TC_WAVES
+#define XQA_TC_WAVES 2
+#endif
+// (the mma.sync kernel: 4 waves; measured, 2 or 3 waves are 2.5 % faster on
+// the variable-length Llama-3-8B-shaped workload, where the longest-first
+// order fills the last wave, but 7 % slower on the equal-length fp8 one, one
+// split per sequence leaving 3.4 waves)
+#ifndef XQA_GQA_WAVES
+#define XQA_GQA_WAVES 4
+#endif
 void choose_splits(const xqa_params* p, Plan* pl, int sm_count, int ctas_per_sm, int stage_pages) {
   const int64_t units = int64_t(p->batch_size) * p->num_kv_heads * pl->rg_count;
   const int max_pages = pl->max_pages;
-  const int64_t target = int64_t(std::max(sm_count, 1)) * std::max(ctas_per_sm, 1) * 4;
+  const int64_t target =
+      int64_t(std::max(sm_count, 1)) * std::max(ctas_per_sm, 1) * (pl->tc ? XQA_TC_WAVES : XQA_GQA_WAVES);
   int64_t ns = (target + units - 1) / units;
   const int64_t by_stage = (max_pages + stage_pages - 1) / stage_pages;
   const int64_t by_tokens = std::max<int64_t>(1, (int64_t(max_pages) * p->page_size) / 256);
