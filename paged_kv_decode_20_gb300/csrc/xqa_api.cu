@@ -166,37 +166,62 @@ int pages_bound(const xqa_params* p) {
   return n;
 }
 
-// Splits so that B * Hkv * row_groups * splits covers several waves of the
-// GPU (split count from B, the table bound and the SM count), in whole
-// pipeline stages and never below 256 tokens per split.
-// Splits aim at this many waves of CTAs (the tensor-core kernel: fewer, for
-// its per-CTA costs, the query into tensor memory and the pipeline fill, are
-// larger; measured on the large-group workload: 2 waves 0.232 ms, 4 waves
-// 0.257 ms, 8 waves 0.280 ms)
-#ifndef XQA_TC_WAVES
-#define XQA_TC_WAVES 2
+// Split count.  The kernels are HBM-bound and their CTAs go out in blockIdx
+// order to sm_count x ctas_per_sm slots.  The count minimises a fluid model of
+// the grid's makespan, taking every sequence at the page table's bound (the
+// host does not read the lengths):
+//   - n = units x splits CTAs of p = split tokens + a fixed per-CTA cost
+//     (pipeline fill and drain, epilogue, merge) each;
+//   - full waves share the memory system evenly, so k = n / slots of them take
+//     k p;
+//   - the r = n % slots CTAs of a last partial wave each run at most at twice
+//     an even share, so they take p max(r / slots, 1/2).
+// Fewer splits save the fixed costs; more splits fill the last wave.  Measured
+// per-CTA costs, in tokens of streaming: mma.sync kernel ~128, tensor-core
+// kernel ~1024 (its query into tensor memory and pipeline fill).  The choices
+// on the measured workloads: Llama-3-8B-shaped (512 units) 1 split, 182 us
+// against 192 and 197 us for 2 and 3; fp8 long context (1024 units of 32768
+// tokens) 2 splits, 1.373 ms against 1.426 ms (1) and 1.398 ms (3); large
+// group on the tensor-core kernel 1 split, 0.232 ms against 0.257 ms (2).
+// Splits are whole pipeline stages and never below 256 tokens.
+#ifndef XQA_GQA_CTA_COST_TOKENS
+#define XQA_GQA_CTA_COST_TOKENS 128
 #endif
-// (the mma.sync kernel: 4 waves; measured, 2 or 3 waves are 2.5 % faster on
-// the variable-length Llama-3-8B-shaped workload, where the longest-first
-// order fills the last wave, but 7 % slower on the equal-length fp8 one, one
-// split per sequence leaving 3.4 waves)
-#ifndef XQA_GQA_WAVES
-#define XQA_GQA_WAVES 4
+#ifndef XQA_TC_CTA_COST_TOKENS
+#define XQA_TC_CTA_COST_TOKENS 1024
 #endif
 void choose_splits(const xqa_params* p, Plan* pl, int sm_count, int ctas_per_sm, int stage_pages) {
   const int64_t units = int64_t(p->batch_size) * p->num_kv_heads * pl->rg_count;
   const int max_pages = pl->max_pages;
-  const int64_t target =
-      int64_t(std::max(sm_count, 1)) * std::max(ctas_per_sm, 1) * (pl->tc ? XQA_TC_WAVES : XQA_GQA_WAVES);
-  int64_t ns = (target + units - 1) / units;
+  const int64_t slots = int64_t(std::max(sm_count, 1)) * std::max(ctas_per_sm, 1);
+  const int64_t cost = pl->tc ? XQA_TC_CTA_COST_TOKENS : XQA_GQA_CTA_COST_TOKENS;
   const int64_t by_stage = (max_pages + stage_pages - 1) / stage_pages;
   const int64_t by_tokens = std::max<int64_t>(1, (int64_t(max_pages) * p->page_size) / 256);
-  ns = std::max<int64_t>(1, std::min(ns, std::min(by_stage, by_tokens)));
-  ns = std::min<int64_t>(ns, kMaxSplits);
-  int sp = int((max_pages + ns - 1) / ns);
-  sp = ((sp + stage_pages - 1) / stage_pages) * stage_pages;
-  pl->split_pages = sp;
-  pl->nsplit = (max_pages + sp - 1) / sp;
+  const int ns_cap = int(std::max<int64_t>(1, std::min<int64_t>(kMaxSplits, std::min(by_stage, by_tokens))));
+  int best_sp = 0, best_ns = 0;
+  double best = 0.0;
+  for (int ns = 1; ns <= ns_cap; ++ns) {
+    int sp = (max_pages + ns - 1) / ns;
+    sp = ((sp + stage_pages - 1) / stage_pages) * stage_pages;
+    const int nsr = (max_pages + sp - 1) / sp;  // splits that stage rounding leaves
+    if (nsr != ns) continue;
+    const int64_t n = units * nsr;
+    const double piece = double(int64_t(sp) * p->page_size + cost);
+    const int64_t k = n / slots, r = n % slots;
+    const double waves = double(k) + (r ? std::max(double(r) / double(slots), 0.5) : 0.0);
+    const double m = waves * piece;
+    if (best_ns == 0 || m < best * (1.0 - 1e-9)) {
+      best = m;
+      best_sp = sp;
+      best_ns = nsr;
+    }
+  }
+  if (best_ns == 0) {  // (ns = 1 always qualifies; kept for safety)
+    best_sp = ((max_pages + stage_pages - 1) / stage_pages) * stage_pages;
+    best_ns = 1;
+  }
+  pl->split_pages = std::max(best_sp, 1);
+  pl->nsplit = (max_pages + pl->split_pages - 1) / pl->split_pages;
 }
 
 // Tokens per pipeline stage of the GQA kernel: 128 when a K row is one
