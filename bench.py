@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-read-probe", action="store_true",
+                    help="skip the read-only HBM rate logged beside the copy peak")
     ap.add_argument("--op", default="decode", choices=["decode", "merge", "prep"])
     ap.add_argument("--out-dtype", default=None, choices=["e4m3"],
                     help="fp8 output (workloads with an fp8 cache)")
@@ -98,6 +100,33 @@ def peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def read_only_rate(dev, gib=4, reps=10):
+    """The device's read-only HBM rate, measured now by the library's streaming
+    read kernel over `gib` GiB (larger than L2), back to back between one event
+    pair after 3 warm-up launches.  Context beside the copy peak: the decode
+    kernels read the cache and write little, and a copy writes a byte for every
+    byte it reads."""
+    from paged_kv_decode_20_gb300 import xqa as X
+    buf = torch.ones(gib << 28, dtype=torch.int32, device=dev)
+    sink = torch.zeros(4096, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        X.read_bandwidth_probe(buf, sink, stream)
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(reps):
+        X.read_bandwidth_probe(buf, sink, stream)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = t0.elapsed_time(t1) / reps
+    nbytes = buf.numel() * buf.element_size()
+    del buf, sink
+    torch.cuda.empty_cache()
+    return {"value": round(nbytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "bytes": nbytes,
+            "kernel": "read_stream_kernel (16-byte non-temporal loads, 4 CTAs per SM)"}
 
 
 KERNEL_FILES = {
@@ -421,6 +450,12 @@ def run_gb300(args):
         if world > 1:
             dist.destroy_process_group()
         return
+    read_only = None
+    if not args.no_read_probe:
+        if per_workload is None:
+            del dec, case
+            torch.cuda.empty_cache()
+        read_only = read_only_rate(dev)
     peak, peak_kind = peaks()
     achieved = (kv_bytes + q_bytes) / (avg_launch_ms * 1e-3) / 1e9
     value = kv_bytes * world / (ms_per_step * 1e-3) / 1e9
@@ -453,6 +488,7 @@ def run_gb300(args):
                      "kernel": KERNEL_NAMES[args.workload],
                      "algorithmic_bytes_per_launch": kv_bytes + q_bytes,
                      "avg_launch_ms": round(avg_launch_ms, 5)},
+        "read_only_gbs": read_only,
         "gpu_launches": args.steps * launches_per_call,
         "e2e": e2e,
         "cpu_baseline": cpu,

@@ -266,6 +266,20 @@ typedef struct xqa_mla_prep_params {
 
 xqa_status xqa_mla_decode_prep(const xqa_mla_prep_params* params, xqa_stream_t stream);
 
+/* A measurement aid, not part of the decode path: one launch that streams
+   `bytes` of device memory at `buf` once (16-byte non-temporal loads, a
+   grid-stride loop over 4 CTAs per SM, at most `sink_words` CTAs) and writes
+   nothing but, with negligible probability, one word of `sink`.  Timed with
+   events around it, it gives the device's read-only HBM rate that the decode
+   kernels (which read the cache and write little) are set beside; the copy
+   kernel's rate counts a write for every byte read.
+   Errors: XQA_ERR_INVALID_ARG for a null buf or sink, bytes zero or not a
+   multiple of 16, a buf not 16-byte aligned, or sink_words <= 0;
+   XQA_ERR_CUDA for a failed device query or launch.  Asynchronous on
+   `stream`; buf and sink are caller-owned device memory. */
+xqa_status xqa_read_bandwidth_probe(const void* buf, size_t bytes, uint32_t* sink, int sink_words,
+                                    xqa_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* xqa_status_string(xqa_status status);
 

@@ -126,7 +126,7 @@ class XqaMlaPrepParams(ctypes.Structure):
 
 EXPORTS = ["xqa_workspace_size", "xqa_semaphore_count", "xqa_decode", "xqa_mla_workspace_size",
            "xqa_mla_semaphore_count", "xqa_mla_decode", "xqa_decode_noalloc", "xqa_merge_attn_states", "xqa_mla_decode_prep",
-           "xqa_status_string", "xqa_last_error"]
+           "xqa_read_bandwidth_probe", "xqa_status_string", "xqa_last_error"]
 
 _lock = threading.Lock()
 _lib = None
@@ -165,6 +165,9 @@ def load(path: str = LIB_PATH):
             lib.xqa_merge_attn_states.restype = ctypes.c_int
             lib.xqa_mla_decode_prep.argtypes = [ctypes.POINTER(XqaMlaPrepParams), ctypes.c_void_p]
             lib.xqa_mla_decode_prep.restype = ctypes.c_int
+            lib.xqa_read_bandwidth_probe.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_int,
+                                                     ctypes.c_void_p]
+            lib.xqa_read_bandwidth_probe.restype = ctypes.c_int
             lib.xqa_status_string.argtypes = [ctypes.c_int]
             lib.xqa_status_string.restype = ctypes.c_char_p
             lib.xqa_last_error.argtypes = []
@@ -367,6 +370,17 @@ def xqa_mla(q, kv_cache, page_table, seq_lens, output, workspace_buffer, semapho
                     sm_count=sm_count, rcp_out_scale=rcp_out_scale, q_seq_len=q_seq_len,
                     softmax_scale=softmax_scale, error_word=error_word, lse=lse)
     xqa_mla_decode(p, v_head_dim, workspace_buffer, semaphores, stream)
+
+
+def read_bandwidth_probe(buf, sink, stream=None):
+    """One launch of the library's read-only streaming kernel over the bytes
+    of `buf` (a contiguous CUDA tensor, a multiple of 16 bytes); `sink` is an
+    int32 CUDA tensor of at least one word per CTA (4 per SM).  A
+    measurement aid beside the decode path, not part of it."""
+    if not (buf.is_cuda and sink.is_cuda and buf.is_contiguous() and sink.dtype == torch.int32):
+        raise ValueError("buf: contiguous CUDA tensor; sink: int32 CUDA tensor")
+    _check(load().xqa_read_bandwidth_probe(_ptr(buf), buf.numel() * buf.element_size(), _ptr(sink),
+                                           sink.numel(), _stream(stream)))
 
 
 def merge_attn_states(output, prefix_output, prefix_lse, suffix_output, suffix_lse,

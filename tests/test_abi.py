@@ -114,6 +114,19 @@ def test_null_params_rejected(lib):
     assert lib.xqa_decode(None, None, 0, None, None) == X.XQA_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("buf,nbytes,sink,words", [
+    (None, 1 << 20, 0x10000, 16),     # no buffer
+    (0x10000, 0, 0x10000, 16),        # nothing to read
+    (0x10000, 1000, 0x10000, 16),     # not a multiple of 16 bytes
+    (0x10008, 1 << 20, 0x10000, 16),  # buffer not 16-byte aligned
+    (0x10000, 1 << 20, None, 16),     # no sink
+    (0x10000, 1 << 20, 0x10000, 0),   # no sink words
+])
+def test_read_probe_rejects_bad_arguments_before_launch(lib, buf, nbytes, sink, words):
+    assert lib.xqa_read_bandwidth_probe(buf, nbytes, sink, words, None) == X.XQA_ERR_INVALID_ARG
+    assert "read probe" in lib.xqa_last_error().decode()
+
+
 def test_semaphore_count_is_one_per_row_group(lib):
     assert lib.xqa_semaphore_count(ctypes.byref(fake_params())) == 4 * 8
     # 16-bit K/V: more than 16 rows per kv head (D=128) run 128-row tensor-core tiles
