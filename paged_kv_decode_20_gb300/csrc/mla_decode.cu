@@ -81,11 +81,11 @@ constexpr int kPBytes = kRows * kTok * 2;  // one 16-bit P tile
 constexpr int kFBytes = kRows * 4 + 16;    // one rescale factor per row, then a flag word
 constexpr int kPMsg = kPBytes + kFBytes;
 constexpr int kFinBytes = 2 * kRows * 4;   // the final row maxima and sums
-// epilogue staging (in the output CTA's V ring and P slots, 224 KB), both
-// halves of O: fp32 partial parts of 32 columns (32 KB), bf16 output pairs of
-// parts, 64 columns (32 KB)
+// epilogue staging (in the output CTA's V ring and P slots, 224 KB): 28 KB per
+// epilogue warp, 4 KB buffers of its 32 rows x 128 bytes (fp32 partial: 32
+// columns, seven buffers; bf16 output: 64 columns, four buffers)
 constexpr int kStageF32 = 7;
-constexpr int kStageBf16 = kRows * 128 * 2;
+constexpr int kWarpStage = kStageF32 * 4096;
 constexpr int kCopyPieces = 4;             // P travels as this many bulk copies
 
 // ---- shared memory (offsets from the dynamic base, which is 1024-aligned:
@@ -353,12 +353,18 @@ __device__ __forceinline__ void st_keep4(float* dst, float x, float y, float z, 
 __device__ __forceinline__ void st_keep2(float* dst, float x, float y, uint64_t pol) {
   asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;" ::"l"(dst), "f"(x), "f"(y), "l"(pol) : "memory");
 }
-// One 2-D TMA box from shared memory to global memory (a bulk async-group),
-// optionally with an L2 cache policy.
+// One 2-D (3-D) TMA box from shared memory to global memory (a bulk
+// async-group), optionally with an L2 cache policy.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
                "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
                : "memory");
 }
 __device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* map, const void* src, int x, int y, uint64_t pol) {
@@ -1197,10 +1203,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const float kv_scale = ldscale(a.kv_scale_dev, a.kv_scale);
     bool ok = true;
     // the previous piece's partial stores have had a piece's start to land:
-    // count that piece done for the merge kernel
-    if (st == 0 && pend_b >= 0) {
-      bulk_wait_all_visible();
-      atomicAdd(a.sems + pend_b, 1u);
+    // count that piece done for the merge kernel (every warp's stores)
+    if (pend_b >= 0) {
+      if (lane == 0) bulk_wait_all_visible();
+      named_bar(2, kSoft);
+      if (st == 0) {
+        __threadfence();
+        atomicAdd(a.sems + pend_b, 1u);
+      }
       pend_b = -1;
     }
     if constexpr (F8) {
@@ -1287,59 +1297,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       const int64_t slot = persistent ? 2 * int64_t(k_cl) + (cl_first ? 0 : 1) : int64_t(b) * a.nsplit + split;
       const uint64_t keep = l2_keep_policy();
-      // O leaves through TMA stores of 32-column parts staged in the free V
-      // ring and P slots (a part's two halves, swizzled rows), so that the
-      // epilogue threads write shared memory only: one thread per row writing
-      // its row straight to global memory touches 32 lines per warp store.
-      // fp32 partial: [half][128 rows][128 B] per part, seven 32 KB buffers;
-      // bf16 output: [half][128 rows][128 B] per pair of parts, four 32 KB
-      // buffers, only the R real rows stored (128-byte swizzle).
-      uint8_t* const stage = smem + SL::kOffV;
+      // O leaves through TMA stores that each warp issues for its own 32 rows
+      // (no barrier between warps): a part is staged as [32 rows][128 B]
+      // (128-byte swizzle) in the warp's 28 KB of the free V ring and P
+      // slots, then stored by the warp's first lane.  bf16 output: four
+      // 64-column pairs, each its own buffer, clipped at the sequence's R real
+      // rows by the 3-D output view; fp32 partial: eight 32-column parts
+      // through seven buffers.  The next part's columns come out of tensor
+      // memory while the current one is staged.
+      uint8_t* const wbuf = smem + SL::kOffV + (st >> 5) * kWarpStage;
+      const bool store_rows = single ? 32 * q4 < a.R : true;
 #pragma unroll 1
       for (int part = 0; part < kHalf / 32; ++part) {
-        float o[32];
+        float cur[32];
         if (have_o) {
-          umma::tmem_ld32(o_cols + 32u * part, o);
+          umma::tmem_ld32(o_cols + 32u * part, cur);
           umma::tmem_ld_wait();
         } else {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] = 0.f;
+          for (int k = 0; k < 32; ++k) cur[k] = 0.f;
         }
         if (single) {
           // two parts (64 bf16 columns, 128 bytes) per staged row
-          uint8_t* buf = stage + (part >> 1) * kStageBf16 + h * (kStageBf16 / 2);
+          uint8_t* buf = wbuf + (part >> 1) * 4096;
 #pragma unroll
           for (int v = 0; v < 4; ++v)
-            *reinterpret_cast<uint4*>(buf + umma::sw128(t, 4 * (part & 1) + v)) =
-                make_uint4(pack_f32x2(o[8 * v] * mul, o[8 * v + 1] * mul, true),
-                           pack_f32x2(o[8 * v + 2] * mul, o[8 * v + 3] * mul, true),
-                           pack_f32x2(o[8 * v + 4] * mul, o[8 * v + 5] * mul, true),
-                           pack_f32x2(o[8 * v + 6] * mul, o[8 * v + 7] * mul, true));
-        } else {
-          // the buffer of the part kStageF32 back is free once its stores read it
-          if (part >= kStageF32) {
-            if (st == 0) bulk_wait_read<kStageF32 - 1>();
-            named_bar(2, kSoft);
+            *reinterpret_cast<uint4*>(buf + umma::sw128(lane, 4 * (part & 1) + v)) =
+                make_uint4(pack_f32x2(cur[8 * v] * mul, cur[8 * v + 1] * mul, true),
+                           pack_f32x2(cur[8 * v + 2] * mul, cur[8 * v + 3] * mul, true),
+                           pack_f32x2(cur[8 * v + 4] * mul, cur[8 * v + 5] * mul, true),
+                           pack_f32x2(cur[8 * v + 6] * mul, cur[8 * v + 7] * mul, true));
+          if ((part & 1) == 0) continue;  // (the pair's second part stores both)
+          umma::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && store_rows) {
+            tma_store_3d(&tmO, buf, kHalf * h + 32 * (part - 1), 32 * q4, b);
+            bulk_commit();
           }
-          uint8_t* buf = stage + (part % kStageF32) * (kRows * 256) + h * (kRows * 128);
+        } else {
+          // the buffer of the part kStageF32 back is free once its store read it
+          if (part >= kStageF32) {
+            if (lane == 0) bulk_wait_read<kStageF32 - 1>();
+            __syncwarp();
+          }
+          uint8_t* buf = wbuf + (part % kStageF32) * 4096;
 #pragma unroll
           for (int v = 0; v < 8; ++v)
-            *reinterpret_cast<float4*>(buf + umma::sw128(t, v)) =
-                make_float4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
-        }
-        if (single && (part & 1) == 0) continue;  // (the pair's second part stores both)
-        umma::fence_proxy_async_smem();
-        named_bar(2, kSoft);
-        if (st == 0) {
-          for (int hh = 0; hh < 2; ++hh) {
-            if (single)
-              tma_store_2d(&tmO, stage + (part >> 1) * kStageBf16 + hh * (kStageBf16 / 2),
-                           kHalf * hh + 32 * (part - 1), b * a.R);
-            else
-              tma_store_2d_hint(&tmWs, stage + (part % kStageF32) * (kRows * 256) + hh * (kRows * 128),
-                                kHalf * hh + 32 * part, int(slot) * kRows, keep);
+            *reinterpret_cast<float4*>(buf + umma::sw128(lane, v)) =
+                make_float4(cur[4 * v], cur[4 * v + 1], cur[4 * v + 2], cur[4 * v + 3]);
+          umma::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d_hint(&tmWs, buf, kHalf * h + 32 * part, int(slot) * kRows + 32 * q4, keep);
+            bulk_commit();
           }
-          bulk_commit();
         }
       }
       if (!single && h == 0) {
@@ -1347,12 +1358,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         st_keep2(wrow + kLatent, m_fin, l_fin, keep);
       }
       // the staging is free again before the next piece loads V into it
-      if (st == 0) bulk_wait_read<0>();
+      if (lane == 0) bulk_wait_read<0>();
+      __syncwarp();
     }
     // a partial is counted done once its stores have landed (at the next
     // piece's start, or at the end); also after an abort, which the error
     // word reports, so that the merge does not wait out its time limit
-    if (st == 0 && nvalid > 1) pend_b = b;
+    if (nvalid > 1) pend_b = b;
   }
 
   // ---- end of the piece: no tensor-memory or peer traffic may outlive this
@@ -1379,9 +1391,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }  // pieces
 
   // ---- teardown
-  if (pend_b >= 0) {  // (the output CTA's first epilogue thread)
-    bulk_wait_all_visible();
-    atomicAdd(a.sems + pend_b, 1u);
+  if (pend_b >= 0) {  // (the output CTA's eight epilogue warps)
+    if (lane == 0) bulk_wait_all_visible();
+    named_bar(2, kSoft);
+    if (tid == 32 * kSoftWarp0) {
+      __threadfence();
+      atomicAdd(a.sems + pend_b, 1u);
+    }
   }
   umma::fence_before_sync();
   __syncthreads();
@@ -1790,22 +1806,23 @@ xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_b
       return XQA_ERR_CUDA;
     }
   }
-  // epilogue store views: the output (bf16, 512 per row; a box is 64
-  // columns of one sequence's R real rows) and the split partials (fp32,
-  // 512 + 4 per row; a box is 32 columns of a slot's 128 rows)
+  // epilogue store views, one box per epilogue warp (its 32 rows): the
+  // output (bf16, 512 per row, as [sequence][R rows][512]; a box is 64
+  // columns of 32 rows, clipped at the R real rows) and the split partials
+  // (fp32, 512 + 4 per row; a box is 32 columns of 32 rows of a slot)
   CUtensorMap to, tws = tpf;
   {
     const int R = p->num_q_heads * p->q_seq_len;
-    cuuint64_t odims[2] = {kLatent, cuuint64_t(p->batch_size) * R};
-    cuuint64_t ostrides[1] = {kLatent * 2};
-    cuuint32_t obox[2] = {64, cuuint32_t(R)};
-    r = enc(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->output, odims, ostrides, obox, estr,
+    cuuint64_t odims[3] = {kLatent, cuuint64_t(R), cuuint64_t(p->batch_size)};
+    cuuint64_t ostrides[2] = {kLatent * 2, cuuint64_t(R) * kLatent * 2};
+    cuuint32_t obox[3] = {64, cuuint32_t(std::min(R, 32)), 1};
+    r = enc(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p->output, odims, ostrides, obox, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r == CUDA_SUCCESS && pl.ws_bytes > 0) {
       cuuint64_t wdims[2] = {kLatent + 4, cuuint64_t(pl.ws_bytes / ((kLatent + 4) * sizeof(float)))};
       cuuint64_t wstrides[1] = {(kLatent + 4) * sizeof(float)};
-      cuuint32_t wbox[2] = {32, kRows};
+      cuuint32_t wbox[2] = {32, 32};
       r = enc(&tws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ws, wdims, wstrides, wbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
