@@ -136,8 +136,9 @@ xqa_status xqa_decode(const xqa_params* params, void* workspace, size_t workspac
                       uint32_t* semaphores, xqa_stream_t stream);
 
 /* Same sizing queries for the MLA latent variant (num_kv_heads = 1).  The
-   workspace holds the split partials (fp32); the semaphores (two per
-   sequence) count each sequence's finished pieces and finished merge items. */
+   workspace holds the split partials (fp32); the semaphores (2 B + 2) count
+   each sequence's finished pieces and finished merge items, then hand out the
+   merge kernel's work items and count its finished CTAs. */
 size_t xqa_mla_workspace_size(const xqa_params* params, int v_head_dim, int sm_count);
 size_t xqa_mla_semaphore_count(const xqa_params* params, int v_head_dim);
 
@@ -152,7 +153,8 @@ size_t xqa_mla_semaphore_count(const xqa_params* params, int v_head_dim);
    semaphores (xqa_mla_semaphore_count uint32, 4-byte aligned; may be NULL
    when the workspace size is 0) must be zero on the first call; every call
    that runs to its end leaves them zero, also one that reported a timeout
-   (bit 1 of error_word): a merge that gave up waiting still counts itself. */
+   (bit 1 of error_word): a merge that gave up waiting still counts itself,
+   and the last merge CTA to finish zeroes the work counter. */
 xqa_status xqa_mla_decode(const xqa_params* params, int v_head_dim, void* workspace,
                           size_t workspace_bytes, uint32_t* semaphores, xqa_stream_t stream);
 

@@ -1437,6 +1437,7 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeCtasPerSm) mla_merge_kern
   __shared__ float s_w[kMergeRows * kMaxPieces];  // per (row, piece): the maximum, then the weight
   __shared__ float s_l[kMergeRows * kMaxPieces];
   __shared__ bool s_ready;
+  __shared__ int s_item;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool persistent = a.B <= kOrderMaxB;
   if (persistent) {
@@ -1482,7 +1483,16 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeCtasPerSm) mla_merge_kern
   const int c4 = tid % (kHalf / 4), rq = tid / (kHalf / 4);
   const float out_mul = ldscale(a.kv_scale_dev, a.kv_scale) * a.rcp_out_scale;
   const int items = a.B * 2 * kBlocks;
-  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+  // Items are handed out by a counter (semaphore 2B), so that the CTAs that
+  // start first (on the SMs the first decode clusters leave) take most of
+  // them and the last ones to start find the work done.
+  uint32_t* const next_item = a.sems + 2 * a.B;
+  for (;;) {
+    if (tid == 0) s_item = int(atomicAdd(next_item, 1u));
+    __syncthreads();
+    const int item = s_item;
+    __syncthreads();  // (s_item is rewritten for the next item)
+    if (item >= items) break;
     const int b = item / (2 * kBlocks), c = (item / kBlocks) & 1, r0 = (item % kBlocks) * kMergeRows;
     if (r0 >= a.R) continue;
     // pieces; piece 0's slot, and piece sp >= 1's at slot1 + step (sp - 1):
@@ -1595,6 +1605,15 @@ __global__ void __launch_bounds__(kMergeThreads, kMergeCtasPerSm) mla_merge_kern
       }
     }
   }
+  // the last CTA to leave zeroes the item counter and its own count for the
+  // next call (every CTA has drawn its last, out-of-range item by then)
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(a.sems + 2 * a.B + 1, 1u) == gridDim.x - 1) {
+      *next_item = 0u;
+      a.sems[2 * a.B + 1] = 0u;
+    }
+  }
 }
 
 // ---------------------------------------------------------------- host side
@@ -1692,7 +1711,9 @@ size_t mla_workspace_size(const xqa_params* p, int v_head_dim, int sm_count) {
 
 size_t mla_semaphore_count(const xqa_params* p, int v_head_dim) {
   if (!p || mla::check_shape(p, v_head_dim)) return size_t(-1);
-  return size_t(p->batch_size) * 2;  // per sequence: finished pieces, finished merge items
+  // per sequence: finished pieces, finished merge items; then the merge
+  // kernel's item counter and its count of finished CTAs
+  return size_t(p->batch_size) * 2 + 2;
 }
 
 xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_bytes, uint32_t* sems,
@@ -1725,7 +1746,7 @@ xqa_status mla_decode(const xqa_params* p, int v_head_dim, void* ws, size_t ws_b
       return XQA_ERR_INVALID_ARG;
     }
     if (!sems) {
-      snprintf(err, err_len, "semaphores are required (%zu needed)", size_t(p->batch_size) * 2);
+      snprintf(err, err_len, "semaphores are required (%zu needed)", size_t(p->batch_size) * 2 + 2);
       return XQA_ERR_WORKSPACE_TOO_SMALL;
     }
     if (reinterpret_cast<uintptr_t>(sems) & 3) {

@@ -45,10 +45,12 @@ class Decoder:
         self.semaphores = torch.zeros(max(ns, 1), dtype=torch.int32, device=dev)
 
     def run(self, stream=None):
+        # (the semaphores were sized by the library's query at construction)
         if self.mla:
-            X.xqa_mla_decode(self.params, self.v_head_dim, self.workspace, self.semaphores, stream)
+            X.xqa_mla_decode(self.params, self.v_head_dim, self.workspace, self.semaphores, stream,
+                             check_semaphores=False)
         else:
-            X.xqa_decode(self.params, self.workspace, self.semaphores, stream)
+            X.xqa_decode(self.params, self.workspace, self.semaphores, stream, check_semaphores=False)
         return self.output
 
     def error_bits(self):

@@ -327,15 +327,35 @@ def xqa_mla_semaphore_count(params: XqaParams, v_head_dim: int) -> int:
     return n
 
 
-def xqa_decode(params: XqaParams, workspace, semaphores, stream=None):
-    """Launch through the C ABI.  workspace: uint8 CUDA tensor or None."""
+def _check_semaphores(semaphores, count):
+    """The C ABI takes the semaphores as a bare pointer: a tensor shorter than
+    the count the sizing query returns is refused here, before the launch.
+    (Parameters the sizing query rejects are left to the call's own status.)"""
+    try:
+        needed = count()
+    except XqaError:
+        return
+    if semaphores is not None and needed > 0 and semaphores.numel() * semaphores.element_size() < 4 * needed:
+        raise XqaError(XQA_ERR_WORKSPACE_TOO_SMALL,
+                       f"semaphores hold {semaphores.numel() * semaphores.element_size() // 4} uint32, "
+                       f"{needed} needed")
+
+
+def xqa_decode(params: XqaParams, workspace, semaphores, stream=None, check_semaphores=True):
+    """Launch through the C ABI.  workspace: uint8 CUDA tensor or None.
+    check_semaphores=False skips the size check (a caller that sized the
+    buffer with xqa_semaphore_count for these parameters)."""
+    if check_semaphores:
+        _check_semaphores(semaphores, lambda: xqa_semaphore_count(params))
     ws_ptr = None if workspace is None else _ptr(workspace)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().xqa_decode(ctypes.byref(params), ws_ptr, ws_bytes, _ptr(semaphores),
                              _stream(stream)))
 
 
-def xqa_mla_decode(params: XqaParams, v_head_dim, workspace, semaphores, stream=None):
+def xqa_mla_decode(params: XqaParams, v_head_dim, workspace, semaphores, stream=None, check_semaphores=True):
+    if check_semaphores:
+        _check_semaphores(semaphores, lambda: xqa_mla_semaphore_count(params, v_head_dim))
     ws_ptr = None if workspace is None else _ptr(workspace)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().xqa_mla_decode(ctypes.byref(params), int(v_head_dim), ws_ptr, ws_bytes,

@@ -283,11 +283,25 @@ def mla_params(**over):
 def test_mla_workspace_persistent_clusters(lib, sm, clusters):
     """Up to 256 sequences: one persistent cluster per SM pair (at most 128), two
     partial slots each; a single cluster needs no partials.  Two semaphores
-    per sequence: its finished pieces and its finished merge items."""
+    per sequence (its finished pieces and its finished merge items), then the
+    merge kernel's item counter and its count of finished CTAs."""
     p = mla_params(batch_size=64)
     expect = clusters * 2 * MLA_PARTIAL if clusters > 1 else 0
     assert lib.xqa_mla_workspace_size(ctypes.byref(p), 512, sm) == expect
-    assert lib.xqa_mla_semaphore_count(ctypes.byref(p), 512) == 64 * 2
+    assert lib.xqa_mla_semaphore_count(ctypes.byref(p), 512) == 64 * 2 + 2
+
+
+def test_binding_refuses_short_semaphores_before_launch(lib):
+    """The C ABI takes the semaphores as a bare pointer; the binding checks the
+    tensor against the sizing query and raises before any launch."""
+    import torch
+    short = torch.zeros(64 * 2, dtype=torch.int32)  # two short of 2 B + 2
+    with pytest.raises(X.XqaError) as e:
+        X.xqa_mla_decode(mla_params(batch_size=64), 512, None, short)
+    assert e.value.status == X.XQA_ERR_WORKSPACE_TOO_SMALL
+    with pytest.raises(X.XqaError) as e:
+        X.xqa_decode(fake_params(), None, torch.zeros(4 * 8 - 1, dtype=torch.int32))
+    assert e.value.status == X.XQA_ERR_WORKSPACE_TOO_SMALL
 
 
 def test_mla_workspace_fixed_splits_above_256_sequences(lib):

@@ -170,7 +170,7 @@ def test_mla_e4m3_scales_from_device_and_output_scale():
     c = mla_case([1500, 40], seed=47, dtype=F8, rcp_out_scale=0.5).to("cuda")
     out = torch.empty((2, 1, 128, 512), dtype=torch.bfloat16, device="cuda")
     ws = torch.zeros(1 << 26, dtype=torch.uint8, device="cuda")
-    sems = torch.zeros(4, dtype=torch.int32, device="cuda")
+    sems = torch.zeros(2 * 2 + 2, dtype=torch.int32, device="cuda")
     X.xqa_mla(c.q, c.k_cache, c.page_table, c.seq_lens, out, ws, sems, page_size=64, v_head_dim=512,
               softmax_scale=SCALE, q_scale=torch.tensor([0.05], device="cuda"),
               kv_scale=torch.tensor([0.05], device="cuda"), rcp_out_scale=0.5)

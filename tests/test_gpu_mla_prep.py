@@ -154,7 +154,7 @@ def test_prep_then_decode_e4m3_step():
                            cache_scale_inv=torch.tensor([1 / kv_scale], device=dev))
     out = torch.empty((B, 1, H, Lr), dtype=torch.bfloat16, device=dev)
     ws = torch.zeros(1 << 26, dtype=torch.uint8, device=dev)
-    sems = torch.zeros(2 * B, dtype=torch.int32, device=dev)
+    sems = torch.zeros(2 * B + 2, dtype=torch.int32, device=dev)
     X.xqa_mla(q8.view(B, 1, H, Lr + R), cache_g, c.page_table.to(dev), c.seq_lens.to(dev), out, ws, sems,
               page_size=64, v_head_dim=Lr, softmax_scale=(128 + 64) ** -0.5, q_scale=q_scale, kv_scale=kv_scale)
     torch.cuda.synchronize()
