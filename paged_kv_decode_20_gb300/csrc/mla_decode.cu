@@ -174,7 +174,11 @@ enum BarIdx {
   kDec = kHEmpty + 2,              // [2] e4m3: the MMA thread's rescale decision for a tile
   // both
   kDrain = kDec + 2,               // every MMA this CTA issued is done
-  kNumBars = kDrain + 1
+  kNumBars = kDrain + 1,
+  // bf16 logit CTA, set up once per kernel (in the slot of an e4m3-only
+  // barrier): the output CTA has set up its barriers for the next piece (one
+  // arrival per piece)
+  kPeerReady = kDec
 };
 template <bool F8>
 constexpr int smem_bytes() {
@@ -274,6 +278,12 @@ __device__ __forceinline__ void commit_to(uint64_t* bar, uint16_t mask) {
           smem_u32(bar)),
       "h"(mask)
       : "memory");
+}
+
+// One arrival on a barrier of a peer CTA (its cluster address), ordered
+// after this thread's earlier writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_peer(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
 __device__ __forceinline__ float ldscale(const float* dev, float host) { return dev ? __ldg(dev) : host; }
@@ -471,6 +481,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmWs,
                       const __grid_constant__ CUtensorMap tmO, const MlaArgs a) {
   using SL = Lay<F8>;
+  // pieces overlap across the cluster (see the end of the piece loop)
+  constexpr bool kDecoupled = !F8;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SL::kOffBar);
@@ -548,13 +560,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     __syncthreads();  // the scratch is reused below
   }
-  if (tid == 0) flags[0] = flags[1] = flags[2] = flags[3] = 0;  // also for a cluster with no piece
+  if (tid == 0) {
+    flags[0] = flags[1] = flags[2] = flags[3] = 0;  // also for a cluster with no piece
+    if (kDecoupled && logit_cta) {
+      mbar_init(&bars[kPeerReady], 1);
+      fence_mbar_init();
+    }
+  }
   if (warp == 0) {
     umma::tmem_alloc(tmem_slot, kTmemCols);
     umma::tmem_relinquish();
   }
   umma::fence_before_sync();
   __syncthreads();
+  // bf16: the logit CTA's readiness barrier exists before the output CTA
+  // signals it; from here on the two CTAs meet only through their barriers
+  // (each sets up its own barriers for every piece, the output CTA then
+  // signals the logit CTA, which sends nothing of the piece before that
+  // signal) and once more before they exit
+  if (kDecoupled) cluster_sync();
   umma::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   const uint32_t peer_bars = map_peer(smem_u32(bars), peer);
@@ -662,10 +686,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     flags[0] = flags[1] = flags[2] = 0;
     fence_mbar_init();
+    // the logit CTA may send this piece's messages now
+    if (kDecoupled && !logit_cta) mbar_arrive_peer(map_peer(smem_u32(&bars[kPeerReady]), peer));
   }
   umma::fence_before_sync();
   __syncthreads();
-  cluster_sync();  // the peer's barriers exist before any remote access
+  if (!kDecoupled) cluster_sync();  // the peer's barriers exist before any remote access
   umma::fence_after_sync();
   const int32_t* pt = a.page_table + int64_t(b) * a.pps;
   // this cluster's next sequence (persistent), whose query the logit CTA's
@@ -1044,6 +1070,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     float m_ref = -INFINITY, l_half = 0.f;
     bool ok = true;
+    // The output CTA signals once it has set up this piece's barriers: until
+    // then this piece's tiles are computed and staged but not sent (the
+    // output CTA may still be writing the previous piece out).
+    bool peer_ready = false, peer_ok = false;
+    auto wait_peer = [&]() {
+      if (peer_ready) return;
+      peer_ready = true;
+      peer_ok = mbar_wait(&bars[kPeerReady], uint32_t(order) & 1u);
+      if (!peer_ok) ok = false;
+    };
     // Control flow stays uniform across each warp (tcgen05.ld is
     // warp-collective) and across the eight softmax warps (named barrier 1):
     // waits are voted and the loop is left collectively.
@@ -1145,8 +1181,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       umma::fence_proxy_async_smem();
       // every thread wrote its P and factor; does any row need O rescaled?
       const bool resc = named_bar_or(1, kSoft, f != 1.f);
+      if constexpr (kDecoupled) wait_peer();
       // P in four copies from four warps, the factors and the flag from a fifth
-      if ((st & 31) == 0 && st < 32 * kCopyPieces) {
+      if (kDecoupled && !ok) {
+      } else if ((st & 31) == 0 && st < 32 * kCopyPieces) {
         const uint32_t off = uint32_t(st >> 5) * (kPBytes / kCopyPieces);
         bulk_to_peer(p_peer + p2 * kPBytes + off, smem_u32(pstage) + off, kPBytes / kCopyPieces,
                      peer_bars + 8u * (kPFull + p2));
@@ -1157,6 +1195,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
     }
+    if constexpr (kDecoupled) wait_peer();
     if (!ok) flags[0] = 1;
     // ---- the final row maxima and sums go to the output CTA (also when this
     // split saw no key: m = -inf, l = 0)
@@ -1171,7 +1210,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     umma::fence_proxy_async_smem();
     named_bar(1, kSoft);
     if (st == 0) {
-      bulk_to_peer(map_peer(smem_u32(smem + SL::kOffFin), peer), smem_u32(fin), kFinBytes, peer_bars + 8u * kFin);
+      if (!kDecoupled || peer_ok)
+        bulk_to_peer(map_peer(smem_u32(smem + SL::kOffFin), peer), smem_u32(fin), kFinBytes, peer_bars + 8u * kFin);
       // the peer's completion signals for the last two P slots must land
       // before this CTA may exit
       for (int j = max(0, ntiles - 2); ok && j < ntiles; ++j)
@@ -1367,20 +1407,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (nvalid > 1) pend_b = b;
   }
 
-  // ---- end of the piece: no tensor-memory or peer traffic may outlive this
-  // point.  A wait that gave up in either CTA ends the loop for both (each
-  // reads the other's flag between two cluster barriers), so the CTAs of a
-  // cluster always pass the same cluster barriers.
+  // ---- end of the piece in this CTA: no tensor-memory traffic outlives this
+  // point, and none of the peer's: the output CTA has received every message
+  // of the piece, the logit CTA every completion signal.  bf16: the logit CTA
+  // goes on to the next piece while the output CTA still writes this one out;
+  // a wait that gave up ends the loop for this CTA, and the peer's next wait
+  // on it then gives up too.  e4m3 (bound by the output CTA, so that the
+  // logit CTA gains nothing by running ahead): both CTAs pass two cluster
+  // barriers, between which each reads the other's abort flag, and leave the
+  // loop together.
   umma::fence_before_sync();
   __syncthreads();
-  cluster_sync();
-  if (tid == 0) {
-    uint32_t peer_abort;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(peer_abort) : "r"(map_peer(smem_u32(flags), peer)) : "memory");
-    flags[3] = flags[0] | int(peer_abort);
+  if constexpr (kDecoupled) {
+    if (flags[0]) break;
+  } else {
+    cluster_sync();
+    if (tid == 0) {
+      uint32_t peer_abort;
+      asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(peer_abort) : "r"(map_peer(smem_u32(flags), peer))
+                   : "memory");
+      flags[3] = flags[0] | int(peer_abort);
+    }
+    cluster_sync();
+    if (flags[3]) break;
   }
-  cluster_sync();
-  if (flags[3]) break;
   first_piece = false;
   if (!persistent) break;
   if (!z_now) {
@@ -1389,6 +1439,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   ++order;
   }  // pieces
+  // neither CTA leaves while the peer may still reach its shared memory
+  // (e4m3: the last piece's cluster barriers did that)
+  if (kDecoupled) cluster_sync();
 
   // ---- teardown
   if (pend_b >= 0) {  // (the output CTA's eight epilogue warps)
