@@ -265,11 +265,15 @@ def tensor_roofline(case, ms):
             "flops_per_launch": qk + pv}
 
 
+WORKLOAD_REST_S = 1.0
+
+
 def time_workload(key, dev, launches, flush):
     """Times one named workload's decode call on `dev` and returns its summary
     for the bench line's `workloads` object.
 
-    Workloads whose KV exceeds L2 are timed back to back (one event pair
+    Each workload's timed calls start after a 1 s rest.  Workloads whose KV
+    exceeds L2 are timed back to back (one event pair
     around all calls; consecutive calls overlap their launch latency through
     programmatic dependent launch).  The small ones (KV inside L2) are timed
     twice: with L2 flushed before every call (a 256 MB write outside the
@@ -286,6 +290,9 @@ def time_workload(key, dev, launches, flush):
     for _ in range(5):
         dec.run(stream)
     torch.cuda.synchronize(dev)
+    # a rest before the timed calls: the previous workload's (and the input
+    # generation's) power draw must not carry over into this one's clocks
+    time.sleep(WORKLOAD_REST_S)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(launches)]
     with Clocks(dev.index) as clk:
         b2b = None
