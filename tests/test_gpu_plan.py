@@ -60,3 +60,25 @@ def test_read_probe_streams_a_buffer():
     # the sink is written only when a CTA's folded word equals a fixed
     # constant; all-ones data folds to zero
     assert int(sink.abs().sum()) == 0
+
+
+def test_single_long_sequence_runs_many_splits_and_matches_the_oracle():
+    """One 32768-token sequence: the plan splits it across about one CTA per
+    SM (the last CTA of each kv head merges the partials); every row against
+    the oracle."""
+    import oracle
+    from paged_kv_decode_20_gb300 import workloads as W
+    from paged_kv_decode_20_gb300.runner import Decoder
+    c = W.make_case(batch=1, num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=64, seq_lens=[32768],
+                    kv_layout="HND", pages_per_seq=512, seed=61, device="cuda", poison=False)
+    dec = Decoder(c)
+    assert dec.workspace.numel() > 16  # split partials in use
+    out = dec.run()
+    torch.cuda.synchronize()
+    assert dec.error_bits() == 0
+    assert int(dec.semaphores.abs().sum()) == 0
+    cc = c.to("cpu")
+    ref = oracle.xqa_attention(cc.q, cc.k_cache, cc.v_cache, cc.page_table, cc.seq_lens, **cc.kwargs())
+    got = out.cpu().to(torch.float64)
+    assert (got - ref).abs().max().item() <= 1e-2
+    assert ((got - ref).norm() / ref.norm()).item() <= 1e-2
