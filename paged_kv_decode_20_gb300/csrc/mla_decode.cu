@@ -38,7 +38,10 @@
 // first.  A sequence cut across clusters leaves one partial per piece, counted
 // done on a per-sequence semaphore; a second kernel (mla_merge_kernel) merges
 // each such sequence once its pieces are done.  Larger batches take one
-// cluster per (sequence, fixed-size split), merged the same way.
+// cluster per (sequence, fixed-size split), merged the same way.  In the bf16
+// kernel the logit CTA starts a piece while the output CTA still writes the
+// previous one out: it computes and stages the new piece's first tiles and
+// sends them once the output CTA signals that its barriers are set up.
 //
 // The logit CTA is bound by its MMA instruction rate: an M = 128, N = 128,
 // K = 16 tcgen05.mma accumulating into one tile takes ~140 cycles, and a
