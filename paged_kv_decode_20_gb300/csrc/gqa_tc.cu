@@ -64,7 +64,8 @@ struct Cfg {
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
   static constexpr int kOffP = kOffV + kVStages * kTileBytes;
   static constexpr int kOffRowX = kOffP + 2 * kPBytes;  // [2][128] row maxima / sums of the halves
-  static constexpr int kOffBar = kOffRowX + 2 * kRows * 4;
+  static constexpr int kOffOrd = kOffRowX + 2 * kRows * 4;  // [160] the sequences, longest first
+  static constexpr int kOffBar = kOffOrd + 160 * 4;
   enum {
     kKFull = 0,                     // [kKStages] a K tile landed
     kKEmpty = kKFull + kKStages,    // [kKStages] the Q K^T reading it is done
@@ -74,8 +75,9 @@ struct Cfg {
     kSFree = kSFull + 2,            // [2] S(j) read out of tensor memory (8 warps)
     kPFull = kSFree + 2,            // [2] P(j) written, O rescaled, V tail zeroed (8 warps)
     kPVDone = kPFull + 2,           // [2] P(j) V(j) done
-    kQReady = kPVDone + 2,          // the query is in tensor memory (8 warps)
-    kDrain = kQReady + 1,           // every MMA is done
+    kQReady = kPVDone + 2,          // a unit's query is in tensor memory (8 warps)
+    kOFree = kQReady + 1,           // a unit's O was read out of tensor memory (8 warps)
+    kDrain = kOFree + 1,            // every MMA is done
     kNumBars = kDrain + 1
   };
   static constexpr int kSmem = kOffBar + kNumBars * 8 + 16;
@@ -94,6 +96,55 @@ __device__ __forceinline__ void zero_v_rows(uint8_t* vtile, int r0, int st) {
   }
 }
 
+// One unit of work: (sequence b, kv head kvh, row group rg, KV split) and
+// the stretch of its tokens that the split covers.
+struct Unit {
+  int b, kvh, rg, split;
+  int L, spec0, pg_hi, t_begin, t_end, ntiles, nvalid, rows_here;
+};
+
+// Unit k of this CTA; false past its last.  One CTA per unit (grid = splits x
+// (kv heads x row groups) x sequences, slot z taking the sequence of rank z),
+// or persistent CTAs (a.persist of them): CTA c takes the units of rank
+// k G + c for even k and k G + G - 1 - c for odd k (G CTAs; units ranked by
+// their sequence's length, longest first, then kv head and row group), so
+// that the long and the short units even out across the CTAs.
+__device__ __forceinline__ bool unit_at(const DecodeArgs& a, const int* ord, int k, Unit& u) {
+  if (a.persist == 0) {
+    if (k > 0) return false;
+    u.split = blockIdx.x;
+    u.kvh = blockIdx.y / a.rg_count;
+    u.rg = blockIdx.y % a.rg_count;
+    u.b = a.sort_b ? ord[blockIdx.z] : int(blockIdx.z);
+  } else {
+    const int G = int(gridDim.z), c = int(blockIdx.z);
+    const int r = k * G + ((k & 1) ? G - 1 - c : c);
+    const int per_seq = a.Hkv * a.rg_count;
+    if (r >= a.B * per_seq) return false;
+    u.b = ord[r / per_seq];
+    const int rem = r % per_seq;
+    u.kvh = rem / a.rg_count;
+    u.rg = rem % a.rg_count;
+    u.split = 0;
+  }
+  const int64_t max_len = int64_t(a.pps) * a.ps;
+  const int64_t len_raw = a.seq_lens[u.b];
+  u.L = int(len_raw < max_len ? len_raw : max_len);
+  u.spec0 = u.L - a.qs;
+  const int t_lo_all = a.win > 0 ? max(0, u.spec0 - a.win + 1) : 0;
+  const int pg_first = t_lo_all / a.ps;
+  const int pg_last = (u.L + a.ps - 1) / a.ps;
+  const int npages = max(0, pg_last - pg_first);
+  u.nvalid = (npages + a.split_pages - 1) / a.split_pages;
+  const int pg_lo = pg_first + u.split * a.split_pages;
+  u.pg_hi = min(pg_lo + a.split_pages, pg_last);
+  u.t_begin = pg_lo * a.ps;
+  u.t_end = min(u.pg_hi * a.ps, u.L);
+  u.ntiles = (u.nvalid == 0 || u.t_end <= u.t_begin || u.split >= u.nvalid) ? 0 : (u.t_end - u.t_begin + kT - 1) / kT;
+  u.rows_here = min(kRows, a.R - u.rg * kRows);
+  return true;
+}
+
 template <bool kBf16, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -107,17 +158,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] abort, [1] last CTA
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int split = blockIdx.x;
-  const int kvh = blockIdx.y / a.rg_count, rg = blockIdx.y % a.rg_count;
-  int b = blockIdx.z;
+  int* ord = reinterpret_cast<int*>(smem + C::kOffOrd);
   pdl_wait();
   pdl_launch_dependents();
 
-  // Longest sequences first: CTAs launch in blockIdx order, so grid slot z
-  // takes the sequence with the z-th most visible tokens (ties by index), and
-  // the long CTAs start in the first wave instead of trailing the last one.
-  // Every CTA ranks the (at most 160) sequences itself in shared memory (the
-  // K ring, unused until the first load).
+  // Longest sequences first: ord[z] is the sequence with the z-th most
+  // visible tokens (ties by index).  With one CTA per unit, CTAs launch in
+  // blockIdx order and grid slot z takes sequence ord[z], so the long CTAs
+  // start in the first wave instead of trailing the last one; persistent
+  // CTAs rank their units through it.  Every CTA ranks the (at most 160)
+  // sequences itself (the K ring, unused until the first load, holds the
+  // lengths).
   if (a.sort_b) {
     int* eff = reinterpret_cast<int*>(smem + C::kOffK);
     const int64_t cap = int64_t(a.pps) * a.ps;
@@ -135,32 +186,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int o = eff[j];
         rank += (o > mine) || (o == mine && j < tid);
       }
-      if (rank == b) eff[a.B] = tid;
+      ord[rank] = tid;
     }
-    __syncthreads();
-    b = eff[a.B];
     __syncthreads();  // (read before anything else uses the ring)
   }
 
-  // ---- sequence geometry (identical in every CTA of this (b, kvh, rg))
-  const int64_t max_len = int64_t(a.pps) * a.ps;
-  const int64_t len_raw = a.seq_lens[b];
-  const int L = int(len_raw < max_len ? len_raw : max_len);
-  if (len_raw > max_len && a.err && tid == 0 && split == 0 && blockIdx.y == 0) atomicOr(a.err, kErrClamped);
-  const int spec0 = L - a.qs;
-  const int t_lo_all = a.win > 0 ? max(0, spec0 - a.win + 1) : 0;
-  const int pg_first = t_lo_all / a.ps;
-  const int pg_last = (L + a.ps - 1) / a.ps;
-  const int npages = max(0, pg_last - pg_first);
-  const int nvalid = (npages + a.split_pages - 1) / a.split_pages;
-  if (split >= max(nvalid, 1)) return;
-  const int pg_lo = pg_first + split * a.split_pages;
-  const int pg_hi = min(pg_lo + a.split_pages, pg_last);
-  const int t_begin = pg_lo * a.ps;
-  const int t_end = min(pg_hi * a.ps, L);
-  const int ntiles = (nvalid == 0 || t_end <= t_begin) ? 0 : (t_end - t_begin + kT - 1) / kT;
-  const int unit = (b * a.Hkv + kvh) * a.rg_count + rg;
-  const int rows_here = min(kRows, a.R - rg * kRows);
+  // lengths past the page table's bound are clamped (and reported once)
+  if (a.err && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+    for (int bb = tid; bb < a.B; bb += kThreads)
+      if (int64_t(a.seq_lens[bb]) > int64_t(a.pps) * a.ps) atomicOr(a.err, kErrClamped);
+
+  // a CTA past its unit's last split has nothing to do
+  Unit u0;
+  if (!unit_at(a, ord, 0, u0)) return;
+  if (a.persist == 0 && u0.split >= max(u0.nvalid, 1)) return;
 
   if (tid == 0) {
     for (int s = 0; s < C::kKStages; ++s) {
@@ -178,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars[C::kPVDone + k], 1);
     }
     mbar_init(&bars[C::kQReady], kSoftWarps);
+    mbar_init(&bars[C::kOFree], kSoftWarps);
     mbar_init(&bars[C::kDrain], 1);
     flags[0] = flags[1] = 0;
     fence_mbar_init();
@@ -201,26 +241,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* empty = &bars[is_v ? C::kVEmpty : C::kKEmpty];
     const CUtensorMap* map = is_v ? &tmV : &tmK;
     uint8_t* ring = smem + (is_v ? C::kOffV : C::kOffK);
-    if (ntiles > 0) {
-      if (lane == 0) prefetch_tensormap(map);
-      const int32_t* pt = a.page_table + int64_t(b) * a.pps;
-      const int box_rows = min(a.ps, 64);
-      const int pieces_max = kT / box_rows;  // page pieces of a full tile
+    const volatile int* vflags = flags;
+    if (lane == 0) prefetch_tensormap(map);
+    const int box_rows = min(a.ps, 64);
+    const int pieces_max = kT / box_rows;  // page pieces of a full tile
+    bool ok = true, bad = false;
+    int g = 0;  // tiles issued, over all of this CTA's units (ring slot and phase)
+    Unit u = u0;
+    for (int k = 0; ok; ++k) {
+      if (k > 0 && (vflags[0] || !unit_at(a, ord, k, u))) break;
+      const int32_t* pt = a.page_table + int64_t(u.b) * a.pps;
       // lane l issues box l of the tile: page piece l / chunks, chunk l % chunks
       int win_base = -(1 << 30), my_page = 0;
-      bool ok = true, bad = false;
-      int issued = 0;
-      for (int j = 0; ok && j < ntiles; ++j) {
-        const int s = j % nst, use = j / nst;
+      for (int j = 0; ok && j < u.ntiles; ++j, ++g) {
+        const int s = g % nst, use = g / nst;
         if (use > 0) ok = __all_sync(kAll, mbar_wait(&empty[s], (use - 1) & 1));
         if (!ok) break;
-        const int tok0 = t_begin + j * kT;
-        const int n_piece = min(pieces_max, (pg_hi * a.ps - tok0 + box_rows - 1) / box_rows);
+        const int tok0 = u.t_begin + j * kT;
+        const int n_piece = min(pieces_max, (u.pg_hi * a.ps - tok0 + box_rows - 1) / box_rows);
         const int first = tok0 / a.ps, last = (tok0 + n_piece * box_rows - 1) / a.ps;
         if (first < win_base || last >= win_base + 32) {  // refetch 32 page indices (warp-uniform)
           win_base = first;
           my_page = 0;
-          if (win_base + lane < pg_hi) {
+          if (win_base + lane < u.pg_hi) {
             const int pg = __ldg(pt + win_base + lane);
             my_page = (pg < 0 || int64_t(pg) >= a.num_pages) ? -1 : pg;  // out of the pool: TMA fills zeros
           }
@@ -236,66 +279,85 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int sub = tk % a.ps;
           uint8_t* dst = ring + s * C::kTileBytes + chunk * kT * 128 + l_piece * box_rows * 128;
           if (a.hnd)
-            tma_load_3d(dst, map, &full[s], chunk * 64, sub, page * a.Hkv + kvh);
+            tma_load_3d(dst, map, &full[s], chunk * 64, sub, page * a.Hkv + u.kvh);
           else
-            tma_load_3d(dst, map, &full[s], chunk * 64, kvh, page * a.ps + sub);
+            tma_load_3d(dst, map, &full[s], chunk * 64, u.kvh, page * a.ps + sub);
         }
         __syncwarp();
-        ++issued;
       }
-      bad = __any_sync(kAll, bad);
-      if (lane == 0) {
-        if (bad && a.err) atomicOr(a.err, kErrClamped);
-        // no load of this CTA may land after it exits
-        for (int j = max(0, issued - nst); j < issued; ++j)
-          if (!mbar_wait(&full[j % nst], (j / nst) & 1)) ok = false;
-        if (!ok) flags[0] = 1;
-      }
+    }
+    bad = __any_sync(kAll, bad);
+    if (lane == 0) {
+      if (bad && a.err) atomicOr(a.err, kErrClamped);
+      // no load of this CTA may land after it exits
+      for (int j = max(0, g - nst); j < g; ++j)
+        if (!mbar_wait(&full[j % nst], (j / nst) & 1)) ok = false;
+      if (!ok) flags[0] = 1;
     }
     __syncwarp();
   } else if (warp == 1) {
     // ================= MMA issuer (one thread) =================
-    if (lane == 0 && ntiles > 0) {
-      bool ok = mbar_wait(&bars[C::kQReady], 0);
+    if (lane == 0) {
+      const volatile int* vflags = flags;
+      bool ok = true;
       const uint32_t k0 = smem_u32(smem + C::kOffK), v0 = smem_u32(smem + C::kOffV), p0 = smem_u32(smem + C::kOffP);
-      // O += P(jj) V(jj): K = 128 tokens in steps of 16; P chunks of 64 tokens
-      // 16 KB apart; V MN-major, 64-dim atoms kT * 128 B apart, 8-token groups 1 KB apart
-      auto pv = [&](int jj) {
-        if (ok) ok = mbar_wait(&bars[C::kPFull + (jj & 1)], (jj >> 1) & 1);
-        if (ok) ok = mbar_wait(&bars[C::kVFull + jj % C::kVStages], (jj / C::kVStages) & 1);
-        if (!ok) return;
-        umma::fence_after_sync();
-        const uint32_t pa = p0 + (jj & 1) * C::kPBytes;
-        const uint32_t va = v0 + (jj % C::kVStages) * C::kTileBytes;
+      int g = 0;   // tiles done, over all of this CTA's units (buffers and phases)
+      int nq = 0;  // units with tiles done (the query's and O's barrier phases)
+      bool any = false;  // an MMA was issued
+      Unit u = u0;
+      for (int k = 0; ok; ++k) {
+        if (k > 0 && (vflags[0] || !unit_at(a, ord, k, u))) break;
+        if (u.ntiles == 0) continue;
+        ok = mbar_wait(&bars[C::kQReady], nq & 1);
+        const int gb = g;
+        // O += P(jj) V(jj) (tile jj of the unit): K = 128 tokens in steps of
+        // 16; P chunks of 64 tokens 16 KB apart; V MN-major, 64-dim atoms
+        // kT * 128 B apart, 8-token groups 1 KB apart.  The unit's first
+        // P V overwrites O, once the previous unit's O has been read out.
+        auto pv = [&](int jj) {
+          const int gg = gb + jj;
+          if (ok && jj == 0 && nq > 0) ok = mbar_wait(&bars[C::kOFree], (nq - 1) & 1);
+          if (ok) ok = mbar_wait(&bars[C::kPFull + (gg & 1)], (gg >> 1) & 1);
+          if (ok) ok = mbar_wait(&bars[C::kVFull + gg % C::kVStages], (gg / C::kVStages) & 1);
+          if (!ok) return;
+          umma::fence_after_sync();
+          const uint32_t pa = p0 + (gg & 1) * C::kPBytes;
+          const uint32_t va = v0 + (gg % C::kVStages) * C::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < kT / 16; ++kk)
-          umma::mma_ss(tmem + kColO, umma::smem_desc(pa + (kk >> 2) * 16384 + 32 * (kk & 3), 16, 1024, umma::kSw128),
-                       umma::smem_desc(va + 2048 * kk, kT * 128, 1024, umma::kSw128), kIdescPV, (jj | kk) != 0);
-        umma::commit(&bars[C::kVEmpty + jj % C::kVStages]);
-        umma::commit(&bars[C::kPVDone + (jj & 1)]);
-      };
-      for (int j = 0; ok && j < ntiles; ++j) {
-        const int s = j % C::kKStages;
-        ok = mbar_wait(&bars[C::kKFull + s], (j / C::kKStages) & 1);
-        if (ok && j >= 2) ok = mbar_wait(&bars[C::kSFree + (j & 1)], ((j >> 1) - 1) & 1);
-        if (!ok) break;
-        umma::fence_after_sync();
-        // S(j) = Q K(j)^T: K = D in steps of 16 (32 bytes within a 128-byte chunk)
-        const uint32_t ka = k0 + s * C::kTileBytes;
+          for (int kk = 0; kk < kT / 16; ++kk)
+            umma::mma_ss(tmem + kColO, umma::smem_desc(pa + (kk >> 2) * 16384 + 32 * (kk & 3), 16, 1024, umma::kSw128),
+                         umma::smem_desc(va + 2048 * kk, kT * 128, 1024, umma::kSw128), kIdescPV, (jj | kk) != 0);
+          umma::commit(&bars[C::kVEmpty + gg % C::kVStages]);
+          umma::commit(&bars[C::kPVDone + (gg & 1)]);
+        };
+        for (int j = 0; ok && j < u.ntiles; ++j) {
+          const int gg = gb + j, s = gg % C::kKStages;
+          ok = mbar_wait(&bars[C::kKFull + s], (gg / C::kKStages) & 1);
+          if (ok && gg >= 2) ok = mbar_wait(&bars[C::kSFree + (gg & 1)], ((gg >> 1) - 1) & 1);
+          if (!ok) break;
+          umma::fence_after_sync();
+          any = true;
+          // S(j) = Q K(j)^T: K = D in steps of 16 (32 bytes within a 128-byte chunk)
+          const uint32_t ka = k0 + s * C::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma::mma_ts(tmem + kColS + 128u * uint32_t(j & 1), tmem + kColQ + 8u * kk,
-                       umma::smem_desc(ka + (kk >> 2) * (kT * 128) + 32 * (kk & 3), 16, 1024, umma::kSw128),
-                       kIdescQK, kk != 0);
-        umma::commit(&bars[C::kKEmpty + s]);
-        umma::commit(&bars[C::kSFull + (j & 1)]);
-        if (j > 0) pv(j - 1);
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma::mma_ts(tmem + kColS + 128u * uint32_t(gg & 1), tmem + kColQ + 8u * kk,
+                         umma::smem_desc(ka + (kk >> 2) * (kT * 128) + 32 * (kk & 3), 16, 1024, umma::kSw128),
+                         kIdescQK, kk != 0);
+          umma::commit(&bars[C::kKEmpty + s]);
+          umma::commit(&bars[C::kSFull + (gg & 1)]);
+          if (j > 0) pv(j - 1);
+        }
+        if (ok) pv(u.ntiles - 1);
+        g = gb + u.ntiles;
+        ++nq;
       }
-      if (ok) pv(ntiles - 1);
       if (!ok) flags[0] = 1;
       // nothing this thread issued may still run when tensor memory is read or freed
-      umma::commit(&bars[C::kDrain]);
-      if (!mbar_wait(&bars[C::kDrain], 0)) flags[0] = 1;
+      if (any) {
+        umma::commit(&bars[C::kDrain]);
+        if (!mbar_wait(&bars[C::kDrain], 0)) flags[0] = 1;
+      }
     }
     __syncwarp();
   } else {
@@ -307,29 +369,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = 32 * q4 + lane;  // query row = tensor-memory lane
     const int st = tid - 32 * kSoftWarp0;  // 0 .. kSoft - 1
     const uint32_t lane_base = uint32_t(32 * q4) << 16;
-    const int r = rg * kRows + t;  // row among the kv head's q_seq_len x G rows
-    const bool real = t < rows_here;
-    const int i = real ? r / a.G : a.qs - 1, gg = real ? r % a.G : 0;
     const float q_scale = load_scale_tc(a.q_scale_dev, a.q_scale);
     const float kv_scale = load_scale_tc(a.kv_scale_dev, a.kv_scale);
     const float lscale = a.softmax_scale * q_scale * kv_scale * kLog2e;
     float* rowx = reinterpret_cast<float*>(smem + C::kOffRowX);  // [2][128] the halves' row maxima
     constexpr int kC = kT / 2;  // logit columns per thread
     constexpr int kDh = D / 2;  // O columns per thread
+    const volatile int* vflags = flags;
     bool ok = true;
 
-    // ---- the query row into tensor memory: this thread's half (D / 2 values
-    // as D / 4 columns)
-    {
-      const uint16_t* qrow =
-          static_cast<const uint16_t*>(a.q) + ((int64_t(b) * a.qs + i) * a.Hq + int64_t(kvh) * a.G + gg) * D + kDh * h;
+    // ---- a unit's query rows into tensor memory: this thread's half of row t
+    // (D / 2 values as D / 4 columns; zeros for padding rows)
+    auto load_q = [&](const Unit& uq) {
+      const int rq = uq.rg * kRows + t;
+      const bool rl = t < uq.rows_here;
+      const int iq = rl ? rq / a.G : a.qs - 1, gq = rl ? rq % a.G : 0;
+      const uint16_t* qrow = static_cast<const uint16_t*>(a.q) +
+                             ((int64_t(uq.b) * a.qs + iq) * a.Hq + int64_t(uq.kvh) * a.G + gq) * D + kDh * h;
       const uint4* src = reinterpret_cast<const uint4*>(qrow);
 #pragma unroll
       for (int part = 0; part < kDh / 64; ++part) {
         uint32_t w[32];
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
-          const uint4 x = real ? __ldg(src + part * 8 + v) : make_uint4(0, 0, 0, 0);
+          const uint4 x = rl ? __ldg(src + part * 8 + v) : make_uint4(0, 0, 0, 0);
           w[4 * v + 0] = x.x;
           w[4 * v + 1] = x.y;
           w[4 * v + 2] = x.z;
@@ -341,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t w[16];
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
-          const uint4 x = real ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+          const uint4 x = rl ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
           w[4 * v + 0] = x.x;
           w[4 * v + 1] = x.y;
           w[4 * v + 2] = x.z;
@@ -353,175 +416,207 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[C::kQReady]);
-    }
+    };
 
-    const int row_lb = a.win > 0 ? spec0 + i - a.win + 1 : INT_MIN;
-    uint32_t row_mw = 0xffffffffu;
-    if (a.mask) {
-      const uint16_t* mrow = a.mask + (int64_t(b) * a.qs + i) * a.mask_words;
-      row_mw = uint32_t(__ldg(mrow)) | (uint32_t(__ldg(mrow + 1)) << 16);
-    }
-    // running maximum (log2 units, scale applied) and this half's sum
-    float m_ref = -INFINITY, l_run = 0.f;
-    for (int j = 0; ok && j < ntiles; ++j) {
-      const int sb = j & 1;
-      const int tile0 = t_begin + j * kT + kC * h;  // this thread's first token
-      float x[kC];
-      ok = __all_sync(kAll, mbar_wait(&bars[C::kSFull + sb], (j >> 1) & 1));
-      if (ok) {
-        umma::fence_after_sync();
-        umma::tmem_ld32(tmem + lane_base + kColS + 128u * sb + uint32_t(kC) * h, x);
-        umma::tmem_ld32(tmem + lane_base + kColS + 128u * sb + uint32_t(kC) * h + 32u, x + 32);
-        umma::tmem_ld_wait();
-        umma::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[C::kSFree + sb]);
+    // Unit by unit: the tiles' softmax; then the next unit's query (the last
+    // Q K^T of this unit is done, so its columns are free, and the next
+    // unit's first Q K^T overlaps this unit's epilogue); then the epilogue,
+    // after which the next unit's first P V may overwrite O.  Barrier slots
+    // and phases count tiles over all of the CTA's units (g).
+    int g = 0;
+    Unit u = u0;
+    if (u.ntiles > 0) load_q(u);
+    for (int k = 0;; ++k) {
+      const int r = u.rg * kRows + t;  // row among the kv head's q_seq_len x G rows
+      const bool real = t < u.rows_here;
+      const int i = real ? r / a.G : a.qs - 1, gg = real ? r % a.G : 0;
+      const int b = u.b, kvh = u.kvh, spec0 = u.spec0, t_begin = u.t_begin, t_end = u.t_end;
+      const int row_lb = a.win > 0 ? spec0 + i - a.win + 1 : INT_MIN;
+      uint32_t row_mw = 0xffffffffu;
+      if (a.mask) {
+        const uint16_t* mrow = a.mask + (int64_t(b) * a.qs + i) * a.mask_words;
+        row_mw = uint32_t(__ldg(mrow)) | (uint32_t(__ldg(mrow + 1)) << 16);
       }
-      // scale; window, spec mask and the split's end by select (never
-      // multiply by 0); the maximum in four independent chains
-      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (ok) {
-        const bool edge = tile0 + kC > t_end || tile0 <= row_lb || (a.mask && tile0 + kC > spec0);
-        if (edge) {
-#pragma unroll
-          for (int k = 0; k < kC; ++k) {
-            const int tt = tile0 + k;
-            bool v = tt < t_end && tt >= row_lb;
-            if (a.mask && tt >= spec0) v = v && ((row_mw >> (tt - spec0)) & 1u);
-            x[k] = v ? x[k] * lscale : -INFINITY;
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < kC; ++k) x[k] *= lscale;
-        }
-#pragma unroll
-        for (int k = 0; k < kC; ++k) mx4[k & 3] = fmaxf(mx4[k & 3], x[k]);
-        rowx[h * kRows + t] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      }
-      // both halves of every row published their maxima
-      if (named_bar_or(1, kSoft, !ok)) {
-        ok = false;
-        break;
-      }
-      const float mx = fmaxf(rowx[t], rowx[kRows + t]);
-      const float m_new = fmaxf(m_ref, mx);
-      const bool need = m_new > m_ref + kRescaleLog2 || (m_ref == -INFINITY && m_new != -INFINITY);
-      const float f = (need && m_ref != -INFINITY) ? exp2f(m_ref - m_new) : 1.f;
-      if (need) {
-        l_run *= f;
-        m_ref = m_new;
-      }
-      // P buffer sb is free once P(j - 2) V(j - 2) is done
-      if (j >= 2) ok = __all_sync(kAll, mbar_wait(&bars[C::kPVDone + sb], ((j >> 1) - 1) & 1));
-      if (!ok) {
-        named_bar_or(1, kSoft, true);  // (matched below: every half leaves together)
-        break;
-      }
-      // P (16-bit, rounded; the row sum takes the rounded weights so O / l
-      // stays a convex combination): this thread's 64 tokens are chunk h of
-      // the [64-token chunk][128 rows][128 B] swizzled P tile
-      uint8_t* prow = smem + C::kOffP + sb * C::kPBytes + h * 16384;
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int u = 0; u < kC / 8; ++u) {
-        uint32_t w4[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = m_ref == -INFINITY ? 0.f : ex2(x[8 * u + 2 * e] - m_ref);
-          const float p1 = m_ref == -INFINITY ? 0.f : ex2(x[8 * u + 2 * e + 1] - m_ref);
-          w4[e] = pack_f32x2(p0, p1, kBf16);
-          const float2 rr = unpack_16x2(w4[e], kBf16);
-          ls[e] += rr.x + rr.y;
-        }
-        *reinterpret_cast<uint4*>(prow + umma::sw128(t, u)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-      }
-      l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      // O may change only once P(j - 1) V(j - 1) is done (whole warps: the
-      // tensor-memory accesses are warp-collective); each half scales its columns
-      if (__any_sync(kAll, f != 1.f)) {
-        ok = __all_sync(kAll, mbar_wait(&bars[C::kPVDone + (sb ^ 1)], ((j - 1) >> 1) & 1));
+      // running maximum (log2 units, scale applied) and this half's sum
+      float m_ref = -INFINITY, l_run = 0.f;
+      const int gb = g;
+      for (int j = 0; ok && j < u.ntiles; ++j) {
+        const int gj = gb + j, sb = gj & 1;
+        const int tile0 = t_begin + j * kT + kC * h;  // this thread's first token
+        float x[kC];
+        ok = __all_sync(kAll, mbar_wait(&bars[C::kSFull + sb], (gj >> 1) & 1));
         if (ok) {
           umma::fence_after_sync();
+          umma::tmem_ld32(tmem + lane_base + kColS + 128u * sb + uint32_t(kC) * h, x);
+          umma::tmem_ld32(tmem + lane_base + kColS + 128u * sb + uint32_t(kC) * h + 32u, x + 32);
+          umma::tmem_ld_wait();
+          umma::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[C::kSFree + sb]);
+        }
+        // scale; window, spec mask and the split's end by select (never
+        // multiply by 0); the maximum in four independent chains
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (ok) {
+          const bool edge = tile0 + kC > t_end || tile0 <= row_lb || (a.mask && tile0 + kC > spec0);
+          if (edge) {
+#pragma unroll
+            for (int c2 = 0; c2 < kC; ++c2) {
+              const int tt = tile0 + c2;
+              bool v = tt < t_end && tt >= row_lb;
+              if (a.mask && tt >= spec0) v = v && ((row_mw >> (tt - spec0)) & 1u);
+              x[c2] = v ? x[c2] * lscale : -INFINITY;
+            }
+          } else {
+#pragma unroll
+            for (int c2 = 0; c2 < kC; ++c2) x[c2] *= lscale;
+          }
+#pragma unroll
+          for (int c2 = 0; c2 < kC; ++c2) mx4[c2 & 3] = fmaxf(mx4[c2 & 3], x[c2]);
+          rowx[h * kRows + t] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        }
+        // both halves of every row published their maxima
+        if (named_bar_or(1, kSoft, !ok)) {
+          ok = false;
+          break;
+        }
+        const float mx = fmaxf(rowx[t], rowx[kRows + t]);
+        const float m_new = fmaxf(m_ref, mx);
+        const bool need = m_new > m_ref + kRescaleLog2 || (m_ref == -INFINITY && m_new != -INFINITY);
+        const float f = (need && m_ref != -INFINITY) ? exp2f(m_ref - m_new) : 1.f;
+        if (need) {
+          l_run *= f;
+          m_ref = m_new;
+        }
+        // P buffer sb is free once P V of the tile two back is done
+        if (gj >= 2) ok = __all_sync(kAll, mbar_wait(&bars[C::kPVDone + sb], ((gj >> 1) - 1) & 1));
+        if (!ok) {
+          named_bar_or(1, kSoft, true);  // (matched below: every half leaves together)
+          break;
+        }
+        // P (16-bit, rounded; the row sum takes the rounded weights so O / l
+        // stays a convex combination): this thread's 64 tokens are chunk h of
+        // the [64-token chunk][128 rows][128 B] swizzled P tile
+        uint8_t* prow = smem + C::kOffP + sb * C::kPBytes + h * 16384;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int u8 = 0; u8 < kC / 8; ++u8) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float p0 = m_ref == -INFINITY ? 0.f : ex2(x[8 * u8 + 2 * e] - m_ref);
+            const float p1 = m_ref == -INFINITY ? 0.f : ex2(x[8 * u8 + 2 * e + 1] - m_ref);
+            w4[e] = pack_f32x2(p0, p1, kBf16);
+            const float2 rr = unpack_16x2(w4[e], kBf16);
+            ls[e] += rr.x + rr.y;
+          }
+          *reinterpret_cast<uint4*>(prow + umma::sw128(t, u8)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+        l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        // O may change only once the previous tile's P V is done (whole
+        // warps: the tensor-memory accesses are warp-collective); each half
+        // scales its columns.  (f != 1 only past a unit's first tile.)
+        if (__any_sync(kAll, f != 1.f)) {
+          ok = __all_sync(kAll, mbar_wait(&bars[C::kPVDone + (sb ^ 1)], ((gj - 1) >> 1) & 1));
+          if (ok) {
+            umma::fence_after_sync();
 #pragma unroll 1
-          for (int q = 0; q < kDh / 16; ++q) {
-            float o[16];
+            for (int q = 0; q < kDh / 16; ++q) {
+              float o[16];
+              umma::tmem_ld16(tmem + lane_base + kColO + uint32_t(kDh) * h + 16u * q, o);
+              umma::tmem_ld_wait();
+#pragma unroll
+              for (int c2 = 0; c2 < 16; ++c2) o[c2] *= f;
+              umma::tmem_st16(tmem + lane_base + kColO + uint32_t(kDh) * h + 16u * q,
+                              reinterpret_cast<const uint32_t*>(o));
+            }
+            umma::tmem_st_wait();
+          }
+        }
+        // a tile running past the split's end: its V rows past the end are zeroed
+        const int vtile0 = t_begin + j * kT;
+        if (ok && vtile0 + kT > t_end) {
+          ok = __all_sync(kAll, mbar_wait(&bars[C::kVFull + gj % C::kVStages], (gj / C::kVStages) & 1));
+          if (ok) zero_v_rows<D>(smem + C::kOffV + (gj % C::kVStages) * C::kTileBytes, t_end - vtile0, st);
+        }
+        if (named_bar_or(1, kSoft, !ok)) {
+          ok = false;
+          break;
+        }
+        umma::fence_proxy_async_smem();
+        umma::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[C::kPFull + sb]);
+      }
+      g = gb + u.ntiles;
+      // every half of every row takes the same decision on going on
+      const bool stop = named_bar_or(1, kSoft, !ok || vflags[0] != 0);
+      Unit nu;
+      const bool has_next = !stop && unit_at(a, ord, k + 1, nu);
+      if (has_next && nu.ntiles > 0) load_q(nu);
+      // every P V of the unit is done (in order, so the last one's completion covers all)
+      if (u.ntiles > 0 && ok) {
+        ok = __all_sync(kAll, mbar_wait(&bars[C::kPVDone + ((g - 1) & 1)], ((g - 1) >> 1) & 1));
+        umma::fence_after_sync();
+      }
+      if (!ok) flags[0] = 1;
+      // the row's sum: both halves
+      named_bar(1, kSoft);
+      rowx[h * kRows + t] = l_run;
+      named_bar(1, kSoft);
+      const float l_row = rowx[t] + rowx[kRows + t];
+      named_bar(1, kSoft);
+      const bool aborted = vflags[0] != 0;
+      const bool single = u.nvalid <= 1;
+      const int unit = (b * a.Hkv + kvh) * a.rg_count + u.rg;
+      float* ws_unit = a.ws + int64_t(unit) * a.nsplit * kRows * (D + 4);
+      if (!aborted) {
+        // ---- epilogue: this thread's half of O row t from tensor memory
+        const float out_mul = kv_scale * a.rcp_out_scale;
+        float mul = 1.f;
+        if (single && real) {
+          const float sig = a.sinks ? __ldg(a.sinks + kvh * a.G + gg) * kLog2e : -INFINITY;
+          mul = finalize_row(m_ref, l_row, sig, out_mul,
+                             (a.lse && h == 0) ? a.lse + lse_index(a, b, kvh, r) : nullptr);
+        }
+        float* wrow = ws_unit + (int64_t(u.split) * kRows + t) * (D + 4);
+#pragma unroll 1
+        for (int q = 0; q < kDh / 16; ++q) {
+          float o[16];
+          if (u.ntiles > 0) {
             umma::tmem_ld16(tmem + lane_base + kColO + uint32_t(kDh) * h + 16u * q, o);
             umma::tmem_ld_wait();
+          } else {
 #pragma unroll
-            for (int k = 0; k < 16; ++k) o[k] *= f;
-            umma::tmem_st16(tmem + lane_base + kColO + uint32_t(kDh) * h + 16u * q, reinterpret_cast<const uint32_t*>(o));
+            for (int c2 = 0; c2 < 16; ++c2) o[c2] = 0.f;
           }
-          umma::tmem_st_wait();
+          if (!real) continue;
+          const int col = kDh * h + 16 * q;
+          if (single) {
+            const int64_t oi = ((int64_t(b) * a.qs + i) * a.Hq + int64_t(kvh) * a.G + gg) * a.Dv + col;
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              store_out4(a, oi + 4 * v, make_float4(o[4 * v] * mul, o[4 * v + 1] * mul, o[4 * v + 2] * mul,
+                                                    o[4 * v + 3] * mul));
+          } else {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              reinterpret_cast<float4*>(wrow + col)[v] = make_float4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+          }
+        }
+        if (!single && real && h == 0) {
+          wrow[D] = m_ref;
+          wrow[D + 1] = l_row;
         }
       }
-      // a tile running past the split's end: its V rows past the end are zeroed
-      const int vtile0 = t_begin + j * kT;
-      if (ok && vtile0 + kT > t_end) {
-        ok = __all_sync(kAll, mbar_wait(&bars[C::kVFull + j % C::kVStages], (j / C::kVStages) & 1));
-        if (ok) zero_v_rows<D>(smem + C::kOffV + (j % C::kVStages) * C::kTileBytes, t_end - vtile0, st);
+      // O has been read out: the next unit's first P V may overwrite it
+      if (u.ntiles > 0) {
+        umma::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[C::kOFree]);
       }
-      if (named_bar_or(1, kSoft, !ok)) {
-        ok = false;
-        break;
-      }
-      umma::fence_proxy_async_smem();
-      umma::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[C::kPFull + sb]);
-    }
-    // every P V is done (in order, so the last one's completion covers all)
-    if (ntiles > 0 && ok) {
-      ok = __all_sync(kAll, mbar_wait(&bars[C::kPVDone + ((ntiles - 1) & 1)], ((ntiles - 1) >> 1) & 1));
-      umma::fence_after_sync();
-    }
-    if (!ok) flags[0] = 1;
-    // the row's sum: both halves
-    named_bar(1, kSoft);
-    rowx[h * kRows + t] = l_run;
-    named_bar(1, kSoft);
-    const float l_row = rowx[t] + rowx[kRows + t];
-    named_bar(1, kSoft);
-    const bool aborted = flags[0] != 0;
-    const bool single = nvalid <= 1;
-    float* ws_unit = a.ws + int64_t(unit) * a.nsplit * kRows * (D + 4);
-    if (!aborted) {
-      // ---- epilogue: this thread's half of O row t from tensor memory
-      const float out_mul = kv_scale * a.rcp_out_scale;
-      float mul = 1.f;
-      if (single && real) {
-        const float sig = a.sinks ? __ldg(a.sinks + kvh * a.G + gg) * kLog2e : -INFINITY;
-        mul = finalize_row(m_ref, l_row, sig, out_mul,
-                           (a.lse && h == 0) ? a.lse + lse_index(a, b, kvh, r) : nullptr);
-      }
-      float* wrow = ws_unit + (int64_t(split) * kRows + t) * (D + 4);
-#pragma unroll 1
-      for (int q = 0; q < kDh / 16; ++q) {
-        float o[16];
-        if (ntiles > 0) {
-          umma::tmem_ld16(tmem + lane_base + kColO + uint32_t(kDh) * h + 16u * q, o);
-          umma::tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int k = 0; k < 16; ++k) o[k] = 0.f;
-        }
-        if (!real) continue;
-        const int col = kDh * h + 16 * q;
-        if (single) {
-          const int64_t oi = ((int64_t(b) * a.qs + i) * a.Hq + int64_t(kvh) * a.G + gg) * a.Dv + col;
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            store_out4(a, oi + 4 * v, make_float4(o[4 * v] * mul, o[4 * v + 1] * mul, o[4 * v + 2] * mul,
-                                                  o[4 * v + 3] * mul));
-        } else {
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            reinterpret_cast<float4*>(wrow + col)[v] = make_float4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
-        }
-      }
-      if (!single && real && h == 0) {
-        wrow[D] = m_ref;
-        wrow[D + 1] = l_row;
-      }
+      if (!has_next) break;
+      u = nu;
     }
   }
 
@@ -533,7 +628,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     umma::tmem_dealloc(tmem, kTmemCols);
   }
   if (flags[0] && tid == 0 && a.err) atomicOr(a.err, kErrTimeout);
-  if (nvalid <= 1) return;
+  // (persistent CTAs run unsplit units only)
+  if (a.persist != 0 || u0.nvalid <= 1) return;
+  const int nvalid = u0.nvalid, rows_here = u0.rows_here, b = u0.b, kvh = u0.kvh, rg = u0.rg;
+  const int unit = (b * a.Hkv + kvh) * a.rg_count + rg;
 
   // ---- split-KV: the last CTA of the unit merges every split's partial (a
   // CTA whose wait gave up still takes its ticket, so the semaphore returns

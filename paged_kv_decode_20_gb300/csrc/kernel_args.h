@@ -33,6 +33,8 @@ struct DecodeArgs {
   int hnd;                     // cache layout HND (else NHD)
   int pdl;                     // launched with programmatic stream serialization
   int sort_b;                  // map grid slots to sequences longest first (B <= 160)
+  int persist;                 // tensor-core kernel: this many persistent CTAs take the
+                               // unsplit units in turn (0: one CTA per unit and split)
 };
 
 }  // namespace xqa

@@ -81,6 +81,7 @@ struct Plan {
   int row_blocks = 1, warp_rows = 1, rows = 16, rg_count = 1;
   bool tc = false;  // the tensor-core kernel (large grouped tiles, 16-bit K/V)
   int nsplit = 1, split_pages = 1;
+  int persist = 0;  // tensor-core kernel: persistent CTAs (0: one CTA per unit and split)
   int max_pages = 1;
   size_t ws_bytes = 0;
   size_t nsems = 0;
@@ -287,6 +288,15 @@ xqa_status plan_gqa(const xqa_params* p, int sm_count_in, Plan* pl) {
   const int stage_pages = p->page_size <= tok ? tok / p->page_size : 1;
   choose_splits(p, pl, sm, occ, stage_pages);
   const int64_t units = int64_t(p->batch_size) * p->num_kv_heads * pl->rg_count;
+  // More unsplit tensor-core units than CTA slots: the slots' CTAs stay
+  // resident and take the units in turn (ranked longest first), so each unit
+  // after a CTA's first starts its loads while the one before is finalised,
+  // and no SM waits for the next CTA to be scheduled.  Needs the ranking
+  // (2..160 sequences).
+  const int64_t slots = int64_t(sm) * std::max(occ, 1);
+  pl->persist = (pl->tc && pl->nsplit == 1 && p->batch_size > 1 && p->batch_size <= 160 && units > slots)
+                    ? int(slots)
+                    : 0;
   pl->nsems = size_t(units);
   pl->ws_bytes = pl->nsplit > 1 ? size_t(units) * pl->nsplit * pl->rows * (D + 4) * sizeof(float) : 0;
   return XQA_OK;
@@ -370,6 +380,7 @@ void fill_args(const xqa_params* p, const Plan& pl, void* ws, uint32_t* sems, xq
   a->hnd = p->kv_layout == XQA_HND;
   a->pdl = p->enable_pdl != 0;
   a->sort_b = p->batch_size > 1 && p->batch_size <= 160;
+  a->persist = pl.persist;
 }
 
 xqa_status check_buffers(const Plan& pl, void* ws, size_t ws_bytes, uint32_t* sems) {
@@ -436,7 +447,7 @@ xqa_status xqa_decode(const xqa_params* p, void* ws, size_t ws_bytes, uint32_t* 
   if (st != XQA_OK) return st;
   xqa::DecodeArgs a;
   fill_args(p, pl, ws, sems, &a);
-  dim3 grid(pl.nsplit, p->num_kv_heads * pl.rg_count, p->batch_size);
+  const dim3 grid = pl.persist ? dim3(1, 1, pl.persist) : dim3(pl.nsplit, p->num_kv_heads * pl.rg_count, p->batch_size);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (pl.tc)
