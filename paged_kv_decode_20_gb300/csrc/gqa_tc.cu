@@ -3,10 +3,14 @@
 // with q_seq_len x G > 16 query rows per kv head, e.g. speculative tokens on a
 // large GQA group; 16-bit K/V).
 //
-// One CTA owns (sequence b, kv head kvh, row group rg, KV split).  Its rows
+// A unit is (sequence b, kv head kvh, row group rg, KV split).  Its rows
 // (q_seq_len x G, up to 128, padded to one M = 128 UMMA tile with zero query
 // rows that are never stored) are the A operand of S = Q K^T, held in tensor
-// memory; every KV page is read once.
+// memory; every KV page is read once.  One CTA per unit, or (more unsplit
+// units than CTA slots) one resident CTA per slot taking its units in turn:
+// every role walks the same unit list, the barrier slots and phases run on
+// across units, the next unit's query goes into tensor memory while the
+// last one's epilogue reads O, and that unit's first P V waits for it.
 //
 //   warps 0 and 10 (producers of K and of V): walk page_table (32 page indices
 //     per lane window) and issue a tile's TMA boxes, one per (page piece,
