@@ -147,6 +147,20 @@ def test_large_group_tiles_split_counts(sm_count):
     check(c, sm_count=sm_count)
 
 
+
+@pytest.mark.parametrize("sm_count", [1, 3, 7])
+@pytest.mark.parametrize("layout", ["HND", "NHD"])
+def test_large_group_persistent_ctas_walk_many_units(sm_count, layout):
+    """More unsplit tensor-core units than CTA slots: resident CTAs take the
+    units in turn (here 20 units on 1, 3 or 7 CTAs), with empty and
+    one-token sequences, a window, sinks, a spec mask and two row groups per
+    kv head (144 rows: 128 + 16)."""
+    c = W.make_case(batch=5, num_q_heads=96, num_kv_heads=2, head_dim=128, page_size=32,
+                    seq_lens=[0, 700, 3, 300, 129], q_seq_len=3, mask="causal", sinks=True,
+                    sliding_win_size=200, kv_layout=layout, seed=91)
+    check(c, sm_count=sm_count)
+
+
 @pytest.mark.parametrize("G,qs", [(16, 4), (32, 4), (64, 1)])
 def test_large_group_tiles_d64(G, qs):
     c = W.make_case(batch=2, num_q_heads=2 * G, num_kv_heads=2, head_dim=64, page_size=16,
