@@ -6,7 +6,9 @@ oracle, so that combinations the named sweeps do not cross are covered too.
 Each case is drawn from its own seed; the test id spells the draw out, so a
 failing case can be rebuilt from its id alone.  Tolerances are those of the
 named parity tests: max-abs 1e-2 (16-bit K/V) or 3e-2 (fp8 K/V) beyond the
-output's own rounding, and a relative-L2 bound of 1e-2.
+output's own rounding, and a relative-L2 bound of 1e-2; each draw runs again
+returning the log-sum-exp (max-abs 3e-3, -inf rows alike), which must leave
+the output bit for bit unchanged.
 """
 
 import random
@@ -20,6 +22,7 @@ from paged_kv_decode_20_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 F8 = torch.float8_e4m3fn
+LSE_TOL = 3e-3  # natural-log units, as the named log-sum-exp tests
 DT = {"bf16": torch.bfloat16, "f16": torch.float16, "e4m3": F8}
 
 
@@ -112,6 +115,21 @@ def run_and_compare(c, tol, sm):
     l2 = ((got - ref).norm() / ref.norm().clamp_min(1e-30)).item()
     assert err <= tol, f"max abs error {err:.3e} > {tol}"
     assert l2 <= 1e-2, f"relative L2 error {l2:.3e}"
+    # the same draw with the log-sum-exp returned: the output must not change
+    dec2 = Decoder(c.to("cuda"), lse=True, **kw)
+    dec2.lse.fill_(float("nan"))
+    out2 = dec2.run().clone()
+    torch.cuda.synchronize()
+    assert dec2.error_bits() == 0
+    assert torch.equal(out2, outs[0]), "the log-sum-exp output changed the attention output"
+    _, ref_lse = oracle.xqa_attention(c.q, c.k_cache, c.v_cache, c.page_table, c.seq_lens, return_lse=True,
+                                      **c.kwargs())
+    got_lse = dec2.lse.cpu()
+    assert torch.equal(torch.isneginf(got_lse), torch.isneginf(ref_lse)), "-inf rows differ"
+    fin = torch.isfinite(ref_lse)
+    if fin.any():
+        lerr = (got_lse.to(torch.float64)[fin] - ref_lse[fin]).abs().max().item()
+        assert lerr <= LSE_TOL, f"lse max abs {lerr:.3e}"
 
 
 @pytest.mark.parametrize("seed,d", GQA_CASES, ids=[_id(d) for _, d in GQA_CASES])
